@@ -1,0 +1,200 @@
+"""Seeded synthetic inputs for the batched speculative-sampling verify step.
+
+This module only *makes inputs*. It holds none of the verify step's own arithmetic (no softmax,
+no acceptance ratio, no residual, no inverse CDF). Both the CUDA path and the float64 oracle are
+fed from here, and neither of them imports the other.
+
+The five workloads mirror the Llama/Qwen-class shapes the pages talk about (Llama-3, the
+Llama-2-7B LayerSkip checkpoint and Qwen-3 are named on the SSD and LayerSkip pages); the vocab
+sizes 32000 / 128256 / 152064 are those of the Llama-2, Llama-3 and Qwen families. No dataset is
+read: every logit is drawn from a seeded generator.
+
+Generation recipe (per workload ``c`` and sequence ``b``):
+
+* Target logits ``z_t``: i.i.d. normal (workloads 1, 2) or a Zipf(1.1)-shaped log-prior
+  ``l(v) = -1.1 * ln(1 + pi(v))`` plus N(0, 1) noise (workloads 3-5), where ``pi`` is a seeded
+  permutation of the vocabulary shared by all rows, so frequent ids are spread over the row.
+* Draft logits ``z_d = z_t + N(0, sigma_d^2)``, computed in float32 and then rounded to the
+  storage type (bf16 with round-to-nearest-even, or kept as float32).
+* Draft tokens: the drafter samples from its own distribution at temperature ``T`` with the
+  Gumbel-max rule ``x = argmax_v(z_d[v]/T + ln f(v) + G_v)``, ``G_v ~ Gumbel(0, 1)`` in float64.
+  ``f(v) = beta`` for the ``bias_k`` ids with the largest draft logit (ties to the lower id) and
+  1 elsewhere; this is the Saguaro-style down-weighting of the most likely draft tokens (SSD page,
+  "Method"), applied before drafting. Greedy drafters take ``argmax_v z_d[v]`` (first occurrence).
+* Draft lengths: all ``K``, or uniform on ``1..K`` for the ragged workload (the dynamic
+  draft length of Kangaroo's confidence exit, Kangaroo page, "Double Early Exiting").
+* Uniforms: ``numpy.random.default_rng(0).random((B, K+1), float32)``; ``u[b, i]`` drives accept
+  test ``i`` and ``u[b, K]`` the final sample.
+* Rows that the verify step never reads (target rows ``i > L_b``, draft rows ``i >= L_b``) are
+  filled with NaN so that any stray read shows up as an invalid sequence.
+
+Seeds are ``numpy.random.default_rng([tag, c, b, offset])`` with tags 100 (target), 200 (draft
+noise), 300 (drafting), 400 (Zipf permutation, per workload) and 500 (lengths); ``offset``
+separates replicas (e.g. ranks of a multi-GPU weak-scaling run).
+"""
+from __future__ import annotations
+
+import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
+from typing import Optional, Tuple
+
+import numpy as np
+
+BF16_NAN = np.uint16(0x7FC0)
+F32_NAN = np.float32(np.nan)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic verify workload (shapes, dtype, mode and generation parameters)."""
+
+    cfg_id: int
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str  # "f32" or "bf16"
+    mode: str  # "stochastic" or "greedy"
+    temperature: float
+    sigma_t: float  # std of the target noise
+    sigma_d: float  # std of the draft-vs-target noise
+    zipf: bool
+    ragged: bool = False
+    beta: float = 1.0
+    bias_k: int = 0
+    fanout: Optional[Tuple[int, ...]] = None
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    1: Workload(1, "B1_K4_V32000_f32_stochastic", B=1, K=4, V=32000, dtype="f32",
+                mode="stochastic", temperature=1.0, sigma_t=2.0, sigma_d=0.5, zipf=False),
+    2: Workload(2, "B8_K5_V32000_bf16_greedy", B=8, K=5, V=32000, dtype="bf16",
+                mode="greedy", temperature=0.0, sigma_t=3.0, sigma_d=1.0, zipf=False),
+    3: Workload(3, "B64_K5_V128256_bf16_T0.8", B=64, K=5, V=128256, dtype="bf16",
+                mode="stochastic", temperature=0.8, sigma_t=1.0, sigma_d=0.7, zipf=True),
+    4: Workload(4, "B32_K5_V128256_bf16_saguaro_beta0.5_F84211", B=32, K=5, V=128256,
+                dtype="bf16", mode="stochastic", temperature=1.0, sigma_t=1.0, sigma_d=0.7,
+                zipf=True, beta=0.5, bias_k=8, fanout=(8, 4, 2, 1, 1)),
+    5: Workload(5, "B256_K8_V152064_bf16_ragged", B=256, K=8, V=152064, dtype="bf16",
+                mode="stochastic", temperature=1.0, sigma_t=1.0, sigma_d=0.5, zipf=True,
+                ragged=True),
+}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (round to nearest, ties to even) and return the 16-bit patterns."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = bits + np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1))
+    out = (rounded >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = BF16_NAN
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 (exact)."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def zipf_log_prior(w: Workload, offset: int = 0) -> np.ndarray:
+    """l(v) = -1.1 ln(1 + pi(v)) with a seeded permutation pi, float32 [V]."""
+    perm = np.random.default_rng([400, w.cfg_id, offset]).permutation(w.V)
+    return (-1.1 * np.log1p(perm.astype(np.float64))).astype(np.float32)
+
+
+def draft_lengths(w: Workload, offset: int = 0) -> np.ndarray:
+    if not w.ragged:
+        return np.full(w.B, w.K, dtype=np.int32)
+    return np.random.default_rng([500, w.cfg_id, offset]).integers(
+        1, w.K + 1, size=w.B).astype(np.int32)
+
+
+def uniforms(w: Workload, offset: int = 0) -> np.ndarray:
+    seed = 0 if offset == 0 else [0, offset]
+    return np.random.default_rng(seed).random((w.B, w.K + 1), dtype=np.float32)
+
+
+def _top_set(zd: np.ndarray, k: int) -> np.ndarray:
+    """Ids of the k largest entries (ties to the lower id) -- the drafter's down-weighted set."""
+    k = min(k, zd.shape[0])
+    if k <= 0:
+        return np.zeros(0, dtype=np.int64)
+    order = np.lexsort((np.arange(zd.shape[0]), -zd.astype(np.float64)))
+    return order[:k]
+
+
+def _draw_draft(zd_row: np.ndarray, w: Workload, rng: np.random.Generator) -> int:
+    z = zd_row.astype(np.float64)
+    if w.mode == "greedy":
+        return int(np.argmax(z))
+    score = z / w.temperature
+    if w.beta < 1.0 and w.bias_k > 0:
+        score[_top_set(z, w.bias_k)] += np.log(w.beta)
+    return int(np.argmax(score + rng.gumbel(size=z.shape[0])))
+
+
+def _make_sequence(w: Workload, b: int, L: int, prior, offset: int, tgt_out, dft_out, tok_out):
+    rng_t = np.random.default_rng([100, w.cfg_id, b, offset])
+    rng_d = np.random.default_rng([200, w.cfg_id, b, offset])
+    rng_x = np.random.default_rng([300, w.cfg_id, b, offset])
+    V, K = w.V, w.K
+    rows_t = L + 1
+    zt = rng_t.standard_normal((rows_t, V), dtype=np.float32)
+    zt *= np.float32(w.sigma_t)
+    if prior is not None:
+        zt += prior
+    zd = zt[:L] + np.float32(w.sigma_d) * rng_d.standard_normal((L, V), dtype=np.float32)
+    if w.dtype == "bf16":
+        tgt_out[b, :rows_t] = f32_to_bf16_bits(zt)
+        tgt_out[b, rows_t:] = BF16_NAN
+        zd_store = f32_to_bf16_bits(zd)
+        dft_out[b, :L] = zd_store
+        dft_out[b, L:] = BF16_NAN
+        zd_seen = bf16_bits_to_f32(zd_store)
+    else:
+        tgt_out[b, :rows_t] = zt
+        tgt_out[b, rows_t:] = F32_NAN
+        dft_out[b, :L] = zd
+        dft_out[b, L:] = F32_NAN
+        zd_seen = zd
+    tok_out[b, :] = 0
+    for i in range(L):
+        tok_out[b, i] = _draw_draft(zd_seen[i], w, rng_x)
+
+
+def make_inputs(w: Workload, offset: int = 0, threads: Optional[int] = None) -> dict:
+    """Generate one batch for workload ``w``.
+
+    Returns a dict of numpy arrays: ``target`` [B, K+1, V] and ``draft`` [B, K, V] (uint16 bf16
+    bit patterns or float32), ``draft_tokens`` [B, K] int32, ``draft_lens`` [B] int32 and
+    ``uniforms`` [B, K+1] float32, plus the workload itself under ``workload``.
+    """
+    B, K, V = w.B, w.K, w.V
+    store = np.uint16 if w.dtype == "bf16" else np.float32
+    tgt = np.empty((B, K + 1, V), dtype=store)
+    dft = np.empty((B, K, V), dtype=store)
+    tok = np.zeros((B, K), dtype=np.int32)
+    lens = draft_lengths(w, offset)
+    prior = zipf_log_prior(w, offset) if w.zipf else None
+    if threads is None:
+        threads = min(16, len(os.sched_getaffinity(0)))
+    if B:
+        with ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+            list(ex.map(lambda b: _make_sequence(w, b, int(lens[b]), prior, offset,
+                                                 tgt, dft, tok), range(B)))
+    return {"workload": w, "target": tgt, "draft": dft, "draft_tokens": tok,
+            "draft_lens": lens, "uniforms": uniforms(w, offset)}
+
+
+def small_variant(w: Workload, B: int, V: Optional[int] = None) -> Workload:
+    """Same generation recipe at a smaller batch (and optionally vocabulary)."""
+    return w.replace(B=B, V=V if V is not None else w.V)

@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched speculative-sampling verify step.
+
+Workload: B=256 sequences, K=8 draft positions, V=152064, bf16 logits, temperature 1, ragged
+draft lengths uniform on 1..8, Zipf(1.1) log-prior + N(0,1) target logits, draft = target +
+N(0, 0.5^2) (seeded, synthetic). One step = one verify call over the whole batch.
+
+value     verified draft tokens per second (sum of draft lengths / verify time), whole job
+          over all ranks, inputs resident in HBM, L2 flushed (256 MiB write) before each step.
+e2e       the same metric through the host-buffer entry point spec_verify_host: host->device
+          copy of the rows each sequence has, the verify call and the device->host copy of the
+          outputs, all inside the timed region.
+roofline  algorithmic bytes (the rows the outcome needs: target rows 0..a_b and draft rows
+          0..min(a_b, L_b-1) of each sequence) per launch / mean kernel time, against the
+          measured HBM peak.
+cpu_baseline  the float64 oracle on the host cores over the same batch.
+
+--impl reference times the oracle itself as the reference arm (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/sec and achieved HBM GB/s (% of roofline) at 1 GB300"
+UNIT = "verified draft tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cluster", type=int, default=0, help="CTAs per sequence (0 = library)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sample", type=int, default=16,
+                    help="sequences per step of the reference arm")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+# ---------------------------------------------------------------------------------------------
+# byte accounting
+# ---------------------------------------------------------------------------------------------
+def algorithmic_bytes(w, lens, acc) -> int:
+    """Bytes of the rows the outcome needs: target rows 0..a_b, draft rows 0..min(a_b, L_b-1)
+    (every draft row below L_b when top-F ids are requested), plus ids, lengths, uniforms and
+    outputs."""
+    rows = 0
+    for L, a in zip(lens.tolist(), acc.tolist()):
+        if a < 0:
+            continue
+        rows += a + 1
+        if w.mode == "stochastic":
+            rows += L if w.fanout else min(a, L - 1) + 1
+    small = w.B * (4 * w.K + 4 + 4 * (w.K + 1) + 4 + 4 * (w.K + 1))
+    return rows * w.V * w.elem_bytes + small
+
+
+def input_bytes(w, lens) -> int:
+    """Bytes of every row the sequences have (target 0..L_b, draft 0..L_b-1)."""
+    rows = int(np.sum(lens + 1)) + (int(np.sum(lens)) if w.mode == "stochastic" else 0)
+    return rows * w.V * w.elem_bytes
+
+
+def host_copy_bytes(w, lens):
+    """Bytes spec_verify_host moves per call (mirrors its per-sequence / whole-buffer choice)."""
+    B, K = w.B, w.K
+    need = int(np.sum(lens))
+    per_seq = (2 * need + B) * 4 < 3 * B * (2 * K + 1)
+    rows_t = int(np.sum(lens + 1)) if per_seq else B * (K + 1)
+    rows_d = (need if per_seq else B * K) if w.mode == "stochastic" else 0
+    h2d = (rows_t + rows_d) * w.V * w.elem_bytes + B * K * 4 + B * 4
+    if w.mode == "stochastic":
+        h2d += B * (K + 1) * 4
+    d2h = B * 4 + B * (K + 1) * 4 + (B * K * max(w.fanout) * 4 if w.fanout else 0)
+    return h2d, d2h
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
+
+
+def recorded_traffic(workload: str, digest: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel has not changed."""
+    import glob
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("workload") == workload and fields.get("source_digest") == digest:
+            try:
+                return float(fields["dram_bytes_per_launch"]), os.path.basename(path)
+            except (KeyError, ValueError):
+                pass
+    return None, None
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# multi-rank aggregation (weak scaling: every rank verifies its own batch)
+# ---------------------------------------------------------------------------------------------
+def aggregate(tokens: float, ms: float, group=None):
+    """(sum of tokens over ranks, max of per-rank ms) -- plain values on a single rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return tokens, ms
+    import torch
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([tokens], dtype=torch.float64, device=dev)
+    m = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item()), float(m.item())
+
+
+def oracle_time(d, w, seqs):
+    from oracle import verify as O
+    t0 = time.perf_counter()
+    res = O.verify_batch(d["target"], d["draft"] if w.mode == "stochastic" else None,
+                         d["draft_tokens"], d["draft_lens"], d["uniforms"],
+                         temperature=w.temperature, mode=w.mode, beta=w.beta, bias_k=w.bias_k,
+                         fanout=w.fanout, seqs=seqs)
+    return time.perf_counter() - t0, res
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_33_gb300 import workloads as W
+    w_full = W.WORKLOADS[5]
+    w = W.small_variant(w_full, B=args.sample)  # same seeds: the first `sample` sequences
+    d = W.make_inputs(w)
+    toks = int(np.sum(d["draft_lens"]))
+    for _ in range(args.warmup):
+        oracle_time(d, w, range(w.B))
+    times = [oracle_time(d, w, range(w.B))[0] for _ in range(args.steps)]
+    mean = statistics.mean(times)
+    value = toks / mean
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w_full.name, "B": w_full.B, "K": w_full.K, "V": w_full.V,
+                       "sample_sequences": w.B},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"first {w.B} of {w_full.B} sequences per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_33_gb300 import api, build
+    from speculative_decoding_verification_33_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    w = W.WORKLOADS[5]
+    d = W.make_inputs(w, offset=rank)
+    lens = d["draft_lens"]
+    toks_local = float(np.sum(lens))
+
+    T = api.to_device_logits(d["target"])
+    D = api.to_device_logits(d["draft"])
+    tok = torch.from_numpy(d["draft_tokens"]).cuda()
+    ln = torch.from_numpy(lens).cuda()
+    uni = torch.from_numpy(d["uniforms"]).cuda()
+    acc = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    otok = torch.empty(w.B, w.K + 1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def step():
+        api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, acc, otok, None,
+                        cluster_hint=args.cluster)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record()
+        step()
+        ends[s].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    kms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    mean_ms = statistics.mean(kms)
+    toks_all, ms_max = aggregate(toks_local, mean_ms)
+    value = toks_all / (ms_max * 1e-3)
+
+    g_acc = acc.cpu().numpy()
+    g_tok = otok.cpu().numpy()
+    b_alg = algorithmic_bytes(w, lens, g_acc)
+    b_in = input_bytes(w, lens)
+    peak, peak_src = measured_peak()
+    achieved = b_alg / (mean_ms * 1e-3) / 1e9
+    digest = build.source_digest()
+    traffic, traffic_src = recorded_traffic(w.name, digest)
+
+    # read-only streaming probe (2 GiB), for context
+    probe_gbs = None
+    try:
+        buf = torch.empty(1 << 29, dtype=torch.int32, device="cuda")
+        buf.fill_(1)
+        out = torch.zeros(1, dtype=torch.int64, device="cuda")
+        for _ in range(3):
+            api.hbm_read_probe(buf, out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            api.hbm_read_probe(buf, out)
+        e1.record()
+        torch.cuda.synchronize()
+        probe_gbs = 10 * buf.numel() * 4 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        del buf
+    except Exception as ex:  # pragma: no cover - reported, not fatal
+        probe_gbs = f"unavailable: {ex}"
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Zipf-prior logits, Gumbel-max drafts, NaN padding rows)",
+            "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V,
+                       "temperature": w.temperature, "draft_lens": "uniform 1..8",
+                       "verified_tokens_per_rank": toks_local,
+                       "l2": "flushed before each step (256 MiB write, outside the events)",
+                       "cluster_hint": args.cluster,
+                       "wall_ms_per_step_incl_flush": wall / args.steps * 1e3},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": peak_src, "traffic_source": traffic_src,
+                         "algorithmic_bytes_per_launch": b_alg,
+                         "all_rows_bytes_per_launch": b_in,
+                         "all_rows_gbs": b_in / (mean_ms * 1e-3) / 1e9,
+                         "read_probe_gbs": probe_gbs,
+                         "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms)},
+            "gpu_launches": args.steps, "clocks": clk}
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    if not args.no_e2e:
+        hT = torch.from_numpy(d["target"].view(np.int16)).pin_memory()
+        hD = torch.from_numpy(d["draft"].view(np.int16)).pin_memory()
+        h_tok = torch.from_numpy(d["draft_tokens"]).pin_memory()
+        h_len = torch.from_numpy(lens).pin_memory()
+        h_uni = torch.from_numpy(d["uniforms"]).pin_memory()
+        h_acc = torch.empty(w.B, dtype=torch.int32).pin_memory()
+        h_out = torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory()
+
+        def e2e_step():
+            api.verify_host(hT, hD, h_tok, h_len, h_uni, h_acc, h_out, dtype="bf16",
+                            temperature=w.temperature, beta=w.beta, mode=w.mode)
+
+        for _ in range(2):
+            e2e_step()
+        n_e2e = max(3, min(args.steps, 20))
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        t_e2e = (time.perf_counter() - t0) / n_e2e
+        _, t_e2e_max = aggregate(0.0, t_e2e)
+        h2d, d2h = host_copy_bytes(w, lens)
+        line["e2e"] = {"value": toks_all / t_e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e_max * 1e3,
+                       "matches_device_call": bool(np.array_equal(h_acc.numpy(), g_acc) and
+                                                   np.array_equal(h_out.numpy(), g_tok))}
+
+    # CPU baseline (the oracle, one core, the whole batch) and full-size parity
+    if rank == 0 and world >= 1 and not args.no_cpu:
+        from tests.parity import compare
+        t_cpu, res = oracle_time(d, w, range(w.B))
+        rep = compare(res, range(w.B), g_acc, g_tok)
+        line["cpu_baseline"] = {"value": toks_local / t_cpu, "unit": UNIT, "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"all {w.B} sequences of rank 0's batch, once"}
+        line["parity"] = {"sequences": rep.sequences, "flagged": rep.flagged,
+                          "mismatches": len(rep.mismatches), "invalid": rep.invalid}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

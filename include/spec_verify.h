@@ -1,0 +1,174 @@
+/*
+ * spec_verify.h -- batched speculative-sampling verify step on one GPU (sm_103a).
+ *
+ * One call verifies B sequences. Sequence b carries L_b = draft_lens[b] draft tokens
+ * x[b][0..L_b-1] (1 <= L_b <= K), the target logits of positions 0..L_b (one parallel target
+ * pass scores every draft position plus the position after the last draft) and, in stochastic
+ * mode, the draft logits of positions 0..L_b-1.
+ *
+ * What it computes (per sequence, positions in order):
+ *   p_i = softmax(z_t[b][i] / T), q_i = softmax(z_d[b][i] / T) over the whole vocabulary
+ *     (Kangaroo self-speculative decoding guide, "Exit 1", the softmax draft head).
+ *   q'_i = q_i with the probabilities of its bias_k most likely ids (largest draft logit, ties
+ *     to the lower id) scaled by beta and renormalised; q' = q when beta == 1 or bias_k == 0
+ *     ("Speculative Speculative Decoding" summary, "Key claims" and "Method": Saguaro
+ *     sampling down-weights the most likely draft tokens; drafts must be drawn from q').
+ *   Draft i is accepted iff u[b][i] < p_i(x_i) / q'_i(x_i) (Kangaroo guide, section
+ *     "3. Lossless Speculative Verification"; glossary "speculative decoding llm", "Why It
+ *     Produces Identical Outputs"). q'(x) == 0 counts as an infinite ratio when p(x) > 0.
+ *   Verification stops at the first rejection a_b (Kangaroo guide, section 3). The token at
+ *     position a_b is drawn from max(p_a - q'_a, 0) normalised (same passages) or, when every
+ *     draft was accepted (a_b = L_b), from p_{L_b} (bonus token; SSD summary, "Method": the
+ *     outcome is the accepted-prefix length plus the bonus id). A zero residual mass falls
+ *     back to p_a.
+ *   The draw is the inverse CDF over ascending ids: the smallest v with C(v) > u[b][K] * W.
+ *   Greedy mode (LayerSkip guide, "Systems Mechanics", Verification Phase and Prefix
+ *     Acceptance): accept while x_i equals argmax z_t[b][i] (ties to the lower id), then emit
+ *     the target argmax at a_b (including the bonus position when all drafts match).
+ *   Optional top-F ids (SSD summary, "Key claims", capped geometric fan-out across positions):
+ *     for i < L_b, the first fanout[i] ids of draft row i ordered by logit (descending, ties to
+ *     the lower id), the bonus-token guesses a speculation cache would prepare.
+ *
+ * Outputs: out_accept_len[b] = a_b; out_tokens[b] = x[b][0..a_b-1], the sampled token, then -1.
+ * A sequence whose inputs are unusable (L_b outside [1, K], a draft id outside [0, V), a used
+ * uniform outside [0, 1), or a needed logit row holding NaN / +inf or only -inf) gets
+ * out_accept_len[b] = -1 and all tokens -1. A sequence that a device-side bounded wait gave up
+ * on gets -2 (see spec_verify_device_error). The needed rows are target rows 0..a_b and draft
+ * rows 0..min(a_b, L_b - 1), plus every draft row below L_b when top-F ids are requested;
+ * rows after the outcome is fixed are never read, so padding rows may hold anything.
+ *
+ * Memory: every pointer argument of spec_verify / spec_verify_debug / spec_verify_ws is DEVICE
+ * memory owned by the caller; the library keeps no reference after the call returns. Logit
+ * rows are contiguous; row r of sequence b starts at element (b * rows + r) * row_stride with
+ * rows = K + 1 (target) or K (draft). All calls are asynchronous on `stream` (a cudaStream_t,
+ * NULL for the legacy default stream) and do not synchronise, except spec_verify_host and
+ * spec_verify_device_error.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a bad argument
+ * returns SV_ERR_INVALID_ARG and launches nothing. Shapes the kernels do not handle return
+ * SV_ERR_UNSUPPORTED. A failing CUDA runtime call returns SV_ERR_CUDA. Nothing aborts, throws
+ * or traps.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,
+  SV_ERR_UNSUPPORTED = 2,
+  SV_ERR_CUDA = 3,
+  SV_ERR_DEVICE_TIMEOUT = 4
+} sv_status;
+
+typedef enum { SV_DTYPE_F32 = 0, SV_DTYPE_BF16 = 1 } sv_dtype;
+typedef enum { SV_MODE_GREEDY = 0, SV_MODE_STOCHASTIC = 1 } sv_mode;
+
+/* Shapes and options, in host memory. */
+typedef struct {
+  int B;                        /* sequences, >= 0 (0 launches nothing)                       */
+  int K;                        /* maximum draft length, 1..8                                 */
+  int V;                        /* vocabulary size, 1..262144                                 */
+  sv_dtype dtype;               /* element type of both logit tensors                         */
+  long long target_row_stride;  /* elements between consecutive target rows, >= V            */
+  long long draft_row_stride;   /* elements between consecutive draft rows, >= V             */
+  int bias_k;                   /* size of the beta-down-weighted set, 0..8 (0 = none)        */
+  const int* fanout;            /* host array of K entries F_i in 0..8, or NULL = no top-F    */
+  int cluster_hint;             /* CTAs that share one sequence's rows: 0 = chosen by the
+                                   library, else 1, 2, 4, 8 or 16                             */
+} sv_problem;
+
+/*
+ * The verify step (see the top of this file for what it computes).
+ *   target_logits  [B][K+1][target_row_stride] of dtype.
+ *   draft_logits   [B][K][draft_row_stride] of dtype; may be NULL in greedy mode.
+ *   draft_tokens   [B][K] int32; entries at i >= L_b are ignored.
+ *   draft_lens     [B] int32 in 1..K, or NULL (every sequence has K drafts).
+ *   uniforms       [B][K+1] float32 in [0, 1): u[b][i] drives accept test i, u[b][K] the final
+ *                  draw. Ignored (may be NULL) in greedy mode.
+ *   temperature    stochastic mode: finite, in [1e-4, 1e4]. Ignored in greedy mode.
+ *   beta           stochastic mode: in (0, 1]. Ignored in greedy mode.
+ *   mode           SV_MODE_GREEDY or SV_MODE_STOCHASTIC.
+ *   out_accept_len [B] int32; out_tokens [B][K+1] int32.
+ *   out_residual_topF [B][K][max_i F_i] int32, -1 padded; required iff prob->fanout != NULL
+ *                  (stochastic mode only), otherwise must be NULL.
+ *   stream         cudaStream_t.
+ * The library keeps a small zero-initialised workspace per (device, stream), created on the
+ * first call for that pair; make that first call outside stream capture. Calls that may run
+ * at the same time must use different streams.
+ */
+sv_status spec_verify(const sv_problem* prob, const void* target_logits,
+                      const void* draft_logits, const int32_t* draft_tokens,
+                      const int32_t* draft_lens, const float* uniforms, float temperature,
+                      float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                      int32_t* out_residual_topF, void* stream);
+
+/* Bytes of device workspace spec_verify_ws needs (a small constant). */
+size_t spec_verify_workspace_bytes(const sv_problem* prob);
+
+/*
+ * spec_verify with a caller-owned workspace of spec_verify_workspace_bytes() bytes of device
+ * memory, 16-byte aligned and zero-filled before its first use; the kernel leaves it ready for
+ * the next call. Calls that may overlap on the GPU must use different workspaces. Same
+ * arguments and errors as spec_verify otherwise.
+ */
+sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
+                         const void* draft_logits, const int32_t* draft_tokens,
+                         const int32_t* draft_lens, const float* uniforms, float temperature,
+                         float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                         int32_t* out_residual_topF, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * spec_verify plus per-position diagnostics, for parity checks. It reads every row a sequence
+ * has (target rows 0..L_b, draft rows 0..L_b-1), not only the needed ones, and fills
+ *   out_lse_t [B][K+1]  log-normaliser of z_t/T (natural log),
+ *   out_lse_d [B][K]    log-normaliser of z_d/T,
+ *   out_p_x   [B][K]    p_i(x_i),
+ *   out_q_x   [B][K]    q'_i(x_i),
+ * float32, NaN where a row was not read or holds no distribution (stochastic mode only; the
+ * four pointers are device memory and may individually be NULL). Accept lengths and tokens
+ * are those spec_verify returns.
+ */
+sv_status spec_verify_debug(const sv_problem* prob, const void* target_logits,
+                            const void* draft_logits, const int32_t* draft_tokens,
+                            const int32_t* draft_lens, const float* uniforms,
+                            float temperature, float beta, int mode, int32_t* out_accept_len,
+                            int32_t* out_tokens, int32_t* out_residual_topF, float* out_lse_t,
+                            float* out_lse_d, float* out_p_x, float* out_q_x, void* stream);
+
+/*
+ * End-to-end form: every array argument is HOST memory (pinned memory makes the copies
+ * asynchronous; pageable memory works too). The call copies the rows each sequence has to the
+ * device (target rows 0..L_b, draft rows 0..L_b-1; draft_lens must then be a host array or
+ * NULL), runs spec_verify on `stream`, copies the outputs back and synchronises the stream.
+ * The device staging buffers are owned by the library (per device and stream) and grow on
+ * demand. Returns SV_ERR_DEVICE_TIMEOUT if a bounded wait gave up during the call.
+ */
+sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
+                           const void* draft_logits, const int32_t* draft_tokens,
+                           const int32_t* draft_lens, const float* uniforms, float temperature,
+                           float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                           int32_t* out_residual_topF, void* stream);
+
+/*
+ * Synchronises `stream` and reports whether any spec_verify call on it since the last check
+ * had a device-side bounded wait give up (SV_ERR_DEVICE_TIMEOUT; those sequences read -2).
+ * Clears the flag. SV_OK otherwise.
+ */
+sv_status spec_verify_device_error(void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* spec_verify_status_string(sv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,33 @@
+/*
+ * sv_probe.h -- streaming read probe used to calibrate the attainable HBM read bandwidth.
+ *
+ * This is a measurement aid for the roofline of the verify kernel; the pages define no such
+ * operation. It reads `bytes` of device memory once with 128-bit loads spread over every SM
+ * and adds a checksum of what it read into *out_checksum (device memory, one 64-bit word that
+ * the caller zeroes), so the loads cannot be elided.
+ *   buf           device pointer, 16-byte aligned.
+ *   bytes         multiple of 16.
+ *   out_checksum  device pointer to one unsigned 64-bit word.
+ *   stream        cudaStream_t; the call is asynchronous.
+ * Returns SV_ERR_INVALID_ARG for a null or misaligned pointer or a bad size, SV_ERR_CUDA if
+ * the launch fails.
+ */
+#ifndef SV_PROBE_H
+#define SV_PROBE_H
+
+#include <stddef.h>
+
+#include "spec_verify.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+sv_status sv_hbm_read_probe(const void* buf, size_t bytes, unsigned long long* out_checksum,
+                            void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SV_PROBE_H */

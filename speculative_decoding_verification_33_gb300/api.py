@@ -1,0 +1,182 @@
+"""Python API of the verify step over torch tensors.
+
+``spec_verify`` mirrors the C entry point argument for argument (target_logits, draft_logits,
+draft_tokens, draft_lens, uniforms, temperature, beta, mode, out_accept_len, out_tokens,
+out_residual_topF, stream); shapes, dtype and strides are read from the tensors. ``verify``
+allocates the outputs and returns them. ``verify_host`` is the end-to-end form over host
+(numpy or pinned torch) arrays.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import SV_DTYPE_BF16, SV_DTYPE_F32, SV_MODE_GREEDY, SV_MODE_STOCHASTIC
+
+_MODES = {"greedy": SV_MODE_GREEDY, "stochastic": SV_MODE_STOCHASTIC,
+          SV_MODE_GREEDY: SV_MODE_GREEDY, SV_MODE_STOCHASTIC: SV_MODE_STOCHASTIC}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SV_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return SV_DTYPE_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _row_stride(t: torch.Tensor, rows: int, name: str) -> int:
+    if t.dim() != 3 or t.shape[1] != rows:
+        raise ValueError(f"{name} must be [B, {rows}, V], got {tuple(t.shape)}")
+    if t.stride(2) != 1 or (t.shape[0] > 1 and t.stride(0) != rows * t.stride(1)):
+        raise ValueError(f"{name}: rows must be contiguous with a uniform row stride")
+    return t.stride(1)
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, device=True) -> int:
+    if t is None:
+        return 0
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous() and dtype is not None:
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _problem(target_logits, draft_logits, draft_tokens, mode, bias_k, fanout, cluster_hint):
+    B, K = draft_tokens.shape
+    V = target_logits.shape[2]
+    ts = _row_stride(target_logits, K + 1, "target_logits")
+    ds = _row_stride(draft_logits, K, "draft_logits") if draft_logits is not None else V
+    if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    return _lib.make_problem(B, K, V, _dtype_code(target_logits), ts, ds, bias_k, fanout,
+                             cluster_hint)
+
+
+def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
+                draft_tokens: torch.Tensor, draft_lens: Optional[torch.Tensor],
+                uniforms: Optional[torch.Tensor], temperature: float, beta: float, mode,
+                out_accept_len: torch.Tensor, out_tokens: torch.Tensor,
+                out_residual_topF: Optional[torch.Tensor] = None, stream=None, *,
+                bias_k: int = 0, fanout: Optional[Sequence[int]] = None,
+                cluster_hint: int = 0, workspace: Optional[torch.Tensor] = None,
+                debug: Optional[dict] = None) -> None:
+    """Run the verify step on the GPU (see include/spec_verify.h for the semantics).
+
+    ``debug`` may hold float32 CUDA tensors ``lse_t`` [B, K+1], ``lse_d``, ``p_x``, ``q_x``
+    [B, K]; they are filled by the diagnostic entry point. ``workspace`` selects the
+    caller-owned-workspace entry point.
+    """
+    m = _MODES[mode]
+    prob, keep = _problem(target_logits, draft_logits, draft_tokens, m, bias_k, fanout,
+                          cluster_hint)
+    args = [_ptr(target_logits, "target_logits"), _ptr(draft_logits, "draft_logits"),
+            _ptr(draft_tokens, "draft_tokens", torch.int32),
+            _ptr(draft_lens, "draft_lens", torch.int32),
+            _ptr(uniforms, "uniforms", torch.float32), float(temperature), float(beta), m,
+            _ptr(out_accept_len, "out_accept_len", torch.int32),
+            _ptr(out_tokens, "out_tokens", torch.int32),
+            _ptr(out_residual_topF, "out_residual_topF", torch.int32)]
+    s = _stream_handle(stream)
+    if debug is not None:
+        extra = [_ptr(debug.get(k), k, torch.float32) for k in ("lse_t", "lse_d", "p_x", "q_x")]
+        st = _lib.call("spec_verify_debug", prob, *args, *extra, s)
+        where = "spec_verify_debug"
+    elif workspace is not None:
+        st = _lib.call("spec_verify_ws", prob, *args, _ptr(workspace, "workspace"),
+                       workspace.numel() * workspace.element_size(), s)
+        where = "spec_verify_ws"
+    else:
+        st = _lib.call("spec_verify", prob, *args, s)
+        where = "spec_verify"
+    del keep
+    _lib._check(st, where)
+
+
+def verify(target_logits, draft_logits, draft_tokens, draft_lens=None, uniforms=None, *,
+           temperature: float = 1.0, beta: float = 1.0, mode="stochastic", bias_k: int = 0,
+           fanout: Optional[Sequence[int]] = None, cluster_hint: int = 0, stream=None,
+           debug: bool = False):
+    """Allocate the outputs, run ``spec_verify`` and return them as a dict of tensors."""
+    B, K = draft_tokens.shape
+    dev = target_logits.device
+    out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "tokens": torch.empty(B, K + 1, dtype=torch.int32, device=dev)}
+    fmax = max(fanout) if fanout else 0
+    if fanout is not None:
+        out["topf"] = torch.empty(B, K, max(fmax, 1), dtype=torch.int32, device=dev)
+    dbg = None
+    if debug:
+        dbg = {"lse_t": torch.empty(B, K + 1, dtype=torch.float32, device=dev),
+               "lse_d": torch.empty(B, K, dtype=torch.float32, device=dev),
+               "p_x": torch.empty(B, K, dtype=torch.float32, device=dev),
+               "q_x": torch.empty(B, K, dtype=torch.float32, device=dev)}
+        out.update(dbg)
+    spec_verify(target_logits, draft_logits, draft_tokens, draft_lens, uniforms, temperature,
+                beta, mode, out["accept_len"], out["tokens"], out.get("topf"), stream,
+                bias_k=bias_k, fanout=fanout, cluster_hint=cluster_hint, debug=dbg)
+    return out
+
+
+def _host_ptr(a) -> int:
+    if a is None:
+        return 0
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda:
+            raise ValueError("verify_host takes host arrays")
+        return a.data_ptr()
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("host arrays must be C-contiguous")
+    return a.ctypes.data
+
+
+def verify_host(target, draft, draft_tokens, draft_lens, uniforms, out_accept_len, out_tokens,
+                out_topf=None, *, dtype: str, temperature: float = 1.0, beta: float = 1.0,
+                mode="stochastic", bias_k: int = 0, fanout=None, cluster_hint: int = 0,
+                stream=None) -> None:
+    """End-to-end call over host buffers (numpy arrays or CPU torch tensors, pinned or not):
+    copies the rows each sequence has to the GPU, verifies, copies the outputs back and
+    synchronises. bf16 logits are passed as their 16-bit patterns."""
+    B, K = draft_tokens.shape
+    V = target.shape[2]
+    prob, keep = _lib.make_problem(B, K, V, SV_DTYPE_BF16 if dtype == "bf16" else SV_DTYPE_F32,
+                                   V, V, bias_k, fanout, cluster_hint)
+    m = _MODES[mode]
+    st = _lib.call("spec_verify_host", prob, _host_ptr(target), _host_ptr(draft),
+                   _host_ptr(draft_tokens), _host_ptr(draft_lens), _host_ptr(uniforms),
+                   float(temperature), float(beta), m, _host_ptr(out_accept_len),
+                   _host_ptr(out_tokens), _host_ptr(out_topf), _stream_handle(stream))
+    del keep
+    _lib._check(st, "spec_verify_host")
+
+
+def device_error(stream=None) -> int:
+    """Status of the device-side bounded waits on ``stream`` since the last check."""
+    return _lib.load().spec_verify_device_error(_stream_handle(stream))
+
+
+def hbm_read_probe(buf: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _lib._check(_lib.load().sv_hbm_read_probe(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                              out.data_ptr(), _stream_handle(stream)),
+                "sv_hbm_read_probe")
+
+
+def to_device_logits(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """Upload stored logits (uint16 bf16 bit patterns or float32) as a bf16/f32 tensor."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)

@@ -1,0 +1,411 @@
+// C ABI of the verify library: argument checks, per-(device, stream) workspace, the choice of
+// cluster size, and the launch. Everything here is host code; every step of the verify path
+// runs in the kernels of sv_kernel.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <utility>
+#include <vector>
+
+#include "spec_verify.h"
+#include "sv_internal.h"
+#include "sv_probe.h"
+
+namespace {
+
+using sv::Workspace;
+
+constexpr size_t kSliceBudget = 100 * 1024;  // staged row bytes per CTA (two CTAs per SM)
+constexpr size_t kMaxDynSmem = 200 * 1024;
+
+struct StreamRes {
+  Workspace* ws = nullptr;
+  void* stage = nullptr;  // device staging for spec_verify_host
+  size_t stage_bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, cudaStream_t>, StreamRes> g_res;
+std::map<std::tuple<int, int, int, int, size_t>, int> g_occ;  // (dev, dtype, greedy, C, smem)
+std::map<int, int> g_sms;
+
+struct Checked {
+  int greedy = 0;
+  int fmax = 0;
+  int fan[sv::kMaxK] = {0};
+  size_t elt = 4;
+};
+
+bool finite_in(float v, float lo, float hi) { return std::isfinite(v) && v >= lo && v <= hi; }
+
+sv_status check_args(const sv_problem* p, const void* tgt, const void* dft,
+                     const int32_t* tok, const float* uni, float T, float beta, int mode,
+                     const int32_t* out_acc, const int32_t* out_tok, const int32_t* out_topf,
+                     Checked* c) {
+  if (!p) return SV_ERR_INVALID_ARG;
+  if (p->B < 0 || p->K < 1 || p->K > sv::kMaxK || p->V < 1 || p->V > sv::kMaxV)
+    return SV_ERR_INVALID_ARG;
+  if (p->dtype != SV_DTYPE_F32 && p->dtype != SV_DTYPE_BF16) return SV_ERR_INVALID_ARG;
+  if (mode != SV_MODE_GREEDY && mode != SV_MODE_STOCHASTIC) return SV_ERR_INVALID_ARG;
+  if (p->target_row_stride < p->V) return SV_ERR_INVALID_ARG;
+  const int h = p->cluster_hint;
+  if (!(h == 0 || h == 1 || h == 2 || h == 4 || h == 8 || h == 16)) return SV_ERR_INVALID_ARG;
+  c->greedy = mode == SV_MODE_GREEDY;
+  c->elt = p->dtype == SV_DTYPE_BF16 ? 2 : 4;
+  if (!c->greedy) {
+    if (p->draft_row_stride < p->V) return SV_ERR_INVALID_ARG;
+    if (!finite_in(T, 1e-4f, 1e4f)) return SV_ERR_INVALID_ARG;
+    if (!(std::isfinite(beta) && beta > 0.f && beta <= 1.f)) return SV_ERR_INVALID_ARG;
+    if (p->bias_k < 0 || p->bias_k > 8) return SV_ERR_INVALID_ARG;
+  }
+  c->fmax = 0;
+  if (p->fanout) {
+    if (c->greedy) return SV_ERR_INVALID_ARG;
+    for (int i = 0; i < p->K; ++i) {
+      const int f = p->fanout[i];
+      if (f < 0 || f > 8) return SV_ERR_INVALID_ARG;
+      c->fan[i] = f;
+      c->fmax = std::max(c->fmax, f);
+    }
+  }
+  if (p->B == 0) return SV_OK;
+  if (!tgt || !tok || !out_acc || !out_tok) return SV_ERR_INVALID_ARG;
+  if (!c->greedy && (!dft || !uni)) return SV_ERR_INVALID_ARG;
+  if (c->fmax > 0 && !out_topf) return SV_ERR_INVALID_ARG;
+  if (!p->fanout && out_topf) return SV_ERR_INVALID_ARG;
+  return SV_OK;
+}
+
+int sm_count(int dev) {
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+  g_sms[dev] = n;
+  return n;
+}
+
+int pow2_at_least(long long v) {
+  int c = 1;
+  while (c < sv::kMaxCluster && c < v) c <<= 1;
+  return c;
+}
+
+// Cluster size: enough CTAs per sequence for the staged rows to fit shared memory, and for
+// small batches enough to spread one batch over the whole GPU.
+int choose_cluster(const sv_problem* p, int greedy, size_t elt, int sms) {
+  if (p->cluster_hint) return p->cluster_hint;
+  const size_t rows = greedy ? 1 : 2;
+  int c_mem = 1;
+  while (c_mem < sv::kMaxCluster) {
+    const size_t slice = (static_cast<size_t>(p->V) + c_mem - 1) / c_mem;
+    if (rows * elt * ((slice + 7) / 8 * 8) <= kSliceBudget) break;
+    c_mem <<= 1;
+  }
+  const long long want = p->B > 0 ? (2LL * sms + p->B - 1) / p->B : 1;
+  int c_par = pow2_at_least(want);
+  int c_vocab = 1;  // at least 512 elements per CTA
+  while (c_vocab * 2 <= sv::kMaxCluster && static_cast<long long>(c_vocab) * 2 * 512 <= p->V)
+    c_vocab <<= 1;
+  return std::max(c_mem, std::min(c_par, c_vocab));
+}
+
+StreamRes* resources(int dev, cudaStream_t s, sv_status* st) {
+  StreamRes& r = g_res[{dev, s}];
+  if (!r.ws) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone) {
+      *st = SV_ERR_UNSUPPORTED;  // the workspace must exist before capture
+      return nullptr;
+    }
+    void* w = nullptr;
+    if (cudaMalloc(&w, sizeof(Workspace)) != cudaSuccess ||
+        cudaMemset(w, 0, sizeof(Workspace)) != cudaSuccess) {
+      if (w) cudaFree(w);
+      *st = SV_ERR_CUDA;
+      return nullptr;
+    }
+    r.ws = static_cast<Workspace*>(w);
+  }
+  *st = SV_OK;
+  return &r;
+}
+
+sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32_t* tok,
+              const int32_t* lens, const float* uni, float T, float beta, int mode,
+              int32_t* out_acc, int32_t* out_tok, int32_t* out_topf, float* lse_t,
+              float* lse_d, float* px, float* qx, int debug_all, Workspace* ws_user,
+              cudaStream_t stream) {
+  Checked c;
+  sv_status st = check_args(p, tgt, dft, tok, uni, T, beta, mode, out_acc, out_tok, out_topf, &c);
+  if (st != SV_OK || p->B == 0) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+
+  sv::Launch L;
+  memset(&L, 0, sizeof(L));
+  sv::Params& P = L.p;
+  P.tgt = tgt;
+  P.dft = c.greedy ? nullptr : dft;
+  P.tokens = tok;
+  P.lens = lens;
+  P.uni = c.greedy ? nullptr : uni;
+  P.out_acc = out_acc;
+  P.out_tok = out_tok;
+  P.out_topf = c.fmax > 0 ? out_topf : nullptr;
+  P.dbg_lse_t = lse_t;
+  P.dbg_lse_d = lse_d;
+  P.dbg_px = px;
+  P.dbg_qx = qx;
+  P.t_stride = p->target_row_stride;
+  P.d_stride = c.greedy ? 0 : p->draft_row_stride;
+  P.B = p->B;
+  P.K = p->K;
+  P.V = p->V;
+  P.temperature = c.greedy ? 1.f : T;
+  P.c = c.greedy ? 1.f : static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  P.beta = c.greedy ? 1.f : beta;
+  P.bias_k = (c.greedy || beta >= 1.f) ? 0 : p->bias_k;
+  P.fmax = c.fmax;
+  for (int i = 0; i < sv::kMaxK; ++i) P.fan[i] = c.fan[i];
+  P.top8 = !c.greedy && (P.bias_k > 0 || c.fmax > 0);
+  P.debug_all = debug_all;
+
+  const uintptr_t a_t = reinterpret_cast<uintptr_t>(tgt);
+  const uintptr_t a_d = reinterpret_cast<uintptr_t>(dft);
+  bool aligned = (a_t % 16 == 0) && ((p->target_row_stride * c.elt) % 16 == 0);
+  if (!c.greedy) aligned = aligned && (a_d % 16 == 0) && ((p->draft_row_stride * c.elt) % 16 == 0);
+  P.use_bulk = aligned ? 1 : 0;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int sms = sm_count(dev);
+  if (sms <= 0) return SV_ERR_CUDA;
+  const int C = choose_cluster(p, c.greedy, c.elt, sms);
+  const int slice = static_cast<int>(((static_cast<long long>(p->V) + C - 1) / C + 7) / 8 * 8);
+  P.slice = slice;
+  L.dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
+  L.greedy = c.greedy;
+  L.cluster = C;
+  L.smem = sv::smem_bytes(L.dtype, L.greedy, slice);
+  if (L.smem > kMaxDynSmem) return SV_ERR_UNSUPPORTED;
+  auto key = std::make_tuple(dev, L.dtype, L.greedy, C, L.smem);
+  auto it = g_occ.find(key);
+  int occ = 0;
+  if (it != g_occ.end()) {
+    occ = it->second;
+  } else {
+    occ = sv::max_active_clusters(L.dtype, L.greedy, C, L.smem);
+    g_occ[key] = occ;
+  }
+  if (occ <= 0) return SV_ERR_UNSUPPORTED;
+  P.n_clusters = std::min(p->B, occ);
+
+  if (ws_user) {
+    P.ws = ws_user;
+  } else {
+    StreamRes* r = resources(dev, stream, &st);
+    if (!r) return st;
+    P.ws = r->ws;
+  }
+  return sv::launch(L, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+sv_status spec_verify(const sv_problem* prob, const void* target_logits,
+                      const void* draft_logits, const int32_t* draft_tokens,
+                      const int32_t* draft_lens, const float* uniforms, float temperature,
+                      float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                      int32_t* out_residual_topF, void* stream) {
+  return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
+             temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr,
+             nullptr, nullptr, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t spec_verify_workspace_bytes(const sv_problem* prob) {
+  (void)prob;
+  return sizeof(Workspace);
+}
+
+sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
+                         const void* draft_logits, const int32_t* draft_tokens,
+                         const int32_t* draft_lens, const float* uniforms, float temperature,
+                         float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                         int32_t* out_residual_topF, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (!workspace || workspace_bytes < sizeof(Workspace) ||
+      reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+    return SV_ERR_INVALID_ARG;
+  return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
+             temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr,
+             nullptr, nullptr, nullptr, 0, static_cast<Workspace*>(workspace),
+             static_cast<cudaStream_t>(stream));
+}
+
+sv_status spec_verify_debug(const sv_problem* prob, const void* target_logits,
+                            const void* draft_logits, const int32_t* draft_tokens,
+                            const int32_t* draft_lens, const float* uniforms,
+                            float temperature, float beta, int mode, int32_t* out_accept_len,
+                            int32_t* out_tokens, int32_t* out_residual_topF, float* out_lse_t,
+                            float* out_lse_d, float* out_p_x, float* out_q_x, void* stream) {
+  return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
+             temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, out_lse_t,
+             out_lse_d, out_p_x, out_q_x, 1, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
+                           const void* draft_logits, const int32_t* draft_tokens,
+                           const int32_t* draft_lens, const float* uniforms, float temperature,
+                           float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                           int32_t* out_residual_topF, void* stream) {
+  Checked c;
+  sv_status st = check_args(prob, target_logits, draft_logits, draft_tokens, uniforms,
+                            temperature, beta, mode, out_accept_len, out_tokens,
+                            out_residual_topF, &c);
+  if (st != SV_OK || prob->B == 0) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int B = prob->B, K = prob->K;
+  const size_t elt = c.elt;
+  const size_t t_row = static_cast<size_t>(prob->target_row_stride) * elt;
+  const size_t d_row = c.greedy ? 0 : static_cast<size_t>(prob->draft_row_stride) * elt;
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  const size_t b_t = up(static_cast<size_t>(B) * (K + 1) * t_row);
+  const size_t b_d = up(static_cast<size_t>(B) * K * d_row);
+  const size_t b_tok = up(static_cast<size_t>(B) * K * 4);
+  const size_t b_len = draft_lens ? up(static_cast<size_t>(B) * 4) : 0;
+  const size_t b_uni = c.greedy ? 0 : up(static_cast<size_t>(B) * (K + 1) * 4);
+  const size_t b_acc = up(static_cast<size_t>(B) * 4);
+  const size_t b_otok = up(static_cast<size_t>(B) * (K + 1) * 4);
+  const size_t b_topf = up(static_cast<size_t>(B) * K * c.fmax * 4);
+  const size_t total = b_t + b_d + b_tok + b_len + b_uni + b_acc + b_otok + b_topf;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  char* base = nullptr;
+  Workspace* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    StreamRes* r = resources(dev, s, &st);
+    if (!r) return st;
+    if (r->stage_bytes < total) {
+      if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+      if (r->stage) cudaFree(r->stage);
+      r->stage = nullptr;
+      r->stage_bytes = 0;
+      if (cudaMalloc(&r->stage, total) != cudaSuccess) return SV_ERR_CUDA;
+      r->stage_bytes = total;
+    }
+    base = static_cast<char*>(r->stage);
+    ws = r->ws;
+  }
+  char* d_t = base;
+  char* d_d = d_t + b_t;
+  int32_t* d_tok = reinterpret_cast<int32_t*>(d_d + b_d);
+  int32_t* d_len = draft_lens ? reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_tok) + b_tok) : nullptr;
+  float* d_uni = c.greedy ? nullptr
+                          : reinterpret_cast<float*>(reinterpret_cast<char*>(d_tok) + b_tok + b_len);
+  int32_t* d_acc = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_tok) + b_tok + b_len + b_uni);
+  int32_t* d_otok = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_acc) + b_acc);
+  int32_t* d_topf = c.fmax > 0 ? reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_otok) + b_otok) : nullptr;
+
+  // rows each sequence has: target 0..L_b, draft 0..L_b-1 (one contiguous block each)
+  long long need = 0;
+  for (int b = 0; b < B; ++b) need += draft_lens ? std::clamp(draft_lens[b], 0, K) : K;
+  const bool per_seq = draft_lens && (2 * need + B) * 4 < 3LL * B * (2 * K + 1);
+  auto cp = [&](void* dst, const void* src, size_t n) {
+    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  };
+  bool ok = true;
+  if (per_seq) {
+    for (int b = 0; b < B && ok; ++b) {
+      const int Lb = std::clamp(draft_lens[b], 0, K);
+      const size_t ot = static_cast<size_t>(b) * (K + 1) * t_row;
+      ok = cp(d_t + ot, static_cast<const char*>(target_logits) + ot, (Lb + 1) * t_row);
+      if (ok && !c.greedy) {
+        const size_t od = static_cast<size_t>(b) * K * d_row;
+        ok = cp(d_d + od, static_cast<const char*>(draft_logits) + od, Lb * d_row);
+      }
+    }
+  } else {
+    ok = cp(d_t, target_logits, static_cast<size_t>(B) * (K + 1) * t_row);
+    if (ok && !c.greedy) ok = cp(d_d, draft_logits, static_cast<size_t>(B) * K * d_row);
+  }
+  ok = ok && cp(d_tok, draft_tokens, static_cast<size_t>(B) * K * 4);
+  if (draft_lens) ok = ok && cp(d_len, draft_lens, static_cast<size_t>(B) * 4);
+  if (!c.greedy) ok = ok && cp(d_uni, uniforms, static_cast<size_t>(B) * (K + 1) * 4);
+  if (!ok) return SV_ERR_CUDA;
+  st = run(prob, d_t, c.greedy ? nullptr : d_d, d_tok, d_len, d_uni, temperature, beta, mode,
+           d_acc, d_otok, d_topf, nullptr, nullptr, nullptr, nullptr, 0, ws, s);
+  if (st != SV_OK) return st;
+  if (cudaMemcpyAsync(out_accept_len, d_acc, static_cast<size_t>(B) * 4,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(out_tokens, d_otok, static_cast<size_t>(B) * (K + 1) * 4,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (c.fmax > 0 && cudaMemcpyAsync(out_residual_topF, d_topf,
+                                    static_cast<size_t>(B) * K * c.fmax * 4,
+                                    cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  unsigned int err = 0;
+  if (cudaMemcpyAsync(&err, &ws->error, sizeof(err), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+  if (err) {
+    cudaMemsetAsync(&ws->error, 0, sizeof(err), s);
+    cudaStreamSynchronize(s);
+    return SV_ERR_DEVICE_TIMEOUT;
+  }
+  return SV_OK;
+}
+
+sv_status spec_verify_device_error(void* stream) {
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  Workspace* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_res.find({dev, s});
+    if (it != g_res.end()) ws = it->second.ws;
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+  if (!ws) return SV_OK;
+  unsigned int err = 0;
+  if (cudaMemcpy(&err, &ws->error, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (!err) return SV_OK;
+  if (cudaMemset(&ws->error, 0, sizeof(err)) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_ERR_DEVICE_TIMEOUT;
+}
+
+const char* spec_verify_status_string(sv_status status) {
+  switch (status) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARG: return "invalid argument";
+    case SV_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case SV_ERR_CUDA: return "CUDA runtime error";
+    case SV_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait gave up";
+  }
+  return "unknown status";
+}
+
+sv_status sv_hbm_read_probe(const void* buf, size_t bytes, unsigned long long* out_checksum,
+                            void* stream) {
+  if (!buf || !out_checksum || bytes == 0 || bytes % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(buf) % 16 != 0)
+    return SV_ERR_INVALID_ARG;
+  return sv::launch_probe(buf, bytes, out_checksum, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
+}
+
+}  // extern "C"

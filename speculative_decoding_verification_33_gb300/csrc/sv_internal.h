@@ -1,0 +1,72 @@
+// Internal interface between the host API (sv_api.cu) and the verify kernels (sv_kernel.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;     // threads per CTA
+constexpr int kMaxCluster = 16;   // CTAs that share one sequence's rows
+constexpr int kMaxK = 8;          // maximum draft length
+constexpr int kMaxV = 262144;     // maximum vocabulary
+constexpr int kQScale = 44;       // residual weights are summed as integers of 2^-44
+
+// Device workspace shared by the clusters of one launch. The kernel returns it to all-zero
+// counters when the last cluster leaves, so stream-ordered launches can reuse it.
+struct Workspace {
+  unsigned int next;    // dynamic sequence queue
+  unsigned int done;    // clusters that have finished
+  unsigned int error;   // bit 0: a bounded wait gave up
+  unsigned int pad[61];
+};
+static_assert(sizeof(Workspace) == 256, "workspace layout");
+
+struct Params {
+  const void* tgt;
+  const void* dft;
+  const int32_t* tokens;
+  const int32_t* lens;
+  const float* uni;
+  int32_t* out_acc;
+  int32_t* out_tok;
+  int32_t* out_topf;
+  float* dbg_lse_t;
+  float* dbg_lse_d;
+  float* dbg_px;
+  float* dbg_qx;
+  long long t_stride;
+  long long d_stride;
+  int B, K, V;
+  float temperature;
+  float c;        // log2(e) / T, rounded to float
+  float beta;
+  int bias_k;     // 0 when beta == 1
+  int fmax;       // columns of out_topf (0 = no top-F output)
+  int fan[kMaxK];
+  int top8;       // draft rows need their top-8 ids
+  int debug_all;  // read every row a sequence has and fill the diagnostics
+  int slice;      // elements of a row owned by one CTA (multiple of 8)
+  int use_bulk;   // rows and strides are 16-byte aligned: stage rows with bulk async copies
+  int n_clusters;
+  Workspace* ws;
+};
+
+struct Launch {
+  Params p;
+  int dtype;       // 0 f32, 1 bf16
+  int greedy;
+  int cluster;     // CTAs per cluster
+  size_t smem;     // dynamic shared memory per CTA
+};
+
+// Rows of shared memory a CTA stages per position (1 greedy, 2 stochastic).
+size_t smem_bytes(int dtype, int greedy, int slice);
+// Largest number of co-resident clusters for this configuration (0 on error).
+int max_active_clusters(int dtype, int greedy, int cluster, size_t smem);
+cudaError_t launch(const Launch& L, cudaStream_t stream);
+
+cudaError_t launch_probe(const void* buf, size_t bytes, unsigned long long* out,
+                         cudaStream_t stream);
+
+}  // namespace sv

@@ -243,7 +243,7 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    from speculative_decoding_verification_33_gb300 import api, build
+    from speculative_decoding_verification_33_gb300 import _lib, api, build
     from speculative_decoding_verification_33_gb300 import workloads as W
 
     rank, world, local = dist_env()
@@ -263,6 +263,10 @@ def run_ours(args):
     acc = torch.empty(w.B, dtype=torch.int32, device="cuda")
     otok = torch.empty(w.B, w.K + 1, dtype=torch.int32, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    prob, _keep = _lib.make_problem(w.B, w.K, w.V, _lib.SV_DTYPE_BF16, w.V, w.V,
+                                    cluster_hint=args.cluster)
+    plan_c, plan_n, plan_smem = _lib.plan(prob, _lib.SV_MODE_STOCHASTIC)
 
     def step():
         api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, acc, otok, None,
@@ -334,7 +338,8 @@ def run_ours(args):
                        "temperature": w.temperature, "draft_lens": "uniform 1..8",
                        "verified_tokens_per_rank": toks_local,
                        "l2": "flushed before each step (256 MiB write, outside the events)",
-                       "cluster_hint": args.cluster,
+                       "cluster_hint": args.cluster, "ctas_per_cluster": plan_c,
+                       "clusters": plan_n, "smem_per_cta": plan_smem,
                        "wall_ms_per_step_incl_flush": wall / args.steps * 1e3},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,

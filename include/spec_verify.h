@@ -109,6 +109,15 @@ sv_status spec_verify(const sv_problem* prob, const void* target_logits,
                       float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
                       int32_t* out_residual_topF, void* stream);
 
+/*
+ * The launch spec_verify would make for this problem on the current device: CTAs that share
+ * one sequence (*cluster), clusters launched (*clusters) and dynamic shared memory per CTA
+ * (*smem_bytes). Host-side query; any output pointer may be NULL. Returns the same argument
+ * and shape errors as spec_verify (temperature and beta are not checked here).
+ */
+sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* clusters,
+                           size_t* smem_bytes);
+
 /* Bytes of device workspace spec_verify_ws needs (a small constant). */
 size_t spec_verify_workspace_bytes(const sv_problem* prob);
 

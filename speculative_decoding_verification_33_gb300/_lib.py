@@ -18,6 +18,7 @@ SV_MODE_GREEDY, SV_MODE_STOCHASTIC = 0, 1
 # every entry point the header declares (checked by the tests against include/*.h)
 EXPORTS = ("spec_verify", "spec_verify_workspace_bytes", "spec_verify_ws", "spec_verify_debug",
            "spec_verify_host", "spec_verify_device_error", "spec_verify_status_string",
+           "spec_verify_plan",
            "sv_hbm_read_probe")
 
 
@@ -63,6 +64,7 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.spec_verify_status_string.argtypes = [_I]
         lib.spec_verify_status_string.restype = ctypes.c_char_p
         lib.sv_hbm_read_probe.argtypes = [_P, _SZ, _P, _P]
+        lib.spec_verify_plan.argtypes = [_PROB, _I, _P, _P, _P]
         for name in EXPORTS:
             if name not in ("spec_verify_workspace_bytes", "spec_verify_status_string"):
                 getattr(lib, name).restype = _I
@@ -91,6 +93,14 @@ def make_problem(B: int, K: int, V: int, dtype: int, target_row_stride: int,
                      ctypes.cast(fan, ctypes.POINTER(ctypes.c_int)) if fan is not None else None,
                      int(cluster_hint))
     return prob, fan
+
+
+def plan(prob: SvProblem, mode: int):
+    """(CTAs per cluster, clusters, dynamic shared memory bytes) spec_verify would launch."""
+    c, n, sm = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    _check(load().spec_verify_plan(ctypes.byref(prob), int(mode), ctypes.addressof(c),
+                                   ctypes.addressof(n), ctypes.addressof(sm)), "spec_verify_plan")
+    return c.value, n.value, sm.value
 
 
 def call(name: str, prob: SvProblem, *args) -> int:

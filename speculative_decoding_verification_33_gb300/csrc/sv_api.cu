@@ -137,6 +137,32 @@ StreamRes* resources(int dev, cudaStream_t s, sv_status* st) {
   return &r;
 }
 
+// Cluster size, slice, shared memory and the number of clusters to launch (g_mu held).
+sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L) {
+  const int sms = sm_count(dev);
+  if (sms <= 0) return SV_ERR_CUDA;
+  const int C = choose_cluster(p, c.greedy, c.elt, sms);
+  const int slice = static_cast<int>(((static_cast<long long>(p->V) + C - 1) / C + 7) / 8 * 8);
+  L->p.slice = slice;
+  L->dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
+  L->greedy = c.greedy;
+  L->cluster = C;
+  L->smem = sv::smem_bytes(L->dtype, L->greedy, slice);
+  if (L->smem > kMaxDynSmem) return SV_ERR_UNSUPPORTED;
+  auto key = std::make_tuple(dev, L->dtype, L->greedy, C, L->smem);
+  auto it = g_occ.find(key);
+  int occ = 0;
+  if (it != g_occ.end()) {
+    occ = it->second;
+  } else {
+    occ = sv::max_active_clusters(L->dtype, L->greedy, C, L->smem);
+    g_occ[key] = occ;
+  }
+  if (occ <= 0) return SV_ERR_UNSUPPORTED;
+  L->p.n_clusters = std::max(1, std::min(p->B, occ));
+  return SV_OK;
+}
+
 sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32_t* tok,
               const int32_t* lens, const float* uni, float T, float beta, int mode,
               int32_t* out_acc, int32_t* out_tok, int32_t* out_topf, float* lse_t,
@@ -184,27 +210,8 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   P.use_bulk = aligned ? 1 : 0;
 
   std::lock_guard<std::mutex> lock(g_mu);
-  const int sms = sm_count(dev);
-  if (sms <= 0) return SV_ERR_CUDA;
-  const int C = choose_cluster(p, c.greedy, c.elt, sms);
-  const int slice = static_cast<int>(((static_cast<long long>(p->V) + C - 1) / C + 7) / 8 * 8);
-  P.slice = slice;
-  L.dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
-  L.greedy = c.greedy;
-  L.cluster = C;
-  L.smem = sv::smem_bytes(L.dtype, L.greedy, slice);
-  if (L.smem > kMaxDynSmem) return SV_ERR_UNSUPPORTED;
-  auto key = std::make_tuple(dev, L.dtype, L.greedy, C, L.smem);
-  auto it = g_occ.find(key);
-  int occ = 0;
-  if (it != g_occ.end()) {
-    occ = it->second;
-  } else {
-    occ = sv::max_active_clusters(L.dtype, L.greedy, C, L.smem);
-    g_occ[key] = occ;
-  }
-  if (occ <= 0) return SV_ERR_UNSUPPORTED;
-  P.n_clusters = std::min(p->B, occ);
+  st = plan(p, c, dev, &L);
+  if (st != SV_OK) return st;
 
   if (ws_user) {
     P.ws = ws_user;
@@ -228,6 +235,29 @@ sv_status spec_verify(const sv_problem* prob, const void* target_logits,
   return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
              temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr,
              nullptr, nullptr, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* clusters,
+                           size_t* smem_bytes) {
+  Checked c;
+  const int one = 1;
+  const float u = 0.5f;
+  sv_status st = check_args(prob, &one, &one, &one, &u, 1.f, 1.f, mode, &one, &one,
+                            prob && prob->fanout ? &one : nullptr, &c);
+  if (st != SV_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  sv::Launch L;
+  memset(&L, 0, sizeof(L));
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    st = plan(prob, c, dev, &L);
+  }
+  if (st != SV_OK) return st;
+  if (cluster) *cluster = L.cluster;
+  if (clusters) *clusters = L.p.n_clusters;
+  if (smem_bytes) *smem_bytes = L.smem;
+  return SV_OK;
 }
 
 size_t spec_verify_workspace_bytes(const sv_problem* prob) {

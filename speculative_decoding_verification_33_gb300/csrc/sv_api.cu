@@ -21,7 +21,6 @@ namespace {
 
 using sv::Workspace;
 
-constexpr size_t kSliceBudget = 100 * 1024;  // staged row bytes per CTA (two CTAs per SM)
 constexpr size_t kMaxDynSmem = 200 * 1024;
 
 struct StreamRes {
@@ -32,11 +31,12 @@ struct StreamRes {
 
 std::mutex g_mu;
 std::map<std::pair<int, cudaStream_t>, StreamRes> g_res;
-std::map<std::tuple<int, int, int, int, size_t>, int> g_occ;  // (dev, dtype, greedy, C, smem)
+std::map<std::tuple<int, int, int, int, int, size_t>, int> g_occ;  // dev,dtype,greedy,top8,C,smem
 std::map<int, int> g_sms;
 
 struct Checked {
   int greedy = 0;
+  int beta_lt1 = 0;
   int fmax = 0;
   int fan[sv::kMaxK] = {0};
   size_t elt = 4;
@@ -63,6 +63,7 @@ sv_status check_args(const sv_problem* p, const void* tgt, const void* dft,
     if (!finite_in(T, 1e-4f, 1e4f)) return SV_ERR_INVALID_ARG;
     if (!(std::isfinite(beta) && beta > 0.f && beta <= 1.f)) return SV_ERR_INVALID_ARG;
     if (p->bias_k < 0 || p->bias_k > 8) return SV_ERR_INVALID_ARG;
+    c->beta_lt1 = beta < 1.f;
   }
   c->fmax = 0;
   if (p->fanout) {
@@ -97,19 +98,16 @@ int pow2_at_least(long long v) {
   return c;
 }
 
-// Cluster size: enough CTAs per sequence for the staged rows to fit shared memory, and for
-// small batches enough to spread one batch over the whole GPU.
+// Cluster size: enough CTAs per sequence that one CTA's slice stays within kMaxSlice, and for
+// batches too small to fill every CTA slot, more CTAs per sequence.
 int choose_cluster(const sv_problem* p, int greedy, size_t elt, int sms) {
+  (void)greedy;
+  (void)elt;
   if (p->cluster_hint) return p->cluster_hint;
-  const size_t rows = greedy ? 1 : 2;
   int c_mem = 1;
-  while (c_mem < sv::kMaxCluster) {
-    const size_t slice = (static_cast<size_t>(p->V) + c_mem - 1) / c_mem;
-    if (rows * elt * ((slice + 7) / 8 * 8) <= kSliceBudget) break;
-    c_mem <<= 1;
-  }
-  const long long want = p->B > 0 ? (2LL * sms + p->B - 1) / p->B : 1;
-  int c_par = pow2_at_least(want);
+  while (c_mem < sv::kMaxCluster && (p->V + c_mem - 1) / c_mem > sv::kMaxSlice) c_mem <<= 1;
+  const long long want = p->B > 0 ? (3LL * sms + p->B - 1) / p->B : 1;
+  const int c_par = pow2_at_least(want);
   int c_vocab = 1;  // at least 512 elements per CTA
   while (c_vocab * 2 <= sv::kMaxCluster && static_cast<long long>(c_vocab) * 2 * 512 <= p->V)
     c_vocab <<= 1;
@@ -148,14 +146,16 @@ sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L) {
   L->greedy = c.greedy;
   L->cluster = C;
   L->smem = sv::smem_bytes(L->dtype, L->greedy, slice);
-  if (L->smem > kMaxDynSmem) return SV_ERR_UNSUPPORTED;
-  auto key = std::make_tuple(dev, L->dtype, L->greedy, C, L->smem);
+  if (slice > sv::kMaxSlice || L->smem > kMaxDynSmem) return SV_ERR_UNSUPPORTED;
+  const int top8 = !c.greedy && ((p->bias_k > 0 && c.beta_lt1) || c.fmax > 0);
+  L->p.top8 = top8;
+  auto key = std::make_tuple(dev, L->dtype, L->greedy, top8, C, L->smem);
   auto it = g_occ.find(key);
   int occ = 0;
   if (it != g_occ.end()) {
     occ = it->second;
   } else {
-    occ = sv::max_active_clusters(L->dtype, L->greedy, C, L->smem);
+    occ = sv::max_active_clusters(L->dtype, L->greedy, top8, C, L->smem);
     g_occ[key] = occ;
   }
   if (occ <= 0) return SV_ERR_UNSUPPORTED;
@@ -200,7 +200,6 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   P.bias_k = (c.greedy || beta >= 1.f) ? 0 : p->bias_k;
   P.fmax = c.fmax;
   for (int i = 0; i < sv::kMaxK; ++i) P.fan[i] = c.fan[i];
-  P.top8 = !c.greedy && (P.bias_k > 0 || c.fmax > 0);
   P.debug_all = debug_all;
 
   const uintptr_t a_t = reinterpret_cast<uintptr_t>(tgt);
@@ -242,7 +241,8 @@ sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* 
   Checked c;
   const int one = 1;
   const float u = 0.5f;
-  sv_status st = check_args(prob, &one, &one, &one, &u, 1.f, 1.f, mode, &one, &one,
+  const float beta = prob && prob->bias_k > 0 ? 0.5f : 1.f;  // a bias set implies beta < 1
+  sv_status st = check_args(prob, &one, &one, &one, &u, 1.f, beta, mode, &one, &one,
                             prob && prob->fanout ? &one : nullptr, &c);
   if (st != SV_OK) return st;
   int dev = 0;

@@ -11,6 +11,9 @@ constexpr int kMaxCluster = 16;   // CTAs that share one sequence's rows
 constexpr int kMaxK = 8;          // maximum draft length
 constexpr int kMaxV = 262144;     // maximum vocabulary
 constexpr int kQScale = 44;       // residual weights are summed as integers of 2^-44
+constexpr int NS = 3;             // stages of the per-CTA row ring
+constexpr int kStageRowBytes = 8192;  // bytes of one row in one stage
+constexpr int kMaxSlice = 65536;  // elements of a row one CTA owns (bounds the draw's buffer)
 
 // Device workspace shared by the clusters of one launch. The kernel returns it to all-zero
 // counters when the last cluster leaves, so stream-ordered launches can reuse it.
@@ -60,10 +63,10 @@ struct Launch {
   size_t smem;     // dynamic shared memory per CTA
 };
 
-// Rows of shared memory a CTA stages per position (1 greedy, 2 stochastic).
+// Dynamic shared memory per CTA: the stage ring plus the draw's per-vector masses.
 size_t smem_bytes(int dtype, int greedy, int slice);
 // Largest number of co-resident clusters for this configuration (0 on error).
-int max_active_clusters(int dtype, int greedy, int cluster, size_t smem);
+int max_active_clusters(int dtype, int greedy, int top8, int cluster, size_t smem);
 cudaError_t launch(const Launch& L, cudaStream_t stream);
 
 cudaError_t launch_probe(const void* buf, size_t bytes, unsigned long long* out,

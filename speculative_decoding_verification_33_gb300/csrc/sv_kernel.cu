@@ -2,21 +2,30 @@
 //
 // One thread-block cluster of C CTAs owns one sequence at a time and walks its draft
 // positions in order (Kangaroo guide, section "3. Lossless Speculative Verification":
-// verification terminates at the first rejection). Each CTA owns a contiguous slice of the
-// vocabulary; per position it stages its slice of the target row (and draft row) into its
-// own shared memory with one bulk async copy per row, reduces it (max, sum of exponentials,
-// argmax, top-8), and the CTAs exchange their partials through distributed shared memory.
-// Every CTA then combines the C partials in the same order and reaches the same accept /
-// reject decision. After a rejection (or when every draft is accepted) the residual or bonus
-// draw runs on the rows that are still resident in the cluster's shared memory, so no row is
-// read from HBM twice and rows after the outcome are never read at all.
+// verification terminates at the first rejection), so the rows after the outcome is fixed are
+// not needed. Each CTA owns a contiguous slice of the vocabulary.
 //
-// The residual / bonus mass is summed as 64-bit integers of 2^-44 so the cross-CTA prefix
-// used by the inverse-CDF draw is exact and order independent.
+// Row path. Per CTA, a ring of NS shared-memory stages is filled with bulk async copies
+// (cp.async.bulk, completion on an mbarrier) by one producer thread that runs ahead of the
+// consumers: through the rest of the current position, speculatively into the next position
+// of the sequence, and into the next sequence of the queue. Every thread folds its elements
+// into a running maximum and a running sum of 2^(z c - m c) (single pass), so at the end of
+// a position each CTA holds its slice's (max, sum) for the target and draft rows.
 //
-// Bounded waits: each wait for a bulk copy gives up after ~2 s, raises the workspace error
-// word, and the cluster marks the sequence -2 and leaves. There is no other spin-wait; all
-// cross-CTA ordering uses the hardware cluster barrier.
+// Decision. The CTAs exchange their partials through distributed shared memory; every CTA
+// combines the C partials in the same order and reaches the same accept / reject decision.
+// The producer learns the decision and stops fetching rows the outcome no longer needs.
+//
+// Draw. After a rejection (or when every draft is accepted) each CTA re-reads its slice of the
+// two rows at the decided position (they were streamed microseconds earlier and sit in L2)
+// with 128-bit loads, turns them into residual (or bonus) weights, keeps one partial mass per
+// 8-element vector in shared memory, and sums them as 64-bit integers of 2^-44, so the
+// cross-CTA and block prefix sums of the inverse CDF are exact and order independent. The CTA
+// whose range holds the draw scans its vector masses and walks the one vector that holds it.
+//
+// Bounded waits: each mbarrier wait gives up after ~2 s, raises the workspace error word, and
+// the cluster marks the sequence -2 and leaves. There is no other spin-wait; cross-CTA ordering
+// uses the hardware cluster barrier.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -33,10 +42,18 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 constexpr unsigned XF_ABORT = 1u;
+constexpr int ROW_T = 1, ROW_D = 2;
+constexpr int NC = NT;            // consumer threads (warps 0..7)
+constexpr int NTOT = NT + 32;     // plus one producer warp
+constexpr uint32_t kConsumerBar = 1;
+
+// Barrier among the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void cbar() { named_sync(kConsumerBar, NC); }
+__device__ __forceinline__ bool cbar_or(bool p) { return named_sync_or(kConsumerBar, NC, p); }
 
 // Partial results one CTA publishes to every CTA of its cluster (7 chunks of 16 bytes).
 struct __align__(16) Xchg {
-  float m_t, s_t, m_d, s_d;     // chunk 0: slice maxima (raw logits) and sum 2^((z-m)c)
+  float m_t, s_t, m_d, s_d;     // chunk 0: slice maxima (raw logits) and sums 2^((z-m)c)
   int arg;                      // chunk 1: greedy, lowest index of the slice maximum
   int next_seq;                 //          rank 0, first exchange of a sequence
   unsigned flags;
@@ -47,19 +64,40 @@ struct __align__(16) Xchg {
 };
 static_assert(sizeof(Xchg) == 112, "exchange record layout");
 
-struct CtaState {
-  // sequence header
-  int L, hdr_ok, next;
+struct Hdr {
+  int L, ok;
   int x[kMaxK];
   float u[kMaxK + 1];
-  float zx_t, zx_d;
-  // reduction scratch (one slot per kind, so consecutive reductions need one barrier each)
+};
+
+struct StageDesc {
+  int seq, pos, k, rows;  // rows: ROW_T | ROW_D; pos < 0 marks a chunk of the draw pass
+};
+
+// What the consumers tell the producer warp, published under a sequence lock (consumer thread
+// 0 writes, producer lane 0 reads): the position in the cluster's sequence order (epoch), the
+// current sequence and its decided position, and the next sequence once it is known.
+struct Pub {
+  int ep;      // epoch of the current sequence (0, 1, 2, ...)
+  int seq;     // current sequence
+  int stop;    // -1 undecided, -2 nothing more needed, else the decided position
+  int next;    // next sequence of the queue, -1 unknown
+  int done;    // the consumers have left the sequence loop
+  int cons;    // stages the consumers have taken (valid once done)
+};
+
+struct CtaState {
+  Hdr hdr[2];        // current and next sequence header (cp.async targets)
+  int cur;           // hdr[cur] is the current sequence
+  int n_hdr_wait;    // consumer thread 0 has a header copy in flight
+  unsigned ver;      // sequence lock of `pub` (odd while it is being written)
+  Pub pub;
+  // reduction scratch (one slot per kind)
   float rmax[2][NW];
   float rsum[2][NW];
   int rarg[NW];
   unsigned long long ru[NW];
   unsigned long long wtop[NW][8];
-  // record being published
   Xchg rec;
   // cluster-combined values of the current position (written by warp 0)
   float M_t, M_d, S_t, S_d, N;
@@ -90,6 +128,18 @@ struct Elt<float> {
     z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
     z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
   }
+  static __device__ __forceinline__ void ldg8(const float* g, float (&z)[8]) {
+    const uint4 a = ldg_nc_v4(g), b = ldg_nc_v4(g + 4);
+    z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y);
+    z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
+    z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y);
+    z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
+  }
+  static __device__ __forceinline__ float vmax8(const float* s, int g, float (&z)[8]) {
+    load8(s, g, z);
+    return max_nan(max_nan(max_nan(z[0], z[1]), max_nan(z[2], z[3])),
+                   max_nan(max_nan(z[4], z[5]), max_nan(z[6], z[7])));
+  }
 };
 
 template <>
@@ -98,14 +148,37 @@ struct Elt<uint16_t> {
     return __uint_as_float(static_cast<uint32_t>(v) << 16);
   }
   static __device__ __forceinline__ uint16_t neg_inf() { return 0xFF80u; }
-  static __device__ __forceinline__ void load8(const uint16_t* s, int g, float (&z)[8]) {
-    const uint4 v = reinterpret_cast<const uint4*>(s)[g];
+  static __device__ __forceinline__ void unpack(const uint4 v, float (&z)[8]) {
     z[0] = __uint_as_float(v.x << 16); z[1] = __uint_as_float(v.x & 0xFFFF0000u);
     z[2] = __uint_as_float(v.y << 16); z[3] = __uint_as_float(v.y & 0xFFFF0000u);
     z[4] = __uint_as_float(v.z << 16); z[5] = __uint_as_float(v.z & 0xFFFF0000u);
     z[6] = __uint_as_float(v.w << 16); z[7] = __uint_as_float(v.w & 0xFFFF0000u);
   }
+  static __device__ __forceinline__ void load8(const uint16_t* s, int g, float (&z)[8]) {
+    unpack(reinterpret_cast<const uint4*>(s)[g], z);
+  }
+  static __device__ __forceinline__ void ldg8(const uint16_t* g, float (&z)[8]) {
+    unpack(ldg_nc_v4(g), z);
+  }
+  static __device__ __forceinline__ float vmax8(const uint16_t* s, int g, float (&z)[8]) {
+    const uint4 v = reinterpret_cast<const uint4*>(s)[g];
+    const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(v.x, v.y), max_nan_bf16x2(v.z, v.w));
+    unpack(v, z);
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
 };
+
+// Eight elements of a global row slice starting at slice offset e0 (elements at or past nv
+// read as -inf); vector loads when the row is 16-byte aligned and the vector is whole.
+template <typename T>
+__device__ __forceinline__ void row8(const T* g, int e0, int nv, bool aligned, float (&z)[8]) {
+  if (aligned && e0 + 8 <= nv) {
+    Elt<T>::ldg8(g + e0, z);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) z[k] = (e0 + k < nv) ? Elt<T>::val(g[e0 + k]) : -INFINITY;
+  }
+}
 
 // ------------------------------------------------------------------------------------------
 // small helpers
@@ -185,7 +258,7 @@ __device__ __forceinline__ float2 block_max2(float a, float b, CtaState& S) {
   a = warp_max_nan(a);
   b = warp_max_nan(b);
   if (lane == 0) { S.rmax[0][warp] = a; S.rmax[1][warp] = b; }
-  __syncthreads();
+  cbar();
   float ra = S.rmax[0][0], rb = S.rmax[1][0];
 #pragma unroll
   for (int w = 1; w < NW; ++w) { ra = max_nan(ra, S.rmax[0][w]); rb = max_nan(rb, S.rmax[1][w]); }
@@ -197,8 +270,7 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, CtaState& S) {
   a = warp_sum(a);
   b = warp_sum(b);
   if (lane == 0) { S.rsum[0][warp] = a; S.rsum[1][warp] = b; }
-  __syncthreads();
-  // pairwise over the warps keeps the rounding error at log2(NW) steps
+  cbar();
   float va[NW], vb[NW];
 #pragma unroll
   for (int w = 0; w < NW; ++w) { va[w] = S.rsum[0][w]; vb[w] = S.rsum[1][w]; }
@@ -213,7 +285,7 @@ __device__ __forceinline__ int block_min_int(int v, CtaState& S) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_min_int(v);
   if (lane == 0) S.rarg[warp] = v;
-  __syncthreads();
+  cbar();
   int r = S.rarg[0];
 #pragma unroll
   for (int w = 1; w < NW; ++w) r = min(r, S.rarg[w]);
@@ -224,11 +296,11 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_sum_u64(v);
   if (lane == 0) S.ru[warp] = v;
-  __syncthreads();
+  cbar();
   unsigned long long r = 0;
 #pragma unroll
   for (int w = 0; w < NW; ++w) r += S.ru[w];
-  __syncthreads();
+  cbar();
   return r;
 }
 
@@ -243,93 +315,11 @@ __device__ __forceinline__ unsigned long long block_exclusive_u64(unsigned long 
     if (lane >= o) inc += y;
   }
   if (lane == 31) S.ru[warp] = inc;
-  __syncthreads();
+  cbar();
   unsigned long long base = 0;
   for (int w = 0; w < warp; ++w) base += S.ru[w];
-  __syncthreads();
+  cbar();
   return base + inc - v;
-}
-
-// ------------------------------------------------------------------------------------------
-// row passes over the staged slice (vectors of 8 elements, vector g covers elements 8g..8g+7)
-// ------------------------------------------------------------------------------------------
-template <typename T>
-__device__ __forceinline__ float slice_max(const T* row, int nvec) {
-  if constexpr (sizeof(T) == 2) {
-    uint32_t acc = 0xFF80FF80u;  // (-inf, -inf)
-    for (int g = threadIdx.x; g < nvec; g += NT) {
-      const uint4 v = reinterpret_cast<const uint4*>(row)[g];
-      acc = max_nan_bf16x2(acc, max_nan_bf16x2(max_nan_bf16x2(v.x, v.y), max_nan_bf16x2(v.z, v.w)));
-    }
-    return max_nan(__uint_as_float(acc << 16), __uint_as_float(acc & 0xFFFF0000u));
-  } else {
-    float acc = -INFINITY;
-    for (int g = threadIdx.x; g < nvec; g += NT) {
-      float z[8];
-      Elt<T>::load8(row, g, z);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) acc = max_nan(acc, z[k]);
-    }
-    return acc;
-  }
-}
-
-// Sum of 2^(z c - mc) over the slice; mc is m*c rounded to float.
-template <typename T>
-__device__ __forceinline__ float slice_sum(const T* row, int nvec, float c, float mc) {
-  float s0 = 0.f, s1 = 0.f;
-  for (int g = threadIdx.x; g < nvec; g += NT) {
-    float z[8];
-    Elt<T>::load8(row, g, z);
-#pragma unroll
-    for (int k = 0; k < 8; k += 2) {
-      s0 += ex2_fast(fmaf(z[k], c, -mc));
-      s1 += ex2_fast(fmaf(z[k + 1], c, -mc));
-    }
-  }
-  return s0 + s1;
-}
-
-// Lowest slice-local index whose value equals m (INT_MAX if none).
-template <typename T>
-__device__ __forceinline__ int slice_first_index(const T* row, int nvec, float m) {
-  for (int g = threadIdx.x; g < nvec; g += NT) {
-    float z[8];
-    Elt<T>::load8(row, g, z);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (z[k] == m) return 8 * g + k;
-  }
-  return 0x7FFFFFFF;
-}
-
-template <typename T>
-__device__ __forceinline__ void slice_top8(const T* row, int nv, int nvec, int v0,
-                                           unsigned long long (&keys)[8]) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) keys[j] = 0ull;
-  float thr = -INFINITY;
-  for (int g = threadIdx.x; g < nvec; g += NT) {
-    float z[8];
-    Elt<T>::load8(row, g, z);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = 8 * g + k;
-      if (e < nv && z[k] >= thr) {
-        unsigned long long key = make_key(z[k], static_cast<uint32_t>(v0 + e));
-        if (key > keys[7]) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const unsigned long long hi = key > keys[j] ? key : keys[j];
-            const unsigned long long lo = key > keys[j] ? keys[j] : key;
-            keys[j] = hi;
-            key = lo;
-          }
-          if (keys[7]) thr = key_value(keys[7]);
-        }
-      }
-    }
-  }
 }
 
 // Merge every thread's descending top-8 into the CTA's top-8 (written to S.rec.top8).
@@ -345,7 +335,7 @@ __device__ __forceinline__ void block_top8(unsigned long long (&keys)[8], CtaSta
     }
     if (lane == 0) S.wtop[warp][r] = m;
   }
-  __syncthreads();
+  cbar();
   if (warp == 0) {
     static_assert(NW * 8 == 64, "two candidates per lane");
     unsigned long long a0 = S.wtop[lane >> 3][lane & 7];
@@ -363,45 +353,325 @@ __device__ __forceinline__ void block_top8(unsigned long long (&keys)[8], CtaSta
   }
 }
 
-// Publish chunks [c0, c0 + nc) of S.rec into slot `rank` of buffer `par` of every CTA of the
-// cluster, then wait for every CTA to have done the same.
-__device__ __forceinline__ void exchange(CtaState& S, Xchg (*X)[kMaxCluster], uint32_t par,
-                                         uint32_t rank, uint32_t C, int c0, int nc) {
+// Publish chunks [c0, c0 + nc) of S.rec into slot `rank` of buffer `round & 1` of every CTA
+// of the cluster with st.async, and wait until every CTA's chunks have landed here (counted as
+// transaction bytes on this CTA's exchange barrier). A buffer is rewritten two rounds later,
+// which a CTA can only reach after every peer has pushed the round in between, i.e. after
+// every peer has read this round. Returns false if the wait gave up.
+__device__ __forceinline__ bool exchange(CtaState& S, Xchg (*X)[kMaxCluster], uint64_t* xbar,
+                                         uint32_t& round, uint32_t rank, uint32_t C, int c0,
+                                         int nc) {
   const int tid = threadIdx.x;
+  const uint32_t p = round & 1u, ph = (round >> 1) & 1u;
+  ++round;
+  if (tid == 0) mbar_arrive_expect_tx(&xbar[p], C * static_cast<uint32_t>(nc) * 16u);
   if (tid < static_cast<int>(C) * nc) {
     const uint32_t peer = tid / nc;
     const int ch = c0 + tid % nc;
-    const uint32_t dst = map_to_rank(smem_u32(&X[par][rank]) + 16u * ch, peer);
-    st_cluster_v4(dst, reinterpret_cast<const uint4*>(&S.rec)[ch]);
+    const uint32_t dst = map_to_rank(smem_u32(&X[p][rank]) + 16u * ch, peer);
+    const uint32_t bar = map_to_rank(smem_u32(&xbar[p]), peer);
+    st_async_v4(dst, reinterpret_cast<const uint4*>(&S.rec)[ch], bar);
   }
-  cluster_sync();
+  return mbar_wait_cluster_bounded(&xbar[p], ph, kWaitBudget);
 }
 
-// Stage this CTA's slice of the requested rows into shared memory. Returns true if the bulk
-// copy did not complete within the wait budget (same answer in every thread of the CTA).
-template <typename T>
-__device__ __forceinline__ bool stage_rows(T* rt, T* rd, const T* gt, const T* gd, bool ld_t,
-                                           bool ld_d, int nv, int nb, int nvec, uint64_t* bar,
-                                           uint32_t& tpar) {
-  const int tid = threadIdx.x;
-  if (nb > 0 && tid == 0) {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    const uint32_t bytes = static_cast<uint32_t>(nb * sizeof(T));
-    mbar_arrive_expect_tx(bar, bytes * ((ld_t ? 1u : 0u) + (ld_d ? 1u : 0u)));
-    if (ld_t) bulk_g2s(rt, gt, bytes, bar);
-    if (ld_d) bulk_g2s(rd, gd, bytes, bar);
+// ------------------------------------------------------------------------------------------
+// consumer -> producer publication (sequence lock)
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void pub_write(CtaState& S, const Pub& v) {  // consumer thread 0
+  volatile unsigned* ver = &S.ver;
+  *ver = *ver + 1u;
+  __threadfence_block();
+  volatile Pub* d = &S.pub;
+  d->ep = v.ep;
+  d->seq = v.seq;
+  d->stop = v.stop;
+  d->next = v.next;
+  d->done = v.done;
+  d->cons = v.cons;
+  __threadfence_block();
+  *ver = *ver + 1u;
+}
+
+__device__ __forceinline__ Pub pub_local(const CtaState& S) {  // consumer thread 0's own copy
+  const volatile Pub* d = &S.pub;
+  Pub v;
+  v.ep = d->ep;
+  v.seq = d->seq;
+  v.stop = d->stop;
+  v.next = d->next;
+  v.done = d->done;
+  v.cons = d->cons;
+  return v;
+}
+
+__device__ __forceinline__ Pub pub_read(CtaState& S) {  // producer lane
+  Pub v;
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const unsigned a = *reinterpret_cast<volatile unsigned*>(&S.ver);
+    __threadfence_block();
+    v = pub_local(S);
+    __threadfence_block();
+    const unsigned b = *reinterpret_cast<volatile unsigned*>(&S.ver);
+    if (a == b && !(a & 1u)) return v;
   }
-  // elements the bulk copy does not cover, then -inf padding to a whole vector of 8
-  for (int e = nb + tid; e < 8 * nvec; e += NT) {
-    if (ld_t) rt[e] = e < nv ? gt[e] : Elt<T>::neg_inf();
-    if (ld_d) rd[e] = e < nv ? gd[e] : Elt<T>::neg_inf();
+  v.done = 1;  // the writer never finished: stop producing
+  return v;
+}
+
+// ------------------------------------------------------------------------------------------
+// the stage ring: the producer warp fills stages with bulk async copies, consumers drain them
+// ------------------------------------------------------------------------------------------
+template <typename T, bool GREEDY>
+struct Ring {
+  static constexpr int kRows = GREEDY ? 1 : 2;
+  static constexpr int CH = kStageRowBytes / static_cast<int>(sizeof(T));  // elements / chunk
+  unsigned char* base;
+  uint64_t* full;
+  uint64_t* empty;
+  StageDesc* desc;
+  int nchunk;  // chunks per row of this CTA's slice
+  int nv;      // elements of this CTA's slice
+  int v0;      // first element of the slice
+
+  __device__ __forceinline__ T* row(int s, int r) const {
+    return reinterpret_cast<T*>(base + (static_cast<size_t>(s) * kRows + r) * kStageRowBytes);
   }
-  bool late = false;
+  __device__ __forceinline__ int chunk_len(int k) const { return min(CH, nv - k * CH); }
+};
+
+__device__ __forceinline__ const void* row_ptr(const Params& P, bool draft, int seq, int pos,
+                                               size_t elt) {
+  const char* base = static_cast<const char*>(draft ? P.dft : P.tgt);
+  const long long rows = draft ? P.K : P.K + 1;
+  const long long stride = draft ? P.d_stride : P.t_stride;
+  return base + ((static_cast<long long>(seq) * rows + pos) * stride) * static_cast<long long>(elt);
+}
+
+__device__ __forceinline__ int load_len(const Params& P, int seq) {
+  if (seq < 0 || seq >= P.B) return -1;
+  const int L = P.lens ? P.lens[seq] : P.K;
+  return (L >= 1 && L <= P.K) ? L : -1;
+}
+
+// One chunk of (seq, pos) into stage s; `tag` is the position recorded in the descriptor
+// (negative for the draw pass).
+template <typename T, bool GREEDY>
+__device__ void issue_chunk(const Params& P, const Ring<T, GREEDY>& R, int s, int seq, int pos,
+                            int tag, int k, int rows) {
+  const int e0 = k * R.CH;
+  const int n = R.chunk_len(k);
+  StageDesc d;
+  d.seq = seq;
+  d.pos = tag;
+  d.k = k;
+  d.rows = rows;
+  R.desc[s] = d;
+  if (!P.use_bulk) {
+    mbar_arrive(&R.full[s]);  // the consumers copy this chunk themselves
+    return;
+  }
+  constexpr int kPer16 = 16 / static_cast<int>(sizeof(T));
+  const int nb = (n / kPer16) * kPer16;
+  const int npad = (n + 7) & ~7;
+  uint32_t bytes = 0;
+  for (int r = 0; r < Ring<T, GREEDY>::kRows; ++r) {
+    if (!(rows & (1 << r))) continue;
+    const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + e0;
+    T* dst = R.row(s, r);
+    for (int e = nb; e < npad; ++e) dst[e] = e < n ? src[e] : Elt<T>::neg_inf();
+    bytes += static_cast<uint32_t>(nb * sizeof(T));
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive_expect_tx(&R.full[s], bytes);
   if (nb > 0) {
-    late = !mbar_wait_bounded(bar, tpar, kWaitBudget);
-    tpar ^= 1u;
+    for (int r = 0; r < Ring<T, GREEDY>::kRows; ++r) {
+      if (!(rows & (1 << r))) continue;
+      const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + e0;
+      bulk_g2s(R.row(s, r), src, static_cast<uint32_t>(nb * sizeof(T)), &R.full[s]);
+    }
   }
-  return __syncthreads_or(late) != 0;
+}
+
+// The producer warp's lane 0. It walks the cluster's sequence order: the positions of the
+// current sequence speculatively (all rows up to the bonus row), and once the consumers publish
+// the decision, the draw pass over the decided position, then the rows the diagnostics or the
+// top-F output still need, then the next sequence. It never runs past an undecided stochastic
+// sequence, so the ring always holds chunks in the order the consumers take them.
+template <typename T, bool GREEDY>
+__device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R, int first_seq) {
+  enum { STATS = 0, DRAW = 1, POST = 2 };
+  int q_ep = 0, q_seq = first_seq, q_L = load_len(P, first_seq);
+  int q_ph = STATS, q_pos = 0, q_k = 0;
+  int issued = 0;
+  long long idle0 = clock64();
+  Pub pub;
+  while (true) {
+    pub = pub_read(S);
+    if (pub.done) break;
+    if (clock64() - idle0 > kWaitBudget) {
+      atomicOr(&P.ws->error, 1u);
+      break;
+    }
+    if (R.nchunk == 0) {
+      sleep_ns(256);
+      idle0 = clock64();
+      continue;
+    }
+    if (q_ep < pub.ep) {  // the consumers are past this sequence (it needed no chunks)
+      q_ep = pub.ep;
+      q_seq = pub.seq;
+      q_L = load_len(P, q_seq);
+      q_ph = STATS;
+      q_pos = 0;
+      q_k = 0;
+    }
+    int rows = 0;
+    bool exhausted = q_seq >= P.B;
+    if (!exhausted && q_ep == pub.ep) {
+      const int stop = pub.stop;
+      if (stop == -2) {
+        exhausted = true;
+      } else {
+        if (stop >= 0 && q_ph == STATS) {  // the decision has landed
+          q_ph = GREEDY ? POST : DRAW;
+          q_pos = GREEDY ? stop + 1 : stop;
+          q_k = 0;
+        }
+        if (q_ph == STATS) {
+          if (q_pos <= q_L) rows = (!GREEDY && q_pos < q_L) ? (ROW_T | ROW_D) : ROW_T;
+        } else if (q_ph == DRAW) {
+          rows = (q_pos < q_L) ? (ROW_T | ROW_D) : ROW_T;
+        } else {
+          if (q_pos <= q_L) {
+            rows = P.debug_all ? ROW_T : 0;
+            if (!GREEDY && q_pos < q_L && (P.fmax > 0 || P.debug_all)) rows |= ROW_D;
+          }
+          exhausted = rows == 0;
+        }
+      }
+    } else if (!exhausted && q_ph == STATS && q_pos <= q_L) {  // the next sequence, early
+      rows = (!GREEDY && q_pos < q_L) ? (ROW_T | ROW_D) : ROW_T;
+    }
+    if (exhausted && q_ep == pub.ep && pub.next >= 0 && q_seq < P.B) {
+      ++q_ep;
+      q_seq = pub.next;
+      q_L = load_len(P, q_seq);
+      q_ph = STATS;
+      q_pos = 0;
+      q_k = 0;
+      continue;
+    }
+    if (exhausted || rows == 0) {
+      sleep_ns(32);
+      continue;
+    }
+    const int s = issued % NS;
+    if (issued >= NS && !mbar_test(&R.empty[s], static_cast<uint32_t>((issued / NS) - 1) & 1u)) {
+      continue;  // the oldest stage is still being read
+    }
+    issue_chunk<T, GREEDY>(P, R, s, q_seq, q_pos, q_ph == DRAW ? -1 - q_pos : q_pos, q_k, rows);
+    ++issued;
+    idle0 = clock64();
+    if (++q_k >= R.nchunk) {
+      q_k = 0;
+      if (q_ph == DRAW) q_ph = POST;
+      ++q_pos;
+    }
+  }
+  // wait out the copies still in flight into stages nobody will read
+  pub = pub_read(S);
+  for (int j = pub.done ? pub.cons : issued; j < issued; ++j)
+    mbar_wait_bounded(&R.full[j % NS], static_cast<uint32_t>(j / NS) & 1u, kWaitBudget);
+}
+
+__device__ __forceinline__ void release_stage(uint64_t* empty, int s, int& cons) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
+  ++cons;
+}
+
+// Wait for the stage holding chunk k of (seq, tag), handing back stale speculative chunks on
+// the way. Returns the stage, or -1 once a wait has given up (`late`).
+template <typename T, bool GREEDY>
+__device__ int acquire(const Ring<T, GREEDY>& R, int seq, int tag, int k, int& cons,
+                       bool& late) {
+  while (!late) {
+    const int s = cons % NS;
+    const uint32_t ph = static_cast<uint32_t>(cons / NS) & 1u;
+    if (!mbar_wait_bounded(&R.full[s], ph, kWaitBudget)) {
+      late = true;
+      break;
+    }
+    const StageDesc d = R.desc[s];
+    if (d.seq == seq && d.pos == tag && d.k == k) return s;
+    release_stage(R.empty, s, cons);
+  }
+  return -1;
+}
+
+// Rows that are not 16-byte aligned are not fetched by the producer: every consumer copies its
+// share of the chunk, then the consumers synchronise. All consumers call this, `late` or not.
+template <typename T, bool GREEDY>
+__device__ int fill_unaligned(const Params& P, const Ring<T, GREEDY>& R, int s, int seq,
+                              int pos, int k, bool& late) {
+  if (s >= 0) {
+    const StageDesc d = R.desc[s];
+    const int n = R.chunk_len(k), npad = (n + 7) & ~7;
+    for (int r = 0; r < Ring<T, GREEDY>::kRows; ++r) {
+      if (!(d.rows & (1 << r))) continue;
+      const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + k * R.CH;
+      T* dst = R.row(s, r);
+      for (int e = threadIdx.x; e < npad; e += NC) dst[e] = e < n ? src[e] : Elt<T>::neg_inf();
+    }
+  }
+  late = cbar_or(late || s < 0);
+  return late ? -1 : s;
+}
+
+// ------------------------------------------------------------------------------------------
+// per-thread running statistics of one row
+// ------------------------------------------------------------------------------------------
+struct RowAcc {
+  float m, mc, s0, s1;  // running max, its product with c, and two partial sums of 2^(zc-mc)
+  __device__ __forceinline__ void init() {
+    m = -INFINITY;
+    mc = -INFINITY;
+    s0 = s1 = 0.f;
+  }
+  __device__ __forceinline__ void add8(float vm, const float (&z)[8], float c) {
+    const float mn = max_nan(m, vm);
+    if (mn != m) {  // a new maximum (or NaN): rescale what was summed so far
+      const float mcn = __fmul_rn(mn, c);
+      const float f = exp2f(mc - mcn);
+      s0 *= f;
+      s1 *= f;
+      m = mn;
+      mc = mcn;
+    }
+    if (m > -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        s0 += ex2_fast(fmaf(z[k], c, -mc));
+        s1 += ex2_fast(fmaf(z[k + 1], c, -mc));
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ void top8_insert(unsigned long long (&keys)[8], float& thr, float z,
+                                            uint32_t id) {
+  if (!(z >= thr)) return;
+  unsigned long long key = make_key(z, id);
+  if (key <= keys[7]) return;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const unsigned long long hi = key > keys[j] ? key : keys[j];
+    const unsigned long long lo = key > keys[j] ? keys[j] : key;
+    keys[j] = hi;
+    key = lo;
+  }
+  if (keys[7]) thr = key_value(keys[7]);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -409,39 +679,33 @@ __device__ __forceinline__ bool stage_rows(T* rt, T* rd, const T* gt, const T* g
 // ------------------------------------------------------------------------------------------
 struct WeightConsts {
   float c, mc_t, mc_d, r_t, r_d, r_dS;
-  int nloc;          // S ids that fall in this CTA's slice
-  int loc[8];        // their slice-local indices
+  int nloc;     // ids of the bias set that fall in this CTA's slice
+  int loc[8];   // their slice-local indices
 };
 
-// Weights of vector g: bonus -> 2^(z_t c - mc_t); residual -> max(p - q', 0) with p and q'
-// rebuilt from the staged rows. Returns the sequential sum of the 8 weights.
-template <typename T, bool BONUS>
-__device__ __forceinline__ float weights8(const T* rt, const T* rd, int g,
-                                          const WeightConsts& K, float (&w)[8]) {
-  float zt[8];
-  Elt<T>::load8(rt, g, zt);
+// Weights of the 8 elements at slice offset e0: bonus -> 2^(z_t c - mc_t); residual ->
+// max(p - q', 0) with p and q' rebuilt from the logits. Returns their sequential sum.
+template <bool BONUS>
+__device__ __forceinline__ float weights8(const float (&zt)[8], const float (&zd)[8], int e0,
+                                          const WeightConsts& W, float (&w)[8]) {
   if constexpr (BONUS) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) w[k] = ex2_fast(fmaf(zt[k], K.c, -K.mc_t));
+    for (int k = 0; k < 8; ++k) w[k] = ex2_fast(fmaf(zt[k], W.c, -W.mc_t));
   } else {
-    float zd[8];
-    Elt<T>::load8(rd, g, zd);
     float rdk[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) rdk[k] = K.r_d;
-    for (int j = 0; j < K.nloc; ++j) {
-      const int e = K.loc[j] - 8 * g;
-      if (e >= 0 && e < 8) {
+    for (int k = 0; k < 8; ++k) rdk[k] = W.r_d;
+    for (int j = 0; j < W.nloc; ++j) {
+      const int e = W.loc[j] - e0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k == e) rdk[k] = K.r_dS;
-      }
+      for (int k = 0; k < 8; ++k)
+        if (k == e) rdk[k] = W.r_dS;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const float et = ex2_fast(fmaf(zt[k], K.c, -K.mc_t));
-      const float ed = ex2_fast(fmaf(zd[k], K.c, -K.mc_d));
-      w[k] = fmaxf(fmaf(et, K.r_t, -__fmul_rn(ed, rdk[k])), 0.f);
+      const float et = ex2_fast(fmaf(zt[k], W.c, -W.mc_t));
+      const float ed = ex2_fast(fmaf(zd[k], W.c, -W.mc_d));
+      w[k] = fmaxf(fmaf(et, W.r_t, -__fmul_rn(ed, rdk[k])), 0.f);
     }
   }
   float s = w[0];
@@ -450,19 +714,26 @@ __device__ __forceinline__ float weights8(const T* rt, const T* rd, int g,
   return s;
 }
 
-// The cluster draws the token at position `a` of sequence `seq` and the CTA that owns it
-// writes out_tok. All threads of all CTAs of the cluster call this together.
-template <typename T, bool BONUS>
+// The cluster draws the token at position `a` of sequence `seq`. The rows come back through
+// the ring (the producer fetches them again right after the decision; they are still in L2);
+// each consumer keeps one mass per 8-element vector in `vmass`. The CTA whose range holds the
+// draw writes out_tok. All consumers of all CTAs of the cluster call this together.
+template <typename T, bool GREEDY, bool BONUS>
 __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
-                           uint32_t& xpar, uint32_t rank, uint32_t C, const T* rt,
-                           const T* rd, int nvec, int v0, int nv, int seq, int a) {
+                           uint64_t* xbar, uint32_t& xround, uint32_t rank, uint32_t C,
+                           const Ring<T, GREEDY>& R, int seq, int a, float* vmass, int& cons,
+                           bool& late) {
   const int tid = threadIdx.x;
+  const int v0 = R.v0, nv = R.nv;
+  const int nvec_all = (nv + 7) >> 3;
+  const bool aligned = P.use_bulk != 0;
+  const T* gt = static_cast<const T*>(row_ptr(P, false, seq, a, sizeof(T))) + v0;
+  const T* gd = BONUS ? gt : static_cast<const T*>(row_ptr(P, true, seq, a, sizeof(T))) + v0;
   WeightConsts W;
   W.c = P.c;
   W.mc_t = __fmul_rn(S.M_t, P.c);
   const float err_t = fmaf(S.M_t, P.c, -W.mc_t);
-  // p(v) = 2^(z c - mc_t) * 2^(-err_t) / S_t
-  W.r_t = BONUS ? 1.f : fmaf(-err_t, kLn2, 1.f) / S.S_t;
+  W.r_t = BONUS ? 1.f : fmaf(-err_t, kLn2, 1.f) / S.S_t;  // p(v) = 2^(z c - mc_t) * r_t
   W.mc_d = __fmul_rn(S.M_d, P.c);
   const float err_d = fmaf(S.M_d, P.c, -W.mc_d);
   W.r_d = BONUS ? 0.f : fmaf(-err_d, kLn2, 1.f) / (S.S_d * S.N);
@@ -472,56 +743,97 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
     const int e = S.S_ids[j] - v0;
     if (e >= 0 && e < nv) W.loc[W.nloc++] = e;
   }
-  unsigned long long Wc = 0, Wtot = 0;
+  unsigned long long acc = 0;
+  for (int k = 0; k < R.nchunk; ++k) {
+    int s = acquire<T, GREEDY>(R, seq, -1 - a, k, cons, late);
+    if (!P.use_bulk) s = fill_unaligned<T, GREEDY>(P, R, s, seq, a, k, late);
+    if (s < 0) break;
+    const int n = R.chunk_len(k), nvec = (n + 7) >> 3;
+    const T* rt = R.row(s, 0);
+    const T* rd = R.row(s, GREEDY ? 0 : 1);
+    for (int g = tid; g < nvec; g += NC) {
+      float zt[8], zd[8], w[8];
+      Elt<T>::load8(rt, g, zt);
+      if (!BONUS) Elt<T>::load8(rd, g, zd);
+      const int e0 = k * R.CH + 8 * g;
+      const float sm = weights8<BONUS>(zt, BONUS ? zt : zd, e0, W, w);
+      vmass[e0 >> 3] = sm;
+      acc += qfix(sm);
+    }
+    release_stage(R.empty, s, cons);
+  }
+  late = cbar_or(late);
+  unsigned long long Wtot = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    unsigned long long acc = 0;
-    float w[8];
-    for (int g = tid; g < nvec; g += NT) acc += qfix(weights8<T, BONUS>(rt, rd, g, W, w));
-    Wc = block_sum_u64(acc, S);
-    if (tid == 0) S.rec.w = Wc;
-    __syncthreads();
-    exchange(S, X, xpar, rank, C, 6, 1);
-    const Xchg* XX = X[xpar];
-    xpar ^= 1u;
-    // every thread forms the same prefix over the CTAs
+    if (attempt == 1) {  // zero residual mass: draw from p at this position instead
+      W.r_d = 0.f;
+      W.r_dS = 0.f;
+      W.mc_d = INFINITY;  // the draft term becomes 2^-inf = 0 exactly
+      acc = 0;
+      for (int g = tid; g < nvec_all; g += NC) {
+        float zt[8], w[8];
+        row8<T>(gt, 8 * g, nv, aligned, zt);
+        const float sm = weights8<BONUS>(zt, zt, 8 * g, W, w);
+        vmass[g] = sm;
+        acc += qfix(sm);
+      }
+    }
+    const unsigned long long Wc = block_sum_u64(acc, S);
+    if (tid == 0) {
+      S.rec.w = Wc;
+      S.rec.flags = late ? XF_ABORT : 0u;
+    }
+    cbar();
+    if (!exchange(S, X, xbar, xround, rank, C, 6, 1)) late = true;
+    const Xchg* XX = X[(xround - 1) & 1u];
     Wtot = 0;
     for (uint32_t c = 0; c < C; ++c) Wtot += XX[c].w;
     if (tid == 0) {
-      const unsigned long long t = scale_floor(S.u[P.K], Wtot);
+      const unsigned long long t = scale_floor(S.hdr[S.cur].u[P.K], Wtot);
       unsigned long long pre = 0;
       int cs = -1;
       for (uint32_t c = 0; c < C; ++c) {
-        if (cs < 0 && t < pre + XX[c].w) { cs = static_cast<int>(c); S.t_loc = t - pre; }
+        if (cs < 0 && t < pre + XX[c].w) {
+          cs = static_cast<int>(c);
+          S.t_loc = t - pre;
+        }
         pre += XX[c].w;
       }
       S.cstar = cs;
       S.token = -1;
     }
-    __syncthreads();
-    if (Wtot > 0 || BONUS) break;
-    // zero residual mass: draw from p at this position instead
-    W.r_d = 0.f;
-    W.r_dS = 0.f;
+    late = cbar_or(late);
+    if (late || Wtot > 0 || BONUS) break;
   }
-  if (S.cstar == static_cast<int>(rank)) {
-    // contiguous chunks of vectors per thread, so the CDF follows ascending ids
-    const int lo = static_cast<int>((static_cast<long long>(tid) * nvec) / NT);
-    const int hi = static_cast<int>((static_cast<long long>(tid + 1) * nvec) / NT);
-    float w[8];
+  if (!late && S.cstar == static_cast<int>(rank)) {
+    // contiguous runs of vectors per thread, so the prefix follows ascending ids
+    const int lo = static_cast<int>((static_cast<long long>(tid) * nvec_all) / NC);
+    const int hi = static_cast<int>((static_cast<long long>(tid + 1) * nvec_all) / NC);
     unsigned long long csum = 0;
-    for (int g = lo; g < hi; ++g) csum += qfix(weights8<T, BONUS>(rt, rd, g, W, w));
+    for (int g = lo; g < hi; ++g) csum += qfix(vmass[g]);
     unsigned long long pre = block_exclusive_u64(csum, S);
     const unsigned long long tl = S.t_loc;
     if (pre <= tl && tl < pre + csum) {
       for (int g = lo; g < hi; ++g) {
-        const unsigned long long q = qfix(weights8<T, BONUS>(rt, rd, g, W, w));
+        const unsigned long long q = qfix(vmass[g]);
         if (pre + q > tl) {
+          float zt[8], zd[8], w[8];
+          row8<T>(gt, 8 * g, nv, aligned, zt);
+          if (!BONUS && W.r_d != 0.f) row8<T>(gd, 8 * g, nv, aligned, zd);
+          else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) zd[kk] = zt[kk];
+          }
+          weights8<BONUS>(zt, zd, 8 * g, W, w);
           float s = 0.f;
           int pick = 7;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            s = k ? __fadd_rn(s, w[k]) : w[0];
-            if (pre + qfix(s) > tl) { pick = k; break; }
+          for (int kk = 0; kk < 8; ++kk) {
+            s = kk ? __fadd_rn(s, w[kk]) : w[0];
+            if (pre + qfix(s) > tl) {
+              pick = kk;
+              break;
+            }
           }
           S.token = v0 + 8 * g + pick;
           break;
@@ -529,18 +841,18 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
         pre += q;
       }
     }
-    __syncthreads();
+    cbar();
     if (tid == 0) P.out_tok[static_cast<long long>(seq) * (P.K + 1) + a] = S.token;
   }
-  __syncthreads();
+  cbar();
 }
 
 // ------------------------------------------------------------------------------------------
-// combine the C partials of a position (warp 0); results land in S
+// combine the C partials of a position (consumer warp 0); results land in S
 // ------------------------------------------------------------------------------------------
 template <bool GREEDY>
 __device__ void combine(const Params& P, CtaState& S, const Xchg* XX, uint32_t C, int i,
-                        bool st_t, bool st_d, bool tk, bool ld_d) {
+                        bool st_t, bool st_d, bool tk, bool ld_d, float zx_t, float zx_d) {
   const int lane = threadIdx.x & 31;
   const bool have = lane < static_cast<int>(C);
   const float mt = have ? XX[lane].m_t : -INFINITY;
@@ -550,7 +862,11 @@ __device__ void combine(const Params& P, CtaState& S, const Xchg* XX, uint32_t C
   if constexpr (GREEDY) {
     const int arg = (have && mt == Mt) ? XX[lane].arg : 0x7FFFFFFF;
     const int best = warp_min_int(arg);
-    if (lane == 0) { S.M_t = Mt; S.bad_t = row_bad(Mt); S.arg = best; }
+    if (lane == 0) {
+      S.M_t = Mt;
+      S.bad_t = row_bad(Mt);
+      S.arg = best;
+    }
     return;
   } else {
     const float c = P.c;
@@ -571,237 +887,381 @@ __device__ void combine(const Params& P, CtaState& S, const Xchg* XX, uint32_t C
       }
     }
     if (lane != 0) return;
-    S.M_t = Mt; S.M_d = Md; S.S_t = St; S.S_d = Sd;
+    const int L = S.hdr[S.cur].L;
+    S.M_t = Mt;
+    S.M_d = Md;
+    S.S_t = St;
+    S.S_d = Sd;
     S.bad_t = row_bad(Mt);
     S.bad_d = ld_d ? row_bad(Md) : 0;
-    // Saguaro bias set: the bias_k most likely draft ids
-    float N = 1.f;
+    float N = 1.f;  // Saguaro bias set: the bias_k most likely draft ids
     int nS = 0;
     if (P.bias_k > 0 && tk && !S.bad_d) {
       float sq = 0.f;
       for (int j = 0; j < P.bias_k; ++j) {
         if (mtop[j] == 0ull) break;
-        const float z = key_value(mtop[j]);
-        sq += exp2f((z - Md) * c) / Sd;
+        sq += exp2f((key_value(mtop[j]) - Md) * c) / Sd;
         S.S_ids[nS++] = key_id(mtop[j]);
       }
       N = fmaf(-(1.f - P.beta), sq, 1.f);
     }
     S.nS = nS;
     S.N = N;
-    if (tk && P.fmax > 0 && i < S.L) {
+    if (tk && P.fmax > 0 && i < L) {
       for (int f = 0; f < 8; ++f)
         S.topf[i][f] = (f < P.fan[i] && mtop[f] != 0ull) ? key_id(mtop[f]) : -1;
     }
-    if (st_t && !S.bad_t) S.lse_t[i] = Mt / P.temperature + logf(St);
-    if (st_d && !S.bad_d) S.lse_d[i] = Md / P.temperature + logf(Sd);
+    if (P.debug_all) {
+      if (st_t && !S.bad_t) S.lse_t[i] = Mt / P.temperature + logf(St);
+      if (st_d && !S.bad_d) S.lse_d[i] = Md / P.temperature + logf(Sd);
+    }
     S.accept = 0;
-    if (st_t && st_d && i < S.L && !S.bad_t && !S.bad_d) {
-      const int x = S.x[i];
-      const float zt = S.zx_t, zd = S.zx_d;
+    if (st_t && st_d && i < L && !S.bad_t && !S.bad_d) {
+      const int x = S.hdr[S.cur].x[i];
       bool inS = false;
       for (int j = 0; j < nS; ++j) inS |= (S.S_ids[j] == x);
       const float f = inS ? P.beta : 1.f;
       float ratio;
-      if (zt == -INFINITY) ratio = 0.f;
-      else if (zd == -INFINITY) ratio = INFINITY;
-      else ratio = exp2f(((zt - zd) - (Mt - Md)) * c) * (Sd / St) * (N / f);
-      const float px = zt == -INFINITY ? 0.f : exp2f((zt - Mt) * c) / St;
-      const float qx = zd == -INFINITY ? 0.f : exp2f((zd - Md) * c) * f / (Sd * N);
-      S.px[i] = px;
-      S.qx[i] = qx;
-      S.accept = S.u[i] < ratio;
+      if (zx_t == -INFINITY) ratio = 0.f;
+      else if (zx_d == -INFINITY) ratio = INFINITY;
+      else ratio = exp2f(((zx_t - zx_d) - (Mt - Md)) * c) * (Sd / St) * (N / f);
+      if (P.debug_all) {
+        S.px[i] = zx_t == -INFINITY ? 0.f : exp2f((zx_t - Mt) * c) / St;
+        S.qx[i] = zx_d == -INFINITY ? 0.f : exp2f((zx_d - Md) * c) * f / (Sd * N);
+      }
+      S.accept = S.hdr[S.cur].u[i] < ratio;
     }
   }
 }
 
+// Header of sequence `seq` into hdr[slot] with 4-byte async copies (consumer thread 0).
+__device__ __forceinline__ void fetch_header(const Params& P, CtaState& S, int slot, int seq,
+                                             bool greedy) {
+  Hdr& h = S.hdr[slot];
+  if (P.lens) cp_async4(&h.L, P.lens + seq);
+  else h.L = P.K;
+  for (int i = 0; i < P.K; ++i) cp_async4(&h.x[i], P.tokens + static_cast<long long>(seq) * P.K + i);
+  if (!greedy)
+    for (int i = 0; i <= P.K; ++i)
+      cp_async4(&h.u[i], P.uni + static_cast<long long>(seq) * (P.K + 1) + i);
+  cp_async_commit();
+}
+
+__device__ __forceinline__ int header_ok(const Params& P, const Hdr& h, bool greedy) {
+  const int L = h.L;
+  if (L < 1 || L > P.K) return 0;
+  for (int i = 0; i < L; ++i)
+    if (h.x[i] < 0 || h.x[i] >= P.V) return 0;
+  if (!greedy)
+    for (int i = 0; i <= P.K; ++i)
+      if ((i < L || i == P.K) && !(h.u[i] >= 0.f && h.u[i] < 1.f)) return 0;
+  return 1;
+}
+
 // ------------------------------------------------------------------------------------------
-// the kernel
+// the kernel: consumer warps 0..7 verify, warp 8 produces
 // ------------------------------------------------------------------------------------------
-template <typename T, bool GREEDY>
-__global__ void __launch_bounds__(NT, 2) verify_kernel(const Params P) {
+template <typename T, bool GREEDY, bool TOP8>
+__global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ CtaState S;
   __shared__ Xchg X[2][kMaxCluster];
-  __shared__ uint64_t mbar;
+  __shared__ uint64_t full_bar[NS], empty_bar[NS], xbar[2];
+  __shared__ StageDesc sdesc[NS];
 
+  using RingT = Ring<T, GREEDY>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const uint32_t C = cluster_nctarank();
   const int cid = static_cast<int>(cluster_id_x());
-  T* rt = reinterpret_cast<T*>(dyn);
-  T* rd = rt + P.slice;
-  const int v0 = static_cast<int>(rank) * P.slice;
-  const int nv = max(0, min(P.V - v0, P.slice));
-  const int nvec = (nv + 7) >> 3;
-  constexpr int kPer16 = 16 / static_cast<int>(sizeof(T));
-  const int nb = P.use_bulk ? (nv / kPer16) * kPer16 : 0;
-  const T* gtb = reinterpret_cast<const T*>(P.tgt);
-  const T* gdb = reinterpret_cast<const T*>(P.dft);
   const int K = P.K;
+  RingT R;
+  R.base = dyn;
+  R.full = full_bar;
+  R.empty = empty_bar;
+  R.desc = sdesc;
+  R.v0 = static_cast<int>(rank) * P.slice;
+  R.nv = max(0, min(P.V - R.v0, P.slice));
+  R.nchunk = (R.nv + RingT::CH - 1) / RingT::CH;
+  float* vmass = reinterpret_cast<float*>(dyn + static_cast<size_t>(NS) * RingT::kRows * kStageRowBytes);
+  const float c = P.c;
 
   if (tid == 0) {
-    mbar_init(&mbar, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], NW);
+    }
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     fence_mbar_init();
+    S.cur = 0;
+    S.n_hdr_wait = 0;
+    S.ver = 0;
+    fetch_header(P, S, 0, cid, GREEDY);
+    cp_async_wait_all();
+    S.hdr[0].ok = header_ok(P, S.hdr[0], GREEDY);
+    Pub v;
+    v.ep = 0;
+    v.seq = cid;
+    v.stop = S.hdr[0].ok ? -1 : -2;
+    v.next = -1;
+    v.done = 0;
+    v.cons = 0;
+    pub_write(S, v);
   }
   __syncthreads();
   cluster_sync();  // every CTA of the cluster is running before any shared-memory exchange
 
-  uint32_t xpar = 0, tpar = 0;
-  bool aborted = false;
-  int seq = cid;
-  while (seq < P.B) {
-    // ---- sequence header: every CTA reads the same few words ----
-    if (tid == 0) {
-      const int L = P.lens ? P.lens[seq] : K;
-      int ok = (L >= 1 && L <= K);
-      for (int i = 0; i < K; ++i) {
-        const int x = P.tokens[static_cast<long long>(seq) * K + i];
-        S.x[i] = x;
-        if (i < L && (x < 0 || x >= P.V)) ok = 0;
-      }
-      if (!GREEDY) {
-        for (int i = 0; i <= K; ++i) {
-          const float u = P.uni[static_cast<long long>(seq) * (K + 1) + i];
-          S.u[i] = u;
-          if ((i < L || i == K) && !(u >= 0.f && u < 1.f)) ok = 0;
+  if (warp == NW) {
+    if ((tid & 31) == 0) producer<T, GREEDY>(P, S, R, cid);
+    __syncwarp();
+  } else {
+    uint32_t xround = 0;
+    int cons = 0;
+    bool late = false;
+    bool aborted = false;
+    int seq = cid;
+    while (seq < P.B) {
+      int next_local = 0;
+      if (rank == 0 && tid == 0)
+        next_local = static_cast<int>(atomicAdd(&P.ws->next, 1u)) + P.n_clusters;
+      if (tid == 0 && P.fmax + P.debug_all > 0) {
+        for (int i = 0; i < kMaxK; ++i) {
+          for (int f = 0; f < 8; ++f) S.topf[i][f] = -1;
+          S.lse_d[i] = S.px[i] = S.qx[i] = NAN;
         }
+        for (int i = 0; i <= kMaxK; ++i) S.lse_t[i] = NAN;
       }
-      S.L = L;
-      S.hdr_ok = ok;
-      S.next = rank == 0 ? static_cast<int>(atomicAdd(&P.ws->next, 1u)) + P.n_clusters : 0;
-      for (int i = 0; i < kMaxK; ++i) {
-        for (int f = 0; f < 8; ++f) S.topf[i][f] = -1;
-        S.lse_d[i] = S.px[i] = S.qx[i] = NAN;
-      }
-      for (int i = 0; i <= kMaxK; ++i) S.lse_t[i] = NAN;
-    }
-    __syncthreads();
-    const int L = S.L;
-    bool invalid = !S.hdr_ok;
-    bool decided = invalid;
-    bool first = true;
-    int a = -1;
-    int next = P.B;
-    for (int i = 0;; ++i) {
-      const bool st_t = !invalid && i <= L && (!decided || P.debug_all);
-      const bool st_d = !GREEDY && !invalid && i < L && (!decided || P.debug_all);
-      const bool tk = !GREEDY && !invalid && i < L && P.top8 &&
-                      (!decided || P.fmax > 0 || P.debug_all);
-      const bool ld_t = st_t, ld_d = st_d || tk;
-      if (!ld_t && !ld_d && !first) break;
-      bool late = false;
-      if (ld_t || ld_d) {
-        const T* gt = gtb + (static_cast<long long>(seq) * (K + 1) + i) * P.t_stride + v0;
-        const T* gd = GREEDY ? nullptr
-                             : gdb + (static_cast<long long>(seq) * K + i) * P.d_stride + v0;
+      const int L = S.hdr[S.cur].L;
+      bool invalid = !S.hdr[S.cur].ok;
+      bool decided = invalid;
+      bool first = true;
+      int a = -1;
+      int next = P.B;
+      for (int i = 0;; ++i) {
+        const bool st_t = !invalid && i <= L && (!decided || P.debug_all);
+        const bool st_d = !GREEDY && !invalid && i < L && (!decided || P.debug_all);
+        const bool tk = TOP8 && !invalid && i < L && (!decided || P.fmax > 0 || P.debug_all);
+        const bool ld_t = st_t, ld_d = st_d || tk;
+        if (!ld_t && !ld_d && !first) break;
+        // the draft token's logits for the accept test (thread 0; used after the exchange)
+        float zx_t = 0.f, zx_d = 0.f;
         if (!GREEDY && tid == 0 && st_t && st_d && i < L) {
-          const long long x = S.x[i] - v0;  // gathered logits of the draft token
-          S.zx_t = Elt<T>::val(gt[x]);
-          S.zx_d = Elt<T>::val(gd[x]);
+          const int x = S.hdr[S.cur].x[i];
+          zx_t = Elt<T>::val(static_cast<const T*>(row_ptr(P, false, seq, i, sizeof(T)))[x]);
+          zx_d = Elt<T>::val(static_cast<const T*>(row_ptr(P, true, seq, i, sizeof(T)))[x]);
         }
-        late = stage_rows<T>(rt, rd, gt, gd, ld_t, ld_d, nv, nb, nvec, &mbar, tpar);
-      }
-      // ---- this CTA's partials ----
-      const float2 mm = block_max2(ld_t && !late ? slice_max<T>(rt, nvec) : -INFINITY,
-                                   ld_d && !late ? slice_max<T>(rd, nvec) : -INFINITY, S);
-      float2 ss = make_float2(0.f, 0.f);
-      int arg = 0x7FFFFFFF;
-      if constexpr (GREEDY) {
-        if (ld_t && !late && !row_bad(mm.x)) {
-          const int e = slice_first_index<T>(rt, nvec, mm.x);
-          arg = block_min_int(e, S);
-          if (arg != 0x7FFFFFFF) arg += v0;
+        // ---- stream this CTA's slice of the position's rows ----
+        RowAcc at, ad;
+        at.init();
+        ad.init();
+        int garg = 0x7FFFFFFF;
+        unsigned long long keys[8];
+        float thr = -INFINITY;
+        if (TOP8) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) keys[j] = 0ull;
         }
-      } else {
-        const float c = P.c;
-        const bool sum_t = st_t && !late && !row_bad(mm.x);
-        const bool sum_d = st_d && !late && !row_bad(mm.y);
-        const float mct = __fmul_rn(mm.x, c), mcd = __fmul_rn(mm.y, c);
-        ss = block_sum2(sum_t ? slice_sum<T>(rt, nvec, c, mct) : 0.f,
-                        sum_d ? slice_sum<T>(rd, nvec, c, mcd) : 0.f, S);
-        // fold the rounding of m*c back in: the sums are relative to exactly m
-        if (sum_t) ss.x *= fmaf(-fmaf(mm.x, c, -mct), kLn2, 1.f);
-        if (sum_d) ss.y *= fmaf(-fmaf(mm.y, c, -mcd), kLn2, 1.f);
-        if (tk && !late) {
-          unsigned long long keys[8];
-          slice_top8<T>(rd, nv, nvec, v0, keys);
-          block_top8(keys, S);
-        } else if (tk && tid == 0) {
-          for (int r = 0; r < 8; ++r) S.rec.top8[r] = 0ull;
-        }
-      }
-      if (tid == 0) {
-        S.rec.m_t = mm.x; S.rec.s_t = ss.x;
-        S.rec.m_d = mm.y; S.rec.s_d = ss.y;
-        S.rec.arg = arg;
-        S.rec.next_seq = first ? S.next : 0;
-        S.rec.flags = late ? XF_ABORT : 0u;
-        if (late) atomicOr(&P.ws->error, 1u);
-      }
-      __syncthreads();
-      exchange(S, X, xpar, rank, C, 0, tk ? 6 : 2);
-      const Xchg* XX = X[xpar];
-      xpar ^= 1u;
-      if (first) { next = XX[0].next_seq; first = false; }
-      bool ab = false;
-      for (uint32_t c = 0; c < C; ++c) ab |= (XX[c].flags & XF_ABORT) != 0u;
-      if (ab) { aborted = true; break; }
-      if (!ld_t && !ld_d) break;  // header was invalid: the exchange only carried `next`
-      if (warp == 0) combine<GREEDY>(P, S, XX, C, i, st_t, st_d, tk, ld_d);
-      __syncthreads();
-      if (!decided) {
-        if (S.bad_t || (i < L && !GREEDY && S.bad_d)) { invalid = true; break; }
-        if constexpr (GREEDY) {
-          if (!(i < L && S.x[i] == S.arg)) { a = i; decided = true; }
-        } else {
-          if (i < L) {
-            if (!S.accept) {
-              a = i;
-              decided = true;
-              draw_token<T, false>(P, S, X, xpar, rank, C, rt, rd, nvec, v0, nv, seq, a);
+        if (ld_t || ld_d) {
+          for (int k = 0; k < R.nchunk; ++k) {
+            int s = acquire<T, GREEDY>(R, seq, i, k, cons, late);
+            if (!P.use_bulk) s = fill_unaligned<T, GREEDY>(P, R, s, seq, i, k, late);
+            if (s < 0) break;
+            const int n = R.chunk_len(k);
+            const int nvec = (n + 7) >> 3;
+            const T* rt = R.row(s, 0);
+            const T* rd = R.row(s, GREEDY ? 0 : 1);
+            for (int g = tid; g < nvec; g += NC) {
+              float z[8];
+              if (ld_t) {
+                const float vm = Elt<T>::vmax8(rt, g, z);
+                if constexpr (GREEDY) {
+                  if (isnan(vm)) {
+                    at.m = NAN;
+                  } else if (vm > at.m) {
+                    at.m = vm;
+                    int e = 7;
+#pragma unroll
+                    for (int kk = 7; kk >= 0; --kk)
+                      if (z[kk] == vm) e = kk;
+                    garg = R.v0 + k * RingT::CH + 8 * g + e;
+                  }
+                } else {
+                  at.add8(vm, z, c);
+                }
+              }
+              if (!GREEDY && ld_d) {
+                const float vm = Elt<T>::vmax8(rd, g, z);
+                if (st_d) ad.add8(vm, z, c);
+                else ad.m = max_nan(ad.m, vm);
+                if (TOP8 && tk) {
+                  const int eb = k * RingT::CH + 8 * g;
+#pragma unroll
+                  for (int kk = 0; kk < 8; ++kk)
+                    if (8 * g + kk < n)
+                      top8_insert(keys, thr, z[kk], static_cast<uint32_t>(R.v0 + eb + kk));
+                }
+              }
             }
-          } else {
-            a = L;
-            decided = true;
-            draw_token<T, true>(P, S, X, xpar, rank, C, rt, rd, nvec, v0, nv, seq, a);
+            release_stage(R.empty, s, cons);
           }
         }
-      } else if (tk && P.fmax > 0 && S.bad_d) {
-        invalid = true;  // a draft row the top-F output needs holds no distribution
-        break;
-      }
-    }
-    // ---- epilogue: rank 0 writes the outputs of this sequence ----
-    if (rank == 0) {
-      int32_t* tok = P.out_tok + static_cast<long long>(seq) * (K + 1);
-      const bool bad = aborted || invalid;
-      if (tid == 0) P.out_acc[seq] = aborted ? -2 : (invalid ? -1 : a);
-      for (int j = tid; j <= K; j += NT) {
-        if (bad || j > a) tok[j] = -1;
-        else if (j < a) tok[j] = S.x[j];
-        else if (GREEDY) tok[j] = S.arg;
-      }
-      if (P.fmax > 0) {
-        int32_t* tf = P.out_topf + static_cast<long long>(seq) * K * P.fmax;
-        for (int e = tid; e < K * P.fmax; e += NT) {
-          const int i = e / P.fmax, f = e % P.fmax;
-          tf[e] = (!bad && i < L && f < 8) ? S.topf[i][f] : -1;
+        // ---- this CTA's partials ----
+        late = cbar_or(late);
+        const float2 mm = block_max2(at.m, ad.m, S);
+        float2 ss = make_float2(0.f, 0.f);
+        int arg = 0x7FFFFFFF;
+        if constexpr (GREEDY) {
+          if (ld_t && !row_bad(mm.x)) arg = block_min_int(at.m == mm.x ? garg : 0x7FFFFFFF, S);
+        } else {
+          const bool sum_t = st_t && !row_bad(mm.x);
+          const bool sum_d = st_d && !row_bad(mm.y);
+          const float mct = __fmul_rn(mm.x, c), mcd = __fmul_rn(mm.y, c);
+          const float pt = (sum_t && at.m > -INFINITY) ? (at.s0 + at.s1) * exp2f(at.mc - mct) : 0.f;
+          const float pd = (sum_d && ad.m > -INFINITY) ? (ad.s0 + ad.s1) * exp2f(ad.mc - mcd) : 0.f;
+          ss = block_sum2(pt, pd, S);
+          // the sums are relative to m*c rounded; fold the rounding back in
+          if (sum_t) ss.x *= fmaf(-fmaf(mm.x, c, -mct), kLn2, 1.f);
+          if (sum_d) ss.y *= fmaf(-fmaf(mm.y, c, -mcd), kLn2, 1.f);
+          if (TOP8 && tk) block_top8(keys, S);
+        }
+        if (tid == 0) {
+          S.rec.m_t = mm.x;
+          S.rec.s_t = ss.x;
+          S.rec.m_d = mm.y;
+          S.rec.s_d = ss.y;
+          S.rec.arg = arg;
+          S.rec.next_seq = first ? next_local : 0;
+          S.rec.flags = late ? XF_ABORT : 0u;
+          if (TOP8 && tk && !(ld_t || ld_d))
+            for (int r = 0; r < 8; ++r) S.rec.top8[r] = 0ull;
+        }
+        cbar();
+        if (!exchange(S, X, xbar, xround, rank, C, 0, (TOP8 && tk) ? 6 : 2)) late = true;
+        const Xchg* XX = X[(xround - 1) & 1u];
+        bool ab = late;
+        for (uint32_t cc = 0; cc < C; ++cc) ab |= (XX[cc].flags & XF_ABORT) != 0u;
+        ab = cbar_or(ab);  // the same answer in every consumer thread
+        if (ab) {
+          aborted = true;
+          break;
+        }
+        if (first) {
+          next = XX[0].next_seq;
+          first = false;
+          if (tid == 0) {  // start fetching the next sequence's header; tell the producer
+            if (next < P.B) {
+              fetch_header(P, S, S.cur ^ 1, next, GREEDY);
+              S.n_hdr_wait = 1;
+            }
+            Pub v = pub_local(S);
+            v.next = next;
+            pub_write(S, v);
+          }
+        }
+        if (!ld_t && !ld_d) break;  // header was invalid: the exchange only carried `next`
+        if (warp == 0) combine<GREEDY>(P, S, XX, C, i, st_t, st_d, tk, ld_d, zx_t, zx_d);
+        cbar();
+        if (!decided) {
+          int stop = -1;
+          if (S.bad_t || (i < L && !GREEDY && S.bad_d)) {
+            invalid = true;
+            stop = -2;
+          } else if constexpr (GREEDY) {
+            if (!(i < L && S.hdr[S.cur].x[i] == S.arg)) stop = i;
+          } else {
+            if (i == L || !S.accept) stop = i;
+          }
+          if (stop != -1) {
+            decided = true;
+            a = stop;
+            if (tid == 0) {
+              Pub v = pub_local(S);
+              v.stop = stop;
+              pub_write(S, v);
+            }
+          }
+          if (invalid) break;
+          if (!GREEDY && stop >= 0) {
+            if (stop < L)
+              draw_token<T, GREEDY, false>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+            else
+              draw_token<T, GREEDY, true>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+            if (late) {
+              aborted = true;
+              break;
+            }
+          }
+        } else if (tk && P.fmax > 0 && S.bad_d) {
+          invalid = true;  // a draft row the top-F output needs holds no distribution
+          if (tid == 0) {
+            Pub v = pub_local(S);
+            v.stop = -2;
+            pub_write(S, v);
+          }
+          break;
         }
       }
-      if (P.dbg_lse_t && tid <= K) P.dbg_lse_t[static_cast<long long>(seq) * (K + 1) + tid] = S.lse_t[tid];
-      if (tid < K) {
-        const long long o = static_cast<long long>(seq) * K + tid;
-        if (P.dbg_lse_d) P.dbg_lse_d[o] = S.lse_d[tid];
-        if (P.dbg_px) P.dbg_px[o] = S.px[tid];
-        if (P.dbg_qx) P.dbg_qx[o] = S.qx[tid];
+      // ---- epilogue: rank 0 writes the outputs of this sequence ----
+      if (rank == 0) {
+        int32_t* tok = P.out_tok + static_cast<long long>(seq) * (K + 1);
+        const bool bad = aborted || invalid;
+        if (tid == 0) P.out_acc[seq] = aborted ? -2 : (invalid ? -1 : a);
+        for (int j = tid; j <= K; j += NC) {
+          if (bad || j > a) tok[j] = -1;
+          else if (j < a) tok[j] = S.hdr[S.cur].x[j];
+          else if (GREEDY) tok[j] = S.arg;
+        }
+        if (P.fmax > 0) {
+          int32_t* tf = P.out_topf + static_cast<long long>(seq) * K * P.fmax;
+          for (int e = tid; e < K * P.fmax; e += NC) {
+            const int i = e / P.fmax, f = e % P.fmax;
+            tf[e] = (!bad && i < L && f < 8) ? S.topf[i][f] : -1;
+          }
+        }
+        if (P.dbg_lse_t && tid <= K)
+          P.dbg_lse_t[static_cast<long long>(seq) * (K + 1) + tid] = S.lse_t[tid];
+        if (tid < K) {
+          const long long o = static_cast<long long>(seq) * K + tid;
+          if (P.dbg_lse_d) P.dbg_lse_d[o] = S.lse_d[tid];
+          if (P.dbg_px) P.dbg_px[o] = S.px[tid];
+          if (P.dbg_qx) P.dbg_qx[o] = S.qx[tid];
+        }
       }
+      cbar();
+      if (aborted) {
+        if (tid == 0) atomicOr(&P.ws->error, 1u);
+        break;
+      }
+      // ---- move on to the next sequence of the queue ----
+      if (tid == 0) {
+        if (S.n_hdr_wait) {
+          cp_async_wait_all();
+          S.n_hdr_wait = 0;
+        }
+        const int nx = S.cur ^ 1;
+        if (next < P.B) S.hdr[nx].ok = header_ok(P, S.hdr[nx], GREEDY);
+        S.cur = nx;
+        Pub v = pub_local(S);
+        v.ep += 1;
+        v.seq = next;
+        v.stop = (next < P.B && S.hdr[nx].ok) ? -1 : -2;
+        v.next = -1;
+        pub_write(S, v);
+      }
+      cbar();
+      seq = next;
     }
-    __syncthreads();
-    if (aborted) break;
-    seq = next;
+    if (tid == 0) {
+      cp_async_wait_all();
+      Pub v = pub_local(S);
+      v.done = 1;
+      v.cons = cons;
+      pub_write(S, v);
+    }
   }
+  __syncthreads();
   cluster_sync();
   if (rank == 0 && tid == 0) {
     __threadfence();
@@ -813,14 +1273,18 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const Params P) {
   }
 }
 
-template <typename T, bool GREEDY>
+template <typename T, bool GREEDY, bool TOP8>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&verify_kernel<T, GREEDY>);
+  return reinterpret_cast<const void*>(&verify_kernel<T, GREEDY, TOP8>);
 }
 
-const void* pick(int dtype, int greedy) {
-  if (dtype == 1) return greedy ? kernel_ptr<uint16_t, true>() : kernel_ptr<uint16_t, false>();
-  return greedy ? kernel_ptr<float, true>() : kernel_ptr<float, false>();
+const void* pick(int dtype, int greedy, int top8) {
+  if (dtype == 1) {
+    if (greedy) return kernel_ptr<uint16_t, true, false>();
+    return top8 ? kernel_ptr<uint16_t, false, true>() : kernel_ptr<uint16_t, false, false>();
+  }
+  if (greedy) return kernel_ptr<float, true, false>();
+  return top8 ? kernel_ptr<float, false, true>() : kernel_ptr<float, false, false>();
 }
 
 cudaError_t prepare(const void* fn, int cluster, size_t smem) {
@@ -837,17 +1301,18 @@ cudaError_t prepare(const void* fn, int cluster, size_t smem) {
 }  // namespace
 
 size_t smem_bytes(int dtype, int greedy, int slice) {
-  const size_t elt = dtype == 1 ? 2 : 4;
-  const size_t rows = greedy ? 1 : 2;
-  return (rows * elt * static_cast<size_t>(slice) + 127) / 128 * 128;
+  (void)dtype;
+  const size_t ring = static_cast<size_t>(NS) * (greedy ? 1 : 2) * kStageRowBytes;
+  const size_t vmass = greedy ? 0 : (static_cast<size_t>(slice) / 8 * 4 + 127) / 128 * 128;
+  return ring + vmass;
 }
 
-int max_active_clusters(int dtype, int greedy, int cluster, size_t smem) {
-  const void* fn = pick(dtype, greedy);
+int max_active_clusters(int dtype, int greedy, int top8, int cluster, size_t smem) {
+  const void* fn = pick(dtype, greedy, top8);
   if (prepare(fn, cluster, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cluster) * 64u);
-  cfg.blockDim = dim3(NT);
+  cfg.blockDim = dim3(NTOT);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -862,12 +1327,12 @@ int max_active_clusters(int dtype, int greedy, int cluster, size_t smem) {
 }
 
 cudaError_t launch(const Launch& L, cudaStream_t stream) {
-  const void* fn = pick(L.dtype, L.greedy);
+  const void* fn = pick(L.dtype, L.greedy, L.p.top8);
   cudaError_t e = prepare(fn, L.cluster, L.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(L.p.n_clusters * L.cluster));
-  cfg.blockDim = dim3(NT);
+  cfg.blockDim = dim3(NTOT);
   cfg.dynamicSmemBytes = L.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -99,9 +99,10 @@ typedef struct {
  *   out_residual_topF [B][K][max_i F_i] int32, -1 padded; required iff prob->fanout != NULL
  *                  (stochastic mode only), otherwise must be NULL.
  *   stream         cudaStream_t.
- * The library keeps a small zero-initialised workspace per (device, stream), created on the
- * first call for that pair; make that first call outside stream capture. Calls that may run
- * at the same time must use different streams.
+ * The library keeps a zero-initialised workspace per (device, stream) of
+ * spec_verify_workspace_bytes(prob) bytes, created (or enlarged for a larger B) by the first
+ * such call; make that call outside stream capture. Calls that may run at the same time must use
+ * different streams.
  */
 sv_status spec_verify(const sv_problem* prob, const void* target_logits,
                       const void* draft_logits, const int32_t* draft_tokens,
@@ -118,7 +119,7 @@ sv_status spec_verify(const sv_problem* prob, const void* target_logits,
 sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* clusters,
                            size_t* smem_bytes);
 
-/* Bytes of device workspace spec_verify_ws needs (a small constant). */
+/* Bytes of device workspace spec_verify_ws needs for this problem (256 + 4 B, rounded up). */
 size_t spec_verify_workspace_bytes(const sv_problem* prob);
 
 /*

@@ -164,6 +164,12 @@ def verify_host(target, draft, draft_tokens, draft_lens, uniforms, out_accept_le
     _lib._check(st, "spec_verify_host")
 
 
+def workspace_bytes(B: int) -> int:
+    """Device bytes the caller-owned-workspace entry point needs for a batch of B sequences."""
+    prob, _ = _lib.make_problem(B, 1, 1, SV_DTYPE_F32, 1, 1)
+    return int(_lib.call("spec_verify_workspace_bytes", prob))
+
+
 def device_error(stream=None) -> int:
     """Status of the device-side bounded waits on ``stream`` since the last check."""
     return _lib.load().spec_verify_device_error(_stream_handle(stream))

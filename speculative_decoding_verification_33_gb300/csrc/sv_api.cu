@@ -25,6 +25,7 @@ constexpr size_t kMaxDynSmem = 200 * 1024;
 
 struct StreamRes {
   Workspace* ws = nullptr;
+  size_t ws_bytes = 0;
   void* stage = nullptr;  // device staging for spec_verify_host
   size_t stage_bytes = 0;
 };
@@ -114,22 +115,31 @@ int choose_cluster(const sv_problem* p, int greedy, size_t elt, int sms) {
   return std::max(c_mem, std::min(c_par, c_vocab));
 }
 
-StreamRes* resources(int dev, cudaStream_t s, sv_status* st) {
+StreamRes* resources(int dev, cudaStream_t s, size_t need, sv_status* st) {
   StreamRes& r = g_res[{dev, s}];
-  if (!r.ws) {
+  if (!r.ws || r.ws_bytes < need) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone) {
-      *st = SV_ERR_UNSUPPORTED;  // the workspace must exist before capture
+      *st = SV_ERR_UNSUPPORTED;  // the workspace must exist (and be large enough) before capture
       return nullptr;
     }
+    if (r.ws) {
+      if (cudaStreamSynchronize(s) != cudaSuccess) {
+        *st = SV_ERR_CUDA;
+        return nullptr;
+      }
+      cudaFree(r.ws);
+      r.ws = nullptr;
+      r.ws_bytes = 0;
+    }
     void* w = nullptr;
-    if (cudaMalloc(&w, sizeof(Workspace)) != cudaSuccess ||
-        cudaMemset(w, 0, sizeof(Workspace)) != cudaSuccess) {
+    if (cudaMalloc(&w, need) != cudaSuccess || cudaMemset(w, 0, need) != cudaSuccess) {
       if (w) cudaFree(w);
       *st = SV_ERR_CUDA;
       return nullptr;
     }
     r.ws = static_cast<Workspace*>(w);
+    r.ws_bytes = need;
   }
   *st = SV_OK;
   return &r;
@@ -215,10 +225,12 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   if (ws_user) {
     P.ws = ws_user;
   } else {
-    StreamRes* r = resources(dev, stream, &st);
+    StreamRes* r = resources(dev, stream, sv::workspace_bytes_for(p->B), &st);
     if (!r) return st;
     P.ws = r->ws;
   }
+  P.perm = reinterpret_cast<int*>(P.ws + 1);
+  P.lpt = p->B <= sv::kLptMaxB ? 1 : 0;
   return sv::launch(L, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -261,8 +273,7 @@ sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* 
 }
 
 size_t spec_verify_workspace_bytes(const sv_problem* prob) {
-  (void)prob;
-  return sizeof(Workspace);
+  return sv::workspace_bytes_for(prob ? prob->B : 0);
 }
 
 sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
@@ -271,7 +282,7 @@ sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
                          float beta, int mode, int32_t* out_accept_len, int32_t* out_tokens,
                          int32_t* out_residual_topF, void* workspace, size_t workspace_bytes,
                          void* stream) {
-  if (!workspace || workspace_bytes < sizeof(Workspace) ||
+  if (!workspace || !prob || workspace_bytes < sv::workspace_bytes_for(prob->B) ||
       reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
     return SV_ERR_INVALID_ARG;
   return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
@@ -323,7 +334,7 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
   Workspace* ws = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    StreamRes* r = resources(dev, s, &st);
+    StreamRes* r = resources(dev, s, sv::workspace_bytes_for(prob->B), &st);
     if (!r) return st;
     if (r->stage_bytes < total) {
       if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;

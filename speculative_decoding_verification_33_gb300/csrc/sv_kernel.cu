@@ -74,24 +74,42 @@ struct StageDesc {
   int seq, pos, k, rows;  // rows: ROW_T | ROW_D; pos < 0 marks a chunk of the draw pass
 };
 
-// What the consumers tell the producer warp, published under a sequence lock (consumer thread
-// 0 writes, producer lane 0 reads): the position in the cluster's sequence order (epoch), the
-// current sequence and its decided position, and the next sequence once it is known.
+// What the consumers tell the producer warp: two 64-bit shared-memory words, each written and
+// read with one 8-byte access (consumer thread 0 writes, the producer lane reads).
+//   cur:  current sequence (bits 0..31), epoch = its place in the cluster's sequence order
+//         (bits 32..47, mod 2^16), decided position + 2 (bits 48..55; 1 = undecided, 0 = nothing
+//         more needed), consumers done (bit 56).
+//   next: next sequence of the queue (bits 0..31), the epoch it follows (bits 32..47), known
+//         (bit 48).
 struct Pub {
-  int ep;      // epoch of the current sequence (0, 1, 2, ...)
-  int seq;     // current sequence
-  int stop;    // -1 undecided, -2 nothing more needed, else the decided position
-  int next;    // next sequence of the queue, -1 unknown
-  int done;    // the consumers have left the sequence loop
-  int cons;    // stages the consumers have taken (valid once done)
+  int seq, ep, stop, done;
 };
+__device__ __forceinline__ unsigned long long pack_cur(int seq, int ep, int stop, int done) {
+  return static_cast<unsigned long long>(static_cast<uint32_t>(seq)) |
+         (static_cast<unsigned long long>(ep & 0xFFFF) << 32) |
+         (static_cast<unsigned long long>((stop + 2) & 0xFF) << 48) |
+         (static_cast<unsigned long long>(done ? 1 : 0) << 56);
+}
+__device__ __forceinline__ Pub unpack_cur(unsigned long long w) {
+  Pub v;
+  v.seq = static_cast<int>(static_cast<uint32_t>(w));
+  v.ep = static_cast<int>((w >> 32) & 0xFFFF);
+  v.stop = static_cast<int>((w >> 48) & 0xFF) - 2;
+  v.done = static_cast<int>((w >> 56) & 1);
+  return v;
+}
+__device__ __forceinline__ unsigned long long pack_next(int seq, int ep) {
+  return static_cast<unsigned long long>(static_cast<uint32_t>(seq)) |
+         (static_cast<unsigned long long>(ep & 0xFFFF) << 32) | (1ull << 48);
+}
 
 struct CtaState {
   Hdr hdr[2];        // current and next sequence header (cp.async targets)
   int cur;           // hdr[cur] is the current sequence
   int n_hdr_wait;    // consumer thread 0 has a header copy in flight
-  unsigned ver;      // sequence lock of `pub` (odd while it is being written)
-  Pub pub;
+  unsigned long long pub_cur, pub_next;  // consumer -> producer words (see Pub)
+  int cons_final;    // stages the consumers took, published before `done`
+  int seq0;          // this cluster's first sequence
   // reduction scratch (one slot per kind)
   float rmax[2][NW];
   float rsum[2][NW];
@@ -376,47 +394,13 @@ __device__ __forceinline__ bool exchange(CtaState& S, Xchg (*X)[kMaxCluster], ui
 }
 
 // ------------------------------------------------------------------------------------------
-// consumer -> producer publication (sequence lock)
+// consumer -> producer publication
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ void pub_write(CtaState& S, const Pub& v) {  // consumer thread 0
-  volatile unsigned* ver = &S.ver;
-  *ver = *ver + 1u;
-  __threadfence_block();
-  volatile Pub* d = &S.pub;
-  d->ep = v.ep;
-  d->seq = v.seq;
-  d->stop = v.stop;
-  d->next = v.next;
-  d->done = v.done;
-  d->cons = v.cons;
-  __threadfence_block();
-  *ver = *ver + 1u;
+__device__ __forceinline__ void pub_store(unsigned long long* w, unsigned long long v) {
+  *reinterpret_cast<volatile unsigned long long*>(w) = v;
 }
-
-__device__ __forceinline__ Pub pub_local(const CtaState& S) {  // consumer thread 0's own copy
-  const volatile Pub* d = &S.pub;
-  Pub v;
-  v.ep = d->ep;
-  v.seq = d->seq;
-  v.stop = d->stop;
-  v.next = d->next;
-  v.done = d->done;
-  v.cons = d->cons;
-  return v;
-}
-
-__device__ __forceinline__ Pub pub_read(CtaState& S) {  // producer lane
-  Pub v;
-  for (int tries = 0; tries < (1 << 20); ++tries) {
-    const unsigned a = *reinterpret_cast<volatile unsigned*>(&S.ver);
-    __threadfence_block();
-    v = pub_local(S);
-    __threadfence_block();
-    const unsigned b = *reinterpret_cast<volatile unsigned*>(&S.ver);
-    if (a == b && !(a & 1u)) return v;
-  }
-  v.done = 1;  // the writer never finished: stop producing
-  return v;
+__device__ __forceinline__ unsigned long long pub_load(const unsigned long long* w) {
+  return *reinterpret_cast<const volatile unsigned long long*>(w);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -499,15 +483,14 @@ __device__ void issue_chunk(const Params& P, const Ring<T, GREEDY>& R, int s, in
 // top-F output still need, then the next sequence. It never runs past an undecided stochastic
 // sequence, so the ring always holds chunks in the order the consumers take them.
 template <typename T, bool GREEDY>
-__device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R, int first_seq) {
+__device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R) {
   enum { STATS = 0, DRAW = 1, POST = 2 };
-  int q_ep = 0, q_seq = first_seq, q_L = load_len(P, first_seq);
+  int q_ep = 0, q_seq = S.seq0, q_L = load_len(P, S.seq0);
   int q_ph = STATS, q_pos = 0, q_k = 0;
   int issued = 0;
   long long idle0 = clock64();
-  Pub pub;
   while (true) {
-    pub = pub_read(S);
+    const Pub pub = unpack_cur(pub_load(&S.pub_cur));
     if (pub.done) break;
     if (clock64() - idle0 > kWaitBudget) {
       atomicOr(&P.ws->error, 1u);
@@ -518,8 +501,9 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R,
       idle0 = clock64();
       continue;
     }
-    if (q_ep < pub.ep) {  // the consumers are past this sequence (it needed no chunks)
-      q_ep = pub.ep;
+    const int lag = static_cast<int16_t>(static_cast<uint16_t>(pub.ep - q_ep));
+    if (lag > 0) {  // the consumers are past this sequence (it needed no chunks)
+      q_ep += lag;
       q_seq = pub.seq;
       q_L = load_len(P, q_seq);
       q_ph = STATS;
@@ -528,7 +512,7 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R,
     }
     int rows = 0;
     bool exhausted = q_seq >= P.B;
-    if (!exhausted && q_ep == pub.ep) {
+    if (!exhausted && lag >= 0) {  // the consumers' current sequence
       const int stop = pub.stop;
       if (stop == -2) {
         exhausted = true;
@@ -550,17 +534,20 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R,
           exhausted = rows == 0;
         }
       }
+      if (exhausted && q_seq < P.B) {  // move on once the next sequence is known
+        const unsigned long long nw = pub_load(&S.pub_next);
+        if ((nw >> 48) & 1ull && static_cast<int>((nw >> 32) & 0xFFFF) == (q_ep & 0xFFFF)) {
+          ++q_ep;
+          q_seq = static_cast<int>(static_cast<uint32_t>(nw));
+          q_L = load_len(P, q_seq);
+          q_ph = STATS;
+          q_pos = 0;
+          q_k = 0;
+          continue;
+        }
+      }
     } else if (!exhausted && q_ph == STATS && q_pos <= q_L) {  // the next sequence, early
       rows = (!GREEDY && q_pos < q_L) ? (ROW_T | ROW_D) : ROW_T;
-    }
-    if (exhausted && q_ep == pub.ep && pub.next >= 0 && q_seq < P.B) {
-      ++q_ep;
-      q_seq = pub.next;
-      q_L = load_len(P, q_seq);
-      q_ph = STATS;
-      q_pos = 0;
-      q_k = 0;
-      continue;
     }
     if (exhausted || rows == 0) {
       sleep_ns(32);
@@ -580,8 +567,10 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R,
     }
   }
   // wait out the copies still in flight into stages nobody will read
-  pub = pub_read(S);
-  for (int j = pub.done ? pub.cons : issued; j < issued; ++j)
+  __threadfence_block();
+  const int cons = *reinterpret_cast<volatile int*>(&S.cons_final);
+  const bool done = unpack_cur(pub_load(&S.pub_cur)).done != 0;
+  for (int j = done ? cons : issued; j < issued; ++j)
     mbar_wait_bounded(&R.full[j % NS], static_cast<uint32_t>(j / NS) & 1u, kWaitBudget);
 }
 
@@ -639,9 +628,10 @@ struct RowAcc {
     mc = -INFINITY;
     s0 = s1 = 0.f;
   }
-  __device__ __forceinline__ void add8(float vm, const float (&z)[8], float c) {
+  // Raise the running max to include vm (NaN sticks), rescaling what was summed so far.
+  __device__ __forceinline__ void rescale(float vm, float c) {
     const float mn = max_nan(m, vm);
-    if (mn != m) {  // a new maximum (or NaN): rescale what was summed so far
+    if (mn != m) {
       const float mcn = __fmul_rn(mn, c);
       const float f = exp2f(mc - mcn);
       s0 *= f;
@@ -649,13 +639,69 @@ struct RowAcc {
       m = mn;
       mc = mcn;
     }
-    if (m > -INFINITY) {
+  }
+  __device__ __forceinline__ void sum8(const float (&z)[8], float c) {
 #pragma unroll
-      for (int k = 0; k < 8; k += 2) {
-        s0 += ex2_fast(fmaf(z[k], c, -mc));
-        s1 += ex2_fast(fmaf(z[k + 1], c, -mc));
+    for (int k = 0; k < 8; k += 2) {
+      s0 += ex2_fast(fmaf(z[k], c, -mc));
+      s1 += ex2_fast(fmaf(z[k + 1], c, -mc));
+    }
+  }
+};
+
+// This thread's vectors of one staged chunk row (vector g = threadIdx.x + j * NC), loaded into
+// registers before any arithmetic; vectors past nvec read as -inf.
+template <typename T, int VPT>
+struct ChunkRow;
+
+template <int VPT>
+struct ChunkRow<uint16_t, VPT> {
+  uint4 v[VPT];
+  __device__ __forceinline__ void load(const uint16_t* row, int nvec) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int g = threadIdx.x + j * NC;
+      v[j] = g < nvec ? reinterpret_cast<const uint4*>(row)[g]
+                      : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+  }
+  __device__ __forceinline__ float vmax() const {  // NaN-propagating
+    uint32_t m = max_nan_bf16x2(max_nan_bf16x2(v[0].x, v[0].y), max_nan_bf16x2(v[0].z, v[0].w));
+#pragma unroll
+    for (int j = 1; j < VPT; ++j)
+      m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(v[j].x, v[j].y),
+                                           max_nan_bf16x2(v[j].z, v[j].w)));
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
+  __device__ __forceinline__ void get(int j, float (&z)[8]) const { Elt<uint16_t>::unpack(v[j], z); }
+};
+
+template <int VPT>
+struct ChunkRow<float, VPT> {
+  float4 v[VPT][2];
+  __device__ __forceinline__ void load(const float* row, int nvec) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int g = threadIdx.x + j * NC;
+      if (g < nvec) {
+        v[j][0] = reinterpret_cast<const float4*>(row)[2 * g];
+        v[j][1] = reinterpret_cast<const float4*>(row)[2 * g + 1];
+      } else {
+        v[j][0] = v[j][1] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
     }
+  }
+  __device__ __forceinline__ float vmax() const {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+      m = max_nan(m, max_nan(max_nan(max_nan(v[j][0].x, v[j][0].y), max_nan(v[j][0].z, v[j][0].w)),
+                             max_nan(max_nan(v[j][1].x, v[j][1].y), max_nan(v[j][1].z, v[j][1].w))));
+    return m;
+  }
+  __device__ __forceinline__ void get(int j, float (&z)[8]) const {
+    z[0] = v[j][0].x; z[1] = v[j][0].y; z[2] = v[j][0].z; z[3] = v[j][0].w;
+    z[4] = v[j][1].x; z[5] = v[j][1].y; z[6] = v[j][1].z; z[7] = v[j][1].w;
   }
 };
 
@@ -959,6 +1005,72 @@ __device__ __forceinline__ int header_ok(const Params& P, const Hdr& h, bool gre
 }
 
 // ------------------------------------------------------------------------------------------
+// longest-draft-first order of the sequences (built once per launch by one CTA)
+// ------------------------------------------------------------------------------------------
+// Stable counting sort of the sequences by draft length, descending (invalid lengths last),
+// into P.perm. The consumer threads of one CTA run it; `cnt` is NW * (kMaxK + 1) ints of
+// scratch shared memory.
+__device__ void build_order(const Params& P, int* cnt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nb = P.K + 1;
+  __shared__ int base[kMaxK + 1], run[kMaxK + 1];
+  if (tid <= kMaxK) {
+    base[tid] = 0;
+    run[tid] = 0;
+  }
+  cbar();
+  for (int b = tid; b < P.B; b += NC) {  // histogram
+    const int L = P.lens ? P.lens[b] : P.K;
+    atomicAdd(&base[(L >= 1 && L <= P.K) ? P.K - L : P.K], 1);
+  }
+  cbar();
+  if (tid == 0) {
+    int acc = 0;
+    for (int k = 0; k < nb; ++k) {
+      const int c = base[k];
+      base[k] = acc;
+      acc += c;
+    }
+  }
+  cbar();
+  for (int b0 = 0; b0 < P.B; b0 += NC) {  // stable scatter, NC sequences at a time
+    const int b = b0 + tid;
+    int bk = -1;
+    if (b < P.B) {
+      const int L = P.lens ? P.lens[b] : P.K;
+      bk = (L >= 1 && L <= P.K) ? P.K - L : P.K;
+    }
+    unsigned my_mask = 0;
+    for (int k = 0; k < nb; ++k) {
+      const unsigned m = __ballot_sync(FULL, bk == k);
+      if (lane == 0) cnt[warp * (kMaxK + 1) + k] = __popc(m);
+      if (bk == k) my_mask = m;
+    }
+    cbar();
+    if (bk >= 0) {
+      int pos = base[bk] + run[bk] + __popc(my_mask & ((1u << lane) - 1u));
+      for (int w = 0; w < warp; ++w) pos += cnt[w * (kMaxK + 1) + bk];
+      P.perm[pos] = b;
+    }
+    cbar();
+    if (tid < nb) {
+      int t = 0;
+      for (int w = 0; w < NW; ++w) t += cnt[w * (kMaxK + 1) + tid];
+      run[tid] += t;
+    }
+    cbar();
+  }
+  __threadfence();
+  cbar();
+}
+
+// The sequence at place q of the launch's order.
+__device__ __forceinline__ int seq_at(const Params& P, int q) {
+  if (q >= P.B) return P.B;
+  return P.lpt ? __ldcg(P.perm + q) : q;
+}
+
+// ------------------------------------------------------------------------------------------
 // the kernel: consumer warps 0..7 verify, warp 8 produces
 // ------------------------------------------------------------------------------------------
 template <typename T, bool GREEDY, bool TOP8>
@@ -997,35 +1109,55 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     fence_mbar_init();
     S.cur = 0;
     S.n_hdr_wait = 0;
-    S.ver = 0;
-    fetch_header(P, S, 0, cid, GREEDY);
+    S.cons_final = 0;
+  }
+  // the launch's sequence order: cluster 0 / rank 0 builds it, everyone else waits for it
+  if (P.lpt) {
+    if (cid == 0 && rank == 0 && tid < NC) {
+      build_order(P, reinterpret_cast<int*>(dyn));
+      if (tid == 0) {
+        __threadfence();
+        atomicExch(&P.ws->perm_ready, 1u);
+      }
+    }
+    if (tid == 0) {
+      const long long t0 = clock64();
+      while (atomicAdd(&P.ws->perm_ready, 0u) == 0u) {
+        if (clock64() - t0 > kWaitBudget) {
+          atomicOr(&P.ws->error, 1u);
+          break;
+        }
+        sleep_ns(64);
+      }
+      __threadfence();
+    }
+  }
+  if (tid == 0) {
+    const int seq0 = seq_at(P, cid);
+    S.seq0 = seq0;
+    fetch_header(P, S, 0, seq0, GREEDY);
     cp_async_wait_all();
     S.hdr[0].ok = header_ok(P, S.hdr[0], GREEDY);
-    Pub v;
-    v.ep = 0;
-    v.seq = cid;
-    v.stop = S.hdr[0].ok ? -1 : -2;
-    v.next = -1;
-    v.done = 0;
-    v.cons = 0;
-    pub_write(S, v);
+    pub_store(&S.pub_cur, pack_cur(seq0, 0, S.hdr[0].ok ? -1 : -2, 0));
+    pub_store(&S.pub_next, 0ull);
   }
   __syncthreads();
   cluster_sync();  // every CTA of the cluster is running before any shared-memory exchange
 
   if (warp == NW) {
-    if ((tid & 31) == 0) producer<T, GREEDY>(P, S, R, cid);
+    if ((tid & 31) == 0) producer<T, GREEDY>(P, S, R);
     __syncwarp();
   } else {
     uint32_t xround = 0;
     int cons = 0;
     bool late = false;
     bool aborted = false;
-    int seq = cid;
+    int seq = S.seq0;
+    int ep = 0;
     while (seq < P.B) {
       int next_local = 0;
       if (rank == 0 && tid == 0)
-        next_local = static_cast<int>(atomicAdd(&P.ws->next, 1u)) + P.n_clusters;
+        next_local = seq_at(P, static_cast<int>(atomicAdd(&P.ws->next, 1u)) + P.n_clusters);
       if (tid == 0 && P.fmax + P.debug_all > 0) {
         for (int i = 0; i < kMaxK; ++i) {
           for (int f = 0; f < 8; ++f) S.topf[i][f] = -1;
@@ -1070,37 +1202,68 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
             if (s < 0) break;
             const int n = R.chunk_len(k);
             const int nvec = (n + 7) >> 3;
-            const T* rt = R.row(s, 0);
-            const T* rd = R.row(s, GREEDY ? 0 : 1);
-            for (int g = tid; g < nvec; g += NC) {
-              float z[8];
-              if (ld_t) {
-                const float vm = Elt<T>::vmax8(rt, g, z);
-                if constexpr (GREEDY) {
-                  if (isnan(vm)) {
-                    at.m = NAN;
-                  } else if (vm > at.m) {
-                    at.m = vm;
-                    int e = 7;
+            constexpr int VPT = RingT::CH / 8 / NC;
+            static_assert(VPT >= 1 && RingT::CH == VPT * 8 * NC, "whole vectors per thread");
+            if (ld_t) {
+              ChunkRow<T, VPT> cr;
+              cr.load(R.row(s, 0), nvec);
+              const float vm = cr.vmax();
+              if constexpr (GREEDY) {
+                if (isnan(vm)) {
+                  at.m = NAN;
+                } else if (vm > at.m) {  // first index of the new maximum in this thread's elements
+                  at.m = vm;
+                  int e = 0x7FFFFFFF;
+#pragma unroll
+                  for (int j = VPT - 1; j >= 0; --j) {
+                    float z[8];
+                    cr.get(j, z);
 #pragma unroll
                     for (int kk = 7; kk >= 0; --kk)
-                      if (z[kk] == vm) e = kk;
-                    garg = R.v0 + k * RingT::CH + 8 * g + e;
+                      if (z[kk] == vm) e = 8 * (tid + j * NC) + kk;
                   }
-                } else {
-                  at.add8(vm, z, c);
+                  garg = R.v0 + k * RingT::CH + e;
+                }
+              } else {
+                at.rescale(vm, c);
+                if (at.m > -INFINITY) {
+#pragma unroll
+                  for (int j = 0; j < VPT; ++j) {
+                    float z[8];
+                    cr.get(j, z);
+                    at.sum8(z, c);
+                  }
                 }
               }
-              if (!GREEDY && ld_d) {
-                const float vm = Elt<T>::vmax8(rd, g, z);
-                if (st_d) ad.add8(vm, z, c);
-                else ad.m = max_nan(ad.m, vm);
-                if (TOP8 && tk) {
-                  const int eb = k * RingT::CH + 8 * g;
+            }
+            if (!GREEDY && ld_d) {
+              ChunkRow<T, VPT> cr;
+              cr.load(R.row(s, 1), nvec);
+              const float vm = cr.vmax();
+              if (st_d) {
+                ad.rescale(vm, c);
+                if (ad.m > -INFINITY) {
+#pragma unroll
+                  for (int j = 0; j < VPT; ++j) {
+                    float z[8];
+                    cr.get(j, z);
+                    ad.sum8(z, c);
+                  }
+                }
+              } else {
+                ad.m = max_nan(ad.m, vm);
+              }
+              if (TOP8 && tk) {
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                  float z[8];
+                  cr.get(j, z);
+                  const int eb = 8 * (tid + j * NC);
 #pragma unroll
                   for (int kk = 0; kk < 8; ++kk)
-                    if (8 * g + kk < n)
-                      top8_insert(keys, thr, z[kk], static_cast<uint32_t>(R.v0 + eb + kk));
+                    if (eb + kk < n)
+                      top8_insert(keys, thr, z[kk],
+                                  static_cast<uint32_t>(R.v0 + k * RingT::CH + eb + kk));
                 }
               }
             }
@@ -1155,9 +1318,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
               fetch_header(P, S, S.cur ^ 1, next, GREEDY);
               S.n_hdr_wait = 1;
             }
-            Pub v = pub_local(S);
-            v.next = next;
-            pub_write(S, v);
+            pub_store(&S.pub_next, pack_next(next, ep));
           }
         }
         if (!ld_t && !ld_d) break;  // header was invalid: the exchange only carried `next`
@@ -1176,11 +1337,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           if (stop != -1) {
             decided = true;
             a = stop;
-            if (tid == 0) {
-              Pub v = pub_local(S);
-              v.stop = stop;
-              pub_write(S, v);
-            }
+            if (tid == 0) pub_store(&S.pub_cur, pack_cur(seq, ep, stop, 0));
           }
           if (invalid) break;
           if (!GREEDY && stop >= 0) {
@@ -1195,11 +1352,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           }
         } else if (tk && P.fmax > 0 && S.bad_d) {
           invalid = true;  // a draft row the top-F output needs holds no distribution
-          if (tid == 0) {
-            Pub v = pub_local(S);
-            v.stop = -2;
-            pub_write(S, v);
-          }
+          if (tid == 0) pub_store(&S.pub_cur, pack_cur(seq, ep, -2, 0));
           break;
         }
       }
@@ -1243,22 +1396,18 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
         const int nx = S.cur ^ 1;
         if (next < P.B) S.hdr[nx].ok = header_ok(P, S.hdr[nx], GREEDY);
         S.cur = nx;
-        Pub v = pub_local(S);
-        v.ep += 1;
-        v.seq = next;
-        v.stop = (next < P.B && S.hdr[nx].ok) ? -1 : -2;
-        v.next = -1;
-        pub_write(S, v);
+        pub_store(&S.pub_cur, pack_cur(next, ep + 1, (next < P.B && S.hdr[nx].ok) ? -1 : -2, 0));
       }
       cbar();
       seq = next;
+      ++ep;
     }
     if (tid == 0) {
       cp_async_wait_all();
-      Pub v = pub_local(S);
-      v.done = 1;
-      v.cons = cons;
-      pub_write(S, v);
+      *reinterpret_cast<volatile int*>(&S.cons_final) = cons;
+      __threadfence_block();
+      const Pub v = unpack_cur(pub_load(&S.pub_cur));
+      pub_store(&S.pub_cur, pack_cur(v.seq, v.ep, v.stop, 1));
     }
   }
   __syncthreads();
@@ -1268,6 +1417,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     const unsigned old = atomicAdd(&P.ws->done, 1u);
     if (old == static_cast<unsigned>(P.n_clusters) - 1u) {
       atomicExch(&P.ws->next, 0u);
+      atomicExch(&P.ws->perm_ready, 0u);
       atomicExch(&P.ws->done, 0u);
     }
   }

@@ -114,6 +114,13 @@ def test_many_sequences_dynamic_queue():
     assert np.array_equal(g1["tokens"], g2["tokens"])
 
 
+def test_batch_above_ordering_threshold():
+    """Batches above 4096 sequences keep the natural order (no longest-first permutation)."""
+    w = W.small_variant(W.WORKLOADS[5], B=4200, V=64).replace(K=3)
+    d = W.make_inputs(w)
+    check(d, w, run_gpu(d, w, debug=False), seqs=range(0, 4200, 7))
+
+
 def test_greedy_without_draft_logits_and_lens():
     w = W.small_variant(W.WORKLOADS[2], B=9)
     d = W.make_inputs(w)
@@ -198,7 +205,7 @@ def test_workspace_and_host_entry_points():
     acc = torch.empty(w.B, dtype=torch.int32, device="cuda")
     toks = torch.empty(w.B, w.K + 1, dtype=torch.int32, device="cuda")
     topf = torch.empty(w.B, w.K, 8, dtype=torch.int32, device="cuda")
-    ws = torch.zeros(64, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(api.workspace_bytes(w.B) // 4, dtype=torch.int32, device="cuda")
     for _ in range(2):
         api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, acc, toks, topf,
                         bias_k=w.bias_k, fanout=w.fanout, workspace=ws)

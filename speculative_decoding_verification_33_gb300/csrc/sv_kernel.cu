@@ -70,8 +70,28 @@ struct Hdr {
   float u[kMaxK + 1];
 };
 
-struct StageDesc {
-  int seq, pos, k, rows;  // rows: ROW_T | ROW_D; pos < 0 marks a chunk of the draw pass
+// What a stage holds, packed in one 64-bit word: sequence (bits 0..31), position + 64 (bits
+// 32..39; positions below 0 mark chunks of the draw pass), chunk (bits 40..55), rows
+// (ROW_T | ROW_D, bits 56..57).
+__device__ __forceinline__ unsigned long long stage_tag(int seq, int pos, int k) {
+  return static_cast<unsigned long long>(static_cast<uint32_t>(seq)) |
+         (static_cast<unsigned long long>((pos + 64) & 0xFF) << 32) |
+         (static_cast<unsigned long long>(k & 0xFFFF) << 40);
+}
+constexpr unsigned long long kTagMask = (1ull << 56) - 1ull;
+__device__ __forceinline__ int tag_rows(unsigned long long t) { return static_cast<int>(t >> 56); }
+
+// Position in the ring: running count, stage index and phase parity, advanced together.
+struct Cursor {
+  int n = 0, s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void advance() {
+    ++n;
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
 };
 
 // What the consumers tell the producer warp: two 64-bit shared-memory words, each written and
@@ -248,9 +268,16 @@ __device__ __forceinline__ int key_id(unsigned long long k) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
 }
 
-// Integer of 2^-44 units below s (s >= 0, s <= 8).
+// Integer of 2^-44 units below s (0 <= s < 16), from the float's bits: s = m * 2^(e-150)
+// with m the 24-bit significand, so s * 2^44 = m * 2^(e-106), truncated.
 __device__ __forceinline__ unsigned long long qfix(float s) {
-  return __float2ull_rz(__fmul_rn(s, 17592186044416.0f));
+  const uint32_t b = __float_as_uint(s);
+  const int e = static_cast<int>(b >> 23);  // sign is 0 for s >= 0
+  const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;
+  const int sh = e - 106;
+  if (e == 0) return 0ull;  // zero or subnormal: far below 2^-44
+  if (sh >= 0) return m << sh;
+  return sh > -64 ? (m >> -sh) : 0ull;
 }
 
 // floor(u * W) for u in [0, 1) given as a float and W < 2^63, exactly.
@@ -413,7 +440,7 @@ struct Ring {
   unsigned char* base;
   uint64_t* full;
   uint64_t* empty;
-  StageDesc* desc;
+  unsigned long long* desc;  // stage_tag | rows << 56 of what each stage holds
   int nchunk;  // chunks per row of this CTA's slice
   int nv;      // elements of this CTA's slice
   int v0;      // first element of the slice
@@ -438,21 +465,24 @@ __device__ __forceinline__ int load_len(const Params& P, int seq) {
   return (L >= 1 && L <= P.K) ? L : -1;
 }
 
-// One chunk of (seq, pos) into stage s; `tag` is the position recorded in the descriptor
-// (negative for the draw pass).
+// One chunk into stage s: `src_t` / `src_d` point at this CTA's slice of the two rows (bytes),
+// `tag` is the stage tag recorded for the consumers.
 template <typename T, bool GREEDY>
-__device__ void issue_chunk(const Params& P, const Ring<T, GREEDY>& R, int s, int seq, int pos,
-                            int tag, int k, int rows) {
-  const int e0 = k * R.CH;
-  const int n = R.chunk_len(k);
-  StageDesc d;
-  d.seq = seq;
-  d.pos = tag;
-  d.k = k;
-  d.rows = rows;
-  R.desc[s] = d;
+__device__ __forceinline__ void issue_chunk(const Params& P, const Ring<T, GREEDY>& R, int s,
+                                            const char* src_t, const char* src_d,
+                                            unsigned long long tag, int k, int rows) {
+  R.desc[s] = tag | (static_cast<unsigned long long>(rows) << 56);
   if (!P.use_bulk) {
     mbar_arrive(&R.full[s]);  // the consumers copy this chunk themselves
+    return;
+  }
+  const int n = R.chunk_len(k);
+  const size_t off = static_cast<size_t>(k) * kStageRowBytes;
+  if (n == R.CH) {  // a whole chunk: one copy per row, nothing else to fill
+    const uint32_t nrows = (rows & ROW_T ? 1u : 0u) + (rows & ROW_D ? 1u : 0u);
+    mbar_arrive_expect_tx(&R.full[s], nrows * kStageRowBytes);
+    if (rows & ROW_T) bulk_g2s(R.row(s, 0), src_t + off, kStageRowBytes, &R.full[s]);
+    if (!GREEDY && (rows & ROW_D)) bulk_g2s(R.row(s, 1), src_d + off, kStageRowBytes, &R.full[s]);
     return;
   }
   constexpr int kPer16 = 16 / static_cast<int>(sizeof(T));
@@ -461,18 +491,17 @@ __device__ void issue_chunk(const Params& P, const Ring<T, GREEDY>& R, int s, in
   uint32_t bytes = 0;
   for (int r = 0; r < Ring<T, GREEDY>::kRows; ++r) {
     if (!(rows & (1 << r))) continue;
-    const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + e0;
+    const T* src = reinterpret_cast<const T*>((r ? src_d : src_t) + off);
     T* dst = R.row(s, r);
     for (int e = nb; e < npad; ++e) dst[e] = e < n ? src[e] : Elt<T>::neg_inf();
     bytes += static_cast<uint32_t>(nb * sizeof(T));
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_arrive_expect_tx(&R.full[s], bytes);
   if (nb > 0) {
     for (int r = 0; r < Ring<T, GREEDY>::kRows; ++r) {
       if (!(rows & (1 << r))) continue;
-      const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + e0;
-      bulk_g2s(R.row(s, r), src, static_cast<uint32_t>(nb * sizeof(T)), &R.full[s]);
+      bulk_g2s(R.row(s, r), (r ? src_d : src_t) + off, static_cast<uint32_t>(nb * sizeof(T)),
+               &R.full[s]);
     }
   }
 }
@@ -487,7 +516,10 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
   enum { STATS = 0, DRAW = 1, POST = 2 };
   int q_ep = 0, q_seq = S.seq0, q_L = load_len(P, S.seq0);
   int q_ph = STATS, q_pos = 0, q_k = 0;
-  int issued = 0;
+  Cursor cur;
+  int base_seq = -1, base_pos = -1;
+  const char* src_t = nullptr;
+  const char* src_d = nullptr;
   long long idle0 = clock64();
   while (true) {
     const Pub pub = unpack_cur(pub_load(&S.pub_cur));
@@ -550,15 +582,24 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
       rows = (!GREEDY && q_pos < q_L) ? (ROW_T | ROW_D) : ROW_T;
     }
     if (exhausted || rows == 0) {
-      sleep_ns(32);
+      sleep_ns(128);
       continue;
     }
-    const int s = issued % NS;
-    if (issued >= NS && !mbar_test(&R.empty[s], static_cast<uint32_t>((issued / NS) - 1) & 1u)) {
-      continue;  // the oldest stage is still being read
+    if (q_k == 0 || base_seq != q_seq || base_pos != q_pos) {  // row bases of this position
+      base_seq = q_seq;
+      base_pos = q_pos;
+      src_t = static_cast<const char*>(row_ptr(P, false, q_seq, q_pos, sizeof(T))) +
+              static_cast<size_t>(R.v0) * sizeof(T);
+      src_d = GREEDY || q_pos >= P.K ? src_t
+                                     : static_cast<const char*>(row_ptr(P, true, q_seq, q_pos, sizeof(T))) +
+                                           static_cast<size_t>(R.v0) * sizeof(T);
     }
-    issue_chunk<T, GREEDY>(P, R, s, q_seq, q_pos, q_ph == DRAW ? -1 - q_pos : q_pos, q_k, rows);
-    ++issued;
+    if (cur.n >= NS && !mbar_try_wait_hint(&R.empty[cur.s], cur.ph ^ 1u, 1000)) {
+      continue;  // the oldest stage is still being read (the wait above slept on it)
+    }
+    issue_chunk<T, GREEDY>(P, R, cur.s, src_t, src_d,
+                           stage_tag(q_seq, q_ph == DRAW ? -1 - q_pos : q_pos, q_k), q_k, rows);
+    cur.advance();
     idle0 = clock64();
     if (++q_k >= R.nchunk) {
       q_k = 0;
@@ -570,31 +611,29 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
   __threadfence_block();
   const int cons = *reinterpret_cast<volatile int*>(&S.cons_final);
   const bool done = unpack_cur(pub_load(&S.pub_cur)).done != 0;
-  for (int j = done ? cons : issued; j < issued; ++j)
+  for (int j = done ? cons : cur.n; j < cur.n; ++j)
     mbar_wait_bounded(&R.full[j % NS], static_cast<uint32_t>(j / NS) & 1u, kWaitBudget);
 }
 
-__device__ __forceinline__ void release_stage(uint64_t* empty, int s, int& cons) {
+__device__ __forceinline__ void release_stage(uint64_t* empty, Cursor& cons) {
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
-  ++cons;
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[cons.s]);
+  cons.advance();
 }
 
-// Wait for the stage holding chunk k of (seq, tag), handing back stale speculative chunks on
+// Wait for the stage holding chunk k of (seq, pos), handing back stale speculative chunks on
 // the way. Returns the stage, or -1 once a wait has given up (`late`).
 template <typename T, bool GREEDY>
-__device__ int acquire(const Ring<T, GREEDY>& R, int seq, int tag, int k, int& cons,
-                       bool& late) {
+__device__ __forceinline__ int acquire(const Ring<T, GREEDY>& R, int seq, int pos, int k,
+                                       Cursor& cons, bool& late) {
+  const unsigned long long want = stage_tag(seq, pos, k);
   while (!late) {
-    const int s = cons % NS;
-    const uint32_t ph = static_cast<uint32_t>(cons / NS) & 1u;
-    if (!mbar_wait_bounded(&R.full[s], ph, kWaitBudget)) {
+    if (!mbar_wait_bounded(&R.full[cons.s], cons.ph, kWaitBudget)) {
       late = true;
       break;
     }
-    const StageDesc d = R.desc[s];
-    if (d.seq == seq && d.pos == tag && d.k == k) return s;
-    release_stage(R.empty, s, cons);
+    if ((R.desc[cons.s] & kTagMask) == want) return cons.s;
+    release_stage(R.empty, cons);
   }
   return -1;
 }
@@ -605,10 +644,10 @@ template <typename T, bool GREEDY>
 __device__ int fill_unaligned(const Params& P, const Ring<T, GREEDY>& R, int s, int seq,
                               int pos, int k, bool& late) {
   if (s >= 0) {
-    const StageDesc d = R.desc[s];
+    const int rows = tag_rows(R.desc[s]);
     const int n = R.chunk_len(k), npad = (n + 7) & ~7;
     for (int r = 0; r < Ring<T, GREEDY>::kRows; ++r) {
-      if (!(d.rows & (1 << r))) continue;
+      if (!(rows & (1 << r))) continue;
       const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + k * R.CH;
       T* dst = R.row(s, r);
       for (int e = threadIdx.x; e < npad; e += NC) dst[e] = e < n ? src[e] : Elt<T>::neg_inf();
@@ -621,12 +660,16 @@ __device__ int fill_unaligned(const Params& P, const Ring<T, GREEDY>& R, int s, 
 // ------------------------------------------------------------------------------------------
 // per-thread running statistics of one row
 // ------------------------------------------------------------------------------------------
+// Running max and sum of 2^(z c - m c) of one row, for one thread. The sum is kept in two packed
+// fp32 pairs and built with the packed fp32 instructions (one fma for the exponent arguments of
+// two elements, one add to accumulate two exponentials).
 struct RowAcc {
-  float m, mc, s0, s1;  // running max, its product with c, and two partial sums of 2^(zc-mc)
+  float m, mc;      // running max and its product with c (rounded)
+  float2 s0, s1;    // four partial sums of 2^(z c - mc)
   __device__ __forceinline__ void init() {
     m = -INFINITY;
     mc = -INFINITY;
-    s0 = s1 = 0.f;
+    s0 = s1 = make_float2(0.f, 0.f);
   }
   // Raise the running max to include vm (NaN sticks), rescaling what was summed so far.
   __device__ __forceinline__ void rescale(float vm, float c) {
@@ -634,19 +677,23 @@ struct RowAcc {
     if (mn != m) {
       const float mcn = __fmul_rn(mn, c);
       const float f = exp2f(mc - mcn);
-      s0 *= f;
-      s1 *= f;
+      s0 = __fmul2_rn(s0, make_float2(f, f));
+      s1 = __fmul2_rn(s1, make_float2(f, f));
       m = mn;
       mc = mcn;
     }
   }
   __device__ __forceinline__ void sum8(const float (&z)[8], float c) {
+    const float2 c2 = make_float2(c, c), n2 = make_float2(-mc, -mc);
 #pragma unroll
-    for (int k = 0; k < 8; k += 2) {
-      s0 += ex2_fast(fmaf(z[k], c, -mc));
-      s1 += ex2_fast(fmaf(z[k + 1], c, -mc));
+    for (int k = 0; k < 8; k += 4) {
+      const float2 a = __ffma2_rn(make_float2(z[k], z[k + 1]), c2, n2);
+      const float2 b = __ffma2_rn(make_float2(z[k + 2], z[k + 3]), c2, n2);
+      s0 = __fadd2_rn(s0, make_float2(ex2_fast(a.x), ex2_fast(a.y)));
+      s1 = __fadd2_rn(s1, make_float2(ex2_fast(b.x), ex2_fast(b.y)));
     }
   }
+  __device__ __forceinline__ float total() const { return (s0.x + s0.y) + (s1.x + s1.y); }
 };
 
 // This thread's vectors of one staged chunk row (vector g = threadIdx.x + j * NC), loaded into
@@ -724,13 +771,15 @@ __device__ __forceinline__ void top8_insert(unsigned long long (&keys)[8], float
 // residual / bonus draw
 // ------------------------------------------------------------------------------------------
 struct WeightConsts {
-  float c, mc_t, mc_d, r_t, r_d, r_dS;
+  float c, mc_t, mc_d, rho, rho_S;
   int nloc;     // ids of the bias set that fall in this CTA's slice
   int loc[8];   // their slice-local indices
 };
 
-// Weights of the 8 elements at slice offset e0: bonus -> 2^(z_t c - mc_t); residual ->
-// max(p - q', 0) with p and q' rebuilt from the logits. Returns their sequential sum.
+// Weights of the 8 elements at slice offset e0, up to one positive factor per draw (the inverse
+// CDF does not depend on it): bonus -> e_t = 2^(z_t c - mc_t); residual ->
+// max(e_t - rho e_d, 0) with e_d = 2^(z_d c - mc_d) and rho = q' scale / p scale, which is
+// max(p - q', 0) / (p scale). Returns their sequential sum.
 template <bool BONUS>
 __device__ __forceinline__ float weights8(const float (&zt)[8], const float (&zd)[8], int e0,
                                           const WeightConsts& W, float (&w)[8]) {
@@ -738,20 +787,26 @@ __device__ __forceinline__ float weights8(const float (&zt)[8], const float (&zd
 #pragma unroll
     for (int k = 0; k < 8; ++k) w[k] = ex2_fast(fmaf(zt[k], W.c, -W.mc_t));
   } else {
-    float rdk[8];
+    float rk[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) rdk[k] = W.r_d;
+    for (int k = 0; k < 8; ++k) rk[k] = W.rho;
     for (int j = 0; j < W.nloc; ++j) {
       const int e = W.loc[j] - e0;
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (k == e) rdk[k] = W.r_dS;
+        if (k == e) rk[k] = W.rho_S;
     }
+    const float2 c2 = make_float2(W.c, W.c), n2 = make_float2(-W.mc_t, -W.mc_d);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float et = ex2_fast(fmaf(zt[k], W.c, -W.mc_t));
-      const float ed = ex2_fast(fmaf(zd[k], W.c, -W.mc_d));
-      w[k] = fmaxf(fmaf(et, W.r_t, -__fmul_rn(ed, rdk[k])), 0.f);
+    for (int k = 0; k < 8; k += 2) {
+      // exponent arguments of the target and draft element together, then two weights together
+      const float2 a0 = __ffma2_rn(make_float2(zt[k], zd[k]), c2, n2);
+      const float2 a1 = __ffma2_rn(make_float2(zt[k + 1], zd[k + 1]), c2, n2);
+      const float2 wv = __ffma2_rn(make_float2(-ex2_fast(a0.y), -ex2_fast(a1.y)),
+                                   make_float2(rk[k], rk[k + 1]),
+                                   make_float2(ex2_fast(a0.x), ex2_fast(a1.x)));
+      w[k] = fmaxf(wv.x, 0.f);
+      w[k + 1] = fmaxf(wv.y, 0.f);
     }
   }
   float s = w[0];
@@ -767,7 +822,7 @@ __device__ __forceinline__ float weights8(const float (&zt)[8], const float (&zd
 template <typename T, bool GREEDY, bool BONUS>
 __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
                            uint64_t* xbar, uint32_t& xround, uint32_t rank, uint32_t C,
-                           const Ring<T, GREEDY>& R, int seq, int a, float* vmass, int& cons,
+                           const Ring<T, GREEDY>& R, int seq, int a, float* vmass, Cursor& cons,
                            bool& late) {
   const int tid = threadIdx.x;
   const int v0 = R.v0, nv = R.nv;
@@ -777,13 +832,19 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
   const T* gd = BONUS ? gt : static_cast<const T*>(row_ptr(P, true, seq, a, sizeof(T))) + v0;
   WeightConsts W;
   W.c = P.c;
+  // p(v) = 2^(z_t c - mc_t) * (1 - err_t ln 2) / S_t and q'(v) = f(v) 2^(z_d c - mc_d) *
+  // (1 - err_d ln 2) / (S_d N), with err the rounding of M c; weights are taken relative to p's
+  // scale, so rho = q' scale / p scale.
   W.mc_t = __fmul_rn(S.M_t, P.c);
-  const float err_t = fmaf(S.M_t, P.c, -W.mc_t);
-  W.r_t = BONUS ? 1.f : fmaf(-err_t, kLn2, 1.f) / S.S_t;  // p(v) = 2^(z c - mc_t) * r_t
   W.mc_d = __fmul_rn(S.M_d, P.c);
-  const float err_d = fmaf(S.M_d, P.c, -W.mc_d);
-  W.r_d = BONUS ? 0.f : fmaf(-err_d, kLn2, 1.f) / (S.S_d * S.N);
-  W.r_dS = W.r_d * P.beta;
+  if (BONUS) {
+    W.rho = W.rho_S = 0.f;
+  } else {
+    const float ft = fmaf(-fmaf(S.M_t, P.c, -W.mc_t), kLn2, 1.f);
+    const float fd = fmaf(-fmaf(S.M_d, P.c, -W.mc_d), kLn2, 1.f);
+    W.rho = (fd * S.S_t) / (ft * (S.S_d * S.N));
+    W.rho_S = W.rho * P.beta;
+  }
   W.nloc = 0;
   for (int j = 0; j < S.nS; ++j) {
     const int e = S.S_ids[j] - v0;
@@ -806,14 +867,14 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
       vmass[e0 >> 3] = sm;
       acc += qfix(sm);
     }
-    release_stage(R.empty, s, cons);
+    release_stage(R.empty, cons);
   }
   late = cbar_or(late);
   unsigned long long Wtot = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
     if (attempt == 1) {  // zero residual mass: draw from p at this position instead
-      W.r_d = 0.f;
-      W.r_dS = 0.f;
+      W.rho = 0.f;
+      W.rho_S = 0.f;
       W.mc_d = INFINITY;  // the draft term becomes 2^-inf = 0 exactly
       acc = 0;
       for (int g = tid; g < nvec_all; g += NC) {
@@ -865,7 +926,7 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
         if (pre + q > tl) {
           float zt[8], zd[8], w[8];
           row8<T>(gt, 8 * g, nv, aligned, zt);
-          if (!BONUS && W.r_d != 0.f) row8<T>(gd, 8 * g, nv, aligned, zd);
+          if (!BONUS && W.rho != 0.f) row8<T>(gd, 8 * g, nv, aligned, zd);
           else {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) zd[kk] = zt[kk];
@@ -1079,7 +1140,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
   __shared__ CtaState S;
   __shared__ Xchg X[2][kMaxCluster];
   __shared__ uint64_t full_bar[NS], empty_bar[NS], xbar[2];
-  __shared__ StageDesc sdesc[NS];
+  __shared__ unsigned long long sdesc[NS];
 
   using RingT = Ring<T, GREEDY>;
   const int tid = threadIdx.x;
@@ -1149,7 +1210,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     __syncwarp();
   } else {
     uint32_t xround = 0;
-    int cons = 0;
+    Cursor cons;
     bool late = false;
     bool aborted = false;
     int seq = S.seq0;
@@ -1267,7 +1328,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
                 }
               }
             }
-            release_stage(R.empty, s, cons);
+            release_stage(R.empty, cons);
           }
         }
         // ---- this CTA's partials ----
@@ -1281,8 +1342,8 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           const bool sum_t = st_t && !row_bad(mm.x);
           const bool sum_d = st_d && !row_bad(mm.y);
           const float mct = __fmul_rn(mm.x, c), mcd = __fmul_rn(mm.y, c);
-          const float pt = (sum_t && at.m > -INFINITY) ? (at.s0 + at.s1) * exp2f(at.mc - mct) : 0.f;
-          const float pd = (sum_d && ad.m > -INFINITY) ? (ad.s0 + ad.s1) * exp2f(ad.mc - mcd) : 0.f;
+          const float pt = (sum_t && at.m > -INFINITY) ? at.total() * exp2f(at.mc - mct) : 0.f;
+          const float pd = (sum_d && ad.m > -INFINITY) ? ad.total() * exp2f(ad.mc - mcd) : 0.f;
           ss = block_sum2(pt, pd, S);
           // the sums are relative to m*c rounded; fold the rounding back in
           if (sum_t) ss.x *= fmaf(-fmaf(mm.x, c, -mct), kLn2, 1.f);
@@ -1404,7 +1465,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     }
     if (tid == 0) {
       cp_async_wait_all();
-      *reinterpret_cast<volatile int*>(&S.cons_final) = cons;
+      *reinterpret_cast<volatile int*>(&S.cons_final) = cons.n;
       __threadfence_block();
       const Pub v = unpack_cur(pub_load(&S.pub_cur));
       pub_store(&S.pub_cur, pack_cur(v.seq, v.ep, v.stop, 1));

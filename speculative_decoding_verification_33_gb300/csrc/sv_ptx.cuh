@@ -64,24 +64,48 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Suspend-time hint of the waits below, in nanoseconds: a waiting thread sleeps in hardware
+// until the phase completes or the hint runs out, instead of spinning.
+constexpr uint32_t kSuspendNs = 20000;
+constexpr uint32_t kBackoffNs = 64;  // sleep between unsuccessful probes of a long wait
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after `budget` clock cycles.
+// One wait with an explicit suspend-time hint (nanoseconds).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void sleep_ns(uint32_t ns) {
+  asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after `budget` clock cycles. Between
+// unsuccessful probes the thread sleeps briefly, so a long wait costs few issued instructions.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   long long budget) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
+    sleep_ns(kBackoffNs);
     if (mbar_try_wait(bar, parity)) return true;
     if (clock64() - t0 > budget) return false;
   }
@@ -141,10 +165,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -154,6 +178,7 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
+    sleep_ns(kBackoffNs);
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (clock64() - t0 > budget) return false;
   }
@@ -185,10 +210,6 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
       : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
       : "memory");
   return r != 0;
-}
-
-__device__ __forceinline__ void sleep_ns(uint32_t ns) {
-  asm volatile("nanosleep.u32 %0;" ::"r"(ns));
 }
 
 __device__ __forceinline__ float max_nan(float a, float b) {

@@ -136,6 +136,28 @@ sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
                          void* stream);
 
 /*
+ * spec_verify for callers that cannot allocate device memory. This entry point has no
+ * counterpart in the method; it exists for the integration. Code that runs inside CUDA graph
+ * capture, under an allocator that forbids cudaMalloc (a serving loop that reserved all device
+ * memory up front, or a runtime whose allocations go through its own pool), or on a path where
+ * a cudaMalloc would synchronise the device cannot let the library create its workspace. This
+ * variant allocates nothing: its workspace is a fixed array inside the library's device code
+ * (about 256 KB on every GPU that loads the library, held until the process exits), sized for
+ * at most 65536 sequences; a larger B returns SV_ERR_UNSUPPORTED. Inputs and outputs are the
+ * caller's device buffers, exactly as for spec_verify, and the results are identical.
+ * The first call on a device (with that device current) looks the array up with
+ * cudaGetSymbolAddress; make that first call before any stream capture. Each call clears the
+ * array's counters with an asynchronous memset on `stream`, then launches. Every call shares
+ * the one array, so calls that may overlap on the GPU (different streams, or different host
+ * threads) race and must not be issued.
+ */
+sv_status spec_verify_noalloc(const sv_problem* prob, const void* target_logits,
+                              const void* draft_logits, const int32_t* draft_tokens,
+                              const int32_t* draft_lens, const float* uniforms,
+                              float temperature, float beta, int mode, int32_t* out_accept_len,
+                              int32_t* out_tokens, int32_t* out_residual_topF, void* stream);
+
+/*
  * spec_verify plus per-position diagnostics, for parity checks. It reads every row a sequence
  * has (target rows 0..L_b, draft rows 0..L_b-1), not only the needed ones, and fills
  *   out_lse_t [B][K+1]  log-normaliser of z_t/T (natural log),

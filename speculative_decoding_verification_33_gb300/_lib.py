@@ -18,7 +18,7 @@ SV_MODE_GREEDY, SV_MODE_STOCHASTIC = 0, 1
 # every entry point the header declares (checked by the tests against include/*.h)
 EXPORTS = ("spec_verify", "spec_verify_workspace_bytes", "spec_verify_ws", "spec_verify_debug",
            "spec_verify_host", "spec_verify_device_error", "spec_verify_status_string",
-           "spec_verify_plan",
+           "spec_verify_plan", "spec_verify_noalloc",
            "sv_hbm_read_probe")
 
 
@@ -58,6 +58,7 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.spec_verify_ws.argtypes = _COMMON + [_P, _SZ, _P]
         lib.spec_verify_debug.argtypes = _COMMON + [_P, _P, _P, _P, _P]
         lib.spec_verify_host.argtypes = _COMMON + [_P]
+        lib.spec_verify_noalloc.argtypes = _COMMON + [_P]
         lib.spec_verify_workspace_bytes.argtypes = [_PROB]
         lib.spec_verify_workspace_bytes.restype = _SZ
         lib.spec_verify_device_error.argtypes = [_P]

@@ -74,12 +74,12 @@ def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
                 out_residual_topF: Optional[torch.Tensor] = None, stream=None, *,
                 bias_k: int = 0, fanout: Optional[Sequence[int]] = None,
                 cluster_hint: int = 0, workspace: Optional[torch.Tensor] = None,
-                debug: Optional[dict] = None) -> None:
+                debug: Optional[dict] = None, no_alloc: bool = False) -> None:
     """Run the verify step on the GPU (see include/spec_verify.h for the semantics).
 
     ``debug`` may hold float32 CUDA tensors ``lse_t`` [B, K+1], ``lse_d``, ``p_x``, ``q_x``
     [B, K]; they are filled by the diagnostic entry point. ``workspace`` selects the
-    caller-owned-workspace entry point.
+    caller-owned-workspace entry point, ``no_alloc`` the one that allocates no device memory.
     """
     m = _MODES[mode]
     prob, keep = _problem(target_logits, draft_logits, draft_tokens, m, bias_k, fanout,
@@ -96,6 +96,9 @@ def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
         extra = [_ptr(debug.get(k), k, torch.float32) for k in ("lse_t", "lse_d", "p_x", "q_x")]
         st = _lib.call("spec_verify_debug", prob, *args, *extra, s)
         where = "spec_verify_debug"
+    elif no_alloc:
+        st = _lib.call("spec_verify_noalloc", prob, *args, s)
+        where = "spec_verify_noalloc"
     elif workspace is not None:
         st = _lib.call("spec_verify_ws", prob, *args, _ptr(workspace, "workspace"),
                        workspace.numel() * workspace.element_size(), s)

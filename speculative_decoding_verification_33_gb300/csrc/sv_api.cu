@@ -30,6 +30,15 @@ struct StreamRes {
   size_t stage_bytes = 0;
 };
 
+// Workspace of spec_verify_noalloc: the queue counters, error word and processing order the
+// kernel needs, for batches of up to kNoAllocMaxB sequences, in device memory that belongs to
+// this module rather than to any allocation. Every GPU that loads the library holds it (about
+// 256 KB) until the process exits. Host code must not use the symbol as a pointer: its device
+// address comes from cudaGetSymbolAddress, once per device.
+constexpr int kNoAllocMaxB = 65536;
+static __device__ __align__(256) unsigned char g_noalloc_ws[sv::workspace_bytes_for(kNoAllocMaxB)];
+std::map<int, void*> g_noalloc_ptr;  // device ordinal -> address of g_noalloc_ws there
+
 std::mutex g_mu;
 std::map<std::pair<int, cudaStream_t>, StreamRes> g_res;
 std::map<std::tuple<int, int, int, int, int, size_t>, int> g_occ;  // dev,dtype,greedy,top8,C,smem
@@ -289,6 +298,38 @@ sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
              temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr,
              nullptr, nullptr, nullptr, 0, static_cast<Workspace*>(workspace),
              static_cast<cudaStream_t>(stream));
+}
+
+sv_status spec_verify_noalloc(const sv_problem* prob, const void* target_logits,
+                              const void* draft_logits, const int32_t* draft_tokens,
+                              const int32_t* draft_lens, const float* uniforms,
+                              float temperature, float beta, int mode, int32_t* out_accept_len,
+                              int32_t* out_tokens, int32_t* out_residual_topF, void* stream) {
+  Checked c;
+  sv_status st = check_args(prob, target_logits, draft_logits, draft_tokens, uniforms,
+                            temperature, beta, mode, out_accept_len, out_tokens,
+                            out_residual_topF, &c);
+  if (st != SV_OK || prob->B == 0) return st;
+  if (prob->B > kNoAllocMaxB) return SV_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_noalloc_ptr.find(dev);
+    if (it != g_noalloc_ptr.end()) {
+      ws = it->second;
+    } else {  // first call on this device (with it current): look the array up once
+      if (cudaGetSymbolAddress(&ws, g_noalloc_ws) != cudaSuccess || !ws) return SV_ERR_CUDA;
+      g_noalloc_ptr[dev] = ws;
+    }
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the queue counters and the order-ready flag must start at zero for every call
+  if (cudaMemsetAsync(ws, 0, sizeof(Workspace), s) != cudaSuccess) return SV_ERR_CUDA;
+  return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms, temperature,
+             beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr, nullptr, nullptr,
+             nullptr, 0, static_cast<Workspace*>(ws), s);
 }
 
 sv_status spec_verify_debug(const sv_problem* prob, const void* target_logits,

@@ -62,7 +62,7 @@ struct Params {
 
 constexpr int kLptMaxB = 4096;  // larger batches keep the natural order
 
-inline size_t workspace_bytes_for(int B) {
+constexpr size_t workspace_bytes_for(int B) {
   return sizeof(Workspace) + (static_cast<size_t>(B > 0 ? B : 0) * 4 + 255) / 256 * 256;
 }
 

@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cluster", type=int, default=0, help="CTAs per sequence (0 = library)")
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5],
+                    help="synthetic workload (5 = B256 K8 V152064, the headline)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample", type=int, default=16,
@@ -214,7 +216,7 @@ def run_reference(args):
     if rank != 0:
         return
     from speculative_decoding_verification_33_gb300 import workloads as W
-    w_full = W.WORKLOADS[5]
+    w_full = W.WORKLOADS[args.workload]
     w = W.small_variant(w_full, B=args.sample)  # same seeds: the first `sample` sequences
     d = W.make_inputs(w)
     toks = int(np.sum(d["draft_lens"]))
@@ -250,27 +252,32 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    w = W.WORKLOADS[5]
+    w = W.WORKLOADS[args.workload]
     d = W.make_inputs(w, offset=rank)
     lens = d["draft_lens"]
     toks_local = float(np.sum(lens))
+    greedy = w.mode == "greedy"
 
     T = api.to_device_logits(d["target"])
-    D = api.to_device_logits(d["draft"])
+    D = None if greedy else api.to_device_logits(d["draft"])
     tok = torch.from_numpy(d["draft_tokens"]).cuda()
     ln = torch.from_numpy(lens).cuda()
     uni = torch.from_numpy(d["uniforms"]).cuda()
     acc = torch.empty(w.B, dtype=torch.int32, device="cuda")
     otok = torch.empty(w.B, w.K + 1, dtype=torch.int32, device="cuda")
+    otopf = (torch.empty(w.B, w.K, max(w.fanout), dtype=torch.int32, device="cuda")
+             if w.fanout else None)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
 
-    prob, _keep = _lib.make_problem(w.B, w.K, w.V, _lib.SV_DTYPE_BF16, w.V, w.V,
+    dcode = _lib.SV_DTYPE_BF16 if w.dtype == "bf16" else _lib.SV_DTYPE_F32
+    prob, _keep = _lib.make_problem(w.B, w.K, w.V, dcode, w.V, w.V, w.bias_k, w.fanout,
                                     cluster_hint=args.cluster)
-    plan_c, plan_n, plan_smem = _lib.plan(prob, _lib.SV_MODE_STOCHASTIC)
+    plan_c, plan_n, plan_smem = _lib.plan(
+        prob, _lib.SV_MODE_GREEDY if greedy else _lib.SV_MODE_STOCHASTIC)
 
     def step():
-        api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, acc, otok, None,
-                        cluster_hint=args.cluster)
+        api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, acc, otok, otopf,
+                        bias_k=w.bias_k, fanout=w.fanout, cluster_hint=args.cluster)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -332,10 +339,11 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded Zipf-prior logits, Gumbel-max drafts, NaN padding rows)",
-            "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V,
-                       "temperature": w.temperature, "draft_lens": "uniform 1..8",
+            "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "mode": w.mode,
+                       "temperature": w.temperature,
+                       "draft_lens": f"uniform 1..{w.K}" if w.ragged else f"all {w.K}",
                        "verified_tokens_per_rank": toks_local,
                        "l2": "flushed before each step (256 MiB write, outside the events)",
                        "cluster_hint": args.cluster, "ctas_per_cluster": plan_c,
@@ -353,17 +361,22 @@ def run_ours(args):
 
     # end to end through the host-buffer entry point (pinned host memory)
     if not args.no_e2e:
-        hT = torch.from_numpy(d["target"].view(np.int16)).pin_memory()
-        hD = torch.from_numpy(d["draft"].view(np.int16)).pin_memory()
+        def pinned_logits(a):
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+        hT = pinned_logits(d["target"])
+        hD = None if greedy else pinned_logits(d["draft"])
         h_tok = torch.from_numpy(d["draft_tokens"]).pin_memory()
         h_len = torch.from_numpy(lens).pin_memory()
         h_uni = torch.from_numpy(d["uniforms"]).pin_memory()
         h_acc = torch.empty(w.B, dtype=torch.int32).pin_memory()
         h_out = torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory()
+        h_topf = (torch.empty(w.B, w.K, max(w.fanout), dtype=torch.int32).pin_memory()
+                  if w.fanout else None)
 
         def e2e_step():
-            api.verify_host(hT, hD, h_tok, h_len, h_uni, h_acc, h_out, dtype="bf16",
-                            temperature=w.temperature, beta=w.beta, mode=w.mode)
+            api.verify_host(hT, hD, h_tok, h_len, h_uni, h_acc, h_out, h_topf, dtype=w.dtype,
+                            temperature=w.temperature, beta=w.beta, mode=w.mode,
+                            bias_k=w.bias_k, fanout=w.fanout)
 
         for _ in range(2):
             e2e_step()
@@ -385,7 +398,8 @@ def run_ours(args):
     if rank == 0 and world >= 1 and not args.no_cpu:
         from tests.parity import compare
         t_cpu, res = oracle_time(d, w, range(w.B))
-        rep = compare(res, range(w.B), g_acc, g_tok)
+        rep = compare(res, range(w.B), g_acc, g_tok,
+                      otopf.cpu().numpy() if otopf is not None else None)
         line["cpu_baseline"] = {"value": toks_local / t_cpu, "unit": UNIT, "cores": 1,
                                 "kind": "oracle",
                                 "sample": f"all {w.B} sequences of rank 0's batch, once"}

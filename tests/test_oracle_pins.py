@@ -463,3 +463,17 @@ def test_invalid_sequences():
     one = zt.copy()
     one[0, 0] = -np.inf
     assert O.verify_sequence(one, zd, np.array([1, 2, 3]), 3, u, **kw).valid
+
+
+def test_residual_top_ids_brute_force():
+    """Diagnostic top-f of the exact residual: brute force over a tiny row (SSD page, Method)."""
+    rng = np.random.default_rng(17)
+    for _ in range(20):
+        V = 12
+        zt = (rng.standard_normal(V) * 2).astype(np.float32)
+        zd = (zt + rng.standard_normal(V)).astype(np.float32)
+        p, q = probs_of(zt, 1.0), probs_of(zd, 1.0)
+        r = [max(a - b, 0.0) for a, b in zip(p, q)]
+        ref = [v for v in sorted(range(V), key=lambda v: (-r[v], v)) if r[v] > 0][:4]
+        got = O.residual_top_ids(zt, zd, temperature=1.0, f=4).tolist()
+        assert got == ref

@@ -102,28 +102,6 @@ int sm_count(int dev) {
   return n;
 }
 
-int pow2_at_least(long long v) {
-  int c = 1;
-  while (c < sv::kMaxCluster && c < v) c <<= 1;
-  return c;
-}
-
-// Cluster size: enough CTAs per sequence that one CTA's slice stays within kMaxSlice, and for
-// batches too small to fill every CTA slot, more CTAs per sequence.
-int choose_cluster(const sv_problem* p, int greedy, size_t elt, int sms) {
-  (void)greedy;
-  (void)elt;
-  if (p->cluster_hint) return p->cluster_hint;
-  int c_mem = 1;
-  while (c_mem < sv::kMaxCluster && (p->V + c_mem - 1) / c_mem > sv::kMaxSlice) c_mem <<= 1;
-  const long long want = p->B > 0 ? (3LL * sms + p->B - 1) / p->B : 1;
-  const int c_par = pow2_at_least(want);
-  int c_vocab = 1;  // at least 512 elements per CTA
-  while (c_vocab * 2 <= sv::kMaxCluster && static_cast<long long>(c_vocab) * 2 * 512 <= p->V)
-    c_vocab <<= 1;
-  return std::max(c_mem, std::min(c_par, c_vocab));
-}
-
 StreamRes* resources(int dev, cudaStream_t s, size_t need, sv_status* st) {
   StreamRes& r = g_res[{dev, s}];
   if (!r.ws || r.ws_bytes < need) {
@@ -154,30 +132,61 @@ StreamRes* resources(int dev, cudaStream_t s, size_t need, sv_status* st) {
   return &r;
 }
 
-// Cluster size, slice, shared memory and the number of clusters to launch (g_mu held).
-sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L) {
-  const int sms = sm_count(dev);
-  if (sms <= 0) return SV_ERR_CUDA;
-  const int C = choose_cluster(p, c.greedy, c.elt, sms);
-  const int slice = static_cast<int>(((static_cast<long long>(p->V) + C - 1) / C + 7) / 8 * 8);
-  L->p.slice = slice;
-  L->dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
-  L->greedy = c.greedy;
-  L->cluster = C;
-  L->smem = sv::smem_bytes(L->dtype, L->greedy, slice);
-  if (slice > sv::kMaxSlice || L->smem > kMaxDynSmem) return SV_ERR_UNSUPPORTED;
-  const int top8 = !c.greedy && ((p->bias_k > 0 && c.beta_lt1) || c.fmax > 0);
-  L->p.top8 = top8;
-  auto key = std::make_tuple(dev, L->dtype, L->greedy, top8, C, L->smem);
+// Resident clusters of C CTAs for this problem (cached per device and kernel variant); fills the
+// slice and shared-memory size of that C. 0 when C cannot be launched.
+int resident_clusters(const sv_problem* p, int dev, int dtype, int greedy, int top8, int C,
+                      int* slice_out, size_t* smem_out) {
+  const long long slice = ((static_cast<long long>(p->V) + C - 1) / C + 7) / 8 * 8;
+  *slice_out = static_cast<int>(slice);
+  *smem_out = sv::smem_bytes(dtype, greedy, static_cast<int>(slice));
+  if (slice > sv::kMaxSlice || *smem_out > kMaxDynSmem) return 0;
+  auto key = std::make_tuple(dev, dtype, greedy, top8, C, *smem_out);
   auto it = g_occ.find(key);
-  int occ = 0;
-  if (it != g_occ.end()) {
-    occ = it->second;
+  if (it != g_occ.end()) return it->second;
+  const int occ = sv::max_active_clusters(dtype, greedy, top8, C, *smem_out);
+  g_occ[key] = occ;
+  return occ;
+}
+
+// Cluster size, slice, shared memory and the number of clusters to launch (g_mu held).
+//
+// One sequence is verified by one cluster, position after position, so a sequence's latency
+// falls as C grows while the work per byte (exchanges, barriers) rises. The choice: the largest C
+// whose co-resident clusters still hold the whole batch at once, each CTA keeping at least 512
+// vocabulary entries; when no C holds the batch, the smallest C whose slice fits shared memory
+// (throughput). A cluster_hint overrides the choice.
+sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L) {
+  if (sm_count(dev) <= 0) return SV_ERR_CUDA;
+  const int dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
+  const int top8 = !c.greedy && ((p->bias_k > 0 && c.beta_lt1) || c.fmax > 0);
+  int C = p->cluster_hint, slice = 0, occ = 0;
+  size_t smem = 0;
+  if (C) {
+    occ = resident_clusters(p, dev, dtype, c.greedy, top8, C, &slice, &smem);
   } else {
-    occ = sv::max_active_clusters(L->dtype, L->greedy, top8, C, L->smem);
-    g_occ[key] = occ;
+    int c_max = 1;
+    while (c_max * 2 <= sv::kMaxCluster && static_cast<long long>(c_max) * 2 * 512 <= p->V)
+      c_max <<= 1;
+    int fallback = 0;  // smallest launchable C
+    for (int cand = c_max; cand >= 1 && !C; cand >>= 1) {
+      int s = 0;
+      size_t m = 0;
+      const int n = resident_clusters(p, dev, dtype, c.greedy, top8, cand, &s, &m);
+      if (n <= 0) continue;
+      fallback = cand;
+      if (n >= p->B) C = cand;
+    }
+    if (!C) C = fallback;
+    if (!C) return SV_ERR_UNSUPPORTED;
+    occ = resident_clusters(p, dev, dtype, c.greedy, top8, C, &slice, &smem);
   }
   if (occ <= 0) return SV_ERR_UNSUPPORTED;
+  L->p.slice = slice;
+  L->dtype = dtype;
+  L->greedy = c.greedy;
+  L->cluster = C;
+  L->smem = smem;
+  L->p.top8 = top8;
   L->p.n_clusters = std::max(1, std::min(p->B, occ));
   return SV_OK;
 }

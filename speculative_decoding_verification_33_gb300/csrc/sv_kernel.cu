@@ -712,6 +712,10 @@ struct ChunkRow<uint16_t, VPT> {
                       : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
     }
   }
+  __device__ __forceinline__ void load_full(const uint16_t* row) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) v[j] = reinterpret_cast<const uint4*>(row)[threadIdx.x + j * NC];
+  }
   __device__ __forceinline__ float vmax() const {  // NaN-propagating
     uint32_t m = max_nan_bf16x2(max_nan_bf16x2(v[0].x, v[0].y), max_nan_bf16x2(v[0].z, v[0].w));
 #pragma unroll
@@ -738,6 +742,14 @@ struct ChunkRow<float, VPT> {
       }
     }
   }
+  __device__ __forceinline__ void load_full(const float* row) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int g = threadIdx.x + j * NC;
+      v[j][0] = reinterpret_cast<const float4*>(row)[2 * g];
+      v[j][1] = reinterpret_cast<const float4*>(row)[2 * g + 1];
+    }
+  }
   __device__ __forceinline__ float vmax() const {
     float m = -INFINITY;
 #pragma unroll
@@ -751,6 +763,44 @@ struct ChunkRow<float, VPT> {
     z[4] = v[j][1].x; z[5] = v[j][1].y; z[6] = v[j][1].z; z[7] = v[j][1].w;
   }
 };
+
+// The stochastic stats pass over the whole chunks [0, kf) of a position: running max and sum of
+// the target row and, when TWO, of the draft row. Same arithmetic, in the same order, as the
+// general chunk loop; no per-vector bounds, no per-chunk mode tests. Returns the chunks done
+// (fewer than kf only when a wait gave up).
+template <typename T, bool TWO>
+__device__ __forceinline__ int stream_whole(const Ring<T, false>& R, int seq, int i, int kf,
+                                            Cursor& cons, bool& late, RowAcc& at, RowAcc& ad,
+                                            float c) {
+  constexpr int VPT = Ring<T, false>::CH / 8 / NC;
+  for (int k = 0; k < kf; ++k) {
+    const int s = acquire<T, false>(R, seq, i, k, cons, late);
+    if (s < 0) return k;
+    ChunkRow<T, VPT> ct, cd;
+    ct.load_full(R.row(s, 0));
+    if (TWO) cd.load_full(R.row(s, 1));
+    at.rescale(ct.vmax(), c);
+    if (TWO) ad.rescale(cd.vmax(), c);
+    if (at.m > -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        float z[8];
+        ct.get(j, z);
+        at.sum8(z, c);
+      }
+    }
+    if (TWO && ad.m > -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        float z[8];
+        cd.get(j, z);
+        ad.sum8(z, c);
+      }
+    }
+    release_stage(R.empty, cons);
+  }
+  return kf;
+}
 
 __device__ __forceinline__ void top8_insert(unsigned long long (&keys)[8], float& thr, float z,
                                             uint32_t id) {
@@ -858,7 +908,7 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
     const int n = R.chunk_len(k), nvec = (n + 7) >> 3;
     const T* rt = R.row(s, 0);
     const T* rd = R.row(s, GREEDY ? 0 : 1);
-    for (int g = tid; g < nvec; g += NC) {
+    auto vec = [&](int g) {
       float zt[8], zd[8], w[8];
       Elt<T>::load8(rt, g, zt);
       if (!BONUS) Elt<T>::load8(rd, g, zd);
@@ -866,6 +916,13 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
       const float sm = weights8<BONUS>(zt, BONUS ? zt : zd, e0, W, w);
       vmass[e0 >> 3] = sm;
       acc += qfix(sm);
+    };
+    constexpr int VPT = Ring<T, GREEDY>::CH / 8 / NC;
+    if (n == R.CH) {  // a whole chunk: exactly VPT vectors per thread
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) vec(tid + j * NC);
+    } else {
+      for (int g = tid; g < nvec; g += NC) vec(g);
     }
     release_stage(R.empty, cons);
   }
@@ -1257,7 +1314,15 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           for (int j = 0; j < 8; ++j) keys[j] = 0ull;
         }
         if (ld_t || ld_d) {
-          for (int k = 0; k < R.nchunk; ++k) {
+          int k = 0;
+          if constexpr (!GREEDY) {
+            if (P.use_bulk && st_t && !tk && st_d == ld_d) {  // the common case: whole chunks first
+              const int kf = R.nv / RingT::CH;
+              k = st_d ? stream_whole<T, true>(R, seq, i, kf, cons, late, at, ad, c)
+                       : stream_whole<T, false>(R, seq, i, kf, cons, late, at, ad, c);
+            }
+          }
+          for (; k < R.nchunk; ++k) {
             int s = acquire<T, GREEDY>(R, seq, i, k, cons, late);
             if (!P.use_bulk) s = fill_unaligned<T, GREEDY>(P, R, s, seq, i, k, late);
             if (s < 0) break;

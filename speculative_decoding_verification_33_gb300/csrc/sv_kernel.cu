@@ -70,21 +70,27 @@ struct Hdr {
   float u[kMaxK + 1];
 };
 
-// What a stage holds, packed in one 64-bit word: sequence (bits 0..31), position + 64 (bits
-// 32..39; positions below 0 mark chunks of the draw pass), chunk (bits 40..55), rows
-// (ROW_T | ROW_D, bits 56..57).
-__device__ __forceinline__ unsigned long long stage_tag(int seq, int pos, int k) {
-  return static_cast<unsigned long long>(static_cast<uint32_t>(seq)) |
+// What a stage holds, packed in one 64-bit word: sequence (bits 0..23), its epoch in the
+// cluster's order mod 256 (bits 24..31), position + 64 (bits 32..39; positions below 0 mark
+// chunks of the draw pass), chunk (bits 40..55), rows (ROW_T | ROW_D, bits 56..57).
+__device__ __forceinline__ unsigned long long stage_tag(int seq, int ep, int pos, int k) {
+  return static_cast<unsigned long long>((static_cast<uint32_t>(seq) & 0xFFFFFFu) |
+                                         ((static_cast<uint32_t>(ep) & 0xFFu) << 24)) |
          (static_cast<unsigned long long>((pos + 64) & 0xFF) << 32) |
          (static_cast<unsigned long long>(k & 0xFFFF) << 40);
 }
+__device__ __forceinline__ int tag_ep(unsigned long long t) { return static_cast<int>((t >> 24) & 0xFF); }
+__device__ __forceinline__ int tag_pos(unsigned long long t) { return static_cast<int>((t >> 32) & 0xFF) - 64; }
+__device__ __forceinline__ int tag_k(unsigned long long t) { return static_cast<int>((t >> 40) & 0xFFFF); }
 constexpr unsigned long long kTagMask = (1ull << 56) - 1ull;
 __device__ __forceinline__ int tag_rows(unsigned long long t) { return static_cast<int>(t >> 56); }
 
-// Position in the ring: running count, stage index and phase parity, advanced together.
+// Position in the ring: running count, stage index and phase parity, advanced together; for the
+// consumers also the epoch of the sequence they are on.
 struct Cursor {
   int n = 0, s = 0;
   uint32_t ph = 0;
+  int ep = 0;
   __device__ __forceinline__ void advance() {
     ++n;
     if (++s == NS) {
@@ -130,6 +136,9 @@ struct CtaState {
   unsigned long long pub_cur, pub_next;  // consumer -> producer words (see Pub)
   int cons_final;    // stages the consumers took, published before `done`
   int seq0;          // this cluster's first sequence
+  int dec;           // decision of the last combined position: -1 accept, a >= 0 stop at a,
+                     // -2 unusable row, -3 a wait gave up (written by consumer warp 0)
+  int next;          // the sequence this cluster takes next (from the first exchange)
   // reduction scratch (one slot per kind)
   float rmax[2][NW];
   float rsum[2][NW];
@@ -403,11 +412,11 @@ __device__ __forceinline__ void block_top8(unsigned long long (&keys)[8], CtaSta
 // transaction bytes on this CTA's exchange barrier). A buffer is rewritten two rounds later,
 // which a CTA can only reach after every peer has pushed the round in between, i.e. after
 // every peer has read this round. Returns false if the wait gave up.
-__device__ __forceinline__ bool exchange(CtaState& S, Xchg (*X)[kMaxCluster], uint64_t* xbar,
-                                         uint32_t& round, uint32_t rank, uint32_t C, int c0,
-                                         int nc) {
+__device__ __forceinline__ void exchange_post(CtaState& S, Xchg (*X)[kMaxCluster],
+                                              uint64_t* xbar, uint32_t& round, uint32_t rank,
+                                              uint32_t C, int c0, int nc) {
   const int tid = threadIdx.x;
-  const uint32_t p = round & 1u, ph = (round >> 1) & 1u;
+  const uint32_t p = round & 1u;
   ++round;
   if (tid == 0) mbar_arrive_expect_tx(&xbar[p], C * static_cast<uint32_t>(nc) * 16u);
   if (tid < static_cast<int>(C) * nc) {
@@ -417,7 +426,13 @@ __device__ __forceinline__ bool exchange(CtaState& S, Xchg (*X)[kMaxCluster], ui
     const uint32_t bar = map_to_rank(smem_u32(&xbar[p]), peer);
     st_async_v4(dst, reinterpret_cast<const uint4*>(&S.rec)[ch], bar);
   }
-  return mbar_wait_cluster_bounded(&xbar[p], ph, kWaitBudget);
+}
+__device__ __forceinline__ bool exchange(CtaState& S, Xchg (*X)[kMaxCluster], uint64_t* xbar,
+                                         uint32_t& round, uint32_t rank, uint32_t C, int c0,
+                                         int nc) {
+  const uint32_t r = round;
+  exchange_post(S, X, xbar, round, rank, C, c0, nc);
+  return mbar_wait_cluster_bounded(&xbar[r & 1u], (r >> 1) & 1u, kWaitBudget);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -598,7 +613,7 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
       continue;  // the oldest stage is still being read (the wait above slept on it)
     }
     issue_chunk<T, GREEDY>(P, R, cur.s, src_t, src_d,
-                           stage_tag(q_seq, q_ph == DRAW ? -1 - q_pos : q_pos, q_k), q_k, rows);
+                           stage_tag(q_seq, q_ep, q_ph == DRAW ? -1 - q_pos : q_pos, q_k), q_k, rows);
     cur.advance();
     idle0 = clock64();
     if (++q_k >= R.nchunk) {
@@ -626,13 +641,36 @@ __device__ __forceinline__ void release_stage(uint64_t* empty, Cursor& cons) {
 template <typename T, bool GREEDY>
 __device__ __forceinline__ int acquire(const Ring<T, GREEDY>& R, int seq, int pos, int k,
                                        Cursor& cons, bool& late) {
-  const unsigned long long want = stage_tag(seq, pos, k);
+  const unsigned long long want = stage_tag(seq, cons.ep, pos, k);
   while (!late) {
     if (!mbar_wait_bounded(&R.full[cons.s], cons.ph, kWaitBudget)) {
       late = true;
       break;
     }
     if ((R.desc[cons.s] & kTagMask) == want) return cons.s;
+    release_stage(R.empty, cons);
+  }
+  return -1;
+}
+
+// Stats chunk k of position pos of the current sequence, while the decision of the previous
+// position may still be open: stale chunks (an earlier sequence, or what this sequence's
+// consumers have already moved past) are handed back; a chunk of the draw pass or of a later
+// sequence means the producer has acted on a stop, and returns -2 without taking the stage.
+// -1 once a wait has given up.
+template <typename T, bool GREEDY>
+__device__ __forceinline__ int acquire_open(const Ring<T, GREEDY>& R, int pos, int k,
+                                           Cursor& cons, bool& late) {
+  while (!late) {
+    if (!mbar_wait_bounded(&R.full[cons.s], cons.ph, kWaitBudget)) {
+      late = true;
+      break;
+    }
+    const unsigned long long t = R.desc[cons.s];
+    const int d = static_cast<int8_t>(static_cast<uint8_t>(tag_ep(t) - cons.ep));
+    const int tp = tag_pos(t), tk = tag_k(t);
+    if (d == 0 && tp == pos && tk == k) return cons.s;
+    if (d > 0 || (d == 0 && (tp < 0 || tp > pos || (tp == pos && tk > k)))) return -2;
     release_stage(R.empty, cons);
   }
   return -1;
@@ -1123,6 +1161,108 @@ __device__ __forceinline__ int header_ok(const Params& P, const Hdr& h, bool gre
 }
 
 // ------------------------------------------------------------------------------------------
+// decisions taken while the next position streams
+// ------------------------------------------------------------------------------------------
+// One staged chunk of a stats position: the target row (and, when `two`, the draft row) into
+// this thread's running statistics; whole chunks without per-vector bounds.
+template <typename T, bool GREEDY>
+__device__ __forceinline__ void stats_chunk(const Ring<T, GREEDY>& R, int s, int k, bool two,
+                                            RowAcc& at, RowAcc& ad, int& garg, float c) {
+  using RingT = Ring<T, GREEDY>;
+  constexpr int VPT = RingT::CH / 8 / NC;
+  const int n = R.chunk_len(k);
+  const bool whole = n == RingT::CH;
+  const int nvec = (n + 7) >> 3;
+  ChunkRow<T, VPT> ct;
+  if (whole) ct.load_full(R.row(s, 0));
+  else ct.load(R.row(s, 0), nvec);
+  const float vm = ct.vmax();
+  if constexpr (GREEDY) {
+    if (isnan(vm)) {
+      at.m = NAN;
+    } else if (vm > at.m) {  // first index of the new maximum in this thread's elements
+      at.m = vm;
+      int e = 0x7FFFFFFF;
+#pragma unroll
+      for (int j = VPT - 1; j >= 0; --j) {
+        float z[8];
+        ct.get(j, z);
+#pragma unroll
+        for (int kk = 7; kk >= 0; --kk)
+          if (z[kk] == vm) e = 8 * (static_cast<int>(threadIdx.x) + j * NC) + kk;
+      }
+      garg = R.v0 + k * RingT::CH + e;
+    }
+  } else {
+    at.rescale(vm, c);
+    if (at.m > -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        float z[8];
+        ct.get(j, z);
+        at.sum8(z, c);
+      }
+    }
+    if (two) {
+      ChunkRow<T, VPT> cd;
+      if (whole) cd.load_full(R.row(s, 1));
+      else cd.load(R.row(s, 1), nvec);
+      ad.rescale(cd.vmax(), c);
+      if (ad.m > -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+          float z[8];
+          cd.get(j, z);
+          ad.sum8(z, c);
+        }
+      }
+    }
+  }
+}
+
+// Consumer warp 0: wait for exchange round r (posted for position `pos`), combine it and take
+// the decision into S.dec; on a stop or an unusable row tell the producer, which then stops
+// streaming the positions after it. The round of position 0 also names the next sequence.
+template <bool GREEDY>
+__device__ void resolve_open(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
+                             uint64_t* xbar, uint32_t r, uint32_t C, int seq, int ep, int pos,
+                             int L, float zx_t, float zx_d) {
+  const int lane = threadIdx.x & 31;
+  const bool ok = mbar_wait_cluster_bounded(&xbar[r & 1u], (r >> 1) & 1u, kWaitBudget);
+  const Xchg* XX = X[r & 1u];
+  bool ab = !ok;
+  if (ok)
+    for (uint32_t cc = 0; cc < C; ++cc) ab |= (XX[cc].flags & XF_ABORT) != 0u;
+  ab = __any_sync(FULL, ab);
+  if (pos == 0 && lane == 0) {
+    const int next = ok ? XX[0].next_seq : P.B;
+    S.next = next;
+    if (next < P.B) {
+      fetch_header(P, S, S.cur ^ 1, next, GREEDY);
+      S.n_hdr_wait = 1;
+    }
+    pub_store(&S.pub_next, pack_next(next, ep));
+  }
+  int stop = -3;
+  if (!ab) {
+    const bool st_d = !GREEDY && pos < L;
+    combine<GREEDY>(P, S, XX, C, pos, true, st_d, false, st_d, zx_t, zx_d);
+    __syncwarp();
+    if (S.bad_t || (st_d && S.bad_d)) stop = -2;
+    else if (GREEDY) stop = (pos < L && S.hdr[S.cur].x[pos] == S.arg) ? -1 : pos;
+    else stop = (pos == L || !S.accept) ? pos : -1;
+  }
+  if (lane == 0) {
+    S.dec = stop;
+    if (stop != -1 && stop != -3) {
+      __threadfence_block();  // S before the word the producer acts on
+      pub_store(&S.pub_cur, pack_cur(seq, ep, stop, 0));
+    }
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------------------------------
 // longest-draft-first order of the sequences (built once per launch by one CTA)
 // ------------------------------------------------------------------------------------------
 // Stable counting sort of the sequences by draft length, descending (invalid lengths last),
@@ -1273,6 +1413,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     int seq = S.seq0;
     int ep = 0;
     while (seq < P.B) {
+      cons.ep = ep;
       int next_local = 0;
       if (rank == 0 && tid == 0)
         next_local = seq_at(P, static_cast<int>(atomicAdd(&P.ws->next, 1u)) + P.n_clusters);
@@ -1289,6 +1430,124 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
       bool first = true;
       int a = -1;
       int next = P.B;
+      if (!TOP8 && !P.debug_all && !invalid && P.use_bulk) {
+        // ---- decisions taken while the next position streams: position i is read while
+        // consumer warp 0 combines the round of position i - 1 (polled between chunks, else
+        // waited for at the end of position i); a stop makes the producer switch to the draw,
+        // which cuts position i short in every consumer at the same stage ----
+        int pend = -1;             // position whose round is posted but not yet combined
+        uint32_t pend_round = 0;
+        bool resolved = true;      // warp 0's view
+        float pzx_t = 0.f, pzx_d = 0.f;
+        int outcome = -3;
+        for (int i = 0;; ++i) {
+          const bool two = !GREEDY && i < L;
+          float zx_t = 0.f, zx_d = 0.f;
+          if (!GREEDY && tid == 0 && i < L) {
+            const int x = S.hdr[S.cur].x[i];
+            zx_t = Elt<T>::val(static_cast<const T*>(row_ptr(P, false, seq, i, sizeof(T)))[x]);
+            zx_d = Elt<T>::val(static_cast<const T*>(row_ptr(P, true, seq, i, sizeof(T)))[x]);
+          }
+          RowAcc at, ad;
+          at.init();
+          ad.init();
+          int garg = 0x7FFFFFFF;
+          bool cut = false;
+          for (int k = 0; k < R.nchunk; ++k) {
+            if (warp == 0 && !resolved) {
+              const int ready = __shfl_sync(
+                  FULL, tid == 0 ? static_cast<int>(mbar_test_cluster(&xbar[pend_round & 1u], (pend_round >> 1) & 1u)) : 0, 0);
+              if (ready) {
+                resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, seq, ep, pend, L, pzx_t, pzx_d);
+                resolved = true;
+              }
+            }
+            const int s = acquire_open<T, GREEDY>(R, i, k, cons, late);
+            if (s == -2) {
+              cut = true;
+              break;
+            }
+            if (s < 0) break;
+            stats_chunk<T, GREEDY>(R, s, k, two, at, ad, garg, c);
+            release_stage(R.empty, cons);
+          }
+          late = cbar_or(late);
+          if (late) break;
+          if (cut) {  // the producer acted on a stop of `pend`; warp 0 holds the decision
+            outcome = *reinterpret_cast<volatile int*>(&S.dec);
+            break;
+          }
+          // this CTA's partials of position i
+          const float2 mm = block_max2(at.m, ad.m, S);
+          float2 ss = make_float2(0.f, 0.f);
+          int arg = 0x7FFFFFFF;
+          if constexpr (GREEDY) {
+            if (!row_bad(mm.x)) arg = block_min_int(at.m == mm.x ? garg : 0x7FFFFFFF, S);
+          } else {
+            const bool sum_t = !row_bad(mm.x);
+            const bool sum_d = two && !row_bad(mm.y);
+            const float mct = __fmul_rn(mm.x, c), mcd = __fmul_rn(mm.y, c);
+            const float pt = (sum_t && at.m > -INFINITY) ? at.total() * exp2f(at.mc - mct) : 0.f;
+            const float pd = (sum_d && ad.m > -INFINITY) ? ad.total() * exp2f(ad.mc - mcd) : 0.f;
+            ss = block_sum2(pt, pd, S);
+            if (sum_t) ss.x *= fmaf(-fmaf(mm.x, c, -mct), kLn2, 1.f);
+            if (sum_d) ss.y *= fmaf(-fmaf(mm.y, c, -mcd), kLn2, 1.f);
+          }
+          // the previous position's decision, at the latest now
+          if (warp == 0 && !resolved) {
+            resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, seq, ep, pend, L, pzx_t, pzx_d);
+            resolved = true;
+          }
+          cbar();
+          if (pend >= 0 && S.dec != -1) {  // position i is not needed
+            outcome = S.dec;
+            break;
+          }
+          if (tid == 0) {
+            S.rec.m_t = mm.x;
+            S.rec.s_t = ss.x;
+            S.rec.m_d = mm.y;
+            S.rec.s_d = ss.y;
+            S.rec.arg = arg;
+            S.rec.next_seq = i == 0 ? next_local : 0;
+            S.rec.flags = 0u;
+          }
+          cbar();
+          pend_round = xround;
+          exchange_post(S, X, xbar, xround, rank, C, 0, 2);
+          pend = i;
+          resolved = false;
+          pzx_t = zx_t;
+          pzx_d = zx_d;
+          if (i == L) {  // nothing after this position: its decision now
+            if (warp == 0) {
+              resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, seq, ep, pend, L, pzx_t, pzx_d);
+              resolved = true;
+            }
+            cbar();
+            outcome = S.dec;
+            break;
+          }
+        }
+        cbar();
+        next = S.next;
+        if (late || outcome == -3 || outcome == -1) {
+          aborted = true;
+        } else if (outcome == -2) {
+          invalid = true;
+          decided = true;
+        } else {
+          decided = true;
+          a = outcome;
+          if (!GREEDY) {
+            if (a < L)
+              draw_token<T, GREEDY, false>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+            else
+              draw_token<T, GREEDY, true>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+            if (late) aborted = true;
+          }
+        }
+      } else
       for (int i = 0;; ++i) {
         const bool st_t = !invalid && i <= L && (!decided || P.debug_all);
         const bool st_d = !GREEDY && !invalid && i < L && (!decided || P.debug_all);

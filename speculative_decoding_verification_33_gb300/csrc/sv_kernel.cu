@@ -277,16 +277,10 @@ __device__ __forceinline__ int key_id(unsigned long long k) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
 }
 
-// Integer of 2^-44 units below s (0 <= s < 16), from the float's bits: s = m * 2^(e-150)
-// with m the 24-bit significand, so s * 2^44 = m * 2^(e-106), truncated.
+// Integer of 2^-44 units below s (0 <= s < 16): s * 2^44 is exact in float (a power-of-two
+// scale, below 2^48), and the conversion truncates it.
 __device__ __forceinline__ unsigned long long qfix(float s) {
-  const uint32_t b = __float_as_uint(s);
-  const int e = static_cast<int>(b >> 23);  // sign is 0 for s >= 0
-  const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;
-  const int sh = e - 106;
-  if (e == 0) return 0ull;  // zero or subnormal: far below 2^-44
-  if (sh >= 0) return m << sh;
-  return sh > -64 ? (m >> -sh) : 0ull;
+  return __float2ull_rz(__fmul_rn(s, 17592186044416.0f));
 }
 
 // floor(u * W) for u in [0, 1) given as a float and W < 2^63, exactly.

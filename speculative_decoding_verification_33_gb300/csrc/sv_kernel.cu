@@ -653,14 +653,16 @@ __device__ __forceinline__ int acquire(const Ring<T, GREEDY>& R, int seq, int po
 // sequence means the producer has acted on a stop, and returns -2 without taking the stage.
 // -1 once a wait has given up.
 template <typename T, bool GREEDY>
-__device__ __forceinline__ int acquire_open(const Ring<T, GREEDY>& R, int pos, int k,
+__device__ __forceinline__ int acquire_open(const Ring<T, GREEDY>& R, int seq, int pos, int k,
                                            Cursor& cons, bool& late) {
+  const unsigned long long want = stage_tag(seq, cons.ep, pos, k);
   while (!late) {
     if (!mbar_wait_bounded(&R.full[cons.s], cons.ph, kWaitBudget)) {
       late = true;
       break;
     }
     const unsigned long long t = R.desc[cons.s];
+    if ((t & kTagMask) == want) return cons.s;
     const int d = static_cast<int8_t>(static_cast<uint8_t>(tag_ep(t) - cons.ep));
     const int tp = tag_pos(t), tk = tag_k(t);
     if (d == 0 && tp == pos && tk == k) return cons.s;
@@ -1456,7 +1458,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
                 resolved = true;
               }
             }
-            const int s = acquire_open<T, GREEDY>(R, i, k, cons, late);
+            const int s = acquire_open<T, GREEDY>(R, seq, i, k, cons, late);
             if (s == -2) {
               cut = true;
               break;

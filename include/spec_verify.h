@@ -119,7 +119,8 @@ sv_status spec_verify(const sv_problem* prob, const void* target_logits,
 sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* clusters,
                            size_t* smem_bytes);
 
-/* Bytes of device workspace spec_verify_ws needs for this problem (256 + 4 B, rounded up). */
+/* Bytes of device workspace spec_verify_ws needs for this problem (256: the sequence queue and
+ * the error word; the size does not depend on the problem). */
 size_t spec_verify_workspace_bytes(const sv_problem* prob);
 
 /*
@@ -142,8 +143,8 @@ sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
  * memory up front, or a runtime whose allocations go through its own pool), or on a path where
  * a cudaMalloc would synchronise the device cannot let the library create its workspace. This
  * variant allocates nothing: its workspace is a fixed array inside the library's device code
- * (about 256 KB on every GPU that loads the library, held until the process exits), sized for
- * at most 65536 sequences; a larger B returns SV_ERR_UNSUPPORTED. Inputs and outputs are the
+ * (256 bytes on every GPU that loads the library, held until the process exits); it accepts at
+ * most 65536 sequences, a larger B returns SV_ERR_UNSUPPORTED. Inputs and outputs are the
  * caller's device buffers, exactly as for spec_verify, and the results are identical.
  * The first call on a device (with that device current) looks the array up with
  * cudaGetSymbolAddress; make that first call before any stream capture. Each call clears the

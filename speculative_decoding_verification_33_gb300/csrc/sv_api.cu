@@ -30,10 +30,10 @@ struct StreamRes {
   size_t stage_bytes = 0;
 };
 
-// Workspace of spec_verify_noalloc: the queue counters, error word and processing order the
-// kernel needs, for batches of up to kNoAllocMaxB sequences, in device memory that belongs to
-// this module rather than to any allocation. Every GPU that loads the library holds it (about
-// 256 KB) until the process exits. Host code must not use the symbol as a pointer: its device
+// Workspace of spec_verify_noalloc: the queue counters and error word the kernel needs (256
+// bytes), for batches of up to kNoAllocMaxB sequences, in device memory that belongs to this
+// module rather than to any allocation. Every GPU that loads the library holds it until the
+// process exits. Host code must not use the symbol as a pointer: its device
 // address comes from cudaGetSymbolAddress, once per device.
 constexpr int kNoAllocMaxB = 65536;
 static __device__ __align__(256) unsigned char g_noalloc_ws[sv::workspace_bytes_for(kNoAllocMaxB)];
@@ -247,7 +247,6 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
     if (!r) return st;
     P.ws = r->ws;
   }
-  P.perm = reinterpret_cast<int*>(P.ws + 1);
   P.lpt = p->B <= sv::kLptMaxB ? 1 : 0;
   return sv::launch(L, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -15,16 +15,14 @@ constexpr int NS = 3;             // stages of the per-CTA row ring
 constexpr int kStageRowBytes = 8192;  // bytes of one row in one stage
 constexpr int kMaxSlice = 65536;  // elements of a row one CTA owns (bounds the draw's buffer)
 
-// Device workspace shared by the clusters of one launch, followed by `perm` (B ints): the
-// order in which the clusters take the sequences (longest draft first). The kernel returns the
-// counters and the flag to zero when the last cluster leaves, so stream-ordered launches (and
-// replays of a captured launch) can reuse it.
+// Device workspace shared by the clusters of one launch. The kernel returns the counters to
+// zero when the last cluster leaves, so stream-ordered launches (and replays of a captured
+// launch) can reuse it.
 struct Workspace {
-  unsigned int next;        // dynamic sequence queue
-  unsigned int done;        // clusters that have finished
-  unsigned int error;       // bit 0: a bounded wait gave up
-  unsigned int perm_ready;  // 1 once perm holds this launch's order
-  unsigned int pad[60];
+  unsigned int next;   // dynamic sequence queue
+  unsigned int done;   // clusters that have finished
+  unsigned int error;  // bit 0: a bounded wait gave up
+  unsigned int pad[61];
 };
 static_assert(sizeof(Workspace) == 256, "workspace layout");
 
@@ -55,16 +53,14 @@ struct Params {
   int slice;      // elements of a row owned by one CTA (multiple of 8)
   int use_bulk;   // rows and strides are 16-byte aligned: stage rows with bulk async copies
   int n_clusters;
-  int lpt;         // take sequences longest draft first (perm built in the workspace)
+  int lpt;         // take sequences longest draft first
   Workspace* ws;
-  int* perm;       // B ints after the workspace header
 };
 
 constexpr int kLptMaxB = 4096;  // larger batches keep the natural order
 
-constexpr size_t workspace_bytes_for(int B) {
-  return sizeof(Workspace) + (static_cast<size_t>(B > 0 ? B : 0) * 4 + 255) / 256 * 256;
-}
+// The workspace does not grow with the batch.
+constexpr size_t workspace_bytes_for(int /*B*/) { return sizeof(Workspace); }
 
 struct Launch {
   Params p;

@@ -1261,67 +1261,49 @@ __device__ void resolve_open(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster
 // ------------------------------------------------------------------------------------------
 // longest-draft-first order of the sequences (built once per launch by one CTA)
 // ------------------------------------------------------------------------------------------
-// Stable counting sort of the sequences by draft length, descending (invalid lengths last),
-// into P.perm. The consumer threads of one CTA run it; `cnt` is NW * (kMaxK + 1) ints of
-// scratch shared memory.
-__device__ void build_order(const Params& P, int* cnt) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nb = P.K + 1;
-  __shared__ int base[kMaxK + 1], run[kMaxK + 1];
-  if (tid <= kMaxK) {
-    base[tid] = 0;
-    run[tid] = 0;
-  }
-  cbar();
-  for (int b = tid; b < P.B; b += NC) {  // histogram
-    const int L = P.lens ? P.lens[b] : P.K;
-    atomicAdd(&base[(L >= 1 && L <= P.K) ? P.K - L : P.K], 1);
-  }
-  cbar();
-  if (tid == 0) {
-    int acc = 0;
-    for (int k = 0; k < nb; ++k) {
-      const int c = base[k];
-      base[k] = acc;
-      acc += c;
-    }
-  }
-  cbar();
-  for (int b0 = 0; b0 < P.B; b0 += NC) {  // stable scatter, NC sequences at a time
-    const int b = b0 + tid;
-    int bk = -1;
-    if (b < P.B) {
-      const int L = P.lens ? P.lens[b] : P.K;
-      bk = (L >= 1 && L <= P.K) ? P.K - L : P.K;
-    }
-    unsigned my_mask = 0;
-    for (int k = 0; k < nb; ++k) {
-      const unsigned m = __ballot_sync(FULL, bk == k);
-      if (lane == 0) cnt[warp * (kMaxK + 1) + k] = __popc(m);
-      if (bk == k) my_mask = m;
-    }
-    cbar();
-    if (bk >= 0) {
-      int pos = base[bk] + run[bk] + __popc(my_mask & ((1u << lane) - 1u));
-      for (int w = 0; w < warp; ++w) pos += cnt[w * (kMaxK + 1) + bk];
-      P.perm[pos] = b;
-    }
-    cbar();
-    if (tid < nb) {
-      int t = 0;
-      for (int w = 0; w < NW; ++w) t += cnt[w * (kMaxK + 1) + tid];
-      run[tid] += t;
-    }
-    cbar();
-  }
-  __threadfence();
-  cbar();
+// Longest draft first: place r of the order is the sequence with the r-th largest draft length,
+// ties in index order, unusable lengths last. Every CTA counts the lengths per bucket once
+// (bucket K - L for L in 1..K, bucket K for the rest); a place is then found by one warp.
+__device__ __forceinline__ int lpt_bucket(const Params& P, int b) {
+  const int L = P.lens ? P.lens[b] : P.K;
+  return (L >= 1 && L <= P.K) ? P.K - L : P.K;
 }
 
-// The sequence at place q of the launch's order.
-__device__ __forceinline__ int seq_at(const Params& P, int q) {
-  if (q >= P.B) return P.B;
-  return P.lpt ? __ldcg(P.perm + q) : q;
+// Sequence at place r (P.B when r >= P.B); all 32 lanes of one warp call it.
+__device__ int lpt_seq(const Params& P, const int* cnt, int r) {
+  const int lane = threadIdx.x & 31;
+  if (r >= P.B) return P.B;
+  if (!P.lpt) return r;
+  int bk = 0, start = 0;
+  while (bk < P.K && start + cnt[bk] <= r) {
+    start += cnt[bk];
+    ++bk;
+  }
+  const int want = r - start;  // rank inside bucket bk
+  const int per = (P.B + 31) / 32;
+  const int lo = min(P.B, lane * per), hi = min(P.B, lo + per);
+  int n = 0;
+  for (int b = lo; b < hi; ++b) n += lpt_bucket(P, b) == bk;
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int found = 0x7FFFFFFF;
+  if (want >= incl - n && want < incl) {
+    int q = want - (incl - n);
+    for (int b = lo; b < hi; ++b)
+      if (lpt_bucket(P, b) == bk) {
+        if (q == 0) {
+          found = b;
+          break;
+        }
+        --q;
+      }
+  }
+  found = warp_min_int(found);
+  return found == 0x7FFFFFFF ? P.B : found;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1334,6 +1316,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
   __shared__ Xchg X[2][kMaxCluster];
   __shared__ uint64_t full_bar[NS], empty_bar[NS], xbar[2];
   __shared__ unsigned long long sdesc[NS];
+  __shared__ int lcnt[kMaxK + 1];
 
   using RingT = Ring<T, GREEDY>;
   const int tid = threadIdx.x;
@@ -1365,29 +1348,16 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     S.n_hdr_wait = 0;
     S.cons_final = 0;
   }
-  // the launch's sequence order: cluster 0 / rank 0 builds it, everyone else waits for it
+  // the draft-length counts of the longest-first order (every CTA its own copy)
   if (P.lpt) {
-    if (cid == 0 && rank == 0 && tid < NC) {
-      build_order(P, reinterpret_cast<int*>(dyn));
-      if (tid == 0) {
-        __threadfence();
-        atomicExch(&P.ws->perm_ready, 1u);
-      }
-    }
-    if (tid == 0) {
-      const long long t0 = clock64();
-      while (atomicAdd(&P.ws->perm_ready, 0u) == 0u) {
-        if (clock64() - t0 > kWaitBudget) {
-          atomicOr(&P.ws->error, 1u);
-          break;
-        }
-        sleep_ns(64);
-      }
-      __threadfence();
-    }
+    if (tid <= kMaxK) lcnt[tid] = 0;
+    __syncthreads();
+    for (int b = tid; b < P.B; b += NTOT) atomicAdd(&lcnt[lpt_bucket(P, b)], 1);
+    __syncthreads();
   }
+  int seq0 = 0;
+  if (warp == 0) seq0 = lpt_seq(P, lcnt, cid);
   if (tid == 0) {
-    const int seq0 = seq_at(P, cid);
     S.seq0 = seq0;
     fetch_header(P, S, 0, seq0, GREEDY);
     cp_async_wait_all();
@@ -1411,8 +1381,12 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     while (seq < P.B) {
       cons.ep = ep;
       int next_local = 0;
-      if (rank == 0 && tid == 0)
-        next_local = seq_at(P, static_cast<int>(atomicAdd(&P.ws->next, 1u)) + P.n_clusters);
+      if (rank == 0 && warp == 0) {  // this cluster's next sequence, named in the first exchange
+        int q = 0;
+        if (tid == 0) q = static_cast<int>(atomicAdd(&P.ws->next, 1u));
+        q = __shfl_sync(FULL, q, 0);
+        next_local = lpt_seq(P, lcnt, q + P.n_clusters);
+      }
       if (tid == 0 && P.fmax + P.debug_all > 0) {
         for (int i = 0; i < kMaxK; ++i) {
           for (int f = 0; f < 8; ++f) S.topf[i][f] = -1;
@@ -1798,7 +1772,6 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     const unsigned old = atomicAdd(&P.ws->done, 1u);
     if (old == static_cast<unsigned>(P.n_clusters) - 1u) {
       atomicExch(&P.ws->next, 0u);
-      atomicExch(&P.ws->perm_ready, 0u);
       atomicExch(&P.ws->done, 0u);
     }
   }

@@ -47,10 +47,10 @@ def test_status_strings():
 
 
 def test_workspace_bytes():
-    # a 256-byte header plus one int per sequence (the processing order), rounded to 256
-    for B, want in ((0, 256), (1, 512), (64, 512), (65, 768), (5000, 256 + 20224)):
+    # a fixed 256-byte header: the sequence queue counter, the finished-cluster count, the error word
+    for B in (0, 1, 64, 65, 5000, 70000):
         prob, _ = _lib.make_problem(B, 1, 1, 0, 1, 1)
-        assert _lib.call("spec_verify_workspace_bytes", prob) == want
+        assert _lib.call("spec_verify_workspace_bytes", prob) == 256
 
 
 def _status(entry="spec_verify", mode=1, T=1.0, beta=1.0, ptrs=1, topf=0, extra=(), **kw):
@@ -101,7 +101,7 @@ def test_workspace_entry_checks_workspace():
     assert _status("spec_verify_ws", extra=(0, 256)) == _lib.SV_ERR_INVALID_ARG
     assert _status("spec_verify_ws", extra=(16, 100)) == _lib.SV_ERR_INVALID_ARG
     assert _status("spec_verify_ws", extra=(8, 256)) == _lib.SV_ERR_INVALID_ARG
-    assert _status("spec_verify_ws", B=64, extra=(16, 256)) == _lib.SV_ERR_INVALID_ARG
+    assert _status("spec_verify_ws", B=64, extra=(16, 240)) == _lib.SV_ERR_INVALID_ARG
 
 
 def test_probe_checks_arguments():

@@ -54,6 +54,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample", type=int, default=16,
                     help="sequences per step of the reference arm")
+    ap.add_argument("--kernel", choices=["verify", "draft_sample", "residual_topf"],
+                    default="verify",
+                    help="verify: the verify step (default); draft_sample / residual_topf: the "
+                         "row kernels on the draft rows / draft positions of the same batch")
     return ap.parse_args(argv)
 
 
@@ -290,6 +294,129 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------------------------
+# the row kernels (draft draw + exit confidence; exact-residual top-F + cache hits)
+# ---------------------------------------------------------------------------------------------
+ROW_FANOUT = (8, 4, 2, 1, 1, 1, 1, 1)
+
+
+def row_workload(W, args):
+    """The headline batch with a Saguaro bias (beta 0.5 on the 8 most likely draft ids) and
+    geometric top-F widths, so both row kernels do their full work."""
+    w = W.WORKLOADS[args.workload]
+    return w.replace(beta=0.5, bias_k=8, fanout=ROW_FANOUT[: w.K], mode="stochastic",
+                     temperature=w.temperature or 1.0)
+
+
+def run_rows(args):
+    import torch
+
+    from speculative_decoding_verification_33_gb300 import api, build
+    from speculative_decoding_verification_33_gb300 import workloads as W
+    from oracle import rows as RO
+
+    torch.cuda.set_device(dist_env()[2])
+    w = row_workload(W, args)
+    d = W.make_inputs(w)
+    lens = d["draft_lens"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    tau = 0.1
+    if args.kernel == "draft_sample":
+        # every draft row the batch has (rows i < L_b), packed
+        sel = [(b, i) for b in range(w.B) for i in range(int(lens[b]))]
+        rows = np.stack([d["draft"][b, i] for b, i in sel])
+        uni = np.ascontiguousarray(np.array([d["uniforms"][b, i] for b, i in sel], np.float32))
+        R = rows.shape[0]
+        D = api.to_device_logits(rows)
+        U = torch.from_numpy(uni).cuda()
+        out = {"tokens": torch.empty(R, dtype=torch.int32, device="cuda"),
+               "conf": torch.empty(R, dtype=torch.float32, device="cuda"),
+               "exit": torch.empty(R, dtype=torch.int32, device="cuda")}
+
+        def step():
+            api.draft_sample(D, U, temperature=w.temperature, beta=w.beta, bias_k=w.bias_k,
+                             tau=tau, out=out)
+        units, unit = R, "draft rows sampled/s"
+        b_alg = R * (w.V * w.elem_bytes + 4 + 4 + 4 + 4)
+    else:
+        T = api.to_device_logits(d["target"])
+        D = api.to_device_logits(d["draft"])
+        vo = api.verify(T, D, torch.from_numpy(d["draft_tokens"]).cuda(),
+                        torch.from_numpy(lens).cuda(), torch.from_numpy(d["uniforms"]).cuda(),
+                        temperature=w.temperature, beta=w.beta, bias_k=w.bias_k,
+                        fanout=w.fanout)
+        LN = torch.from_numpy(lens).cuda()
+
+        def step():
+            return api.residual_topf(T, D, LN, w.fanout, temperature=w.temperature,
+                                     beta=w.beta, bias_k=w.bias_k, verify_out=vo)
+        R = int(np.sum(lens))
+        units, unit = R, "draft positions/s"
+        b_alg = R * (2 * w.V * w.elem_bytes + 4 * max(w.fanout)) + w.B * (4 + 4 * 5)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(dist_env()[2])
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        res = step()
+        b.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    kms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = statistics.mean(kms)
+    peak, peak_src = measured_peak()
+    achieved = b_alg / (mean_ms * 1e-3) / 1e9
+    traffic, traffic_src = recorded_traffic(f"{args.kernel} {w.name}", build.kernel_digest("rows"))
+    line = {"metric": f"{unit} and achieved HBM GB/s (% of roofline) at 1 GB300",
+            "value": units / (mean_ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{args.kernel} {w.name}", "rows_or_positions": units,
+                       "beta": w.beta, "bias_k": w.bias_k, "fanout": list(w.fanout),
+                       "tau": tau, "l2": "flushed before each step (256 MiB write)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                         "traffic_source": traffic_src, "algorithmic_bytes_per_launch": b_alg,
+                         "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms)},
+            "gpu_launches": args.steps * (1 if args.kernel == "draft_sample" else 2),
+            "clocks": clk}
+    if not args.no_cpu:  # the oracle on a bounded sample, one core
+        n = 32
+        if args.kernel == "draft_sample":
+            t0 = time.perf_counter()
+            ref = [RO.draft_sample(rows[r], float(uni[r]), temperature=w.temperature,
+                                   beta=w.beta, bias_k=w.bias_k, tau=tau) for r in range(n)]
+            dt = time.perf_counter() - t0
+            g = out["tokens"][:n].cpu().numpy()
+            same = sum(int(g[r]) == o.token for r, o in enumerate(ref) if o.margin >= 1e-6)
+            line["parity_sample"] = {"rows": n, "tokens_equal_unflagged": same,
+                                     "flagged": sum(o.margin < 1e-6 for o in ref)}
+        else:
+            seqs = list(range(8))
+            t0 = time.perf_counter()
+            ref = RO.residual_topf(d["target"], d["draft"], lens, temperature=w.temperature,
+                                   fanout=w.fanout, beta=w.beta, bias_k=w.bias_k, seqs=seqs)
+            dt = time.perf_counter() - t0
+            n = int(np.sum(lens[seqs]))
+            g = res["r2"].cpu().numpy()[seqs]
+            line["parity_sample"] = {"positions": n,
+                                     "id_lists_equal": int(sum(
+                                         np.array_equal(g[j, i], ref[j, i])
+                                         for j in range(len(seqs))
+                                         for i in range(int(lens[seqs[j]]))))}
+        line["cpu_baseline"] = {"value": n / dt, "unit": unit, "cores": 1, "kind": "oracle",
+                                "sample": f"first {n} {'rows' if args.kernel == 'draft_sample' else 'positions'}"}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------------
 def run_ours(args):
@@ -368,7 +495,7 @@ def run_ours(args):
     b_in = input_bytes(w, lens)
     peak, peak_src = measured_peak()
     achieved = b_alg / (mean_ms * 1e-3) / 1e9
-    digest = build.source_digest()
+    digest = build.kernel_digest("verify")
     traffic, traffic_src = recorded_traffic(w.name, digest)
 
     # read-only streaming probe (2 GiB), for context
@@ -475,6 +602,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel != "verify":
+        run_rows(args)
     else:
         run_ours(args)
 

@@ -197,6 +197,42 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
  */
 sv_status spec_verify_device_error(void* stream);
 
+/*
+ * The draft generator's step, for `rows` independent rows of draft-head logits (row r at element
+ * r * row_stride of draft_logits, device memory of dtype; uniforms [rows] fp32 in [0, 1)):
+ *   out_tokens[r] = a token drawn from q'_r, the beta-biased softmax(z_r / T) (bias set: the
+ *     bias_k ids with the largest logit, ties to the lower id, probabilities scaled by beta and
+ *     renormalised; Saguaro summary, "Method": drafts are drawn from q'), by the same inverse CDF
+ *     the verify step uses: the smallest v with C(v) > uniforms[r] * W over ascending ids;
+ *   out_conf[r] = max_v q_r(v), the unbiased softmax's largest probability (Kangaroo guide,
+ *     "Exit 2": c_i = max_v P-hat(v), drafting halts when c_i < tau);
+ *   out_exit[r] (may be NULL) = 1 if out_conf[r] < tau, else 0.
+ * A row holding NaN / +inf or only -inf gives token -1, conf NaN, exit -1. Same temperature and
+ * beta checks as spec_verify; bias_k in 0..8. Asynchronous on `stream`.
+ */
+sv_status spec_draft_sample(int rows, int V, sv_dtype dtype, long long row_stride,
+                            const void* draft_logits, const float* uniforms, float temperature,
+                            float beta, int bias_k, float tau, int32_t* out_tokens,
+                            float* out_conf, int32_t* out_exit, void* stream);
+
+/*
+ * Exact-residual top-F ids: for every sequence b and position i < L_b, out_r2[b][i][f] for
+ * f < F_i (prob->fanout, required) = the f-th id of the residual r_i = max(p_i - q'_i, 0) ordered by
+ * value (descending, ties to the lower id), restricted to r > 0; -1 elsewhere and for invalid
+ * sequences or rows. These are the ids the verify step's residual draw is most likely to emit
+ * after a rejection at i, to be compared with the top-F draft ids a speculation cache prepares
+ * (Saguaro summary, "Key claims"). With the outputs of a spec_verify call on the same inputs
+ * (accept_len, out_tokens, and its out_residual_topF as r1_topF, all device memory), out_hit[b] =
+ * 1 if the drawn token at the decided position a_b < L_b is among r1_topF[b][a_b][0..F_{a_b}), 0
+ * if not, -1 when every draft was accepted or the sequence is invalid; pass all four as NULL to
+ * skip. out_r2 is [B][K][max_i F_i] int32. Same shape and scalar checks as spec_verify.
+ */
+sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
+                             const void* draft_logits, const int32_t* draft_lens,
+                             float temperature, float beta, const int32_t* accept_len,
+                             const int32_t* out_tokens, const int32_t* r1_topF, int32_t* out_r2,
+                             int32_t* out_hit, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* spec_verify_status_string(sv_status status);
 

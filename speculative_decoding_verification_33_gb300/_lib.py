@@ -18,7 +18,7 @@ SV_MODE_GREEDY, SV_MODE_STOCHASTIC = 0, 1
 # every entry point the header declares (checked by the tests against include/*.h)
 EXPORTS = ("spec_verify", "spec_verify_workspace_bytes", "spec_verify_ws", "spec_verify_debug",
            "spec_verify_host", "spec_verify_device_error", "spec_verify_status_string",
-           "spec_verify_plan", "spec_verify_noalloc",
+           "spec_verify_plan", "spec_verify_noalloc", "spec_draft_sample", "spec_residual_topf",
            "sv_hbm_read_probe")
 
 
@@ -66,6 +66,9 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.spec_verify_status_string.restype = ctypes.c_char_p
         lib.sv_hbm_read_probe.argtypes = [_P, _SZ, _P, _P]
         lib.spec_verify_plan.argtypes = [_PROB, _I, _P, _P, _P]
+        lib.spec_draft_sample.argtypes = [_I, _I, _I, ctypes.c_longlong, _P, _P, _F, _F, _I,
+                                          _F, _P, _P, _P, _P]
+        lib.spec_residual_topf.argtypes = [_PROB, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P, _P]
         for name in EXPORTS:
             if name not in ("spec_verify_workspace_bytes", "spec_verify_status_string"):
                 getattr(lib, name).restype = _I

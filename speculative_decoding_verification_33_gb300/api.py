@@ -135,6 +135,68 @@ def verify(target_logits, draft_logits, draft_tokens, draft_lens=None, uniforms=
     return out
 
 
+def draft_sample(draft_logits: torch.Tensor, uniforms: torch.Tensor, *, temperature: float = 1.0,
+                 beta: float = 1.0, bias_k: int = 0, tau: float = 0.0, stream=None, out=None):
+    """Draw one token per row from the beta-biased draft distribution q' and report the exit
+    confidence max q (see ``spec_draft_sample`` in include/spec_verify.h).
+
+    ``draft_logits`` is [R, V] (rows contiguous, any row stride) bf16 or f32 on the GPU,
+    ``uniforms`` [R] float32. Returns {"tokens": [R] int32, "conf": [R] float32,
+    "exit": [R] int32}; ``out`` may supply those tensors.
+    """
+    if draft_logits.dim() != 2 or draft_logits.stride(1) != 1:
+        raise ValueError("draft_logits must be [R, V] with contiguous rows")
+    R, V = draft_logits.shape
+    if uniforms.shape != (R,):
+        raise ValueError(f"uniforms must be [{R}]")
+    dev = draft_logits.device
+    if out is None:
+        out = {"tokens": torch.empty(R, dtype=torch.int32, device=dev),
+               "conf": torch.empty(R, dtype=torch.float32, device=dev),
+               "exit": torch.empty(R, dtype=torch.int32, device=dev)}
+    stride = draft_logits.stride(0) if R > 1 else V
+    st = _lib.load().spec_draft_sample(
+        int(R), int(V), _dtype_code(draft_logits), int(stride), _ptr(draft_logits, "draft_logits"),
+        _ptr(uniforms, "uniforms", torch.float32), float(temperature), float(beta), int(bias_k),
+        float(tau), _ptr(out["tokens"], "tokens", torch.int32),
+        _ptr(out["conf"], "conf", torch.float32), _ptr(out.get("exit"), "exit", torch.int32),
+        _stream_handle(stream))
+    _lib._check(st, "spec_draft_sample")
+    return out
+
+
+def residual_topf(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                  draft_lens: Optional[torch.Tensor], fanout: Sequence[int], *,
+                  temperature: float = 1.0, beta: float = 1.0, bias_k: int = 0,
+                  verify_out: Optional[dict] = None, stream=None):
+    """Top-F ids of the exact residual max(p - q', 0) at every draft position, and (given the
+    ``verify`` outputs with ``topf`` of the same call) the per-sequence cache-hit flags (see
+    ``spec_residual_topf`` in include/spec_verify.h). Returns {"r2": [B, K, max F] int32} plus
+    "hit": [B] int32 when ``verify_out`` is given."""
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    ts = _row_stride(target_logits, K + 1, "target_logits")
+    ds = _row_stride(draft_logits, K, "draft_logits")
+    if draft_logits.dtype != target_logits.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    prob, keep = _lib.make_problem(B, K, V, _dtype_code(target_logits), ts, ds, bias_k, fanout)
+    dev = target_logits.device
+    out = {"r2": torch.empty(B, K, max(max(fanout), 1), dtype=torch.int32, device=dev)}
+    acc = tok = r1 = hit = None
+    if verify_out is not None:
+        acc, tok, r1 = verify_out["accept_len"], verify_out["tokens"], verify_out["topf"]
+        out["hit"] = hit = torch.empty(B, dtype=torch.int32, device=dev)
+    st = _lib.call("spec_residual_topf", prob, _ptr(target_logits, "target_logits"),
+                   _ptr(draft_logits, "draft_logits"),
+                   _ptr(draft_lens, "draft_lens", torch.int32), float(temperature), float(beta),
+                   _ptr(acc, "accept_len", torch.int32), _ptr(tok, "tokens", torch.int32),
+                   _ptr(r1, "topf", torch.int32), _ptr(out["r2"], "r2", torch.int32),
+                   _ptr(hit, "hit", torch.int32), _stream_handle(stream))
+    del keep
+    _lib._check(st, "spec_residual_topf")
+    return out
+
+
 def _host_ptr(a) -> int:
     if a is None:
         return 0

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspecverify.so"
-SOURCES = ["sv_kernel.cu", "sv_api.cu", "sv_probe.cu"]
+SOURCES = ["sv_kernel.cu", "sv_api.cu", "sv_probe.cu", "sv_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
@@ -44,6 +44,24 @@ def source_digest() -> str:
             h.update(f.encode())
             with open(p, "rb") as fh:
                 h.update(fh.read())
+    h.update(" ".join(ARCH + FLAGS[:4]).encode())
+    return h.hexdigest()[:16]
+
+
+# the files each kernel's code comes from (a recorded profile stays valid while they are unchanged)
+KERNEL_SOURCES = {
+    "verify": ("sv_kernel.cu", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h"),
+    "rows": ("sv_rows.cu", "sv_rows.h", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h"),
+}
+
+
+def kernel_digest(kernel: str) -> str:
+    """Hash of the sources one kernel is compiled from, plus the code-generation flags."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(f.encode())
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
     h.update(" ".join(ARCH + FLAGS[:4]).encode())
     return h.hexdigest()[:16]
 

@@ -15,6 +15,7 @@
 
 #include "spec_verify.h"
 #include "sv_internal.h"
+#include "sv_rows.h"
 #include "sv_probe.h"
 
 namespace {
@@ -474,6 +475,114 @@ sv_status spec_verify_device_error(void* stream) {
   if (!err) return SV_OK;
   if (cudaMemset(&ws->error, 0, sizeof(err)) != cudaSuccess) return SV_ERR_CUDA;
   return SV_ERR_DEVICE_TIMEOUT;
+}
+
+// ---------------------------------------------------------------------------------------------
+// row kernels: draft sampling and the exact-residual top-F
+// ---------------------------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+// Cluster size and slice of the row kernels: about 40 KB of a row per CTA (20480 bf16 or 10240
+// fp32 entries), up to 16 CTAs per row.
+void row_split(int V, size_t elt, int* C, int* slice) {
+  const long long per_cta = elt == 2 ? 20480 : 10240;
+  int c = 1;
+  while (c < 16 && static_cast<long long>(c) * per_cta < V) c <<= 1;
+  *C = c;
+  *slice = static_cast<int>(((static_cast<long long>(V) + c - 1) / c + 7) / 8 * 8);
+}
+
+bool aligned16(const void* p, long long stride, size_t elt) {
+  return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (stride * static_cast<long long>(elt)) % 16 == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+sv_status spec_draft_sample(int rows, int V, sv_dtype dtype, long long row_stride,
+                            const void* draft_logits, const float* uniforms, float temperature,
+                            float beta, int bias_k, float tau, int32_t* out_tokens,
+                            float* out_conf, int32_t* out_exit, void* stream) {
+  if (rows < 0 || V < 1 || V > sv::kMaxV || row_stride < V) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_INVALID_ARG;
+  if (!finite_in(temperature, 1e-4f, 1e4f)) return SV_ERR_INVALID_ARG;
+  if (!(std::isfinite(beta) && beta > 0.f && beta <= 1.f)) return SV_ERR_INVALID_ARG;
+  if (bias_k < 0 || bias_k > 8 || !std::isfinite(tau)) return SV_ERR_INVALID_ARG;
+  if (rows == 0) return SV_OK;
+  if (!draft_logits || !uniforms || !out_tokens || !out_conf) return SV_ERR_INVALID_ARG;
+  const size_t elt = dtype == SV_DTYPE_BF16 ? 2 : 4;
+  sv::RowParams P;
+  memset(&P, 0, sizeof(P));
+  P.dft = draft_logits;
+  P.d_stride = row_stride;
+  P.V = V;
+  P.K = 1;
+  P.B = rows;
+  P.uni = uniforms;
+  P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  P.beta = beta;
+  P.bias_k = beta < 1.f ? bias_k : 0;
+  P.tau = tau;
+  P.out_tok = out_tokens;
+  P.out_conf = out_conf;
+  P.out_exit = out_exit;
+  int C = 1;
+  row_split(V, elt, &C, &P.slice);
+  P.use_vec = aligned16(draft_logits, row_stride, elt) ? 1 : 0;
+  const cudaError_t e = sv::launch_rows(P, 0, dtype == SV_DTYPE_BF16 ? 1 : 0, rows, C, nullptr,
+                                        nullptr, nullptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
+                             const void* draft_logits, const int32_t* draft_lens,
+                             float temperature, float beta, const int32_t* accept_len,
+                             const int32_t* out_tokens, const int32_t* r1_topF, int32_t* out_r2,
+                             int32_t* out_hit, void* stream) {
+  Checked c;
+  const int one = 1;
+  const float u = 0.5f;
+  sv_status st = check_args(prob, target_logits, draft_logits, &one, &u, temperature, beta,
+                            SV_MODE_STOCHASTIC, &one, &one, prob && prob->fanout ? &one : nullptr,
+                            &c);
+  if (st != SV_OK) return st;
+  if (c.fmax < 1) return SV_ERR_INVALID_ARG;  // the top-F widths come from prob->fanout
+  const bool want_hit = out_hit != nullptr;
+  if (want_hit != (accept_len != nullptr) || want_hit != (out_tokens != nullptr) ||
+      want_hit != (r1_topF != nullptr))
+    return SV_ERR_INVALID_ARG;
+  if (prob->B == 0) return SV_OK;
+  if (!out_r2) return SV_ERR_INVALID_ARG;
+  sv::RowParams P;
+  memset(&P, 0, sizeof(P));
+  P.tgt = target_logits;
+  P.dft = draft_logits;
+  P.t_stride = prob->target_row_stride;
+  P.d_stride = prob->draft_row_stride;
+  P.V = prob->V;
+  P.K = prob->K;
+  P.B = prob->B;
+  P.lens = draft_lens;
+  P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  P.beta = beta;
+  P.bias_k = beta < 1.f ? prob->bias_k : 0;
+  P.fmax = c.fmax;
+  for (int i = 0; i < sv::kMaxK; ++i) P.fan[i] = c.fan[i];
+  P.out_r2 = out_r2;
+  P.out_hit = out_hit;
+  int C = 1;
+  row_split(prob->V, c.elt, &C, &P.slice);
+  P.use_vec = (aligned16(target_logits, prob->target_row_stride, c.elt) &&
+               aligned16(draft_logits, prob->draft_row_stride, c.elt))
+                  ? 1
+                  : 0;
+  const cudaError_t e = sv::launch_rows(P, 1, prob->dtype == SV_DTYPE_BF16 ? 1 : 0,
+                                        prob->B * prob->K, C, accept_len, out_tokens, r1_topF,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 const char* spec_verify_status_string(sv_status status) {

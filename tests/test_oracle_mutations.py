@@ -85,3 +85,54 @@ def test_higher_id_tie_break_is_caught(monkeypatch):
         return np.asarray(order[:k], dtype=np.int64)
     monkeypatch.setattr(O, "top_ids", wrong)
     _fails(P.test_top_ids_planted_ties)
+
+
+# ---- row steps (oracle/rows.py) ----
+from oracle import rows as RO  # noqa: E402
+from tests import test_oracle_rows_pins as RP  # noqa: E402
+
+
+def test_confidence_from_biased_draft_is_caught(monkeypatch):
+    real = RO.draft_sample
+
+    def wrong(row, u, *, temperature, beta=1.0, bias_k=0, tau=0.0):
+        d = real(row, u, temperature=temperature, beta=beta, bias_k=bias_k, tau=tau)
+        z = O.row_to_f64(np.asarray(row))
+        if O.row_is_bad(z):
+            return d
+        q, _ = O.softmax(z, temperature)
+        qb, _ = O.biased_draft(q, z, beta, bias_k)
+        d.conf = float(np.max(qb))
+        return d
+    monkeypatch.setattr(RO, "draft_sample", wrong)
+    _fails(RP.test_confidence_ignores_the_bias_and_sets_the_exit_flag)
+
+
+def test_draw_from_unbiased_draft_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "biased_draft", lambda q, zd, beta, k: (q, np.zeros(0, np.int64)))
+    _fails(RP.test_draw_frequencies_by_exact_enumeration, 1.0, 0.5, 2)
+
+
+def test_residual_against_unbiased_draft_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "biased_draft", lambda q, zd, beta, k: (q, np.zeros(0, np.int64)))
+    _fails(RP.test_residual_order_hand_examples)
+
+
+def test_residual_ties_to_higher_id_are_caught(monkeypatch):
+    real = RO.residual_order
+
+    def wrong(t, d, **kw):
+        r, ids = real(t, d, **kw)
+        return r, np.asarray(sorted(ids.tolist(), key=lambda v: (-round(r[v], 12), -v)))
+    monkeypatch.setattr(RO, "residual_order", wrong)
+    _fails(RP.test_residual_order_hand_examples)
+
+
+def test_hit_at_the_bonus_position_is_caught(monkeypatch):
+    def wrong(a, tokens, topf, L, fanout):
+        if a < 0:
+            return -1
+        a = min(a, L - 1)
+        return 1 if int(tokens[a]) in [int(v) for v in topf[a, :fanout[a]]] else 0
+    monkeypatch.setattr(RO, "cache_hit", wrong)
+    _fails(RP.test_cache_hit_hand_examples)

@@ -1,0 +1,220 @@
+"""GPU parity of the row kernels (draft draw with exit confidence, exact-residual top-F and the
+cache-hit flag), called through the C ABI, against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from oracle import rows as RO  # noqa: E402
+from oracle import verify as O  # noqa: E402
+from speculative_decoding_verification_33_gb300 import api  # noqa: E402
+from speculative_decoding_verification_33_gb300 import workloads as W  # noqa: E402
+
+REL_TOL = 1e-5
+MARGIN = 1e-6
+
+
+# ---------------------------------------------------------------------------------------------
+# draft draw
+# ---------------------------------------------------------------------------------------------
+def draft_rows(w, R, offset=0):
+    """[R, V] draft rows and [R] uniforms from the workload's generator (rows past a sequence's
+    draft length are NaN, so some rows are bad on purpose)."""
+    d = W.make_inputs(w, offset=offset)
+    rows = d["draft"].reshape(-1, w.V)[:R]
+    uni = d["uniforms"].reshape(-1)[:R].copy()
+    return rows, uni
+
+
+def check_draws(rows, uni, *, T, beta, bias_k, tau, pad=0, seqs=None):
+    host = np.pad(rows, ((0, 0), (0, pad))) if pad else rows
+    D = api.to_device_logits(host)
+    if pad:
+        D = D[:, : rows.shape[1]]
+    out = api.draft_sample(D, torch.from_numpy(uni).cuda(), temperature=T, beta=beta,
+                           bias_k=bias_k, tau=tau)
+    torch.cuda.synchronize()
+    tok, conf, ex = (out[k].cpu().numpy() for k in ("tokens", "conf", "exit"))
+    seqs = range(rows.shape[0]) if seqs is None else seqs
+    flagged = checked = 0
+    for r in seqs:
+        o = RO.draft_sample(rows[r], float(uni[r]), temperature=T, beta=beta, bias_k=bias_k,
+                            tau=tau)
+        checked += 1
+        if math.isnan(o.conf):
+            assert tok[r] == -1 and ex[r] == -1 and math.isnan(conf[r]), r
+            continue
+        assert abs(float(conf[r]) - o.conf) <= REL_TOL * o.conf, (r, conf[r], o.conf)
+        if abs(o.conf - tau) > REL_TOL * o.conf:
+            assert ex[r] == o.exit, (r, ex[r], o.exit)
+        if o.margin < MARGIN:
+            flagged += 1
+            assert tok[r] >= 0
+            continue
+        assert tok[r] == o.token, (r, tok[r], o.token, o.margin)
+    return checked, flagged
+
+
+@pytest.mark.parametrize("cfg", [1, 3, 4, 5])
+def test_draft_draw_workload_rows(cfg):
+    w = W.small_variant(W.WORKLOADS[cfg], B=8)
+    rows, uni = draft_rows(w, 8 * w.K)
+    T = w.temperature if w.mode == "stochastic" else 1.0
+    checked, flagged = check_draws(rows, uni, T=T, beta=w.beta, bias_k=w.bias_k, tau=0.05)
+    assert flagged <= checked // 10
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 1000, 12289, 40000, 98305, 262144])
+def test_draft_draw_vocab_sizes(V):
+    """Cluster sizes 1 to 16 and ragged slice tails."""
+    w = W.small_variant(W.WORKLOADS[4], B=3, V=V).replace(bias_k=min(8, V))
+    rows, uni = draft_rows(w, 3 * w.K)
+    check_draws(rows, uni, T=1.0, beta=0.5, bias_k=w.bias_k, tau=0.2)
+    check_draws(rows, uni, T=0.7, beta=1.0, bias_k=0, tau=0.2)
+
+
+def test_draft_draw_unaligned_stride_and_f32():
+    w = W.small_variant(W.WORKLOADS[1], B=4, V=5003)
+    rows, uni = draft_rows(w, 4 * w.K)
+    check_draws(rows, uni, T=1.3, beta=0.3, bias_k=4, tau=0.01, pad=3)
+
+
+def test_draft_draw_bad_uniforms_and_rows():
+    w = W.small_variant(W.WORKLOADS[3], B=2, V=3000)
+    rows, uni = draft_rows(w, 2 * w.K)
+    rows = rows.copy()
+    uni[0], uni[1], uni[2] = 1.0, -0.5, np.nan
+    rows[3, 11] = W.BF16_NAN
+    rows[4, :] = 0xFF80  # all -inf
+    check_draws(rows, uni, T=0.8, beta=1.0, bias_k=0, tau=0.5)
+
+
+def test_draft_draw_frequencies_follow_biased_draft():
+    """Many draws of one row: token frequencies match q' (chi-square style bound)."""
+    V, n = 64, 1 << 16
+    rng = np.random.default_rng(9)
+    z = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    D = torch.from_numpy(np.tile(z, (n, 1))).cuda()
+    uni = torch.from_numpy(rng.random(n, dtype=np.float32)).cuda()
+    out = api.draft_sample(D, uni, temperature=0.9, beta=0.4, bias_k=3)
+    tok = out["tokens"].cpu().numpy()
+    q, _ = O.softmax(z.astype(np.float64), 0.9)
+    qb, _ = O.biased_draft(q, z.astype(np.float64), 0.4, 3)
+    freq = np.bincount(tok, minlength=V) / n
+    assert np.all(np.abs(freq - qb) <= 5 * np.sqrt(qb * (1 - qb) / n) + 1e-9)
+
+
+def test_draft_draw_empty_and_full_size_sample():
+    e = api.draft_sample(torch.zeros(0, 16, dtype=torch.bfloat16, device="cuda"),
+                         torch.zeros(0, dtype=torch.float32, device="cuda"))
+    assert e["tokens"].numel() == 0
+    w = W.WORKLOADS[5]
+    rows, uni = draft_rows(w, w.B * w.K)
+    check_draws(rows, uni, T=1.0, beta=0.5, bias_k=8, tau=0.1, seqs=range(0, w.B * w.K, 37))
+
+
+# ---------------------------------------------------------------------------------------------
+# exact-residual top-F and cache hits
+# ---------------------------------------------------------------------------------------------
+def residual_gpu(d, w, verify_out=None, pad=0):
+    tgt, dft = d["target"], d["draft"]
+    if pad:
+        tgt = np.pad(tgt, ((0, 0), (0, 0), (0, pad)))
+        dft = np.pad(dft, ((0, 0), (0, 0), (0, pad)))
+    T = api.to_device_logits(tgt)
+    D = api.to_device_logits(dft)
+    if pad:
+        T, D = T[:, :, : w.V], D[:, :, : w.V]
+    ln = torch.from_numpy(d["draft_lens"]).cuda()
+    out = api.residual_topf(T, D, ln, w.fanout, temperature=w.temperature, beta=w.beta,
+                            bias_k=w.bias_k, verify_out=verify_out)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def compare_residual(d, w, r2, seqs):
+    """Exact ids where the oracle's residual values are separated; at a near tie (within the
+    float32 error of p and q') any id of equal residual is accepted."""
+    near = 0
+    fmax = r2.shape[2]
+    for b in seqs:
+        L = int(d["draft_lens"][b])
+        for i in range(w.K):
+            got = r2[b, i].tolist()
+            if i >= L:
+                assert got == [-1] * fmax, (b, i, got)
+                continue
+            zt, zd = O.row_to_f64(d["target"][b, i]), O.row_to_f64(d["draft"][b, i])
+            if O.row_is_bad(zt) or O.row_is_bad(zd):
+                assert got == [-1] * fmax, (b, i, got)
+                continue
+            p, _ = O.softmax(zt, w.temperature)
+            q, _ = O.softmax(zd, w.temperature)
+            qb, _ = O.biased_draft(q, zd, w.beta, w.bias_k)
+            r, ids = RO.residual_order(d["target"][b, i], d["draft"][b, i],
+                                       temperature=w.temperature, beta=w.beta, bias_k=w.bias_k)
+            tol = 4e-6 * (p + qb) + 1e-12
+            F = min(w.fanout[i], 8)
+            assert got[F:] == [-1] * (fmax - F), (b, i, got)
+            real = [g for g in got[:F] if g >= 0]
+            assert len(set(real)) == len(real), (b, i, got)
+            for f in range(F):
+                o = int(ids[f]) if f < len(ids) else -1
+                g = got[f]
+                if g == o:
+                    continue
+                near += 1
+                ro = r[o] if o >= 0 else 0.0
+                to = tol[o] if o >= 0 else 0.0
+                rg = (p[g] - qb[g]) if g >= 0 else 0.0
+                tg = tol[g] if g >= 0 else 0.0
+                assert abs(rg - ro) <= tg + to, (b, i, f, g, o, rg, ro)
+    return near
+
+
+@pytest.mark.parametrize("cfg", [4, 3, 5])
+def test_residual_topf_and_hits(cfg):
+    w = W.WORKLOADS[cfg]
+    if w.fanout is None:
+        w = w.replace(fanout=(8, 4, 2, 1, 1, 1, 1, 1)[: w.K])
+    if cfg == 5:
+        w = w.replace(B=24)
+    d = W.make_inputs(w)
+    Tt = api.to_device_logits(d["target"])
+    Dd = api.to_device_logits(d["draft"])
+    vo = api.verify(Tt, Dd, torch.from_numpy(d["draft_tokens"]).cuda(),
+                    torch.from_numpy(d["draft_lens"]).cuda(),
+                    torch.from_numpy(d["uniforms"]).cuda(), temperature=w.temperature,
+                    beta=w.beta, mode="stochastic", bias_k=w.bias_k, fanout=w.fanout)
+    g = residual_gpu(d, w, verify_out=vo)
+    near = compare_residual(d, w, g["r2"], range(w.B))
+    assert near <= w.B * w.K // 20
+    # hit flags: the oracle's own verify outcome against its own top-F keys
+    res = O.verify_batch(d["target"], d["draft"], d["draft_tokens"], d["draft_lens"],
+                         d["uniforms"], temperature=w.temperature, mode="stochastic",
+                         beta=w.beta, bias_k=w.bias_k, fanout=w.fanout)
+    hits = 0
+    for b, r in enumerate(res):
+        if r.first_flag() is not None:
+            continue
+        ref = RO.cache_hit(r.accept_len, r.tokens, r.topf, int(d["draft_lens"][b]), w.fanout)
+        assert g["hit"][b] == ref, (b, g["hit"][b], ref)
+        hits += ref == 1
+    print(w.name, "near ties", near, "hits", hits)
+
+
+@pytest.mark.parametrize("V", [1, 9, 3001, 50000])
+def test_residual_topf_vocab_sizes_and_stride(V):
+    w = W.small_variant(W.WORKLOADS[4], B=4, V=V).replace(bias_k=min(8, V))
+    d = W.make_inputs(w)
+    d["draft_lens"][1] = 0  # invalid length: every position -1
+    compare_residual(d, w, residual_gpu(d, w)["r2"], range(w.B))
+    compare_residual(d, w, residual_gpu(d, w, pad=5)["r2"], range(w.B))
+    w1 = w.replace(beta=1.0, bias_k=0)
+    compare_residual(d, w1, residual_gpu(d, w1)["r2"], range(w.B))

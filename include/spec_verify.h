@@ -208,7 +208,9 @@ sv_status spec_verify_device_error(void* stream);
  *     "Exit 2": c_i = max_v P-hat(v), drafting halts when c_i < tau);
  *   out_exit[r] (may be NULL) = 1 if out_conf[r] < tau, else 0.
  * A row holding NaN / +inf or only -inf gives token -1, conf NaN, exit -1. Same temperature and
- * beta checks as spec_verify; bias_k in 0..8. Asynchronous on `stream`.
+ * beta checks as spec_verify; bias_k in 0..8. Asynchronous on `stream`, on the stream's workspace
+ * (allocated on first use, like spec_verify's); a device-side wait that gave up is reported by
+ * spec_verify_device_error on the same stream.
  */
 sv_status spec_draft_sample(int rows, int V, sv_dtype dtype, long long row_stride,
                             const void* draft_logits, const float* uniforms, float temperature,
@@ -225,7 +227,8 @@ sv_status spec_draft_sample(int rows, int V, sv_dtype dtype, long long row_strid
  * (accept_len, out_tokens, and its out_residual_topF as r1_topF, all device memory), out_hit[b] =
  * 1 if the drawn token at the decided position a_b < L_b is among r1_topF[b][a_b][0..F_{a_b}), 0
  * if not, -1 when every draft was accepted or the sequence is invalid; pass all four as NULL to
- * skip. out_r2 is [B][K][max_i F_i] int32. Same shape and scalar checks as spec_verify.
+ * skip. out_r2 is [B][K][max_i F_i] int32. Same shape and scalar checks as spec_verify
+ * (prob->cluster_hint is not used). Asynchronous on `stream`, on the stream's workspace.
  */
 sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
                              const void* draft_logits, const int32_t* draft_lens,

@@ -484,18 +484,48 @@ sv_status spec_verify_device_error(void* stream) {
 
 namespace {
 
-// Cluster size and slice of the row kernels: about 40 KB of a row per CTA (20480 bf16 or 10240
-// fp32 entries), up to 16 CTAs per row.
-void row_split(int V, size_t elt, int* C, int* slice) {
-  const long long per_cta = elt == 2 ? 20480 : 10240;
-  int c = 1;
-  while (c < 16 && static_cast<long long>(c) * per_cta < V) c <<= 1;
-  *C = c;
-  *slice = static_cast<int>(((static_cast<long long>(V) + c - 1) / c + 7) / 8 * 8);
-}
+// dev, mode, dtype, bias, V -> (ring stages, CTAs per SM)
+std::map<std::tuple<int, int, int, int, int>, std::pair<int, int>> g_row_occ;
 
 bool aligned16(const void* p, long long stride, size_t elt) {
   return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (stride * static_cast<long long>(elt)) % 16 == 0;
+}
+
+// Launch one row kernel over `units` rows / pairs with persistent CTAs (as many as fit on the
+// device, at most one per unit), on the stream's workspace (queue counters and error word). The
+// ring gets the most stages that still let two CTAs share an SM (at least 3); failing that, one
+// CTA per SM with up to kRowMaxStages.
+sv_status run_rows(sv::RowParams& P, int mode, int dtype, int units, const int32_t* acc,
+                   const int32_t* tok, const int32_t* r1, cudaStream_t stream) {
+  const bool bias = P.bias_k > 0 && P.beta < 1.f;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const auto key = std::make_tuple(dev, mode, dtype, bias ? 1 : 0, P.V);
+  auto it = g_row_occ.find(key);
+  if (it == g_row_occ.end()) {
+    int nst = 0, per_sm = 0;
+    for (int st = sv::kRowMaxStages; st >= 3 && !nst; --st)
+      if (sv::row_smem_bytes(mode, P.V, st) <= 112 * 1024) nst = st;
+    if (nst) per_sm = sv::row_ctas_per_sm(mode, dtype, bias, P.V, nst);
+    if (per_sm < 2) {
+      nst = 0;
+      for (int st = sv::kRowMaxStages; st >= 2 && !nst; --st)
+        if (sv::row_smem_bytes(mode, P.V, st) <= sv::kRowMaxSmem) nst = st;
+      per_sm = nst ? sv::row_ctas_per_sm(mode, dtype, bias, P.V, nst) : 0;
+    }
+    it = g_row_occ.emplace(key, std::make_pair(nst, per_sm)).first;
+  }
+  const int nst = it->second.first, per_sm = it->second.second;
+  if (nst < 2 || per_sm < 1) return SV_ERR_UNSUPPORTED;
+  P.nstages = nst;
+  sv_status st = SV_OK;
+  StreamRes* r = resources(dev, stream, sv::workspace_bytes_for(0), &st);
+  if (!r) return st;
+  P.ws = r->ws;
+  const int ctas = std::min(units, per_sm * sm_count(dev));
+  return sv::launch_rows(P, mode, dtype, ctas, acc, tok, r1, stream) == cudaSuccess ? SV_OK
+                                                                                     : SV_ERR_CUDA;
 }
 
 }  // namespace
@@ -529,12 +559,9 @@ sv_status spec_draft_sample(int rows, int V, sv_dtype dtype, long long row_strid
   P.out_tok = out_tokens;
   P.out_conf = out_conf;
   P.out_exit = out_exit;
-  int C = 1;
-  row_split(V, elt, &C, &P.slice);
   P.use_vec = aligned16(draft_logits, row_stride, elt) ? 1 : 0;
-  const cudaError_t e = sv::launch_rows(P, 0, dtype == SV_DTYPE_BF16 ? 1 : 0, rows, C, nullptr,
-                                        nullptr, nullptr, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  return run_rows(P, 0, dtype == SV_DTYPE_BF16 ? 1 : 0, rows, nullptr, nullptr, nullptr,
+                  static_cast<cudaStream_t>(stream));
 }
 
 sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
@@ -556,6 +583,7 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
     return SV_ERR_INVALID_ARG;
   if (prob->B == 0) return SV_OK;
   if (!out_r2) return SV_ERR_INVALID_ARG;
+  if (static_cast<long long>(prob->B) * prob->K > (1LL << 30)) return SV_ERR_UNSUPPORTED;
   sv::RowParams P;
   memset(&P, 0, sizeof(P));
   P.tgt = target_logits;
@@ -573,16 +601,12 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
   for (int i = 0; i < sv::kMaxK; ++i) P.fan[i] = c.fan[i];
   P.out_r2 = out_r2;
   P.out_hit = out_hit;
-  int C = 1;
-  row_split(prob->V, c.elt, &C, &P.slice);
   P.use_vec = (aligned16(target_logits, prob->target_row_stride, c.elt) &&
                aligned16(draft_logits, prob->draft_row_stride, c.elt))
                   ? 1
                   : 0;
-  const cudaError_t e = sv::launch_rows(P, 1, prob->dtype == SV_DTYPE_BF16 ? 1 : 0,
-                                        prob->B * prob->K, C, accept_len, out_tokens, r1_topF,
-                                        static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  return run_rows(P, 1, prob->dtype == SV_DTYPE_BF16 ? 1 : 0, prob->B * prob->K, accept_len,
+                  out_tokens, r1_topF, static_cast<cudaStream_t>(stream));
 }
 
 const char* spec_verify_status_string(sv_status status) {

@@ -237,6 +237,19 @@ __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Packed bf16 pairs: maximum that ignores NaN, and difference rounded to nearest.
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // 2^x on the special-function unit (flushes subnormal results to zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2_fast(float x) {
   float y;

@@ -10,26 +10,27 @@
 //    ids a speculation cache prepares (Saguaro summary, "Key claims" and "Method"), and whether
 //    the realised token at the decided position was among the cache's guesses.
 //
-// One thread-block cluster of C CTAs per row (sampling) or per (sequence, position) pair
-// (residual); each CTA owns a contiguous slice of the vocabulary, read with 128-bit loads issued
-// a batch at a time so that every thread keeps several in flight.
+// Persistent CTAs with three kinds of warps, one row (sampling) or one (sequence, position) pair
+// (residual) -- a unit -- at a time, taken from a device queue:
+//  - a producer warp streams the units' rows through a ring of shared-memory stages with bulk
+//    asynchronous copies;
+//  - eight chunk warps reduce every 64-element group of a row to its maximum g and (sampling)
+//    its mass, the sum of 2^(z c - fl(g c)), written to one of two group buffers, and each
+//    row to its maximum and softmax sum;
+//  - a team of four epilogue warps finishes a unit from its group buffer while the chunk warps
+//    fill the other buffer with the next unit, so the stream never waits for an epilogue.
 //
-// Sampling reads its row once. Each 8-element vector's mass, the sum of 2^(z c - m c), is kept in
-// shared memory relative to the thread's running maximum m (rescaled when m rises); once the
-// cluster has combined the row maximum and sum, every mass is brought to the row maximum with
-// one factor per thread and the (at most 8) biased ids are corrected. That gives the fixed-point
-// masses of the inverse CDF without a second pass over the row: only the 8 elements of the
-// chosen vector are read again.
-//
-// The residual needs the normalisers of both rows before any weight is known, so it reads the
-// pair twice (the second pass mostly from L2). In that pass an element whose target weight
-// 2^(z_t c - M_t c) is already below the warp's 8th best residual cannot enter the top 8 (the
-// residual never exceeds it): the test is a compare in the log domain, and only the elements
-// that pass it pay for exponentials.
-//
-// Top-8 selections (the bias set, the residual ids) keep one running list per warp, spread over
-// lanes 0..7, with a threshold every lane shares: after the first few offers almost every
-// element fails one compare and the warp moves on after a single vote.
+// The epilogue works from the group values, with a handful of groups read again:
+//  - the row maximum and sum come with the buffer (softmax normaliser, exit confidence 1 / sum);
+//  - the bias set (the bias_k largest draft logits): a lower bound of the 8th largest element is
+//    the largest of the warps' 8th-largest per-thread maxima, and only the groups whose maximum
+//    reaches it (a few) are looked at element by element;
+//  - the draw: group masses scaled to the row maximum (the biased ids corrected) give the
+//    fixed-point masses of the inverse CDF; the chosen group's 64 weights are recomputed to find
+//    the element;
+//  - the residual top 8: the residual never exceeds the target weight 2^(z_t c - M_t c), so the
+//    groups holding the largest target elements give a lower bound of the 8th best residual, and
+//    only the groups whose largest target weight reaches it are evaluated.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -42,151 +43,59 @@
 namespace sv {
 namespace {
 
-constexpr int RT = kRowThreads;
-constexpr int RW = RT / 32;
+constexpr int NCW = kRowChunkWarps;     // chunk warps
+constexpr int NEW = kRowEpilogueWarps;  // epilogue warps
+constexpr int CT = NCW * 32;            // chunk threads: 0 .. CT-1
+constexpr int ET = NEW * 32;            // epilogue threads: CT .. CT+ET-1
+constexpr int RT = kRowThreads;         // then the producer warp
+constexpr uint32_t kBarC = 1;           // named barrier of the chunk threads
+constexpr uint32_t kBarE = 2;           // named barrier of the epilogue threads
+constexpr int kStage = kRowStageBytes;  // bytes per ring stage
+constexpr int kGroup = 64;              // elements per group (8 vectors of 8)
 constexpr float kLn2r = 0.69314718055994531f;
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per barrier wait
 constexpr int MODE_SAMPLE = 0, MODE_RESID = 1;
+constexpr int kEnd = -1;  // unit tag after the last unit
+constexpr int kBatch = 4;  // candidate groups whose loads an epilogue warp keeps in flight
 
-// ------------------------------------------------------------------------------------------
-// raw 8-element vectors (loaded first, converted when used)
-// ------------------------------------------------------------------------------------------
-template <typename T>
-struct Raw8;
-
-template <>
-struct Raw8<uint16_t> {
-  uint4 a;
-  static constexpr int kBatch = 4;  // vectors per thread per batch of loads
-  __device__ __forceinline__ void load(const uint16_t* row, int e, int nv, bool vec) {
-    if (vec && e + 8 <= nv) {
-      a = ldg_nc_v4(row + e);
-      return;
-    }
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = (e + 2 * k < nv) ? row[e + 2 * k] : 0xFF80u;
-      const uint32_t hi = (e + 2 * k + 1 < nv) ? row[e + 2 * k + 1] : 0xFF80u;
-      w[k] = lo | (hi << 16);
-    }
-    a = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  __device__ __forceinline__ void get(float (&z)[8]) const { Elt<uint16_t>::unpack(a, z); }
-};
-
-template <>
-struct Raw8<float> {
-  uint4 a, b;
-  static constexpr int kBatch = 2;
-  __device__ __forceinline__ void load(const float* row, int e, int nv, bool vec) {
-    if (vec && e + 8 <= nv) {
-      a = ldg_nc_v4(row + e);
-      b = ldg_nc_v4(row + e + 4);
-      return;
-    }
-    float t[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = (e + k < nv) ? row[e + k] : -INFINITY;
-    a = make_uint4(__float_as_uint(t[0]), __float_as_uint(t[1]), __float_as_uint(t[2]),
-                   __float_as_uint(t[3]));
-    b = make_uint4(__float_as_uint(t[4]), __float_as_uint(t[5]), __float_as_uint(t[6]),
-                   __float_as_uint(t[7]));
-  }
-  __device__ __forceinline__ void get(float (&z)[8]) const {
-    z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y);
-    z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
-    z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y);
-    z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
-  }
-};
-
-__device__ __forceinline__ float max8(const float (&z)[8]) {
-  return max_nan(max_nan(max_nan(z[0], z[1]), max_nan(z[2], z[3])),
-                 max_nan(max_nan(z[4], z[5]), max_nan(z[6], z[7])));
-}
-
-// ------------------------------------------------------------------------------------------
-// shared state and block / cluster reductions
-// ------------------------------------------------------------------------------------------
-// A CTA's pass-1 partial, read by every CTA of the cluster.
-struct __align__(16) StatPart {
-  float m_t, s_t, m_d, s_d;   // slice maxima and sums 2^(z c - M c) (rounding of M c folded in)
-  unsigned long long top[8];  // the draft slice's top-8 keys (bias set), descending
-};
+static_assert(RT == CT + ET + 32, "chunk warps, epilogue warps, one producer warp");
+static_assert(kStage % (8 * kGroup) == 0, "whole groups per stage");
 
 struct RowShared {
-  float rmax[2][RW], rsum[2][RW];
-  unsigned long long ru[RW];
-  unsigned long long wtop[RW][8];
-  StatPart part;
-  alignas(16) unsigned long long part_w[2];  // sampling: the slice's fixed-point mass
-  alignas(16) unsigned long long part_r[8];  // residual: the slice's top-8 residual keys
-  // cluster-combined values (identical in every CTA)
-  float Mt, St, Md, Sd, N;
-  int bad, nS;
+  uint64_t full[kRowMaxStages], empty[kRowMaxStages];  // the ring
+  uint64_t gfull[2], gfree[2];                         // the two group buffers
+  int tag[kRowMaxStages];  // unit of the stage's chunk, or kEnd
+  int gunit[2];            // unit of the group buffer, or kEnd
+  float hdr[2][4];         // per buffer: row maximum and sum (target, then draft for a residual)
+  float cm[NCW], cs[NCW];  // chunk-warp scratch
+  // epilogue scratch
+  float rmax[NEW], rsum[NEW], rb[NEW];
+  unsigned long long ru[NEW];
+  unsigned long long wtop[NEW][8];
+  unsigned long long top[8];  // the last team top 8
+  float N;
+  int nS, gstar;
   int S_ids[8];
   float S_z[8];
   unsigned long long t_loc;
-  int cstar, token;
 };
 
-__device__ __forceinline__ void bsync() { __syncthreads(); }
+// The epilogue team: thread t of ET, warp t / 32.
+__device__ __forceinline__ int et() { return static_cast<int>(threadIdx.x) - CT; }
+__device__ __forceinline__ void esync() { named_sync(kBarE, ET); }
 
-// The two halves of cluster_sync(), for work that may run between them.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-__device__ float2 row_block_max2(float a, float b, RowShared& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  a = warp_max_nan(a);
-  b = warp_max_nan(b);
-  if (lane == 0) {
-    S.rmax[0][warp] = a;
-    S.rmax[1][warp] = b;
-  }
-  bsync();
-  float ra = S.rmax[0][0], rb = S.rmax[1][0];
-#pragma unroll
-  for (int w = 1; w < RW; ++w) {
-    ra = max_nan(ra, S.rmax[0][w]);
-    rb = max_nan(rb, S.rmax[1][w]);
-  }
-  bsync();
-  return make_float2(ra, rb);
-}
-
-__device__ float2 row_block_sum2(float a, float b, RowShared& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  a = warp_sum(a);
-  b = warp_sum(b);
-  if (lane == 0) {
-    S.rsum[0][warp] = a;
-    S.rsum[1][warp] = b;
-  }
-  bsync();
-  float va = 0.f, vb = 0.f;
-#pragma unroll
-  for (int w = 0; w < RW; ++w) {
-    va += S.rsum[0][w];
-    vb += S.rsum[1][w];
-  }
-  bsync();
-  return make_float2(va, vb);
-}
-
-__device__ unsigned long long row_block_sum_u64(unsigned long long v, RowShared& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// ------------------------------------------------------------------------------------------
+// epilogue team reductions
+// ------------------------------------------------------------------------------------------
+__device__ unsigned long long team_sum_u64(unsigned long long v, RowShared& S) {
+  const int lane = threadIdx.x & 31, warp = et() >> 5;
   v = warp_sum_u64(v);
   if (lane == 0) S.ru[warp] = v;
-  bsync();
+  esync();
   unsigned long long r = 0;
 #pragma unroll
-  for (int w = 0; w < RW; ++w) r += S.ru[w];
-  bsync();
+  for (int w = 0; w < NEW; ++w) r += S.ru[w];
+  esync();
   return r;
 }
 
@@ -200,24 +109,27 @@ __device__ __forceinline__ unsigned long long warp_inclusive_u64(unsigned long l
   return v;
 }
 
-__device__ unsigned long long row_block_exclusive_u64(unsigned long long v, RowShared& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ unsigned long long team_exclusive_u64(unsigned long long v, RowShared& S) {
+  const int lane = threadIdx.x & 31, warp = et() >> 5;
   const unsigned long long inc = warp_inclusive_u64(v);
   if (lane == 31) S.ru[warp] = inc;
-  bsync();
+  esync();
   unsigned long long base = 0;
   for (int w = 0; w < warp; ++w) base += S.ru[w];
-  bsync();
+  esync();
   return base + inc - v;
 }
 
-// The insertion behind WarpTop8::offer, out of line (its loop is long and rarely taken); state in
-// and out by value so that it stays in registers.
+// ------------------------------------------------------------------------------------------
+// top-8 selection: one running list per warp
+// ------------------------------------------------------------------------------------------
 struct Top8State {
   unsigned long long L;
   float thr;
 };
 
+// The insertion behind WarpTop8::offer, out of line (its loop is long and rarely taken); state in
+// and out by value so that it stays in registers.
 __device__ __noinline__ Top8State warp_top8_insert(unsigned pend, float z, uint32_t id,
                                                    Top8State st) {
   const int lane = threadIdx.x & 31;
@@ -241,448 +153,889 @@ __device__ __noinline__ Top8State warp_top8_insert(unsigned pend, float z, uint3
 }
 
 // A warp's running top 8: the keys, descending, in lanes 0..7 (0 = empty; the other lanes hold
-// 0), and the value of the 8th (-inf until 8 are held). An offer below it cannot enter, so after
-// the first few the common case is one compare and one vote per element.
+// 0), and a threshold every lane shares: nothing below it can enter (the 8th key's value once 8
+// are held, or a known lower bound of the final 8th).
 struct WarpTop8 {
   unsigned long long L;
   float thr;
-  __device__ __forceinline__ void init() {
+  __device__ __forceinline__ void init(float lower) {
     L = 0ull;
-    thr = -INFINITY;
+    thr = lower;
   }
-  // Every lane of the warp calls this; lane offers (z, id) when ok. True if the threshold rose.
-  __device__ __forceinline__ bool offer(bool ok, float z, uint32_t id) {
+  // Every lane of the warp calls this; a lane offers (z, id) when ok.
+  __device__ __forceinline__ void offer(bool ok, float z, uint32_t id) {
     const unsigned pend = __ballot_sync(FULL, ok && z >= thr);
-    if (!pend) return false;
-    const float before = thr;
+    if (!pend) return;
     const Top8State st = warp_top8_insert(pend, z, id, Top8State{L, thr});
     L = st.L;
     thr = st.thr;
-    return thr != before;
   }
 };
 
-// The warps' lists into the CTA's top 8 at dst (written by warp 0).
-__device__ void row_block_top8w(const WarpTop8& W, RowShared& S, unsigned long long* dst) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// The warps' lists into the team's top 8, S.top (every epilogue thread may read it on return).
+__device__ void team_top8(const WarpTop8& W, RowShared& S) {
+  const int lane = threadIdx.x & 31, warp = et() >> 5;
   if (lane < 8) S.wtop[warp][lane] = W.L;
-  bsync();
+  esync();
   if (warp == 0) {
-    static_assert(RW * 8 == 64, "two candidates per lane");
-    const unsigned long long c0 = S.wtop[lane >> 3][lane & 7];
-    const unsigned long long c1 = S.wtop[(lane >> 3) + 4][lane & 7];
+    static_assert(NEW * 8 == 32, "one candidate per lane");
     unsigned long long k8[8];
-    k8[0] = c0 > c1 ? c0 : c1;
-    k8[1] = c0 > c1 ? c1 : c0;
+    k8[0] = S.wtop[lane >> 3][lane & 7];
 #pragma unroll
-    for (int j = 2; j < 8; ++j) k8[j] = 0ull;
+    for (int j = 1; j < 8; ++j) k8[j] = 0ull;
     unsigned long long merged[8];
     warp_top8(k8, merged);
-    if (lane == 0)
+    if (lane < 8) {
+      unsigned long long mine = merged[0];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) dst[r] = merged[r];
+      for (int r = 1; r < 8; ++r) mine = lane == r ? merged[r] : mine;
+      S.top[lane] = mine;
+    }
   }
-  bsync();
+  esync();
 }
 
-// 16 bytes of a peer CTA's shared memory.
-__device__ __forceinline__ uint4 ld_peer_v4(const void* local_addr, uint32_t rank) {
-  const uint32_t a = map_to_rank(smem_u32(local_addr), rank);
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a)
-               : "memory");
+// The 8th largest of the warp's 32 values (on every lane): bitonic sort, descending by lane.
+__device__ __forceinline__ float warp_8th_largest(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(FULL, v, j);
+      const bool desc = (lane & k) == 0;
+      const bool low = (lane & j) == 0;
+      v = (low == desc) ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return __shfl_sync(FULL, v, 7);
+}
+
+// A lower bound of the 8th largest of the elements whose per-thread maxima are m (distinct
+// elements): some warp has 8 lanes whose maxima reach the largest of the warps' 8th-largest.
+__device__ float team_bound(float m, RowShared& S) {
+  const float w8 = warp_8th_largest(m);
+  if ((threadIdx.x & 31) == 0) S.rb[et() >> 5] = w8;
+  esync();
+  float b = S.rb[0];
+#pragma unroll
+  for (int w = 1; w < NEW; ++w) b = fmaxf(b, S.rb[w]);
+  esync();
+  return b;
+}
+
+// ------------------------------------------------------------------------------------------
+// element access and per-group values
+// ------------------------------------------------------------------------------------------
+// Two consecutive elements e, e+1 of a global row (e even; -inf past V); one load of both when
+// the row is 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ void ld2(const T* row, int e, int V, bool vec, float& a, float& b) {
+  if (vec && e + 1 < V) {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(row + e);
+      a = __uint_as_float(w << 16);
+      b = __uint_as_float(w & 0xFFFF0000u);
+    } else {
+      const float2 w = *reinterpret_cast<const float2*>(row + e);
+      a = w.x;
+      b = w.y;
+    }
+  } else {
+    a = e < V ? Elt<T>::val(row[e]) : -INFINITY;
+    b = e + 1 < V ? Elt<T>::val(row[e + 1]) : -INFINITY;
+  }
+}
+
+// Elements of a row per ring stage.
+template <typename T>
+__host__ __device__ constexpr int chunk_elems() {
+  return kStage / static_cast<int>(sizeof(T));
+}
+
+// A thread's running maximum m and sum 2^(z c - fl(m c)) over the groups it has reduced.
+struct RowRun {
+  float m, mc, s;
+  __device__ __forceinline__ void init() {
+    m = -INFINITY;
+    mc = -INFINITY;
+    s = 0.f;
+  }
+  // a group with maximum g (gc = fl(g c)) and mass sm relative to gc
+  __device__ __forceinline__ void add(float g, float gc, float sm) {
+    const float mn = max_nan(m, g);
+    if (mn != m) {
+      s = (m > -INFINITY ? s * exp2f(mc - gc) : 0.f) + sm;
+      m = mn;
+      mc = gc;
+    } else if (g > -INFINITY) {
+      s += sm * exp2f(gc - mc);
+    }
+  }
+};
+
+// Chunk geometry per lane: EPL contiguous elements, PPL 16-byte pieces of EPP elements; a group
+// of 64 elements spans LPG lanes.
+template <typename T>
+struct Lanes {
+  static constexpr int EPL = chunk_elems<T>() / CT;
+  static constexpr int EPP = 16 / static_cast<int>(sizeof(T));
+  static constexpr int PPL = EPL / EPP;
+  static constexpr int LPG = kGroup / EPL;
+  static_assert((PPL == 2 || PPL == 4) && LPG >= 2 && LPG <= 8, "lane geometry");
+  // The piece a lane reads in its j-th load: lanes take their pieces in rotated orders so that
+  // the eight lanes of each shared-memory phase hit eight distinct 16-byte bank groups.
+  static __device__ __forceinline__ int piece(int j, int lane) {
+    return (j + (lane >> (PPL == 4 ? 1 : 2))) & (PPL - 1);
+  }
+};
+
+// The lane's pieces of a staged chunk (n valid elements; elements at or past n read as -inf).
+// Max and sum do not care in which order the pieces sit.
+template <typename T>
+__device__ __forceinline__ void load_pieces(const T* stage, int n, uint4 (&q)[Lanes<T>::PPL]) {
+  using G = Lanes<T>;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int e_lane = G::EPL * tid;
+  const uint4* src = reinterpret_cast<const uint4*>(stage) + G::PPL * tid;
+#pragma unroll
+  for (int j = 0; j < G::PPL; ++j) q[j] = src[G::piece(j, lane)];
+  if (e_lane + G::EPL > n) {  // the row's last chunk
+#pragma unroll
+    for (int j = 0; j < G::PPL; ++j) {
+      const int e = e_lane + G::EPP * G::piece(j, lane);
+      uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t lo = e + 2 * h < n ? (w[h] & 0xFFFFu) : 0xFF80u;
+          const uint32_t hi = e + 2 * h + 1 < n ? (w[h] & 0xFFFF0000u) : 0xFF800000u;
+          w[h] = lo | hi;
+        } else {
+          w[h] = e + h < n ? w[h] : __float_as_uint(-INFINITY);
+        }
+      }
+      q[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack_piece(const uint4& q, float (&z)[16 / sizeof(T)]) {
+  if constexpr (sizeof(T) == 2) {
+    Elt<uint16_t>::unpack(q, z);
+  } else {
+    z[0] = __uint_as_float(q.x);
+    z[1] = __uint_as_float(q.y);
+    z[2] = __uint_as_float(q.z);
+    z[3] = __uint_as_float(q.w);
+  }
+}
+
+// Maximum over the lane's pieces.
+template <typename T>
+__device__ __forceinline__ float pieces_max(const uint4 (&q)[Lanes<T>::PPL]) {
+  if constexpr (sizeof(T) == 2) {
+    uint32_t mx = 0xFF80FF80u;
+#pragma unroll
+    for (int j = 0; j < Lanes<T>::PPL; ++j)
+      mx = max_nan_bf16x2(mx, max_nan_bf16x2(max_nan_bf16x2(q[j].x, q[j].y),
+                                             max_nan_bf16x2(q[j].z, q[j].w)));
+    return max_nan(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < Lanes<T>::PPL; ++j)
+      m = max_nan(max_nan(m, max_nan(__uint_as_float(q[j].x), __uint_as_float(q[j].y))),
+                  max_nan(__uint_as_float(q[j].z), __uint_as_float(q[j].w)));
+    return m;
+  }
+}
+
+// Sum of 2^(z c - gc) over the lane's pieces, two elements per packed instruction.
+template <typename T>
+__device__ __forceinline__ float pieces_mass(const uint4 (&q)[Lanes<T>::PPL], float c, float gc) {
+  const float2 c2 = make_float2(c, c), n2 = make_float2(-gc, -gc);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < Lanes<T>::PPL; ++j) {
+    float z[Lanes<T>::EPP];
+    unpack_piece<T>(q[j], z);
+#pragma unroll
+    for (int k = 0; k < Lanes<T>::EPP; k += 2) {
+      const float2 a = __ffma2_rn(make_float2(z[k], z[k + 1]), c2, n2);
+      acc = __fadd2_rn(acc, make_float2(ex2_fast(a.x), ex2_fast(a.y)));
+    }
+  }
+  return acc.x + acc.y;
+}
+
+template <int LPG>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = 1; o < LPG; o <<= 1) v = max_nan(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+template <int LPG>
+__device__ __forceinline__ float group_fmax(float v) {
+#pragma unroll
+  for (int o = 1; o < LPG; o <<= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+template <int LPG>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < LPG; o <<= 1) v += __shfl_xor_sync(FULL, v, o);
   return v;
 }
 
-// The top 8 of the C lists of 8 keys held at `list` in the CTAs of the cluster (one warp; the
-// result on every lane).
-__device__ void cluster_top8(const unsigned long long* list, uint32_t C,
-                             unsigned long long (&out)[8]) {
-  const int lane = threadIdx.x & 31;
-  const bool have = lane < static_cast<int>(C);
-  unsigned long long l[8];
-#pragma unroll
-  for (int r = 0; r < 8; r += 2) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (have) v = ld_peer_v4(list + r, static_cast<uint32_t>(lane));
-    l[r] = (static_cast<unsigned long long>(v.y) << 32) | v.x;
-    l[r + 1] = (static_cast<unsigned long long>(v.w) << 32) | v.z;
+// Group maxima and masses of one staged chunk (n valid elements) into gmax / gmass at the
+// chunk's first group; the groups also go into the thread's running row stats.
+template <typename T>
+__device__ __forceinline__ void chunk_groups(const T* stage, int n, float c, float* gmax,
+                                             float* gmass, RowRun& run) {
+  using G = Lanes<T>;
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint4 q[G::PPL];
+  load_pieces<T>(stage, n, q);
+  const float g = group_max<G::LPG>(pieces_max<T>(q));
+  const float gc = __fmul_rn(g, c);
+  const float sm = group_sum<G::LPG>(g > -INFINITY ? pieces_mass<T>(q, c, gc) : 0.f);
+  if ((lane & (G::LPG - 1)) == 0 && G::EPL * tid < n) {
+    gmax[tid / G::LPG] = g;
+    gmass[tid / G::LPG] = sm;
+    run.add(g, gc, sm);
   }
-  warp_top8(l, out);
 }
 
-// Warp 0 merges the C partials of the cluster (read from every CTA's shared memory, in rank
-// order, so every CTA reaches the same values) into S.Mt .. S.S_z; with a bias set, also the
-// draft row's top 8 and the Saguaro renormalisation N.
-__device__ void row_combine(const RowParams& P, RowShared& S, uint32_t C, bool two, bool bias) {
-  const int lane = threadIdx.x & 31;
-  const float c = P.c;
-  const bool have = lane < static_cast<int>(C);
-  float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
-  if (have) {
-    const uint4 a = ld_peer_v4(&S.part.m_t, static_cast<uint32_t>(lane));
-    mt = __uint_as_float(a.x);
-    st = __uint_as_float(a.y);
-    md = __uint_as_float(a.z);
-    sd = __uint_as_float(a.w);
-  }
-  const float Mt = warp_max_nan(mt), Md = warp_max_nan(md);
-  const float tt = (two && have && mt > -INFINITY && !row_bad(Mt)) ? st * exp2f((mt - Mt) * c) : 0.f;
-  const float td = (have && md > -INFINITY && !row_bad(Md)) ? sd * exp2f((md - Md) * c) : 0.f;
-  const float St = warp_sum(tt), Sd = warp_sum(td);
-  unsigned long long mtop[8];
-  if (bias) cluster_top8(S.part.top, C, mtop);
-  if (lane == 0) {
-    S.Mt = Mt;
-    S.St = St;
-    S.Md = Md;
-    S.Sd = Sd;
-    S.bad = (two && row_bad(Mt)) || row_bad(Md);
-    float N = 1.f;
-    int nS = 0;
-    if (bias && !S.bad) {  // Saguaro bias set: the bias_k most likely draft ids
-      float sq = 0.f;
-      for (int j = 0; j < P.bias_k; ++j) {
-        if (mtop[j] == 0ull) break;
-        const float z = key_value(mtop[j]);
-        sq += exp2f((z - Md) * c) / Sd;
-        S.S_z[nS] = z;
-        S.S_ids[nS++] = key_id(mtop[j]);
-      }
-      N = fmaf(-(1.f - P.beta), sq, 1.f);
+// Residual chunks: the same for a target and a draft chunk at once (n valid elements each), plus
+// each group's largest log-ratio max (z_t - z_d), which bounds the group's residual from above
+// once the normalisers are known.
+template <typename T>
+__device__ __forceinline__ void chunk_pair(const T* st_t, const T* st_d, int n, float c,
+                                           float* gmax_t, float* gmax_d, float* gdel,
+                                           RowRun& run_t, RowRun& run_d) {
+  using G = Lanes<T>;
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint4 qt[G::PPL], qd[G::PPL];
+  load_pieces<T>(st_t, n, qt);
+  load_pieces<T>(st_d, n, qd);
+  float dl = -INFINITY;
+  if constexpr (sizeof(T) == 2) {
+    // the largest difference of packed bf16 pairs (-inf - -inf is NaN, which the plain max
+    // ignores), rounded to bf16 and corrected upward: a bf16 difference is within half a unit
+    // in the last place (2^-8 relative) of the exact one
+    uint32_t xl = 0xFF80FF80u;
+#pragma unroll
+    for (int j = 0; j < G::PPL; ++j) {
+      xl = max_bf16x2(xl, sub_bf16x2(qt[j].x, qd[j].x));
+      xl = max_bf16x2(xl, sub_bf16x2(qt[j].y, qd[j].y));
+      xl = max_bf16x2(xl, sub_bf16x2(qt[j].z, qd[j].z));
+      xl = max_bf16x2(xl, sub_bf16x2(qt[j].w, qd[j].w));
     }
-    S.N = N;
-    S.nS = nS;
+    dl = fmaxf(__uint_as_float(xl << 16), __uint_as_float(xl & 0xFFFF0000u));
+    dl = dl + fabsf(dl) * 0.0078125f;
+  } else {
+#pragma unroll
+    for (int j = 0; j < G::PPL; ++j) {
+      // (-inf - -inf is NaN, which fmaxf ignores; a finite target over a -inf draft is +inf)
+      dl = fmaxf(dl, __uint_as_float(qt[j].x) - __uint_as_float(qd[j].x));
+      dl = fmaxf(dl, __uint_as_float(qt[j].y) - __uint_as_float(qd[j].y));
+      dl = fmaxf(dl, __uint_as_float(qt[j].z) - __uint_as_float(qd[j].z));
+      dl = fmaxf(dl, __uint_as_float(qt[j].w) - __uint_as_float(qd[j].w));
+    }
   }
-  __syncwarp();
+  const float gt = group_max<G::LPG>(pieces_max<T>(qt));
+  const float gd = group_max<G::LPG>(pieces_max<T>(qd));
+  const float gl = group_fmax<G::LPG>(dl);
+  const float gtc = __fmul_rn(gt, c), gdc = __fmul_rn(gd, c);
+  const float smt = group_sum<G::LPG>(gt > -INFINITY ? pieces_mass<T>(qt, c, gtc) : 0.f);
+  const float smd = group_sum<G::LPG>(gd > -INFINITY ? pieces_mass<T>(qd, c, gdc) : 0.f);
+  if ((lane & (G::LPG - 1)) == 0 && G::EPL * tid < n) {
+    gmax_t[tid / G::LPG] = gt;
+    gmax_d[tid / G::LPG] = gd;
+    gdel[tid / G::LPG] = gl;
+    run_t.add(gt, gtc, smt);
+    run_d.add(gd, gdc, smd);
+  }
 }
 
-// ------------------------------------------------------------------------------------------
-// sampling: one cluster per row
-// ------------------------------------------------------------------------------------------
-template <typename T, bool BIAS>
-__global__ void __launch_bounds__(RT, 4) sample_kernel(const RowParams P) {
-  extern __shared__ __align__(16) float vmass[];  // one mass per 8-element vector of the slice
-  __shared__ RowShared S;
-  constexpr int NB = Raw8<T>::kBatch;
-  const int tid = threadIdx.x;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t C = cluster_nctarank();
-  const int cid = static_cast<int>(cluster_id_x());
-  const float c = P.c;
-  const int v0 = static_cast<int>(rank) * P.slice;
-  const int nv = max(0, min(P.V - v0, P.slice));
-  const int nvec = (nv + 7) >> 3;
-  const bool vec = P.use_vec != 0;
-  const T* row = static_cast<const T*>(P.dft) + static_cast<long long>(cid) * P.d_stride + v0;
-
-  // ---- the one pass: running max, per-vector masses, the bias set's candidates ----
-  float m = -INFINITY, mc = -INFINITY, s = 0.f;
-  WarpTop8 top;
-  top.init();
-  int cnt = 0;  // vectors this thread has stored (at tid + i * RT)
-  // (the loop runs to the warp's last vector so that every lane takes part in the votes)
-  const int nvec_w = nvec + ((RT - (nvec % RT)) % RT);
-  for (int g0 = tid; g0 < nvec_w; g0 += RT * NB) {
-    Raw8<T> r[NB];
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (g0 + j * RT < nvec) r[j].load(row, 8 * (g0 + j * RT), nv, vec);
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      const int g = g0 + j * RT;
-      if (__all_sync(FULL, g >= nvec)) break;
-      float z[8];
-      if (g < nvec) r[j].get(z);
-      else
-#pragma unroll
-        for (int k = 0; k < 8; ++k) z[k] = -INFINITY;
-      if (BIAS)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          top.offer(8 * g + k < nv, z[k], static_cast<uint32_t>(v0 + 8 * g + k));
-      if (g >= nvec) continue;
-      const float mn = max_nan(m, max8(z));
-      if (mn != m) {  // the running max rises: rescale what is stored
-        const float mcn = __fmul_rn(mn, c);
-        const float f = exp2f(mc - mcn);
-        s *= f;
-        for (int i = 0; i < cnt; ++i) vmass[tid + i * RT] *= f;
-        m = mn;
-        mc = mcn;
-      }
-      float vs = 0.f;
-      if (m > -INFINITY) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) vs += ex2_fast(fmaf(z[k], c, -mc));
-      }
-      vmass[g] = vs;
-      s += vs;
-      ++cnt;
-    }
-  }
-
-  // ---- the CTA's partial; cluster combine ----
-  const float M = row_block_max2(-INFINITY, m, S).y;
+// The chunk threads' running stats into a row maximum and sum 2^(z c - M c) (rounding of
+// fl(M c) folded in), written to *hdr by chunk thread 0. Every chunk thread calls it.
+__device__ void chunk_row_stats(const RowRun& run, float c, RowShared& S, float* hdr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float M = warp_max_nan(run.m);
   const float Mc = __fmul_rn(M, c);
-  const float pd = (m > -INFINITY && !row_bad(M)) ? s * exp2f(mc - Mc) : 0.f;
-  float sd = row_block_sum2(0.f, pd, S).y;
-  if (!row_bad(M)) sd *= fmaf(-fmaf(M, c, -Mc), kLn2r, 1.f);
-  if (BIAS) row_block_top8w(top, S, S.part.top);
-  if (tid == 0) {
-    S.part.m_t = 0.f;
-    S.part.s_t = 0.f;
-    S.part.m_d = M;
-    S.part.s_d = sd;
-    S.token = -1;
+  const float part = (run.m > -INFINITY && !row_bad(M)) ? run.s * exp2f(run.mc - Mc) : 0.f;
+  const float sw = warp_sum(part);
+  if (lane == 0) {
+    S.cm[warp] = M;
+    S.cs[warp] = sw;
   }
-  cluster_sync();
-  if (tid < 32) row_combine(P, S, C, false, BIAS);
-  bsync();
-  if (S.bad) {
-    if (rank == 0 && tid == 0) {
-      P.out_tok[cid] = -1;
-      P.out_conf[cid] = NAN;
-      if (P.out_exit) P.out_exit[cid] = -1;
+  named_sync(kBarC, CT);
+  if (threadIdx.x == 0) {
+    float Mt = S.cm[0];
+    for (int w = 1; w < NCW; ++w) Mt = max_nan(Mt, S.cm[w]);
+    float St = 0.f;
+    if (!row_bad(Mt)) {
+      const float Mtc = __fmul_rn(Mt, c);
+      for (int w = 0; w < NCW; ++w)
+        if (S.cm[w] > -INFINITY) St += S.cs[w] * exp2f(__fmul_rn(S.cm[w], c) - Mtc);
+      St *= fmaf(-fmaf(Mt, c, -Mtc), kLn2r, 1.f);
     }
-    cluster_sync();  // peers may still be reading this CTA's partial
-    return;
+    hdr[0] = Mt;
+    hdr[1] = St;
   }
+  named_sync(kBarC, CT);  // the scratch is free again
+}
 
-  // ---- masses relative to the row maximum, bias corrections, fixed-point slice mass ----
-  const float Mdc = __fmul_rn(S.Md, c);
-  const float F = m > -INFINITY ? exp2f(mc - Mdc) : 0.f;
-  const float bm1 = P.beta - 1.f;
-  const int nS = BIAS ? S.nS : 0;
-  unsigned long long acc = 0;
-  for (int g = tid; g < nvec; g += RT) {
-    float v = vmass[g] * F;
-    for (int j = 0; j < nS; ++j)
-      if (((S.S_ids[j] - v0) >> 3) == g)
-        v = fmaxf(fmaf(bm1, ex2_fast(fmaf(S.S_z[j], c, -Mdc)), v), 0.f);
-    vmass[g] = v;
-    acc += qfix(v);
+// The row's top-8 elements (the bias set's candidates) into S.top. They lie in the 8 groups with
+// the largest maxima (ties to the lower group): an element outside them is beaten by those 8
+// maxima. The groups are found from the group maxima alone (only those at or above a lower bound
+// of the 8th are offered), then read again, two per epilogue warp, and their elements offered.
+template <typename T>
+__device__ void row_top8(const T* row, int V, bool vec, const float* gmax, int ng,
+                         RowShared& S) {
+  const int t = et(), lane = t & 31, warp = t >> 5;
+  float m = -INFINITY;
+  for (int g = t; g < ng; g += ET) m = fmaxf(m, gmax[g]);
+  const float B = team_bound(m, S);
+  WarpTop8 gtop;
+  gtop.init(B);
+  const int per = (ng + ET - 1) / ET;
+  for (int k = 0; k < per; ++k) {
+    const int g = t + k * ET;
+    const float v = g < ng ? gmax[g] : -INFINITY;
+    gtop.offer(g < ng && v >= B, v, static_cast<uint32_t>(g));
   }
-  const unsigned long long Wc = row_block_sum_u64(acc, S);
-  if (tid == 0) S.part_w[0] = Wc;
-  cluster_sync();
+  team_top8(gtop, S);
+  static_assert(NEW * 2 == 8, "two groups per epilogue warp");
+  const unsigned long long k0 = S.top[2 * warp], k1 = S.top[2 * warp + 1];
+  esync();  // S.top is read by every warp before it is rewritten
+  const int g0 = k0 ? key_id(k0) : -1, g1 = k1 ? key_id(k1) : -1;
+  float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;
+  if (g0 >= 0) ld2<T>(row, kGroup * g0 + 2 * lane, V, vec, a0, b0);
+  if (g1 >= 0) ld2<T>(row, kGroup * g1 + 2 * lane, V, vec, a1, b1);
+  WarpTop8 top;
+  top.init(-INFINITY);
+  const int e0 = kGroup * g0 + 2 * lane, e1 = kGroup * g1 + 2 * lane;
+  top.offer(g0 >= 0 && e0 < V, a0, static_cast<uint32_t>(e0));
+  top.offer(g0 >= 0 && e0 + 1 < V, b0, static_cast<uint32_t>(e0 + 1));
+  top.offer(g1 >= 0 && e1 < V, a1, static_cast<uint32_t>(e1));
+  top.offer(g1 >= 0 && e1 + 1 < V, b1, static_cast<uint32_t>(e1 + 1));
+  team_top8(top, S);
+}
 
-  // ---- which CTA holds the draw (every CTA reaches the same answer) ----
-  if (tid < 32) {
-    const int lane = tid;
-    unsigned long long w = 0ull;
-    if (lane < static_cast<int>(C)) {
-      const uint4 v = ld_peer_v4(S.part_w, static_cast<uint32_t>(lane));
-      w = (static_cast<unsigned long long>(v.y) << 32) | v.x;
+// Epilogue thread 0: the Saguaro bias set (the bias_k largest draft logits, from S.top) and the
+// renormalisation N = 1 - (1 - beta) sum_S q.
+__device__ void bias_set(const RowParams& P, RowShared& S, float Md, float Sd) {
+  if (et() != 0) return;
+  float sq = 0.f;
+  int nS = 0;
+  for (int j = 0; j < P.bias_k; ++j) {
+    const unsigned long long k = S.top[j];
+    if (k == 0ull) break;
+    const float z = key_value(k);
+    sq += exp2f((z - Md) * P.c) / Sd;
+    S.S_z[nS] = z;
+    S.S_ids[nS++] = key_id(k);
+  }
+  S.nS = nS;
+  S.N = fmaf(-(1.f - P.beta), sq, 1.f);
+}
+
+// ------------------------------------------------------------------------------------------
+// the producer: units from the queue, their rows through the ring
+// ------------------------------------------------------------------------------------------
+template <typename T, int MODE>
+__device__ void producer(const RowParams& P, RowShared& S, unsigned char* ring) {
+  const int lane = threadIdx.x & 31;
+  const int nst = P.nstages;
+  constexpr int CE = chunk_elems<T>();
+  const int nch = (P.V + CE - 1) / CE;
+  const int nunits = MODE == MODE_SAMPLE ? P.B : P.B * P.K;
+  const bool vec = P.use_vec != 0;
+  int it = 0;  // stage fills so far
+  bool ok = true;
+  while (ok) {
+    int u = 0;
+    if (lane == 0) u = static_cast<int>(atomicAdd(&P.ws->next, 1u));
+    u = __shfl_sync(FULL, u, 0);
+    if (u >= nunits) break;
+    const T* rows[2] = {nullptr, nullptr};
+    int nrows = 1;
+    if (MODE == MODE_SAMPLE) {
+      rows[0] = static_cast<const T*>(P.dft) + static_cast<long long>(u) * P.d_stride;
+    } else {
+      const int b = u / P.K, i = u % P.K;
+      const int L = P.lens ? P.lens[b] : P.K;
+      if (L < 1 || L > P.K || i >= L) {  // no residual here: its ids are -1
+        if (lane < P.fmax) P.out_r2[static_cast<long long>(u) * P.fmax + lane] = -1;
+        continue;
+      }
+      rows[0] = static_cast<const T*>(P.tgt) +
+                (static_cast<long long>(b) * (P.K + 1) + i) * P.t_stride;
+      rows[1] = static_cast<const T*>(P.dft) + (static_cast<long long>(b) * P.K + i) * P.d_stride;
+      nrows = 2;
     }
-    const unsigned long long inc = warp_inclusive_u64(w);
-    const unsigned long long Wt = __shfl_sync(FULL, inc, 31);
-    const float u = P.uni[cid];
-    const unsigned long long t = scale_floor(u, Wt);
-    const unsigned hit = __ballot_sync(FULL, lane < static_cast<int>(C) && t < inc);
-    const int cs = (u >= 0.f && u < 1.f && hit) ? __ffs(hit) - 1 : -1;
-    if (lane == 0) S.cstar = cs;
-    if (cs >= 0 && lane == cs) S.t_loc = t - (inc - w);
-  }
-  bsync();
-  cluster_arrive();  // no more reads of the peers' shared memory from here on
-
-  if (S.cstar == static_cast<int>(rank)) {
-    // contiguous runs of vectors per thread, so the prefix follows ascending ids
-    const int lo = static_cast<int>((static_cast<long long>(tid) * nvec) / RT);
-    const int hi = static_cast<int>((static_cast<long long>(tid + 1) * nvec) / RT);
-    unsigned long long csum = 0;
-    for (int g = lo; g < hi; ++g) csum += qfix(vmass[g]);
-    unsigned long long pre = row_block_exclusive_u64(csum, S);
-    const unsigned long long tl = S.t_loc;
-    if (pre <= tl && tl < pre + csum) {
-      for (int g = lo; g < hi; ++g) {
-        const unsigned long long q = qfix(vmass[g]);
-        if (pre + q > tl) {
-          Raw8<T> rv;
-          rv.load(row, 8 * g, nv, vec);
-          float z[8];
-          rv.get(z);
-          const int e0 = v0 + 8 * g;
-          float sacc = 0.f;
-          int pick = 7;
-          for (int k = 0; k < 8; ++k) {
-            float f = 1.f;
-            for (int j = 0; j < nS; ++j) f = (S.S_ids[j] == e0 + k) ? P.beta : f;
-            const float wk = (8 * g + k < nv) ? f * ex2_fast(fmaf(z[k], c, -Mdc)) : 0.f;
-            sacc = k ? __fadd_rn(sacc, wk) : wk;
-            if (pre + qfix(sacc) > tl) {
-              pick = k;
-              break;
-            }
-          }
-          S.token = e0 + pick;
+    for (int ch = 0; ch < nch && ok; ++ch) {
+      const int e0 = ch * CE;
+      const int n = min(CE, P.V - e0);
+      const int npad = (n + 7) & ~7;
+      for (int r = 0; r < nrows && ok; ++r) {
+        const int s = it % nst;
+        // the chunk warps must have released the stage's previous fill
+        if (it >= nst && !mbar_wait_bounded(&S.empty[s], ((it / nst) - 1) & 1, kWaitBudget)) {
+          ok = false;
+          if (lane == 0) atomicOr(&P.ws->error, 1u);
           break;
         }
-        pre += q;
+        T* st = reinterpret_cast<T*>(ring + static_cast<size_t>(s) * kStage);
+        const T* src = rows[r] + e0;
+        if (vec) {
+          // whole 16-byte units by one bulk copy; the last few elements and the padding by hand
+          const int nb = static_cast<int>((static_cast<size_t>(n) * sizeof(T)) &
+                                          ~static_cast<size_t>(15)) /
+                         static_cast<int>(sizeof(T));
+          for (int e = nb + lane; e < npad; e += 32) st[e] = e < n ? src[e] : Elt<T>::neg_inf();
+          __syncwarp();
+          if (lane == 0) {
+            S.tag[s] = u;
+            const uint32_t bytes = static_cast<uint32_t>(nb * sizeof(T));
+            mbar_arrive_expect_tx(&S.full[s], bytes);
+            if (bytes) bulk_g2s(st, src, bytes, &S.full[s]);
+          }
+        } else {
+          for (int e = lane; e < npad; e += 32) st[e] = e < n ? src[e] : Elt<T>::neg_inf();
+          __syncwarp();
+          if (lane == 0) {
+            S.tag[s] = u;
+            mbar_arrive(&S.full[s]);
+          }
+        }
+        ++it;
       }
     }
-    bsync();
-    if (tid == 0) P.out_tok[cid] = S.token;
   }
-  if (rank == 0 && tid == 0) {
-    if (S.cstar < 0) P.out_tok[cid] = -1;  // uniform outside [0, 1)
-    const float conf = 1.f / S.Sd;        // the unbiased softmax's largest probability
-    P.out_conf[cid] = conf;
-    if (P.out_exit) P.out_exit[cid] = conf < P.tau ? 1 : 0;
+  if (ok) {  // the end marker
+    const int s = it % nst;
+    if (it >= nst && !mbar_wait_bounded(&S.empty[s], ((it / nst) - 1) & 1, kWaitBudget)) {
+      ok = false;
+      if (lane == 0) atomicOr(&P.ws->error, 1u);
+    } else {
+      if (lane == 0) {
+        S.tag[s] = kEnd;
+        mbar_arrive(&S.full[s]);
+      }
+      ++it;
+    }
   }
-  cluster_wait();  // no CTA leaves while a peer may still read its shared memory
+  if (!ok) {
+    // a wait gave up: let the copies already issued land before leaving (bounded)
+    for (int j = max(0, it - nst); j < it; ++j)
+      mbar_wait_bounded(&S.full[j % nst], (j / nst) & 1, kWaitBudget);
+  }
+  // the queue is reset by the last CTA to stop taking units
+  if (lane == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(&P.ws->done, 1u);
+    if (old == gridDim.x - 1u) {
+      atomicExch(&P.ws->next, 0u);
+      atomicExch(&P.ws->done, 0u);
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------------
-// exact-residual top-F: one cluster per (sequence, position) pair
+// the chunk warps: group values of every unit into the two group buffers in turn
+// ------------------------------------------------------------------------------------------
+template <typename T, int MODE>
+__device__ void chunk_warps(const RowParams& P, RowShared& S, unsigned char* ring, float* gbuf0,
+                            float* gbuf1, int ngmax) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nst = P.nstages;
+  constexpr int CE = chunk_elems<T>();
+  const int nch = (P.V + CE - 1) / CE;
+  int it = 0;        // ring stages taken
+  int k = 0;         // units finished
+  bool ab = false;   // a wait gave up: stop waiting (what is read from here on is meaningless)
+  // wait for stage use number j (it, it + 1, ...) to be filled; returns its stage
+  auto wait_full = [&](int j) {
+    const int s = j % nst;
+    if (!ab && !mbar_wait_bounded(&S.full[s], (j / nst) & 1, kWaitBudget)) {
+      ab = true;
+      atomicOr(&P.ws->error, 1u);
+    }
+    return s;
+  };
+  auto release = [&](int s) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+    ++it;
+  };
+  // the group buffer of unit k, once the epilogue is done with unit k - 2
+  auto take_buffer = [&]() {
+    const int b = k & 1;
+    if (k >= 2 && !ab && !mbar_wait_bounded(&S.gfree[b], ((k >> 1) - 1) & 1, kWaitBudget)) {
+      ab = true;
+      atomicOr(&P.ws->error, 1u);
+    }
+    return b;
+  };
+  auto hand_over = [&](int b, int u) {
+    if (tid == 0) S.gunit[b] = u;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.gfull[b]);
+  };
+  for (;;) {
+    const int s0 = wait_full(it);
+    const int u = S.tag[s0];
+    if (named_sync_or(kBarC, CT, ab || u == kEnd)) break;
+    const int b = take_buffer();
+    float* gb = b ? gbuf1 : gbuf0;
+    RowRun run[2];
+    run[0].init();
+    run[1].init();
+    const int go = CE / kGroup;  // groups per chunk
+    for (int ch = 0; ch < nch; ++ch) {
+      const int n = min(CE, P.V - ch * CE);
+      const int s = ch == 0 ? s0 : wait_full(it);
+      const T* st = reinterpret_cast<const T*>(ring + static_cast<size_t>(s) * kStage);
+      if (MODE == MODE_SAMPLE) {  // maxima, then masses
+        chunk_groups<T>(st, n, P.c, gb + ch * go, gb + ngmax + ch * go, run[0]);
+        release(s);
+      } else {  // target maxima, draft maxima, log-ratio maxima
+        const int s2 = wait_full(it + 1);
+        chunk_pair<T>(st, reinterpret_cast<const T*>(ring + static_cast<size_t>(s2) * kStage), n,
+                      P.c, gb + ch * go, gb + ngmax + ch * go, gb + 2 * ngmax + ch * go, run[0],
+                      run[1]);
+        release(s);
+        release(s2);
+      }
+    }
+    chunk_row_stats(run[0], P.c, S, &S.hdr[b][0]);
+    if (MODE == MODE_RESID) chunk_row_stats(run[1], P.c, S, &S.hdr[b][2]);
+    hand_over(b, u);
+    ++k;
+  }
+  hand_over(take_buffer(), kEnd);  // no more units
+}
+
+// ------------------------------------------------------------------------------------------
+// epilogue: sampling
 // ------------------------------------------------------------------------------------------
 template <typename T, bool BIAS>
-__global__ void __launch_bounds__(RT, 3) resid_kernel(const RowParams P) {
-  __shared__ RowShared S;
-  constexpr int NB = (Raw8<T>::kBatch + 1) / 2;  // two rows per vector index
-  const int tid = threadIdx.x;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t C = cluster_nctarank();
-  const int cid = static_cast<int>(cluster_id_x());
+__device__ void sample_epilogue(const RowParams& P, RowShared& S, int u, float* gmax,
+                                float* gmass, const float* hdr) {
+  const int t = et(), lane = t & 31;
   const float c = P.c;
-  const int b = cid / P.K, i = cid % P.K;
-  const int L = P.lens ? P.lens[b] : P.K;
-  int32_t* out = P.out_r2 + static_cast<long long>(cid) * P.fmax;
-  if (L < 1 || L > P.K || i >= L) {  // no residual at this position (uniform over the cluster)
-    if (rank == 0 && tid < P.fmax) out[tid] = -1;
-    return;
-  }
-  const int v0 = static_cast<int>(rank) * P.slice;
-  const int nv = max(0, min(P.V - v0, P.slice));
-  const int nvec = (nv + 7) >> 3;
+  const int V = P.V;
+  const int ng = (V + kGroup - 1) / kGroup;
+  const T* row = static_cast<const T*>(P.dft) + static_cast<long long>(u) * P.d_stride;
   const bool vec = P.use_vec != 0;
-  const T* zt = static_cast<const T*>(P.tgt) +
-                (static_cast<long long>(b) * (P.K + 1) + i) * P.t_stride + v0;
-  const T* zd = static_cast<const T*>(P.dft) +
-                (static_cast<long long>(b) * P.K + i) * P.d_stride + v0;
 
-  // ---- pass 1: maxima and sums of both rows; the draft row's top 8 for the bias set ----
-  RowAcc at, ad;
-  at.init();
-  ad.init();
-  WarpTop8 top;
-  top.init();
-  // (the loops run to the warp's last vector so that every lane takes part in the votes)
-  const int nvec_w = nvec + ((RT - (nvec % RT)) % RT);
-  for (int g0 = tid; g0 < nvec_w; g0 += RT * NB) {
-    Raw8<T> rt[NB], rd[NB];
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (g0 + j * RT < nvec) {
-        rd[j].load(zd, 8 * (g0 + j * RT), nv, vec);
-        rt[j].load(zt, 8 * (g0 + j * RT), nv, vec);
-      }
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      const int g = g0 + j * RT;
-      if (__all_sync(FULL, g >= nvec)) break;
-      float z[8];
-      if (g < nvec) rd[j].get(z);
-      else
-#pragma unroll
-        for (int k = 0; k < 8; ++k) z[k] = -INFINITY;
-      if (BIAS)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          top.offer(8 * g + k < nv, z[k], static_cast<uint32_t>(v0 + 8 * g + k));
-      if (g >= nvec) continue;
-      ad.rescale(max8(z), c);
-      if (ad.m > -INFINITY) ad.sum8(z, c);
-      rt[j].get(z);
-      at.rescale(max8(z), c);
-      if (at.m > -INFINITY) at.sum8(z, c);
+  const float M = hdr[0], Sd = hdr[1];
+  if (row_bad(M)) {
+    if (t == 0) {
+      P.out_tok[u] = -1;
+      P.out_conf[u] = NAN;
+      if (P.out_exit) P.out_exit[u] = -1;
     }
-  }
-  const float2 mm = row_block_max2(at.m, ad.m, S);
-  const float mct = __fmul_rn(mm.x, c), mcd = __fmul_rn(mm.y, c);
-  const float pt = (at.m > -INFINITY && !row_bad(mm.x)) ? at.total() * exp2f(at.mc - mct) : 0.f;
-  const float pd = (ad.m > -INFINITY && !row_bad(mm.y)) ? ad.total() * exp2f(ad.mc - mcd) : 0.f;
-  float2 ss = row_block_sum2(pt, pd, S);
-  if (!row_bad(mm.x)) ss.x *= fmaf(-fmaf(mm.x, c, -mct), kLn2r, 1.f);
-  if (!row_bad(mm.y)) ss.y *= fmaf(-fmaf(mm.y, c, -mcd), kLn2r, 1.f);
-  if (BIAS) row_block_top8w(top, S, S.part.top);
-  if (tid == 0) {
-    S.part.m_t = mm.x;
-    S.part.s_t = ss.x;
-    S.part.m_d = mm.y;
-    S.part.s_d = ss.y;
-  }
-  cluster_sync();
-  if (tid < 32) row_combine(P, S, C, true, BIAS);
-  bsync();
-  if (S.bad) {
-    if (rank == 0 && tid < P.fmax) out[tid] = -1;
-    cluster_sync();  // peers may still be reading this CTA's partial
     return;
   }
+  int nS = 0;
+  if (BIAS) {
+    row_top8<T>(row, V, vec, gmax, ng, S);
+    bias_set(P, S, M, Sd);
+    esync();
+    nS = S.nS;
+  }
 
-  // ---- pass 2: residual weights relative to p's scale, max(e_t - rho_v e_d, 0) ----
-  const float Mtc = __fmul_rn(S.Mt, c), Mdc = __fmul_rn(S.Md, c);
-  const float ft = fmaf(-fmaf(S.Mt, c, -Mtc), kLn2r, 1.f);
-  const float fd = fmaf(-fmaf(S.Md, c, -Mdc), kLn2r, 1.f);
-  const float rho = (fd * S.St) / (ft * (S.Sd * S.N));
+  // group masses relative to the row maximum, the biased ids corrected; fixed-point total
+  const float Mdc = __fmul_rn(M, c);
+  unsigned long long acc = 0;
+  for (int g = t; g < ng; g += ET) {
+    const float gm = gmax[g];
+    float w = gm > -INFINITY ? gmass[g] * exp2f(__fmul_rn(gm, c) - Mdc) : 0.f;
+    for (int j = 0; j < nS; ++j)
+      if (S.S_ids[j] / kGroup == g)
+        w = fmaxf(fmaf(P.beta - 1.f, ex2_fast(fmaf(S.S_z[j], c, -Mdc)), w), 0.f);
+    gmass[g] = w;
+    acc += qfix(w);
+  }
+  const unsigned long long W = team_sum_u64(acc, S);  // (its barriers publish gmass)
+  const float uu = P.uni[u];
+  const bool uok = uu >= 0.f && uu < 1.f;
+  const unsigned long long tt = scale_floor(uu, W);
+
+  // the group holding tt: contiguous runs of groups per thread, so the prefix follows the ids
+  const int lo = static_cast<int>((static_cast<long long>(t) * ng) / ET);
+  const int hi = static_cast<int>((static_cast<long long>(t + 1) * ng) / ET);
+  unsigned long long csum = 0;
+  for (int g = lo; g < hi; ++g) csum += qfix(gmass[g]);
+  unsigned long long pre = team_exclusive_u64(csum, S);
+  if (t == 0) S.gstar = -1;
+  esync();
+  if (uok && pre <= tt && tt < pre + csum) {
+    for (int g = lo; g < hi; ++g) {
+      const unsigned long long q = qfix(gmass[g]);
+      if (pre + q > tt) {
+        S.gstar = g;
+        S.t_loc = tt - pre;
+        break;
+      }
+      pre += q;
+    }
+  }
+  esync();
+  // warp 0 of the team: the element within the group, by a warp prefix over its 64 weights
+  if (t < 32) {
+    const int gs = S.gstar;
+    int token = -1;
+    if (gs >= 0) {
+      const unsigned long long tl = S.t_loc;
+      const int e = kGroup * gs + 2 * lane;
+      float a, b;
+      ld2<T>(row, e, V, vec, a, b);
+      float fa = 1.f, fb = 1.f;
+      for (int j = 0; j < nS; ++j) {
+        fa = S.S_ids[j] == e ? P.beta : fa;
+        fb = S.S_ids[j] == e + 1 ? P.beta : fb;
+      }
+      const float wa = e < V ? fa * ex2_fast(fmaf(a, c, -Mdc)) : 0.f;
+      const float wb = e + 1 < V ? fb * ex2_fast(fmaf(b, c, -Mdc)) : 0.f;
+      const float pair = wa + wb;
+      float inc = pair;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(FULL, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const float pa = inc - pair + wa;
+      const unsigned hit_b = __ballot_sync(FULL, qfix(inc) > tl);
+      const unsigned hit_a = __ballot_sync(FULL, qfix(pa) > tl);
+      const unsigned pos_b = __ballot_sync(FULL, wb > 0.f), pos_a = __ballot_sync(FULL, wa > 0.f);
+      if (hit_b) {
+        const int l = __ffs(hit_b) - 1;
+        token = kGroup * gs + 2 * l + (((hit_a >> l) & 1u) ? 0 : 1);
+      } else {  // rounding left t past the recomputed total: the last element with weight
+        const int lb = pos_b ? 31 - __clz(pos_b) : -1, la = pos_a ? 31 - __clz(pos_a) : -1;
+        token = (lb >= 0 && lb >= la) ? kGroup * gs + 2 * lb + 1
+                                      : (la >= 0 ? kGroup * gs + 2 * la : -1);
+      }
+    }
+    if (lane == 0) {
+      P.out_tok[u] = token;
+      const float conf = 1.f / Sd;  // the unbiased softmax's largest probability
+      P.out_conf[u] = conf;
+      if (P.out_exit) P.out_exit[u] = conf < P.tau ? 1 : 0;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// epilogue: exact-residual top-F
+// ------------------------------------------------------------------------------------------
+// Residual weights of groups (one warp, two elements per lane and group) offered to the warp's
+// list, for up to kBatch groups at once (g < 0: none); all loads are issued before the first use.
+template <typename T, bool BIAS>
+__device__ __forceinline__ void offer_groups(WarpTop8& top, const T* zt, const T* zd,
+                                             const int (&gs)[kBatch], int V, bool vec, float c,
+                                             float Mtc, float Mdc, float rho, float rhoS,
+                                             const RowShared& S, int nS) {
+  const int lane = threadIdx.x & 31;
+  float ta[kBatch], tb[kBatch], da[kBatch], db[kBatch];
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k) {
+    ta[k] = tb[k] = da[k] = db[k] = -INFINITY;
+    if (gs[k] >= 0) {
+      const int e = kGroup * gs[k] + 2 * lane;
+      ld2<T>(zt, e, V, vec, ta[k], tb[k]);
+      ld2<T>(zd, e, V, vec, da[k], db[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k) {
+    const int e = kGroup * gs[k] + 2 * lane;
+    float ra = rho, rb = rho;
+    if (BIAS)
+      for (int j = 0; j < nS; ++j) {
+        ra = S.S_ids[j] == e ? rhoS : ra;
+        rb = S.S_ids[j] == e + 1 ? rhoS : rb;
+      }
+    const float wa =
+        fmaxf(fmaf(-ra, ex2_fast(fmaf(da[k], c, -Mdc)), ex2_fast(fmaf(ta[k], c, -Mtc))), 0.f);
+    const float wb =
+        fmaxf(fmaf(-rb, ex2_fast(fmaf(db[k], c, -Mdc)), ex2_fast(fmaf(tb[k], c, -Mtc))), 0.f);
+    top.offer(gs[k] >= 0 && e < V && wa > 0.f, wa, static_cast<uint32_t>(e));
+    top.offer(gs[k] >= 0 && e + 1 < V && wb > 0.f, wb, static_cast<uint32_t>(e + 1));
+  }
+}
+
+// A warp's candidate groups (bits of the ballot over groups base + lane) in batches of kBatch.
+template <typename Body>
+__device__ __forceinline__ void batches(unsigned bits, int base, Body body) {
+  while (bits) {
+    int gs[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      gs[k] = bits ? base + __ffs(bits) - 1 : -1;
+      bits &= bits - 1;
+    }
+    body(gs);
+  }
+}
+
+template <typename T, bool BIAS>
+__device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const float* gmax_t,
+                               const float* gmax_d, float* gdel, const float* hdr) {
+  const int t = et();
+  const float c = P.c;
+  const int V = P.V;
+  const int ng = (V + kGroup - 1) / kGroup;
+  const int b = u / P.K, i = u % P.K;
+  const T* zt =
+      static_cast<const T*>(P.tgt) + (static_cast<long long>(b) * (P.K + 1) + i) * P.t_stride;
+  const T* zd = static_cast<const T*>(P.dft) + (static_cast<long long>(b) * P.K + i) * P.d_stride;
+  int32_t* out = P.out_r2 + static_cast<long long>(u) * P.fmax;
+  const bool vec = P.use_vec != 0;
+
+  const float2 T2 = make_float2(hdr[0], hdr[1]);
+  const float2 D2 = make_float2(hdr[2], hdr[3]);
+  if (row_bad(T2.x) || row_bad(D2.x)) {
+    if (t < P.fmax) out[t] = -1;
+    return;
+  }
+  int nS = 0;
+  float N = 1.f;
+  if (BIAS) {
+    row_top8<T>(zd, V, vec, gmax_d, ng, S);
+    bias_set(P, S, D2.x, D2.y);
+    esync();
+    nS = S.nS;
+    N = S.N;
+  }
+  // residual weights relative to p's scale: max(e_t - rho_v e_d, 0)
+  const float Mtc = __fmul_rn(T2.x, c), Mdc = __fmul_rn(D2.x, c);
+  const float ft = fmaf(-fmaf(T2.x, c, -Mtc), kLn2r, 1.f);
+  const float fd = fmaf(-fmaf(D2.x, c, -Mdc), kLn2r, 1.f);
+  const float rho = (fd * T2.y) / (ft * (D2.y * N));
   const float rhoS = rho * P.beta;
-  const int nS = BIAS ? S.nS : 0;
-  WarpTop8 rtop;
-  rtop.init();
-  float thrl = -INFINITY;  // log2 of the warp's 8th best residual, less a margin for rounding
-  for (int g0 = tid; g0 < nvec_w; g0 += RT * NB) {
-    Raw8<T> rt[NB], rd[NB];
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (g0 + j * RT < nvec) {
-        rt[j].load(zt, 8 * (g0 + j * RT), nv, vec);
-        rd[j].load(zd, 8 * (g0 + j * RT), nv, vec);
-      }
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      const int g = g0 + j * RT;
-      if (__all_sync(FULL, g >= nvec)) break;
-      float a[8], d[8];
-      if (g < nvec) {
-        rt[j].get(a);
-        rd[j].get(d);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) a[k] = d[k] = -INFINITY;
-      }
-      const int e0 = v0 + 8 * g;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        // e_t, hence the residual, below the warp's 8th best: no exponentials needed
-        const float lt = fmaf(a[k], c, -Mtc);
-        const bool pass = lt >= thrl && 8 * g + k < nv;
-        if (!__any_sync(FULL, pass)) continue;
-        float w = 0.f;
-        if (pass) {
-          float r = rho;
-          for (int j2 = 0; j2 < nS; ++j2) r = (S.S_ids[j2] == e0 + k) ? rhoS : r;
-          w = fmaxf(fmaf(-r, ex2_fast(fmaf(d[k], c, -Mdc)), ex2_fast(lt)), 0.f);
-        }
-        if (rtop.offer(pass && w > 0.f, w, static_cast<uint32_t>(e0 + k)))
-          thrl = __log2f(rtop.thr) - 1e-3f;
-      }
-    }
+
+  // An upper bound of each group's residual: with delta = max (z_t - z_d) c over the group,
+  // w = e_t (1 - rho_v 2^((z_d - z_t) c + Mtc - Mdc)) <= e_t,max (1 - 2^-(delta - kappa)),
+  // kappa = log2(min rho_v) + Mtc - Mdc; 1 - 2^-x <= min(1, x ln 2). A small margin covers the
+  // rounding of both sides. Stored over the log-ratio maxima.
+  const float kappa = __log2f(BIAS ? rhoS : rho) + Mtc - Mdc;
+  float bm = -INFINITY;
+  for (int g = t; g < ng; g += ET) {
+    const float x = fmaf(gdel[g], c, -kappa) + 1e-4f;
+    const float et = ex2_fast(fmaf(gmax_t[g], c, -Mtc));
+    const float f = x <= 0.f ? 0.f : (x < 0.25f ? x * 0.69314718f : 1.f - ex2_fast(-x) + 1e-6f);
+    const float bnd = gmax_t[g] > -INFINITY ? et * fminf(f, 1.f) * 1.001f + 1e-30f : 0.f;
+    gdel[g] = bnd;
+    bm = fmaxf(bm, bnd);
   }
-  row_block_top8w(rtop, S, S.part_r);
-  cluster_sync();
-  if (rank == 0 && tid < 32) {
-    unsigned long long top[8];
-    cluster_top8(S.part_r, C, top);
-    if (tid < P.fmax) {
-      const int F = P.fan[i];
-      out[tid] = (tid < F && tid < 8 && top[tid] != 0ull) ? key_id(top[tid]) : -1;
+  // Tiers of groups in decreasing bound: each tier is the groups (not yet visited) whose bound
+  // reaches both the 8th best residual so far and a lower bound of the 8th largest remaining
+  // bound; a visited group's bound is set to -1. It ends when no group's bound reaches the 8th
+  // best residual; after kTiers tiers, every group that still could is visited at once.
+  constexpr int kTiers = 6;
+  WarpTop8 top;
+  top.init(-INFINITY);
+  const int per = (ng + ET - 1) / ET;
+  auto offer_batch = [&](const int (&gs)[kBatch]) {
+    offer_groups<T, BIAS>(top, zt, zd, gs, V, vec, c, Mtc, Mdc, rho, rhoS, S, nS);
+  };
+  float thr = 0.f;  // the team's 8th best residual so far (0 until 8 are known)
+  for (int tier = 0;; ++tier) {
+    float bt = -INFINITY;
+    if (tier < kTiers) {
+      float bm2 = -INFINITY;
+      for (int g = t; g < ng; g += ET) {
+        const float bg = gdel[g];
+        if (bg > 0.f && bg >= thr) bm2 = fmaxf(bm2, bg);
+      }
+      bt = team_bound(bm2, S);
     }
+    const float lo = fmaxf(bt, thr);
+    bool any = false;
+    for (int k = 0; k < per; ++k) {
+      const int g = t + k * ET;  // warp w of the team scans groups base .. base + 31
+      const float bg = g < ng ? gdel[g] : -1.f;
+      const bool pick = bg > 0.f && bg >= lo;
+      any |= pick;
+      batches(__ballot_sync(FULL, pick), g - (t & 31), offer_batch);
+      if (pick) gdel[g] = -1.f;
+    }
+    if (!named_sync_or(kBarE, ET, any)) break;  // nothing left that can reach the top 8
+    team_top8(top, S);
+    const unsigned long long k8 = S.top[7];
+    thr = k8 ? key_value(k8) : 0.f;
+    if (thr > top.thr) top.thr = thr;
+    if (bt == -INFINITY) break;  // that tier took every group still in reach
   }
-  cluster_sync();  // no CTA leaves while rank 0 may still read its shared memory
+  team_top8(top, S);
+  if (t < P.fmax) {
+    const int F = P.fan[i];
+    const unsigned long long k = t < 8 ? S.top[t] : 0ull;
+    out[t] = (t < F && k != 0ull) ? key_id(k) : -1;
+  }
+}
+
+template <typename T, int MODE, bool BIAS>
+__device__ void epilogue_warps(const RowParams& P, RowShared& S, float* gbuf0, float* gbuf1,
+                               int ngmax) {
+  int k = 0;
+  for (;;) {
+    const int b = k & 1;
+    const bool ok = mbar_wait_bounded(&S.gfull[b], (k >> 1) & 1, kWaitBudget);
+    if (!ok && et() == 0) atomicOr(&P.ws->error, 1u);
+    const int u = S.gunit[b];
+    if (named_sync_or(kBarE, ET, !ok || u == kEnd)) break;
+    float* gb = b ? gbuf1 : gbuf0;
+    if (MODE == MODE_SAMPLE)
+      sample_epilogue<T, BIAS>(P, S, u, gb, gb + ngmax, S.hdr[b]);
+    else
+      resid_epilogue<T, BIAS>(P, S, u, gb, gb + ngmax, gb + 2 * ngmax, S.hdr[b]);
+    esync();  // every epilogue thread is done with the buffer and the scratch
+    if (et() == 0) mbar_arrive(&S.gfree[b]);
+    ++k;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------------
+template <typename T, int MODE, bool BIAS>
+__global__ void __launch_bounds__(RT, 2) row_kernel(const RowParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ RowShared S;
+  const int nst = P.nstages;
+  unsigned char* ring = smem;
+  const int ngmax = (P.V + kGroup - 1) / kGroup;
+  const int narr = MODE == MODE_SAMPLE ? 2 : 3;  // per-group arrays of a buffer
+  float* gbuf0 = reinterpret_cast<float*>(smem + static_cast<size_t>(nst) * kStage);
+  float* gbuf1 = gbuf0 + static_cast<size_t>(narr) * ngmax;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], NCW);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.gfull[b], NCW);
+      mbar_init(&S.gfree[b], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid >= CT + ET)
+    producer<T, MODE>(P, S, ring);
+  else if (tid >= CT)
+    epilogue_warps<T, MODE, BIAS>(P, S, gbuf0, gbuf1, ngmax);
+  else
+    chunk_warps<T, MODE>(P, S, ring, gbuf0, gbuf1, ngmax);
 }
 
 // Cache-hit flags: 1 if the token the verify step drew at a rejected position is among the
@@ -705,51 +1058,49 @@ __global__ void hit_kernel(const RowParams P, const int32_t* acc, const int32_t*
   P.out_hit[b] = hit;
 }
 
-template <int MODE, typename T, bool BIAS>
-const void* row_fn() {
-  if constexpr (MODE == MODE_SAMPLE)
-    return reinterpret_cast<const void*>(&sample_kernel<T, BIAS>);
-  else
-    return reinterpret_cast<const void*>(&resid_kernel<T, BIAS>);
-}
-
 template <int MODE>
 const void* pick_fn(int dtype, bool bias) {
-  if (dtype == 1) return bias ? row_fn<MODE, uint16_t, true>() : row_fn<MODE, uint16_t, false>();
-  return bias ? row_fn<MODE, float, true>() : row_fn<MODE, float, false>();
+  if (dtype == 1)
+    return bias ? reinterpret_cast<const void*>(&row_kernel<uint16_t, MODE, true>)
+                : reinterpret_cast<const void*>(&row_kernel<uint16_t, MODE, false>);
+  return bias ? reinterpret_cast<const void*>(&row_kernel<float, MODE, true>)
+              : reinterpret_cast<const void*>(&row_kernel<float, MODE, false>);
 }
 
 }  // namespace
 
-cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int nclusters, int C,
-                        const int32_t* acc, const int32_t* tok, const int32_t* r1,
-                        cudaStream_t stream) {
+size_t row_smem_bytes(int mode, int V, int nstages) {
+  const size_t ng = static_cast<size_t>((V + kGroup - 1) / kGroup);
+  return static_cast<size_t>(nstages) * kStage + 2 * ng * 4 * (mode == MODE_SAMPLE ? 2 : 3);
+}
+
+int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages) {
+  const void* fn = mode == MODE_SAMPLE ? pick_fn<MODE_SAMPLE>(dtype, bias)
+                                       : pick_fn<MODE_RESID>(dtype, bias);
+  const size_t smem = row_smem_bytes(mode, V, nstages);
+  if (smem > kRowMaxSmem) return 0;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, RT, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const int32_t* acc,
+                        const int32_t* tok, const int32_t* r1, cudaStream_t stream) {
   const bool bias = P.bias_k > 0 && P.beta < 1.f;
   const void* fn = mode == MODE_SAMPLE ? pick_fn<MODE_SAMPLE>(dtype, bias)
                                        : pick_fn<MODE_RESID>(dtype, bias);
-  const size_t smem = mode == MODE_SAMPLE ? static_cast<size_t>((P.slice + 7) / 8) * 4 : 0;
+  if (P.nstages < 2 || P.nstages > kRowMaxStages) return cudaErrorInvalidValue;
+  const size_t smem = row_smem_bytes(mode, P.V, P.nstages);
+  if (smem > kRowMaxSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  if (C > 8) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
-  if (nclusters > 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nclusters) * static_cast<unsigned>(C));
-    cfg.blockDim = dim3(RT);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  if (ctas > 0) {
     void* args[] = {const_cast<RowParams*>(&P)};
-    e = cudaLaunchKernelExC(&cfg, fn, args);
+    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(RT), args, smem, stream);
     if (e != cudaSuccess) return e;
   }
   if (mode == MODE_RESID && P.out_hit && P.B > 0) {

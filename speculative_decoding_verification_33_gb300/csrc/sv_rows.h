@@ -8,7 +8,12 @@
 
 namespace sv {
 
-constexpr int kRowThreads = 256;  // threads per CTA of the row kernels
+constexpr int kRowChunkWarps = 8;      // warps reducing the streamed chunks
+constexpr int kRowEpilogueWarps = 4;   // warps finishing units from their group values
+constexpr int kRowThreads = (kRowChunkWarps + kRowEpilogueWarps + 1) * 32;  // + the producer
+constexpr int kRowMaxStages = 8;       // ring stages per CTA (the launch picks 2 .. 8)
+constexpr int kRowStageBytes = 16384;  // bytes per stage
+constexpr size_t kRowMaxSmem = 227 * 1024;
 
 struct RowParams {
   const void* tgt;
@@ -22,19 +27,25 @@ struct RowParams {
   int bias_k;                    // 0 = no bias set
   int fmax;                      // residual: columns of out_r2
   int fan[kMaxK];
-  int slice;                     // vocabulary entries per CTA (multiple of 8)
-  int use_vec;                   // rows and strides 16-byte aligned: vector loads
+  int use_vec;                   // rows and strides 16-byte aligned: bulk copies
+  int nstages;                   // ring stages (2 .. kRowMaxStages)
   float tau;                     // sampling: exit threshold for out_exit
   int32_t* out_tok;              // sampling
   float* out_conf;
   int32_t* out_exit;             // may be NULL
   int32_t* out_r2;               // residual
   int32_t* out_hit;              // may be NULL
+  Workspace* ws;                 // unit queue and error word (bit 0: a bounded wait gave up)
 };
 
-// mode 0: sampling (one cluster per row), 1: residual top-F (one cluster per (b, i) pair)
-cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int nclusters, int C,
-                        const int32_t* acc, const int32_t* tok, const int32_t* r1,
-                        cudaStream_t stream);
+// Dynamic shared memory of one CTA: the ring and two buffers of per-group values.
+size_t row_smem_bytes(int mode, int V, int nstages);
+// Co-resident CTAs per SM of the kernel for this configuration (0: does not fit).
+int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages);
+
+// mode 0: sampling (B rows), 1: residual top-F (B * K (sequence, position) pairs); `ctas`
+// persistent CTAs. With out_hit set, the residual launch is followed by the cache-hit flags.
+cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const int32_t* acc,
+                        const int32_t* tok, const int32_t* r1, cudaStream_t stream);
 
 }  // namespace sv

@@ -149,6 +149,41 @@ int resident_clusters(const sv_problem* p, int dev, int dtype, int greedy, int t
   return occ;
 }
 
+// The draft rows' top 8 are needed (bias set or top-F ids).
+bool needs_top8(const sv_problem* p, const Checked& c) {
+  return !c.greedy && ((p->bias_k > 0 && c.beta_lt1) || c.fmax > 0);
+}
+
+// Bytes of the top-8 prepass keys in a workspace (after the counters): 8 keys per position.
+size_t keys_bytes(const sv_problem* p) {
+  return static_cast<size_t>(p->B) * static_cast<size_t>(p->K) * 8 * sizeof(unsigned long long);
+}
+
+// Ring stages and co-resident CTAs per SM of a row kernel (g_mu held): the most stages that
+// still let two CTAs share an SM (at least 3); failing that, one CTA per SM with up to
+// kRowMaxStages.
+// dev, mode, dtype, bias, V -> (ring stages, CTAs per SM)
+std::map<std::tuple<int, int, int, int, int>, std::pair<int, int>> g_row_occ;
+
+std::pair<int, int> row_config(int dev, int mode, int dtype, bool bias, int V) {
+  const auto key = std::make_tuple(dev, mode, dtype, bias ? 1 : 0, V);
+  auto it = g_row_occ.find(key);
+  if (it == g_row_occ.end()) {
+    int nst = 0, per_sm = 0;
+    for (int st = sv::kRowMaxStages; st >= 3 && !nst; --st)
+      if (sv::row_smem_bytes(mode, V, st) <= 112 * 1024) nst = st;
+    if (nst) per_sm = sv::row_ctas_per_sm(mode, dtype, bias, V, nst);
+    if (per_sm < 2) {
+      nst = 0;
+      for (int st = sv::kRowMaxStages; st >= 2 && !nst; --st)
+        if (sv::row_smem_bytes(mode, V, st) <= sv::kRowMaxSmem) nst = st;
+      per_sm = nst ? sv::row_ctas_per_sm(mode, dtype, bias, V, nst) : 0;
+    }
+    it = g_row_occ.emplace(key, std::make_pair(nst, per_sm)).first;
+  }
+  return it->second;
+}
+
 // Cluster size, slice, shared memory and the number of clusters to launch (g_mu held).
 //
 // One sequence is verified by one cluster, position after position, so a sequence's latency
@@ -156,10 +191,13 @@ int resident_clusters(const sv_problem* p, int dev, int dtype, int greedy, int t
 // whose co-resident clusters still hold the whole batch at once, each CTA keeping at least 512
 // vocabulary entries; when no C holds the batch, the smallest C whose slice fits shared memory
 // (throughput). A cluster_hint overrides the choice.
-sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L) {
+// With `prepass`, the draft rows' top 8 come from the top-8 prepass and the verify kernel needs
+// no in-stream top-8.
+sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L,
+               bool prepass = false) {
   if (sm_count(dev) <= 0) return SV_ERR_CUDA;
   const int dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
-  const int top8 = !c.greedy && ((p->bias_k > 0 && c.beta_lt1) || c.fmax > 0);
+  const int top8 = !prepass && needs_top8(p, c);
   int C = p->cluster_hint, slice = 0, occ = 0;
   size_t smem = 0;
   if (C) {
@@ -196,7 +234,7 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
               const int32_t* lens, const float* uni, float T, float beta, int mode,
               int32_t* out_acc, int32_t* out_tok, int32_t* out_topf, float* lse_t,
               float* lse_d, float* px, float* qx, int debug_all, Workspace* ws_user,
-              cudaStream_t stream) {
+              size_t ws_user_bytes, cudaStream_t stream) {
   Checked c;
   sv_status st = check_args(p, tgt, dft, tok, uni, T, beta, mode, out_acc, out_tok, out_topf, &c);
   if (st != SV_OK || p->B == 0) return st;
@@ -237,18 +275,52 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   if (!c.greedy) aligned = aligned && (a_d % 16 == 0) && ((p->draft_row_stride * c.elt) % 16 == 0);
   P.use_bulk = aligned ? 1 : 0;
 
+  // The draft rows' top 8 (bias set, top-F ids) come from a prepass over the draft rows when the
+  // workspace has room for its keys; otherwise (the fixed workspace of spec_verify_noalloc, or
+  // the diagnostics entry point) from the verify kernel's own stream.
+  const size_t kb = keys_bytes(p);
+  const bool prepass = needs_top8(p, c) && !debug_all && (!ws_user || ws_user_bytes >= sizeof(Workspace) + kb);
   std::lock_guard<std::mutex> lock(g_mu);
-  st = plan(p, c, dev, &L);
+  st = plan(p, c, dev, &L, prepass);
   if (st != SV_OK) return st;
 
   if (ws_user) {
     P.ws = ws_user;
   } else {
-    StreamRes* r = resources(dev, stream, sv::workspace_bytes_for(p->B), &st);
+    StreamRes* r = resources(dev, stream, sv::workspace_bytes_for(p->B) + (prepass ? kb : 0), &st);
     if (!r) return st;
     P.ws = r->ws;
   }
   P.lpt = p->B <= sv::kLptMaxB ? 1 : 0;
+  if (prepass) {
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(P.ws + 1);
+    P.keys = keys;
+    sv::RowParams R;
+    memset(&R, 0, sizeof(R));
+    R.dft = dft;
+    R.d_stride = p->draft_row_stride;
+    R.V = p->V;
+    R.K = p->K;
+    R.B = p->B;
+    R.lens = lens;
+    R.c = P.c;
+    R.fmax = c.fmax;
+    for (int i = 0; i < sv::kMaxK; ++i) R.fan[i] = c.fan[i];
+    R.use_vec = (reinterpret_cast<uintptr_t>(dft) % 16 == 0 &&
+                 (p->draft_row_stride * static_cast<long long>(c.elt)) % 16 == 0)
+                    ? 1
+                    : 0;
+    R.out_keys = keys;
+    R.out_topf = c.fmax > 0 ? out_topf : nullptr;
+    R.ws = P.ws;
+    const std::pair<int, int> rc = row_config(dev, 2, L.dtype, false, p->V);
+    if (rc.first < 2 || rc.second < 1) return SV_ERR_UNSUPPORTED;
+    R.nstages = rc.first;
+    const int units = p->B * p->K;
+    const int ctas = std::min(units, rc.second * sm_count(dev));
+    if (sv::launch_rows(R, 2, L.dtype, ctas, nullptr, nullptr, nullptr, stream) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
   return sv::launch(L, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -263,7 +335,7 @@ sv_status spec_verify(const sv_problem* prob, const void* target_logits,
                       int32_t* out_residual_topF, void* stream) {
   return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
              temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr,
-             nullptr, nullptr, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream));
+             nullptr, nullptr, nullptr, 0, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
 sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* clusters,
@@ -291,7 +363,11 @@ sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* 
 }
 
 size_t spec_verify_workspace_bytes(const sv_problem* prob) {
-  return sv::workspace_bytes_for(prob ? prob->B : 0);
+  if (!prob) return sv::workspace_bytes_for(0);
+  // a bias set or top-F ids: room for the top-8 prepass keys as well
+  const bool top8 = prob->bias_k > 0 || prob->fanout != nullptr;
+  return sv::workspace_bytes_for(prob->B) +
+         (top8 && prob->B > 0 && prob->K > 0 ? keys_bytes(prob) : 0);
 }
 
 sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
@@ -305,7 +381,7 @@ sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
     return SV_ERR_INVALID_ARG;
   return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
              temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr,
-             nullptr, nullptr, nullptr, 0, static_cast<Workspace*>(workspace),
+             nullptr, nullptr, nullptr, 0, static_cast<Workspace*>(workspace), workspace_bytes,
              static_cast<cudaStream_t>(stream));
 }
 
@@ -338,7 +414,7 @@ sv_status spec_verify_noalloc(const sv_problem* prob, const void* target_logits,
   if (cudaMemsetAsync(ws, 0, sizeof(Workspace), s) != cudaSuccess) return SV_ERR_CUDA;
   return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms, temperature,
              beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr, nullptr, nullptr,
-             nullptr, 0, static_cast<Workspace*>(ws), s);
+             nullptr, 0, static_cast<Workspace*>(ws), sizeof(Workspace), s);
 }
 
 sv_status spec_verify_debug(const sv_problem* prob, const void* target_logits,
@@ -349,7 +425,7 @@ sv_status spec_verify_debug(const sv_problem* prob, const void* target_logits,
                             float* out_lse_d, float* out_p_x, float* out_q_x, void* stream) {
   return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms,
              temperature, beta, mode, out_accept_len, out_tokens, out_residual_topF, out_lse_t,
-             out_lse_d, out_p_x, out_q_x, 1, nullptr, static_cast<cudaStream_t>(stream));
+             out_lse_d, out_p_x, out_q_x, 1, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
 sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
@@ -381,7 +457,6 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
   char* base = nullptr;
-  Workspace* ws = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     StreamRes* r = resources(dev, s, sv::workspace_bytes_for(prob->B), &st);
@@ -395,7 +470,6 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
       r->stage_bytes = total;
     }
     base = static_cast<char*>(r->stage);
-    ws = r->ws;
   }
   char* d_t = base;
   char* d_d = d_t + b_t;
@@ -433,9 +507,15 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
   if (draft_lens) ok = ok && cp(d_len, draft_lens, static_cast<size_t>(B) * 4);
   if (!c.greedy) ok = ok && cp(d_uni, uniforms, static_cast<size_t>(B) * (K + 1) * 4);
   if (!ok) return SV_ERR_CUDA;
+  // (the stream's own workspace, sized by run for this problem)
   st = run(prob, d_t, c.greedy ? nullptr : d_d, d_tok, d_len, d_uni, temperature, beta, mode,
-           d_acc, d_otok, d_topf, nullptr, nullptr, nullptr, nullptr, 0, ws, s);
+           d_acc, d_otok, d_topf, nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0, s);
   if (st != SV_OK) return st;
+  Workspace* ws = nullptr;  // the workspace run used (it may have grown it)
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ws = g_res[{dev, s}].ws;
+  }
   if (cudaMemcpyAsync(out_accept_len, d_acc, static_cast<size_t>(B) * 4,
                       cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaMemcpyAsync(out_tokens, d_otok, static_cast<size_t>(B) * (K + 1) * 4,
@@ -484,9 +564,6 @@ sv_status spec_verify_device_error(void* stream) {
 
 namespace {
 
-// dev, mode, dtype, bias, V -> (ring stages, CTAs per SM)
-std::map<std::tuple<int, int, int, int, int>, std::pair<int, int>> g_row_occ;
-
 bool aligned16(const void* p, long long stride, size_t elt) {
   return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (stride * static_cast<long long>(elt)) % 16 == 0;
 }
@@ -501,22 +578,8 @@ sv_status run_rows(sv::RowParams& P, int mode, int dtype, int units, const int32
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  const auto key = std::make_tuple(dev, mode, dtype, bias ? 1 : 0, P.V);
-  auto it = g_row_occ.find(key);
-  if (it == g_row_occ.end()) {
-    int nst = 0, per_sm = 0;
-    for (int st = sv::kRowMaxStages; st >= 3 && !nst; --st)
-      if (sv::row_smem_bytes(mode, P.V, st) <= 112 * 1024) nst = st;
-    if (nst) per_sm = sv::row_ctas_per_sm(mode, dtype, bias, P.V, nst);
-    if (per_sm < 2) {
-      nst = 0;
-      for (int st = sv::kRowMaxStages; st >= 2 && !nst; --st)
-        if (sv::row_smem_bytes(mode, P.V, st) <= sv::kRowMaxSmem) nst = st;
-      per_sm = nst ? sv::row_ctas_per_sm(mode, dtype, bias, P.V, nst) : 0;
-    }
-    it = g_row_occ.emplace(key, std::make_pair(nst, per_sm)).first;
-  }
-  const int nst = it->second.first, per_sm = it->second.second;
+  const std::pair<int, int> rc = row_config(dev, mode, dtype, bias, P.V);
+  const int nst = rc.first, per_sm = rc.second;
   if (nst < 2 || per_sm < 1) return SV_ERR_UNSUPPORTED;
   P.nstages = nst;
   sv_status st = SV_OK;

@@ -54,6 +54,7 @@ struct Params {
   int use_bulk;   // rows and strides are 16-byte aligned: stage rows with bulk async copies
   int n_clusters;
   int lpt;         // take sequences longest draft first
+  const unsigned long long* keys;  // top-8 keys of every draft row from the prepass, or NULL
   Workspace* ws;
 };
 

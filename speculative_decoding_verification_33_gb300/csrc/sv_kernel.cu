@@ -64,7 +64,8 @@ struct __align__(16) Xchg {
 };
 static_assert(sizeof(Xchg) == 112, "exchange record layout");
 
-struct Hdr {
+struct __align__(16) Hdr {
+  unsigned long long key[kMaxK][8];  // the prepass's top-8 keys of each draft row (if any)
   int L, ok;
   int x[kMaxK];
   float u[kMaxK + 1];
@@ -893,6 +894,11 @@ __device__ void combine(const Params& P, CtaState& S, const Xchg* XX, uint32_t C
     }
     if (lane != 0) return;
     const int L = S.hdr[S.cur].L;
+    // the prepass's keys of this draft row stand in for the in-stream top 8
+    const bool kk = P.keys != nullptr && st_d && i < L;
+    if (kk)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mtop[j] = S.hdr[S.cur].key[i][j];
     S.M_t = Mt;
     S.M_d = Md;
     S.S_t = St;
@@ -901,7 +907,7 @@ __device__ void combine(const Params& P, CtaState& S, const Xchg* XX, uint32_t C
     S.bad_d = ld_d ? row_bad(Md) : 0;
     float N = 1.f;  // Saguaro bias set: the bias_k most likely draft ids
     int nS = 0;
-    if (P.bias_k > 0 && tk && !S.bad_d) {
+    if (P.bias_k > 0 && (tk || kk) && !S.bad_d) {
       float sq = 0.f;
       for (int j = 0; j < P.bias_k; ++j) {
         if (mtop[j] == 0ull) break;
@@ -946,6 +952,10 @@ __device__ __forceinline__ void fetch_header(const Params& P, CtaState& S, int s
   if (P.lens) cp_async4(&h.L, P.lens + seq);
   else h.L = P.K;
   for (int i = 0; i < P.K; ++i) cp_async4(&h.x[i], P.tokens + static_cast<long long>(seq) * P.K + i);
+  if (P.keys)
+    for (int i = 0; i < P.K; ++i)
+      for (int j = 0; j < 8; j += 2)
+        cp_async16(&h.key[i][j], P.keys + (static_cast<long long>(seq) * P.K + i) * 8 + j);
   if (!greedy)
     for (int i = 0; i <= P.K; ++i)
       cp_async4(&h.u[i], P.uni + static_cast<long long>(seq) * (P.K + 1) + i);
@@ -960,6 +970,11 @@ __device__ __forceinline__ int header_ok(const Params& P, const Hdr& h, bool gre
   if (!greedy)
     for (int i = 0; i <= P.K; ++i)
       if ((i < L || i == P.K) && !(h.u[i] >= 0.f && h.u[i] < 1.f)) return 0;
+  // with top-F ids, every draft row below L must hold a distribution (the prepass marks one that
+  // does not with the key ~0)
+  if (P.keys && P.fmax > 0)
+    for (int i = 0; i < L; ++i)
+      if (h.key[i][0] == ~0ull) return 0;
   return 1;
 }
 
@@ -1532,7 +1547,11 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           int32_t* tf = P.out_topf + static_cast<long long>(seq) * K * P.fmax;
           for (int e = tid; e < K * P.fmax; e += NC) {
             const int i = e / P.fmax, f = e % P.fmax;
-            tf[e] = (!bad && i < L && f < 8) ? S.topf[i][f] : -1;
+            if (P.keys) {  // the prepass wrote the ids of the rows below L
+              if (bad || i >= L) tf[e] = -1;
+            } else {
+              tf[e] = (!bad && i < L && f < 8) ? S.topf[i][f] : -1;
+            }
           }
         }
         if (P.dbg_lse_t && tid <= K)

@@ -54,7 +54,7 @@ constexpr int kStage = kRowStageBytes;  // bytes per ring stage
 constexpr int kGroup = 64;              // elements per group (8 vectors of 8)
 constexpr float kLn2r = 0.69314718055994531f;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per barrier wait
-constexpr int MODE_SAMPLE = 0, MODE_RESID = 1;
+constexpr int MODE_SAMPLE = 0, MODE_RESID = 1, MODE_TOP8 = 2;
 constexpr int kEnd = -1;  // unit tag after the last unit
 constexpr int kBatch = 4;  // candidate groups whose loads an epilogue warp keeps in flight
 
@@ -408,6 +408,21 @@ __device__ __forceinline__ void chunk_groups(const T* stage, int n, float c, flo
   }
 }
 
+// Group maxima only (the top-8 prepass), and the row maximum in the thread's running stats.
+template <typename T>
+__device__ __forceinline__ void chunk_maxima(const T* stage, int n, float c, float* gmax,
+                                             RowRun& run) {
+  using G = Lanes<T>;
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint4 q[G::PPL];
+  load_pieces<T>(stage, n, q);
+  const float g = group_max<G::LPG>(pieces_max<T>(q));
+  if ((lane & (G::LPG - 1)) == 0 && G::EPL * tid < n) {
+    gmax[tid / G::LPG] = g;
+    run.add(g, __fmul_rn(g, c), 0.f);
+  }
+}
+
 // Residual chunks: the same for a target and a draft chunk at once (n valid elements each), plus
 // each group's largest log-ratio max (z_t - z_d), which bounds the group's residual from above
 // once the normalisers are known.
@@ -566,6 +581,11 @@ __device__ void producer(const RowParams& P, RowShared& S, unsigned char* ring) 
     int nrows = 1;
     if (MODE == MODE_SAMPLE) {
       rows[0] = static_cast<const T*>(P.dft) + static_cast<long long>(u) * P.d_stride;
+    } else if (MODE == MODE_TOP8) {
+      const int b = u / P.K, i = u % P.K;
+      const int L = P.lens ? P.lens[b] : P.K;
+      if (L < 1 || L > P.K || i >= L) continue;  // a row the verify step never asks about
+      rows[0] = static_cast<const T*>(P.dft) + (static_cast<long long>(b) * P.K + i) * P.d_stride;
     } else {
       const int b = u / P.K, i = u % P.K;
       const int L = P.lens ? P.lens[b] : P.K;
@@ -703,6 +723,9 @@ __device__ void chunk_warps(const RowParams& P, RowShared& S, unsigned char* rin
       const T* st = reinterpret_cast<const T*>(ring + static_cast<size_t>(s) * kStage);
       if (MODE == MODE_SAMPLE) {  // maxima, then masses
         chunk_groups<T>(st, n, P.c, gb + ch * go, gb + ngmax + ch * go, run[0]);
+        release(s);
+      } else if (MODE == MODE_TOP8) {  // maxima
+        chunk_maxima<T>(st, n, P.c, gb + ch * go, run[0]);
         release(s);
       } else {  // target maxima, draft maxima, log-ratio maxima
         const int s2 = wait_full(it + 1);
@@ -983,6 +1006,34 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const fl
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// epilogue: the top-8 prepass of the verify step's draft rows
+// ------------------------------------------------------------------------------------------
+// Keys of the 8 largest logits of draft row (b, i) = u (ties to the lower id), for the verify
+// step's bias set and its top-F ids; a row that holds no distribution gets the key ~0 first. With
+// top-F output requested, also the first F_i ids of the row.
+template <typename T>
+__device__ void top8_epilogue(const RowParams& P, RowShared& S, int u, const float* gmax,
+                              const float* hdr) {
+  const int t = et();
+  const int V = P.V;
+  const int ng = (V + kGroup - 1) / kGroup;
+  const int i = u % P.K;
+  const T* row = static_cast<const T*>(P.dft) +
+                 (static_cast<long long>(u / P.K) * P.K + i) * P.d_stride;
+  unsigned long long* keys = P.out_keys + static_cast<long long>(u) * 8;
+  if (row_bad(hdr[0])) {
+    if (t < 8) keys[t] = t == 0 ? ~0ull : 0ull;
+    return;
+  }
+  row_top8<T>(row, V, P.use_vec != 0, gmax, ng, S);
+  if (t < 8) keys[t] = S.top[t];
+  if (P.out_topf && t < P.fmax) {
+    const unsigned long long k = t < 8 ? S.top[t] : 0ull;
+    P.out_topf[static_cast<long long>(u) * P.fmax + t] = (t < P.fan[i] && k != 0ull) ? key_id(k) : -1;
+  }
+}
+
 template <typename T, int MODE, bool BIAS>
 __device__ void epilogue_warps(const RowParams& P, RowShared& S, float* gbuf0, float* gbuf1,
                                int ngmax) {
@@ -996,6 +1047,8 @@ __device__ void epilogue_warps(const RowParams& P, RowShared& S, float* gbuf0, f
     float* gb = b ? gbuf1 : gbuf0;
     if (MODE == MODE_SAMPLE)
       sample_epilogue<T, BIAS>(P, S, u, gb, gb + ngmax, S.hdr[b]);
+    else if (MODE == MODE_TOP8)
+      top8_epilogue<T>(P, S, u, gb, S.hdr[b]);
     else
       resid_epilogue<T, BIAS>(P, S, u, gb, gb + ngmax, gb + 2 * ngmax, S.hdr[b]);
     esync();  // every epilogue thread is done with the buffer and the scratch
@@ -1014,7 +1067,7 @@ __global__ void __launch_bounds__(RT, 2) row_kernel(const RowParams P) {
   const int nst = P.nstages;
   unsigned char* ring = smem;
   const int ngmax = (P.V + kGroup - 1) / kGroup;
-  const int narr = MODE == MODE_SAMPLE ? 2 : 3;  // per-group arrays of a buffer
+  const int narr = MODE == MODE_SAMPLE ? 2 : (MODE == MODE_TOP8 ? 1 : 3);  // arrays per buffer
   float* gbuf0 = reinterpret_cast<float*>(smem + static_cast<size_t>(nst) * kStage);
   float* gbuf1 = gbuf0 + static_cast<size_t>(narr) * ngmax;
   const int tid = threadIdx.x;
@@ -1071,12 +1124,14 @@ const void* pick_fn(int dtype, bool bias) {
 
 size_t row_smem_bytes(int mode, int V, int nstages) {
   const size_t ng = static_cast<size_t>((V + kGroup - 1) / kGroup);
-  return static_cast<size_t>(nstages) * kStage + 2 * ng * 4 * (mode == MODE_SAMPLE ? 2 : 3);
+  return static_cast<size_t>(nstages) * kStage +
+         2 * ng * 4 * (mode == MODE_SAMPLE ? 2 : (mode == MODE_TOP8 ? 1 : 3));
 }
 
 int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages) {
   const void* fn = mode == MODE_SAMPLE ? pick_fn<MODE_SAMPLE>(dtype, bias)
-                                       : pick_fn<MODE_RESID>(dtype, bias);
+                   : mode == MODE_TOP8  ? pick_fn<MODE_TOP8>(dtype, false)
+                                        : pick_fn<MODE_RESID>(dtype, bias);
   const size_t smem = row_smem_bytes(mode, V, nstages);
   if (smem > kRowMaxSmem) return 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1091,7 +1146,8 @@ cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const
                         const int32_t* tok, const int32_t* r1, cudaStream_t stream) {
   const bool bias = P.bias_k > 0 && P.beta < 1.f;
   const void* fn = mode == MODE_SAMPLE ? pick_fn<MODE_SAMPLE>(dtype, bias)
-                                       : pick_fn<MODE_RESID>(dtype, bias);
+                   : mode == MODE_TOP8  ? pick_fn<MODE_TOP8>(dtype, false)
+                                        : pick_fn<MODE_RESID>(dtype, bias);
   if (P.nstages < 2 || P.nstages > kRowMaxStages) return cudaErrorInvalidValue;
   const size_t smem = row_smem_bytes(mode, P.V, P.nstages);
   if (smem > kRowMaxSmem) return cudaErrorInvalidValue;

@@ -35,6 +35,8 @@ struct RowParams {
   int32_t* out_exit;             // may be NULL
   int32_t* out_r2;               // residual
   int32_t* out_hit;              // may be NULL
+  unsigned long long* out_keys;  // top-8 prepass: 8 keys per (sequence, position)
+  int32_t* out_topf;             // top-8 prepass: [B][K][fmax] top-F ids (may be NULL)
   Workspace* ws;                 // unit queue and error word (bit 0: a bounded wait gave up)
 };
 
@@ -43,8 +45,9 @@ size_t row_smem_bytes(int mode, int V, int nstages);
 // Co-resident CTAs per SM of the kernel for this configuration (0: does not fit).
 int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages);
 
-// mode 0: sampling (B rows), 1: residual top-F (B * K (sequence, position) pairs); `ctas`
-// persistent CTAs. With out_hit set, the residual launch is followed by the cache-hit flags.
+// mode 0: sampling (B rows), 1: residual top-F, 2: top-8 prepass of the verify step's draft rows
+// (both over B * K (sequence, position) pairs); `ctas` persistent CTAs. With out_hit set, the
+// residual launch is followed by the cache-hit flags.
 cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const int32_t* acc,
                         const int32_t* tok, const int32_t* r1, cudaStream_t stream);
 

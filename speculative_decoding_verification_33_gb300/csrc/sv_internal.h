@@ -11,8 +11,8 @@ constexpr int kMaxCluster = 16;   // CTAs that share one sequence's rows
 constexpr int kMaxK = 8;          // maximum draft length
 constexpr int kMaxV = 262144;     // maximum vocabulary
 constexpr int kQScale = 44;       // residual weights are summed as integers of 2^-44
-constexpr int NS = 3;             // stages of the per-CTA row ring
-constexpr int kStageRowBytes = 8192;  // bytes of one row in one stage
+constexpr int NS = 2;             // stages of the per-CTA row ring
+constexpr int kStageRowBytes = 16384;  // bytes of one row in one stage
 constexpr int kMaxSlice = 65536;  // elements of a row one CTA owns (bounds the draw's buffer)
 
 // Device workspace shared by the clusters of one launch. The kernel returns the counters to

@@ -236,6 +236,25 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
                              const int32_t* out_tokens, const int32_t* r1_topF, int32_t* out_r2,
                              int32_t* out_hit, void* stream);
 
+/*
+ * The LM head fused with the softmax statistics (Kangaroo guide, "Exit 1": the head is
+ * Softmax(W h)): logits z = h W^T for `rows` hidden states h (bf16, rows of d elements at row
+ * stride hidden_stride) and a head W (bf16, V rows of d at row stride weight_stride), reduced on
+ * the GPU to, per row r:
+ *   out_max[r] = max_v z[r][v],
+ *   out_lse[r] = log sum_v exp(z[r][v] / T)   (natural log),
+ *   out_zx[r]  = z[r][ids[r]] (NaN when ids[r] is outside [0, V)); out_zx may be NULL.
+ * No logit is written to memory unless out_logits ([rows][V] fp32, for tests) is given. The
+ * logits are accumulated in fp32 from bf16 products on the tensor cores. d must be a multiple
+ * of 64, strides multiples of 8 elements, both pointers 16-byte aligned; V <= 2^24.
+ * Asynchronous on `stream`, on the stream's workspace; SV_ERR_UNSUPPORTED when the driver's
+ * tensor-map encoder cannot be had.
+ */
+sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long long hidden_stride,
+                            const void* weight, long long weight_stride, float temperature,
+                            const int32_t* ids, float* out_max, float* out_lse, float* out_zx,
+                            float* out_logits, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* spec_verify_status_string(sv_status status);
 

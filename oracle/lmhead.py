@@ -1,0 +1,80 @@
+"""Float64 CPU oracle for the LM head of the verify step and its softmax statistics.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference legs of ``bench.py`` may import this module. The product path never calls it and it
+shares no code with that path.
+
+* Logits (Kangaroo page, section 2, "Exit 1": the head maps a hidden state ``h`` to
+  ``Softmax(W h)``; LayerSkip page: the early exit reuses the full model's head): ``z = h W^T``
+  for bf16 ``h`` [R, d] and ``W`` [V, d], every product and sum taken in float64 (a bf16 x bf16
+  product is exact there; the sum of ``d`` such terms carries one float64 rounding each).
+* Statistics of the temperature softmax ``p = softmax(z / T)`` that the verify step needs per
+  row (speculative sampling page, "Algorithm": the accept ratio ``p(x) / q(x)``): the largest
+  logit ``max_v z_v``, the natural log-sum-exp ``ln sum_v exp(z_v / T)`` (so that
+  ``ln p(x) = z_x / T - lse``), and the logit ``z_x`` of a requested id (NaN for an id outside
+  ``[0, V)``). The log-sum-exp is taken about the maximum, ``M / T + ln sum exp((z - M) / T)``.
+
+Parity pins: ``tests/test_oracle_lmhead_pins.py`` (one-hot heads, closed-form sums, shift and
+scale laws, brute-force products on tiny inputs).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) to float64, exactly: the pattern is the top half of a float32."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def head_logits(hidden, weight) -> np.ndarray:
+    """z = h W^T in float64 for ``hidden`` [R, d] and ``weight`` [V, d] (bf16 bits or floats)."""
+    h = bf16_to_f64(hidden) if np.asarray(hidden).dtype == np.uint16 else np.asarray(hidden, np.float64)
+    w = bf16_to_f64(weight) if np.asarray(weight).dtype == np.uint16 else np.asarray(weight, np.float64)
+    if h.shape[-1] != w.shape[-1]:
+        raise ValueError("hidden and weight disagree on d")
+    return h @ w.T
+
+
+@dataclass
+class HeadStats:
+    max: np.ndarray  # [R] largest logit
+    lse: np.ndarray  # [R] ln sum_v exp(z_v / T)
+    zx: np.ndarray   # [R] logit of the requested id (NaN when out of range or not asked)
+
+
+def softmax_stats(z, temperature: float, ids: Optional[np.ndarray] = None) -> HeadStats:
+    """The row statistics of ``softmax(z / T)`` for a float64 logit matrix ``z`` [R, V]."""
+    z = np.asarray(z, dtype=np.float64)
+    T = float(temperature)
+    if not (T > 0.0):
+        raise ValueError("temperature must be positive")
+    R, V = z.shape
+    M = z.max(axis=1)
+    lse = M / T + np.log(np.exp((z - M[:, None]) / T).sum(axis=1))
+    zx = np.full(R, math.nan)
+    if ids is not None:
+        ids = np.asarray(ids, dtype=np.int64)
+        ok = (ids >= 0) & (ids < V)
+        zx[ok] = z[np.nonzero(ok)[0], ids[ok]]
+    return HeadStats(M, lse, zx)
+
+
+def head_stats(hidden, weight, temperature: float, ids=None) -> HeadStats:
+    """Logits of the head and their softmax statistics, in one call."""
+    return softmax_stats(head_logits(hidden, weight), temperature, ids)
+
+
+def logit_error_bound(hidden, weight) -> np.ndarray:
+    """Bound on |fl32(z) - z| for logits summed in float32 from exact bf16 products, per
+    (row, id): d * 2^-23 * sum_j |h_j w_j| (the classical bound for a sum of d terms, with a
+    unit roundoff of 2^-23 so that truncating adders are covered too), times 1.01."""
+    h = np.abs(bf16_to_f64(hidden))
+    w = np.abs(bf16_to_f64(weight))
+    d = h.shape[-1]
+    return (d * 2.0 ** -23 * 1.01) * (h @ w.T)

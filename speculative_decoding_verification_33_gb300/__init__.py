@@ -4,8 +4,8 @@ The hot path is one CUDA library (``_build/libspecverify.so``, sources in ``csrc
 ``include/spec_verify.h``); ``api`` is its thin torch binding and ``workloads`` makes the seeded
 synthetic inputs.
 """
-from .api import (device_error, draft_sample, hbm_read_probe, residual_topf, spec_verify,
-                  to_device_logits, verify, verify_host)
+from .api import (device_error, draft_sample, hbm_read_probe, lmhead_stats, residual_topf,
+                  spec_verify, to_device_logits, verify, verify_host)
 
 __all__ = ["spec_verify", "verify", "verify_host", "draft_sample", "residual_topf",
-           "device_error", "hbm_read_probe", "to_device_logits"]
+           "lmhead_stats", "device_error", "hbm_read_probe", "to_device_logits"]

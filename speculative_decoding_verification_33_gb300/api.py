@@ -197,6 +197,35 @@ def residual_topf(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     return out
 
 
+def lmhead_stats(hidden: torch.Tensor, weight: torch.Tensor, ids: Optional[torch.Tensor] = None,
+                 *, temperature: float = 1.0, logits: bool = False, stream=None):
+    """Row statistics of hidden @ weight.T on the tensor cores, without writing the logits (see
+    ``spec_lmhead_stats`` in include/spec_verify.h). ``hidden`` [R, d] and ``weight`` [V, d] are
+    bf16 CUDA tensors with contiguous rows; ``ids`` [R] int32. Returns {"max", "lse"[, "zx"]
+    [, "logits"]} (fp32); ``logits=True`` also writes the [R, V] logits (tests)."""
+    for t, n in ((hidden, "hidden"), (weight, "weight")):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{n} must be a 2-D bf16 tensor with contiguous rows")
+    R, d = hidden.shape
+    V = weight.shape[0]
+    if weight.shape[1] != d:
+        raise ValueError("hidden and weight disagree on d")
+    dev = hidden.device
+    out = {"max": torch.empty(R, dtype=torch.float32, device=dev),
+           "lse": torch.empty(R, dtype=torch.float32, device=dev)}
+    if ids is not None:
+        out["zx"] = torch.empty(R, dtype=torch.float32, device=dev)
+    if logits:
+        out["logits"] = torch.empty(R, V, dtype=torch.float32, device=dev)
+    st = _lib.load().spec_lmhead_stats(
+        int(R), int(d), int(V), _ptr(hidden, "hidden"), int(hidden.stride(0) if R > 1 else d),
+        _ptr(weight, "weight"), int(weight.stride(0) if V > 1 else d), float(temperature),
+        _ptr(ids, "ids", torch.int32), _ptr(out["max"], "max"), _ptr(out["lse"], "lse"),
+        _ptr(out.get("zx"), "zx"), _ptr(out.get("logits"), "logits"), _stream_handle(stream))
+    _lib._check(st, "spec_lmhead_stats")
+    return out
+
+
 def _host_ptr(a) -> int:
     if a is None:
         return 0

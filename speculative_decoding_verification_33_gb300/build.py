@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspecverify.so"
-SOURCES = ["sv_kernel.cu", "sv_api.cu", "sv_probe.cu", "sv_rows.cu"]
+SOURCES = ["sv_kernel.cu", "sv_api.cu", "sv_probe.cu", "sv_rows.cu", "sv_lmhead.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
@@ -52,6 +52,7 @@ def source_digest() -> str:
 KERNEL_SOURCES = {
     "verify": ("sv_kernel.cu", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h"),
     "rows": ("sv_rows.cu", "sv_rows.h", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h"),
+    "lmhead": ("sv_lmhead.cu", "sv_lmhead.h", "sv_tc.cuh", "sv_math.cuh", "sv_ptx.cuh"),
 }
 
 

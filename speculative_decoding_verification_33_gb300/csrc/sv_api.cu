@@ -16,6 +16,7 @@
 #include "spec_verify.h"
 #include "sv_internal.h"
 #include "sv_rows.h"
+#include "sv_lmhead.h"
 #include "sv_probe.h"
 
 namespace {
@@ -670,6 +671,47 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
                   : 0;
   return run_rows(P, 1, prob->dtype == SV_DTYPE_BF16 ? 1 : 0, prob->B * prob->K, accept_len,
                   out_tokens, r1_topF, static_cast<cudaStream_t>(stream));
+}
+
+sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long long hidden_stride,
+                            const void* weight, long long weight_stride, float temperature,
+                            const int32_t* ids, float* out_max, float* out_lse, float* out_zx,
+                            float* out_logits, void* stream) {
+  if (rows < 0 || d < 64 || d % 64 != 0 || V < 1 || V > (1 << 24)) return SV_ERR_INVALID_ARG;
+  if (hidden_stride < d || weight_stride < d || (hidden_stride * 2) % 16 != 0 ||
+      (weight_stride * 2) % 16 != 0)
+    return SV_ERR_INVALID_ARG;
+  if (!finite_in(temperature, 1e-4f, 1e4f)) return SV_ERR_INVALID_ARG;
+  if (rows == 0) return SV_OK;
+  if (!hidden || !weight || !out_max || !out_lse) return SV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(hidden) % 16 != 0 || reinterpret_cast<uintptr_t>(weight) % 16 != 0)
+    return SV_ERR_INVALID_ARG;
+  if (out_zx && !ids) return SV_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int sms = sm_count(dev);
+  if (sms <= 0) return SV_ERR_CUDA;
+  sv::HeadParams P;
+  memset(&P, 0, sizeof(P));
+  P.R = rows;
+  P.d = d;
+  P.V = V;
+  P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  P.inv_t = static_cast<float>(1.0 / static_cast<double>(temperature));
+  P.ids = ids;
+  P.out_logits = out_logits;
+  sv::head_split(rows, V, sms, &P.nsplit, &P.tiles_per_split, &P.ntiles);
+  sv_status st = SV_OK;
+  StreamRes* r = resources(dev, s, sizeof(Workspace) + sv::head_part_bytes(rows, P.nsplit), &st);
+  if (!r) return st;
+  P.part = reinterpret_cast<float*>(r->ws + 1);
+  P.err = &r->ws->error;
+  const cudaError_t e = sv::launch_lmhead(hidden, hidden_stride, weight, weight_stride, P, out_max,
+                                          out_lse, out_zx, s);
+  if (e == cudaErrorNotSupported) return SV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 const char* spec_verify_status_string(sv_status status) {

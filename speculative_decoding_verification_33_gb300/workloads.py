@@ -198,3 +198,83 @@ def make_inputs(w: Workload, offset: int = 0, threads: Optional[int] = None) -> 
 def small_variant(w: Workload, B: int, V: Optional[int] = None) -> Workload:
     """Same generation recipe at a smaller batch (and optionally vocabulary)."""
     return w.replace(B=B, V=V if V is not None else w.V)
+
+
+# ---------------------------------------------------------------------------------------------
+# LM-head inputs: hidden states and a head matrix whose product gives logits of the shape above
+# ---------------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class HeadWorkload:
+    """Hidden states [R, d] and an LM head [V, d] (bf16) for the fused head statistics.
+
+    ``R`` counts the rows one verify step scores: ``B * (K + 1)`` target rows plus ``B * K``
+    draft rows of the matching verify workload (the early-exit draft of LayerSkip and Kangaroo
+    shares the full model's head, so both go through the same matrix). ``d`` is the hidden size
+    of the model family the vocabulary belongs to (4096 for Llama-2/3 8B-class models, 3584 for
+    the Qwen model with 152064 ids)."""
+
+    name: str
+    R: int
+    d: int
+    V: int
+    temperature: float
+    sigma: float = 2.0  # standard deviation of the logits' noise part
+    zipf: bool = True
+
+
+HEAD_WORKLOADS = {
+    "head_B64_K5_V128256_d4096": HeadWorkload("head_B64_K5_V128256_d4096", R=64 * 6 + 64 * 5,
+                                              d=4096, V=128256, temperature=0.8),
+    "head_B256_K8_V152064_d3584": HeadWorkload("head_B256_K8_V152064_d3584",
+                                               R=256 * 9 + 256 * 8, d=3584, V=152064,
+                                               temperature=1.0),
+}
+
+
+def head_inputs(w: HeadWorkload, offset: int = 0) -> dict:
+    """Seeded hidden states, head and ids for ``w``.
+
+    Recipe: hidden ``h[r, j] ~ N(0, 1)`` for ``j < d - 1`` and ``h[r, d-1] = 1``; head
+    ``W[v, j] ~ N(0, sigma^2 / (d - 1))`` for ``j < d - 1`` and ``W[v, d-1]`` = the Zipf(1.1)
+    log-prior of the verify workloads (0 when ``zipf`` is off). The logits ``h W^T`` are then
+    about prior + N(0, sigma^2) per row, the shape of the verify workloads' target rows. Both
+    are rounded to bf16 (round to nearest even). ``ids[r]`` is a uniform id in ``[0, V)``.
+    Seeds: ``default_rng([600 | 800 | 400, R, d, V, offset])`` (hidden, ids, prior) and
+    ``default_rng([700, R, d, V, offset, v0])`` for the head's rows ``v0 .. v0 + 4095``.
+    Returns ``hidden`` [R, d] and ``weight`` [V, d] as uint16 bit patterns and ``ids`` [R]
+    int32."""
+    R, d, V = w.R, w.d, w.V
+    rng_h = np.random.default_rng([600, R, d, V, offset])
+    rng_i = np.random.default_rng([800, R, d, V, offset])
+    h = rng_h.standard_normal((R, d), dtype=np.float32)
+    h[:, d - 1] = 1.0
+    hidden = f32_to_bf16_bits(h)
+    del h
+    weight = np.empty((V, d), dtype=np.uint16)
+    scale = np.float32(w.sigma / np.sqrt(max(1, d - 1)))
+    if w.zipf:
+        perm = np.random.default_rng([400, R, d, V, offset]).permutation(V)
+        prior = (-1.1 * np.log1p(perm.astype(np.float64))).astype(np.float32)
+    else:
+        prior = np.zeros(V, dtype=np.float32)
+    step = 4096
+
+    def fill(v0: int) -> None:
+        rng_w = np.random.default_rng([700, R, d, V, offset, v0])
+        blk = rng_w.standard_normal((min(step, V - v0), d), dtype=np.float32)
+        blk *= scale
+        blk[:, d - 1] = prior[v0:v0 + blk.shape[0]]
+        weight[v0:v0 + blk.shape[0]] = f32_to_bf16_bits(blk)
+
+    threads = min(16, len(os.sched_getaffinity(0)))
+    with ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+        list(ex.map(fill, range(0, V, step)))
+    ids = rng_i.integers(0, V, size=R).astype(np.int32)
+    return {"workload": w, "hidden": hidden, "weight": weight, "ids": ids}
+
+
+def small_head(R: int, d: int, V: int, temperature: float = 1.0, zipf: bool = True,
+               sigma: float = 2.0) -> HeadWorkload:
+    """A head workload of the same recipe at other sizes (tests)."""
+    return HeadWorkload(f"head_R{R}_d{d}_V{V}", R=R, d=d, V=V, temperature=temperature,
+                        sigma=sigma, zipf=zipf)

@@ -1,0 +1,164 @@
+"""Pins of the LM-head oracle (logits of a bf16 head and the softmax statistics of a row)
+against textbook values, closed forms, algebraic laws and brute force; nothing here re-types
+its formulas."""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import lmhead as H
+
+
+# ----------------------------------------------------------------------------------------------
+# bf16 patterns (IEEE binary32 with the low 16 bits dropped)
+# ----------------------------------------------------------------------------------------------
+def test_bf16_textbook_patterns():
+    pats = np.array([0x3F80, 0xC000, 0x4049, 0x0001, 0x7F80, 0x0000, 0x8000, 0x3E80], np.uint16)
+    want = [1.0, -2.0, 3.140625, 2.0 ** -133, math.inf, 0.0, -0.0, 0.25]
+    got = H.bf16_to_f64(pats)
+    for g, w in zip(got, want):
+        assert g == w
+    assert math.copysign(1.0, got[6]) == -1.0
+
+
+# ----------------------------------------------------------------------------------------------
+# logits (Kangaroo page, section 2, "Exit 1")
+# ----------------------------------------------------------------------------------------------
+def test_one_hot_head_selects_hidden_units():
+    """A head whose row v is the unit vector e_pi(v) yields z[r, v] = h[r, pi(v)]."""
+    rng = np.random.default_rng(1)
+    R, d, V = 3, 7, 5
+    h = rng.integers(-20, 20, size=(R, d)).astype(np.float64) / 8.0
+    pi = np.array([4, 0, 6, 2, 2])
+    W = np.zeros((V, d))
+    W[np.arange(V), pi] = 1.0
+    z = H.head_logits(h, W)
+    assert z.shape == (R, V)
+    for r in range(R):
+        for v in range(V):
+            assert z[r, v] == h[r, pi[v]]
+
+
+def test_logits_brute_force_on_tiny_integers():
+    """Integer-valued bf16 entries: every logit is an exact integer, summed here term by term."""
+    rng = np.random.default_rng(2)
+    R, d, V = 3, 5, 4
+    h = rng.integers(-9, 10, size=(R, d))
+    W = rng.integers(-9, 10, size=(V, d))
+    hb = np.array([[_bf16_of_int(x) for x in row] for row in h], np.uint16)
+    Wb = np.array([[_bf16_of_int(x) for x in row] for row in W], np.uint16)
+    z = H.head_logits(hb, Wb)
+    for r in range(R):
+        for v in range(V):
+            acc = 0
+            for j in range(d):
+                acc += int(h[r, j]) * int(W[v, j])
+            assert z[r, v] == acc
+
+
+def _bf16_of_int(x: int) -> int:
+    """bf16 pattern of a small integer, built from sign, exponent and mantissa by hand."""
+    if x == 0:
+        return 0
+    x = int(x)
+    s = 0x8000 if x < 0 else 0
+    a = abs(x)
+    e = a.bit_length() - 1
+    mant = (a - (1 << e)) << (7 - e)  # |x| < 256: the 7 fraction bits hold it exactly
+    return s | ((e + 127) << 7) | mant
+
+
+def test_fraction_exact_sum_on_bf16_values():
+    """Random bf16 values: the float64 logit equals the exact rational sum rounded once per
+    addition at most; for d = 6 terms of 16-bit mantissas it is exact."""
+    rng = np.random.default_rng(3)
+    hb = rng.integers(0x3C00, 0x4100, size=(2, 6)).astype(np.uint16)
+    Wb = (rng.integers(0x3C00, 0x4100, size=(3, 6)) | 0x8000 * rng.integers(0, 2, (3, 6))).astype(np.uint16)
+    z = H.head_logits(hb, Wb)
+    hf, wf = H.bf16_to_f64(hb), H.bf16_to_f64(Wb)
+    for r in range(2):
+        for v in range(3):
+            exact = sum(Fraction(float(hf[r, j])) * Fraction(float(wf[v, j])) for j in range(6))
+            assert Fraction(float(z[r, v])) == exact
+
+
+# ----------------------------------------------------------------------------------------------
+# softmax statistics (speculative sampling page, "Algorithm")
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1.0, 0.8, 2.5])
+def test_lse_closed_forms(T):
+    V = 11
+    st = H.softmax_stats(np.full((1, V), 0.75), T)
+    assert st.lse[0] == pytest.approx(0.75 / T + math.log(V), rel=1e-14)
+    assert st.max[0] == 0.75
+    # two ids with p = 1/4, 3/4 at temperature T
+    st = H.softmax_stats(np.array([[0.0, T * math.log(3.0)]]), T)
+    assert st.lse[0] == pytest.approx(math.log(4.0), rel=1e-14)
+    # ln p(x) = z_x / T - lse gives the probabilities back
+    z = np.array([[1.0, -2.0, 0.5, 3.0]])
+    st = H.softmax_stats(z, T)
+    p = np.exp(z[0] / T - st.lse[0])
+    e = [math.exp(v / T) for v in z[0]]
+    for i in range(4):
+        assert p[i] == pytest.approx(e[i] / sum(e), rel=1e-13)
+
+
+def test_lse_shift_scale_and_bounds():
+    rng = np.random.default_rng(4)
+    z = rng.normal(0.0, 3.0, size=(5, 97))
+    for T in (0.7, 1.0, 1.9):
+        a = H.softmax_stats(z, T)
+        b = H.softmax_stats(z + 4.25, T)
+        np.testing.assert_allclose(b.lse - a.lse, 4.25 / T, rtol=1e-12)
+        c = H.softmax_stats(z / T, 1.0)
+        np.testing.assert_allclose(c.lse, a.lse, rtol=1e-13)
+        assert np.all(a.lse >= a.max / T) and np.all(a.lse <= a.max / T + math.log(97) + 1e-12)
+        np.testing.assert_array_equal(a.max, z.max(axis=1))
+
+
+def test_lse_of_large_logits_stays_finite():
+    st = H.softmax_stats(np.array([[1000.0, 1000.0, 990.0]]), 1.0)
+    assert st.lse[0] == pytest.approx(1000.0 + math.log(2.0 + math.exp(-10.0)), rel=1e-15)
+    st = H.softmax_stats(np.array([[-1000.0, -1001.0]]), 0.5)
+    assert st.lse[0] == pytest.approx(-2000.0 + math.log(1.0 + math.exp(-2.0)), rel=1e-15)
+
+
+def test_logit_at_id():
+    z = np.arange(12, dtype=np.float64).reshape(3, 4) * 0.5 - 1.0
+    st = H.softmax_stats(z, 1.0, ids=np.array([2, -1, 4]))
+    assert st.zx[0] == z[0, 2]
+    assert math.isnan(st.zx[1]) and math.isnan(st.zx[2])
+    assert np.all(np.isnan(H.softmax_stats(z, 1.0).zx))
+
+
+def test_temperature_must_be_positive():
+    with pytest.raises(ValueError):
+        H.softmax_stats(np.zeros((1, 3)), 0.0)
+
+
+# ----------------------------------------------------------------------------------------------
+# the float32 error bound used by the parity tests
+# ----------------------------------------------------------------------------------------------
+def test_error_bound_covers_float32_summation_orders():
+    """Sequential and pairwise float32 sums of exact bf16 products stay within the bound."""
+    rng = np.random.default_rng(6)
+    R, d, V = 4, 512, 6
+    hb = (rng.integers(0x3000, 0x4100, size=(R, d)) | 0x8000 * rng.integers(0, 2, (R, d))).astype(np.uint16)
+    Wb = (rng.integers(0x3000, 0x4100, size=(V, d)) | 0x8000 * rng.integers(0, 2, (V, d))).astype(np.uint16)
+    z = H.head_logits(hb, Wb)
+    bound = H.logit_error_bound(hb, Wb)
+    h32 = H.bf16_to_f64(hb).astype(np.float32)
+    w32 = H.bf16_to_f64(Wb).astype(np.float32)
+    for r in range(R):
+        for v in range(V):
+            prods = h32[r] * w32[v]  # exact in float32 (8-bit x 8-bit significands)
+            s = np.float32(0.0)
+            for t in prods:
+                s = np.float32(s + t)
+            assert abs(float(s) - z[r, v]) <= bound[r, v]
+            pw = prods.copy()
+            while pw.size > 1:
+                pw = (pw[0::2] + pw[1::2]).astype(np.float32)
+            assert abs(float(pw[0]) - z[r, v]) <= bound[r, v]
+    assert np.all(bound > 0)

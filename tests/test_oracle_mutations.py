@@ -136,3 +136,59 @@ def test_hit_at_the_bonus_position_is_caught(monkeypatch):
         return 1 if int(tokens[a]) in [int(v) for v in topf[a, :fanout[a]]] else 0
     monkeypatch.setattr(RO, "cache_hit", wrong)
     _fails(RP.test_cache_hit_hand_examples)
+
+
+# ----------------------------------------------------------------------------------------------
+# LM-head oracle
+# ----------------------------------------------------------------------------------------------
+from oracle import lmhead as HO  # noqa: E402
+from tests import test_oracle_lmhead_pins as HP  # noqa: E402
+
+
+def test_transposed_head_is_caught(monkeypatch):
+    real = HO.head_logits
+    # the head read column-wise: z[r, v] = sum_j h[r, j] W[j', v] for the square part
+    monkeypatch.setattr(HO, "head_logits", lambda h, w: real(h, np.asarray(w)[::-1]))
+    _fails(HP.test_one_hot_head_selects_hidden_units)
+
+
+def test_lse_without_temperature_is_caught(monkeypatch):
+    real = HO.softmax_stats
+    monkeypatch.setattr(HO, "softmax_stats", lambda z, T, ids=None: real(z, 1.0, ids))
+    _fails(HP.test_lse_closed_forms, 0.8)
+
+
+def test_log2_sum_is_caught(monkeypatch):
+    real = HO.softmax_stats
+
+    def wrong(z, T, ids=None):
+        st = real(z, T, ids)
+        st.lse = st.max / T + (st.lse - st.max / T) / math.log(2.0)
+        return st
+    monkeypatch.setattr(HO, "softmax_stats", wrong)
+    _fails(HP.test_lse_closed_forms, 1.0)
+
+
+def test_unshifted_exponentials_are_caught(monkeypatch):
+    def wrong(z, T, ids=None):
+        z = np.asarray(z, np.float64)
+        with np.errstate(over="ignore", divide="ignore"):
+            lse = np.log(np.exp(z / T).sum(axis=1))
+        return HO.HeadStats(z.max(axis=1), lse, np.full(z.shape[0], math.nan))
+    monkeypatch.setattr(HO, "softmax_stats", wrong)
+    _fails(HP.test_lse_of_large_logits_stays_finite)
+
+
+def test_off_by_one_logit_at_id_is_caught(monkeypatch):
+    real = HO.softmax_stats
+
+    def wrong(z, T, ids=None):
+        return real(z, T, None if ids is None else np.asarray(ids) + 1)
+    monkeypatch.setattr(HO, "softmax_stats", wrong)
+    _fails(HP.test_logit_at_id)
+
+
+def test_too_tight_error_bound_is_caught(monkeypatch):
+    real = HO.logit_error_bound
+    monkeypatch.setattr(HO, "logit_error_bound", lambda h, w: real(h, w) / 4096.0)
+    _fails(HP.test_error_bound_covers_float32_summation_orders)

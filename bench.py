@@ -54,10 +54,13 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample", type=int, default=16,
                     help="sequences per step of the reference arm")
-    ap.add_argument("--kernel", choices=["verify", "draft_sample", "residual_topf"],
+    ap.add_argument("--kernel", choices=["verify", "draft_sample", "residual_topf", "lmhead"],
                     default="verify",
                     help="verify: the verify step (default); draft_sample / residual_topf: the "
-                         "row kernels on the draft rows / draft positions of the same batch")
+                         "row kernels on the draft rows / draft positions of the same batch; "
+                         "lmhead: the tensor-core LM head with its softmax statistics")
+    ap.add_argument("--head", default="head_B256_K8_V152064_d3584",
+                    help="LM-head workload of --kernel lmhead")
     return ap.parse_args(argv)
 
 
@@ -424,6 +427,91 @@ def run_rows(args):
 
 
 # ---------------------------------------------------------------------------------------------
+# the LM head with its softmax statistics (tensor cores)
+# ---------------------------------------------------------------------------------------------
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback (1.9 PFLOP/s bf16 burst)"
+
+
+def run_lmhead(args):
+    import torch
+
+    from speculative_decoding_verification_33_gb300 import api, build
+    from speculative_decoding_verification_33_gb300 import workloads as W
+    from oracle import lmhead as HO
+
+    torch.cuda.set_device(dist_env()[2])
+    w = W.HEAD_WORKLOADS[args.head]
+    x = W.head_inputs(w)
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    H, Wt = dev(x["hidden"]), dev(x["weight"])
+    ids = torch.from_numpy(x["ids"]).cuda()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def step():
+        return api.lmhead_stats(H, Wt, ids, temperature=w.temperature)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(dist_env()[2])
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        out = step()
+        b.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    kms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = statistics.mean(kms)
+    flops = 2.0 * w.R * w.d * w.V
+    peak, peak_src = measured_tensor_peak()
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    traffic, traffic_src = recorded_traffic(f"lmhead {w.name}", build.kernel_digest("lmhead"))
+    unit = "head rows scored/s"
+    line = {"metric": f"{unit} and achieved bf16 TFLOP/s (% of roofline) at 1 GB300",
+            "value": w.R / (mean_ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"lmhead {w.name}", "R": w.R, "d": w.d, "V": w.V,
+                       "temperature": w.temperature,
+                       "l2": "flushed before each step (256 MiB write)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": peak_src, "traffic_source": traffic_src,
+                         "algorithmic_flops_per_launch": flops,
+                         "min_bytes_per_launch": 2 * (w.R + w.V) * w.d,
+                         "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms)},
+            "gpu_launches": args.steps * 2, "clocks": clk}
+    if not args.no_cpu:  # the oracle on a bounded sample of rows
+        rows = np.arange(0, w.R, max(1, w.R // 8))[:8]
+        t0 = time.perf_counter()
+        ref = HO.head_stats(x["hidden"][rows], x["weight"], w.temperature, x["ids"][rows])
+        dt = time.perf_counter() - t0
+        g = out["lse"].cpu().numpy().astype(np.float64)[rows]
+        line["parity_sample"] = {"rows": len(rows),
+                                 "max_abs_lse_diff": float(np.max(np.abs(g - ref.lse)))}
+        line["cpu_baseline"] = {"value": len(rows) / dt, "unit": unit,
+                                "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                "sample": f"{len(rows)} rows of {w.R} (float64 numpy matmul, "
+                                          "BLAS threads on the host cores)"}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------------
 def run_ours(args):
@@ -609,6 +697,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel == "lmhead":
+        run_lmhead(args)
     elif args.kernel != "verify":
         run_rows(args)
     else:

@@ -54,11 +54,13 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample", type=int, default=16,
                     help="sequences per step of the reference arm")
-    ap.add_argument("--kernel", choices=["verify", "draft_sample", "residual_topf", "lmhead"],
+    ap.add_argument("--kernel", choices=["verify", "draft_sample", "residual_topf", "lmhead",
+                                         "verify_hidden"],
                     default="verify",
                     help="verify: the verify step (default); draft_sample / residual_topf: the "
                          "row kernels on the draft rows / draft positions of the same batch; "
-                         "lmhead: the tensor-core LM head with its softmax statistics")
+                         "lmhead: the tensor-core LM head with its softmax statistics; "
+                         "verify_hidden: the verify step from hidden states through that head")
     ap.add_argument("--head", default="head_B256_K8_V152064_d3584",
                     help="LM-head workload of --kernel lmhead")
     return ap.parse_args(argv)
@@ -511,6 +513,93 @@ def run_lmhead(args):
     print(json.dumps(line), flush=True)
 
 
+def run_hidden(args):
+    """The verify step from hidden states: every row each sequence has goes through the
+    tensor-core head (statistics only), the decided rows again for the draw."""
+    import torch
+
+    from speculative_decoding_verification_33_gb300 import api
+    from speculative_decoding_verification_33_gb300 import workloads as W
+    from oracle import lmhead as HO
+    from tests import parity
+
+    torch.cuda.set_device(dist_env()[2])
+    w = W.HIDDEN_WORKLOADS["hv_B256_K8_V152064_d3584"]
+    x = W.hidden_inputs(w)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(
+            torch.bfloat16)
+    Ht, Hd, Wt = dev(x["hidden_target"]), dev(x["hidden_draft"]), dev(x["weight"])
+    X = torch.from_numpy(x["draft_tokens"]).cuda()
+    LN = torch.from_numpy(x["draft_lens"]).cuda()
+    U = torch.from_numpy(x["uniforms"]).cuda()
+    out = {"accept_len": torch.empty(w.B, dtype=torch.int32, device="cuda"),
+           "tokens": torch.empty(w.B, w.K + 1, dtype=torch.int32, device="cuda")}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def step():
+        api.verify_hidden(Ht, Hd, Wt, X, LN, U, temperature=w.temperature, out=out)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(dist_env()[2])
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    kms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = statistics.mean(kms)
+    lens = x["draft_lens"]
+    rows = int(np.sum(2 * lens + 1))
+    acc = out["accept_len"].cpu().numpy()
+    draws = int(np.sum(acc >= 0))
+    flops = 2.0 * (rows + 2 * 64 * ((w.B + 63) // 64)) * w.d * w.V
+    peak, peak_src = measured_tensor_peak()
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    toks = int(np.sum(lens))
+    line = {"metric": "verified draft tokens/sec from hidden states (tensor-core LM head + "
+                      "verify) and achieved bf16 TFLOP/s at 1 GB300",
+            "value": toks / (mean_ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"verify_hidden {w.name}", "B": w.B, "K": w.K, "V": w.V,
+                       "d": w.d, "rows_scored": rows, "draws": draws,
+                       "l2": "flushed before each step (256 MiB write)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": peak_src,
+                         "scope": "whole step (7 launches; the two head GEMMs are the work)",
+                         "algorithmic_flops_per_step": flops,
+                         "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms)},
+            "gpu_launches": args.steps * 7, "clocks": clk}
+    if not args.no_cpu:  # the oracle on a bounded sample of sequences
+        seqs = list(range(0, w.B, 32))
+        t0 = time.perf_counter()
+        res = HO.verify_hidden_batch(x["hidden_target"], x["hidden_draft"], x["weight"],
+                                     x["draft_tokens"], lens, x["uniforms"],
+                                     temperature=w.temperature, mode=w.mode, seqs=seqs)
+        dt = time.perf_counter() - t0
+        rep = parity.compare(res, seqs, acc, out["tokens"].cpu().numpy(), margin=1e-3)
+        line["parity_sample"] = {"sequences": rep.sequences, "flagged_1e-3": rep.flagged,
+                                 "mismatches": len(rep.mismatches)}
+        n = int(np.sum(lens[seqs]))
+        line["cpu_baseline"] = {"value": n / dt, "unit": UNIT,
+                                "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                "sample": f"{len(seqs)} of {w.B} sequences (float64 numpy "
+                                          "matmul for the logits, BLAS threads)"}
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------------
@@ -699,6 +788,8 @@ def main(argv=None):
         run_reference(args)
     elif args.kernel == "lmhead":
         run_lmhead(args)
+    elif args.kernel == "verify_hidden":
+        run_hidden(args)
     elif args.kernel != "verify":
         run_rows(args)
     else:

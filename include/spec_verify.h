@@ -243,7 +243,8 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
  * the GPU to, per row r:
  *   out_max[r] = max_v z[r][v],
  *   out_lse[r] = log sum_v exp(z[r][v] / T)   (natural log),
- *   out_zx[r]  = z[r][ids[r]] (NaN when ids[r] is outside [0, V)); out_zx may be NULL.
+ *   out_zx[r]  = z[r][ids[r]] (NaN when ids[r] is outside [0, V)); out_zx may be NULL,
+ *   out_argmax[r] = the lowest v with z[r][v] = out_max[r] (-1 for a row with a NaN); may be NULL.
  * No logit is written to memory unless out_logits ([rows][V] fp32, for tests) is given. The
  * logits are accumulated in fp32 from bf16 products on the tensor cores. d must be a multiple
  * of 64, strides multiples of 8 elements, both pointers 16-byte aligned; V <= 2^24.
@@ -253,7 +254,33 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
 sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long long hidden_stride,
                             const void* weight, long long weight_stride, float temperature,
                             const int32_t* ids, float* out_max, float* out_lse, float* out_zx,
-                            float* out_logits, void* stream);
+                            int32_t* out_argmax, float* out_logits, void* stream);
+
+/*
+ * The verify step taken from hidden states instead of logits (Kangaroo guide, "Exit 1" and
+ * section 3; LayerSkip guide, "Verification Phase": the early-exit draft and the full model share
+ * one LM head). The logits of every row are z = h W^T with the head W [V][d] (bf16, row stride
+ * weight_stride), for the target hidden states [B][K+1] rows (bf16, target_row_stride elements
+ * apart) and the draft hidden states [B][K] rows (draft_row_stride apart; unused and may be NULL
+ * in greedy mode). The outcome is the one spec_verify gives for those logits (beta = 1, no bias
+ * set, no top-F ids): out_accept_len [B] and out_tokens [B][K+1], the same layout, validity
+ * rules and uniforms. Only the rows each sequence has are scored (target 0..L_b, draft
+ * 0..L_b-1); each row is reduced on the tensor cores to its maximum, softmax sum, logit at the
+ * draft id and argmax, and the two rows of the decided position are scored again for the draw,
+ * so no row of logits is written to memory. Logits are accumulated in fp32 from bf16 products.
+ * d must be a multiple of 64, K <= 8, V <= 2^24; hidden states and head 16-byte aligned, with
+ * row strides that are multiples of 8 elements. Asynchronous on `stream`, on the stream's
+ * workspace (grown on demand: about B (2K+1) d 2 bytes for the packed rows plus 16 bytes per
+ * sequence and 16 ids for the residual masses); device-side failures are read with
+ * spec_verify_device_error.
+ */
+sv_status spec_verify_hidden(int B, int K, int V, int d, const void* hidden_target,
+                             long long target_row_stride, const void* hidden_draft,
+                             long long draft_row_stride, const void* weight,
+                             long long weight_stride, const int32_t* draft_tokens,
+                             const int32_t* draft_lens, const float* uniforms, float temperature,
+                             int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                             void* stream);
 
 /* A static, human-readable name for a status code. */
 const char* spec_verify_status_string(sv_status status);

@@ -9,21 +9,30 @@ shares no code with that path.
   for bf16 ``h`` [R, d] and ``W`` [V, d], every product and sum taken in float64 (a bf16 x bf16
   product is exact there; the sum of ``d`` such terms carries one float64 rounding each).
 * Statistics of the temperature softmax ``p = softmax(z / T)`` that the verify step needs per
-  row (speculative sampling page, "Algorithm": the accept ratio ``p(x) / q(x)``): the largest
-  logit ``max_v z_v``, the natural log-sum-exp ``ln sum_v exp(z_v / T)`` (so that
-  ``ln p(x) = z_x / T - lse``), and the logit ``z_x`` of a requested id (NaN for an id outside
-  ``[0, V)``). The log-sum-exp is taken about the maximum, ``M / T + ln sum exp((z - M) / T)``.
+  row (Kangaroo guide, section 3, and glossary, "Why It Produces Identical Outputs": the accept
+  ratio ``p(x) / q(x)``): the largest logit ``max_v z_v``, the natural log-sum-exp
+  ``ln sum_v exp(z_v / T)`` (so that ``ln p(x) = z_x / T - lse``), and the logit ``z_x`` of a
+  requested id (NaN for an id outside ``[0, V)``). The log-sum-exp is taken about the maximum,
+  ``M / T + ln sum exp((z - M) / T)``.
+
+* The verify step from hidden states (Kangaroo guide, section 3, with the logits of "Exit 1";
+  LayerSkip guide, "Verification Phase": the early-exit draft and the full model share the
+  head): the logits of each sequence's rows are ``h W^T`` as above, and the outcome is the one
+  ``oracle.verify.verify_sequence`` gives for those float64 rows.
 
 Parity pins: ``tests/test_oracle_lmhead_pins.py`` (one-hot heads, closed-form sums, shift and
-scale laws, brute-force products on tiny inputs).
+scale laws, brute-force products on tiny inputs, and an identity head under which the verify
+step from hidden states is the verify step of the hidden states read as logits).
 """
 from __future__ import annotations
 
 import math
 from dataclasses import dataclass
-from typing import Optional
+from typing import Optional, Sequence
 
 import numpy as np
+
+from . import verify as _v
 
 
 def bf16_to_f64(bits) -> np.ndarray:
@@ -78,3 +87,26 @@ def logit_error_bound(hidden, weight) -> np.ndarray:
     w = np.abs(bf16_to_f64(weight))
     d = h.shape[-1]
     return (d * 2.0 ** -23 * 1.01) * (h @ w.T)
+
+
+def verify_hidden_batch(hidden_target, hidden_draft, weight, draft_tokens, draft_lens, uniforms,
+                        *, temperature: float, mode: str,
+                        seqs: Optional[Sequence[int]] = None):
+    """The verify step on logits computed from hidden states: ``hidden_target`` [B, K+1, d],
+    ``hidden_draft`` [B, K, d] (None in greedy mode) and ``weight`` [V, d], bf16 bits or floats.
+    Only rows 0..L_b (target) and 0..L_b-1 (draft) are scored; the others are NaN rows the verify
+    step never reads. Returns a list of ``oracle.verify.SeqResult``."""
+    B, K = np.asarray(draft_tokens).shape
+    V = np.asarray(weight).shape[0]
+    out = []
+    for b in (range(B) if seqs is None else seqs):
+        L = int(draft_lens[b])
+        zt = np.full((K + 1, V), np.nan)
+        zd = np.full((K, V), np.nan) if hidden_draft is not None else None
+        if 1 <= L <= K:
+            zt[:L + 1] = head_logits(np.asarray(hidden_target)[b, :L + 1], weight)
+            if zd is not None:
+                zd[:L] = head_logits(np.asarray(hidden_draft)[b, :L], weight)
+        out.append(_v.verify_sequence(zt, zd, draft_tokens[b], L, uniforms[b],
+                                      temperature=temperature, mode=mode))
+    return out

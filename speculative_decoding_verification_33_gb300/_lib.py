@@ -19,7 +19,7 @@ SV_MODE_GREEDY, SV_MODE_STOCHASTIC = 0, 1
 EXPORTS = ("spec_verify", "spec_verify_workspace_bytes", "spec_verify_ws", "spec_verify_debug",
            "spec_verify_host", "spec_verify_device_error", "spec_verify_status_string",
            "spec_verify_plan", "spec_verify_noalloc", "spec_draft_sample", "spec_residual_topf",
-           "spec_lmhead_stats", "sv_hbm_read_probe")
+           "spec_lmhead_stats", "spec_verify_hidden", "sv_hbm_read_probe")
 
 
 class SvProblem(ctypes.Structure):
@@ -70,7 +70,10 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                           _F, _P, _P, _P, _P]
         lib.spec_residual_topf.argtypes = [_PROB, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P, _P]
         lib.spec_lmhead_stats.argtypes = [_I, _I, _I, _P, ctypes.c_longlong, _P, ctypes.c_longlong,
-                                          _F, _P, _P, _P, _P, _P, _P]
+                                          _F, _P, _P, _P, _P, _P, _P, _P]
+        _LL = ctypes.c_longlong
+        lib.spec_verify_hidden.argtypes = [_I, _I, _I, _I, _P, _LL, _P, _LL, _P, _LL, _P, _P, _P,
+                                           _F, _I, _P, _P, _P]
         for name in EXPORTS:
             if name not in ("spec_verify_workspace_bytes", "spec_verify_status_string"):
                 getattr(lib, name).restype = _I

@@ -201,8 +201,9 @@ def lmhead_stats(hidden: torch.Tensor, weight: torch.Tensor, ids: Optional[torch
                  *, temperature: float = 1.0, logits: bool = False, stream=None):
     """Row statistics of hidden @ weight.T on the tensor cores, without writing the logits (see
     ``spec_lmhead_stats`` in include/spec_verify.h). ``hidden`` [R, d] and ``weight`` [V, d] are
-    bf16 CUDA tensors with contiguous rows; ``ids`` [R] int32. Returns {"max", "lse"[, "zx"]
-    [, "logits"]} (fp32); ``logits=True`` also writes the [R, V] logits (tests)."""
+    bf16 CUDA tensors with contiguous rows; ``ids`` [R] int32. Returns {"max", "lse", "argmax"
+    [, "zx"][, "logits"]} (fp32; argmax int32); ``logits=True`` also writes the [R, V] logits
+    (tests)."""
     for t, n in ((hidden, "hidden"), (weight, "weight")):
         if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1:
             raise ValueError(f"{n} must be a 2-D bf16 tensor with contiguous rows")
@@ -215,14 +216,61 @@ def lmhead_stats(hidden: torch.Tensor, weight: torch.Tensor, ids: Optional[torch
            "lse": torch.empty(R, dtype=torch.float32, device=dev)}
     if ids is not None:
         out["zx"] = torch.empty(R, dtype=torch.float32, device=dev)
+    out["argmax"] = torch.empty(R, dtype=torch.int32, device=dev)
     if logits:
         out["logits"] = torch.empty(R, V, dtype=torch.float32, device=dev)
     st = _lib.load().spec_lmhead_stats(
         int(R), int(d), int(V), _ptr(hidden, "hidden"), int(hidden.stride(0) if R > 1 else d),
         _ptr(weight, "weight"), int(weight.stride(0) if V > 1 else d), float(temperature),
         _ptr(ids, "ids", torch.int32), _ptr(out["max"], "max"), _ptr(out["lse"], "lse"),
-        _ptr(out.get("zx"), "zx"), _ptr(out.get("logits"), "logits"), _stream_handle(stream))
+        _ptr(out.get("zx"), "zx"), _ptr(out["argmax"], "argmax"), _ptr(out.get("logits"), "logits"),
+        _stream_handle(stream))
     _lib._check(st, "spec_lmhead_stats")
+    return out
+
+
+def verify_hidden(hidden_target: torch.Tensor, hidden_draft: Optional[torch.Tensor],
+                  weight: torch.Tensor, draft_tokens: torch.Tensor,
+                  draft_lens: Optional[torch.Tensor] = None,
+                  uniforms: Optional[torch.Tensor] = None, *, temperature: float = 1.0,
+                  mode="stochastic", stream=None, out=None):
+    """The verify step from hidden states (``spec_verify_hidden`` in include/spec_verify.h).
+
+    ``hidden_target`` [B, K+1, d] and ``hidden_draft`` [B, K, d] (None in greedy mode) are bf16
+    CUDA tensors whose rows are contiguous (any row stride that is a multiple of 8 elements, the
+    same between positions and sequences); ``weight`` [V, d] bf16. Returns
+    {"accept_len" [B], "tokens" [B, K+1]} (int32)."""
+    B, K = draft_tokens.shape
+    d = hidden_target.shape[-1]
+    V = weight.shape[0]
+    m = _MODES[mode]
+
+    def stride(t, rows, name):
+        if t.dtype != torch.bfloat16 or t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError(f"{name} must be a bf16 [B, rows, d] tensor with contiguous rows")
+        if t.shape[0] != B or t.shape[1] != rows or t.shape[2] != d:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {(B, rows, d)}")
+        s1 = t.stride(1) if rows > 1 else d
+        if B > 1 and t.stride(0) != rows * s1:
+            raise ValueError(f"{name}: rows must be evenly spaced across sequences")
+        return s1
+    ts = stride(hidden_target, K + 1, "hidden_target")
+    ds = stride(hidden_draft, K, "hidden_draft") if hidden_draft is not None else d
+    if weight.dtype != torch.bfloat16 or weight.dim() != 2 or weight.stride(1) != 1 or \
+            weight.shape[1] != d:
+        raise ValueError("weight must be a bf16 [V, d] tensor with contiguous rows")
+    dev = hidden_target.device
+    if out is None:
+        out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+               "tokens": torch.empty(B, K + 1, dtype=torch.int32, device=dev)}
+    st = _lib.load().spec_verify_hidden(
+        int(B), int(K), int(V), int(d), _ptr(hidden_target, "hidden_target"), int(ts),
+        _ptr(hidden_draft, "hidden_draft"), int(ds), _ptr(weight, "weight"),
+        int(weight.stride(0) if V > 1 else d), _ptr(draft_tokens, "draft_tokens", torch.int32),
+        _ptr(draft_lens, "draft_lens", torch.int32), _ptr(uniforms, "uniforms", torch.float32),
+        float(temperature), m, _ptr(out["accept_len"], "accept_len", torch.int32),
+        _ptr(out["tokens"], "tokens", torch.int32), _stream_handle(stream))
+    _lib._check(st, "spec_verify_hidden")
     return out
 
 

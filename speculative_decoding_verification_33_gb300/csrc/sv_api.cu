@@ -17,6 +17,7 @@
 #include "sv_internal.h"
 #include "sv_rows.h"
 #include "sv_lmhead.h"
+#include "sv_hverify.h"
 #include "sv_probe.h"
 
 namespace {
@@ -676,7 +677,7 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
 sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long long hidden_stride,
                             const void* weight, long long weight_stride, float temperature,
                             const int32_t* ids, float* out_max, float* out_lse, float* out_zx,
-                            float* out_logits, void* stream) {
+                            int32_t* out_argmax, float* out_logits, void* stream) {
   if (rows < 0 || d < 64 || d % 64 != 0 || V < 1 || V > (1 << 24)) return SV_ERR_INVALID_ARG;
   if (hidden_stride < d || weight_stride < d || (hidden_stride * 2) % 16 != 0 ||
       (weight_stride * 2) % 16 != 0)
@@ -706,10 +707,66 @@ sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long lon
   sv_status st = SV_OK;
   StreamRes* r = resources(dev, s, sizeof(Workspace) + sv::head_part_bytes(rows, P.nsplit), &st);
   if (!r) return st;
-  P.part = reinterpret_cast<float*>(r->ws + 1);
+  P.part = reinterpret_cast<float4*>(r->ws + 1);
   P.err = &r->ws->error;
-  const cudaError_t e = sv::launch_lmhead(hidden, hidden_stride, weight, weight_stride, P, out_max,
-                                          out_lse, out_zx, s);
+  cudaError_t e = sv::launch_head_gemm(sv::HEAD_STATS, hidden, hidden_stride, weight,
+                                       weight_stride, P, sv::head_ctas(sms), s);
+  if (e == cudaSuccess)
+    e = sv::launch_head_combine(P, out_max, out_lse, out_zx, out_argmax, nullptr, s);
+  if (e == cudaErrorNotSupported) return SV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_verify_hidden(int B, int K, int V, int d, const void* hidden_target,
+                             long long target_row_stride, const void* hidden_draft,
+                             long long draft_row_stride, const void* weight,
+                             long long weight_stride, const int32_t* draft_tokens,
+                             const int32_t* draft_lens, const float* uniforms, float temperature,
+                             int mode, int32_t* out_accept_len, int32_t* out_tokens,
+                             void* stream) {
+  if (B < 0 || K < 1 || K > 8 || V < 1 || V > (1 << 24) || d < 64 || d % 64 != 0)
+    return SV_ERR_INVALID_ARG;
+  if (mode != SV_MODE_GREEDY && mode != SV_MODE_STOCHASTIC) return SV_ERR_INVALID_ARG;
+  const bool greedy = mode == SV_MODE_GREEDY;
+  if (!greedy && !finite_in(temperature, 1e-4f, 1e4f)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!hidden_target || !weight || !draft_tokens || !draft_lens || !out_accept_len ||
+      !out_tokens)
+    return SV_ERR_INVALID_ARG;
+  if (!greedy && (!hidden_draft || !uniforms)) return SV_ERR_INVALID_ARG;
+  if (target_row_stride < d || weight_stride < d || (!greedy && draft_row_stride < d))
+    return SV_ERR_INVALID_ARG;
+  if (!aligned16(hidden_target, target_row_stride, 2) || !aligned16(weight, weight_stride, 2) ||
+      (!greedy && !aligned16(hidden_draft, draft_row_stride, 2)))
+    return SV_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int sms = sm_count(dev);
+  if (sms <= 0) return SV_ERR_CUDA;
+  sv::HvProblem p;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.d = d;
+  p.greedy = greedy ? 1 : 0;
+  p.ht = static_cast<const uint16_t*>(hidden_target);
+  p.hts = target_row_stride;
+  p.hd = greedy ? nullptr : static_cast<const uint16_t*>(hidden_draft);
+  p.hds = greedy ? d : draft_row_stride;
+  p.W = static_cast<const uint16_t*>(weight);
+  p.ws = weight_stride;
+  p.x = draft_tokens;
+  p.lens = draft_lens;
+  p.uni = greedy ? nullptr : uniforms;
+  p.temperature = greedy ? 1.f : temperature;
+  p.out_acc = out_accept_len;
+  p.out_tok = out_tokens;
+  sv_status st = SV_OK;
+  StreamRes* r = resources(dev, s, sizeof(Workspace) + sv::hv_workspace_bytes(p, sms), &st);
+  if (!r) return st;
+  const cudaError_t e = sv::hv_run(p, sms, r->ws + 1, &r->ws->error, s);
   if (e == cudaErrorNotSupported) return SV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

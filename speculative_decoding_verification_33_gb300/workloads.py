@@ -278,3 +278,108 @@ def small_head(R: int, d: int, V: int, temperature: float = 1.0, zipf: bool = Tr
     """A head workload of the same recipe at other sizes (tests)."""
     return HeadWorkload(f"head_R{R}_d{d}_V{V}", R=R, d=d, V=V, temperature=temperature,
                         sigma=sigma, zipf=zipf)
+
+
+# ---------------------------------------------------------------------------------------------
+# verify-from-hidden-states inputs
+# ---------------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class HiddenWorkload:
+    """Hidden states of the target and early-exit draft rows of B sequences and an LM head."""
+
+    name: str
+    B: int
+    K: int
+    V: int
+    d: int
+    mode: str = "stochastic"
+    temperature: float = 1.0
+    ragged: bool = True
+    sigma: float = 2.0        # standard deviation of a logit's noise part
+    sigma_d: float = 0.25     # draft hidden state = target's + N(0, sigma_d^2) per unit
+    exact: bool = False       # values on dyadic grids: every logit is exact in float32
+    drafter: str = "head"     # "head": x ~ the draft head's softmax; "prior": x ~ softmax(prior/T)
+
+
+HIDDEN_WORKLOADS = {
+    "hv_B256_K8_V152064_d3584": HiddenWorkload("hv_B256_K8_V152064_d3584", B=256, K=8,
+                                               V=152064, d=3584, drafter="prior"),
+}
+
+
+def _grid(x: np.ndarray, step: float, lim: int) -> np.ndarray:
+    """x rounded to a multiple of `step` with at most `lim` steps either way."""
+    return (np.clip(np.rint(x / step), -lim, lim) * step).astype(np.float32)
+
+
+def hidden_inputs(w: HiddenWorkload, offset: int = 0) -> dict:
+    """Seeded hidden states, head, draft ids, lengths and uniforms for ``w``.
+
+    Recipe: head rows ``W[v, j] ~ N(0, sigma^2 / (d - 1))`` for ``j < d - 1`` and ``W[v, d-1]`` the
+    Zipf(1.1) log-prior; target hidden states ``h ~ N(0, 1)`` with ``h[d-1] = 1``; draft hidden
+    states ``h + N(0, sigma_d^2)`` (last unit 1), so the draft logits are the target's plus noise.
+    With ``exact`` every value sits on a dyadic grid (h on 1/8 within +-31/8, W on 1/256 within
+    +-127/256, the prior on 1/16) so that any float32 sum of d <= 1024 products is exact. All are
+    rounded to bf16. Rows past a sequence's draft length are NaN (never to be read). Draft ids:
+    with ``drafter="head"`` the drafter scores its rows with the head in float32 and samples by
+    the Gumbel-max rule at temperature T (greedy: argmax); with ``"prior"`` it samples from
+    softmax(prior / T) alone (cheap at full size). Lengths: all K, or uniform on 1..K when
+    ragged; uniforms as ``uniforms``. Seeds: ``default_rng([tag, B, K, V, d, offset])`` with tags
+    900 (head), 901 (hidden), 902 (draft noise), 903 (drafting), 904 (prior), 905 (lengths).
+    """
+    B, K, V, d = w.B, w.K, w.V, w.d
+    key = [B, K, V, d, offset]
+    perm = np.random.default_rng([904] + key).permutation(V)
+    prior = (-1.1 * np.log1p(perm.astype(np.float64))).astype(np.float32)
+    if w.exact:
+        prior = _grid(prior, 1.0 / 16, 255)
+    weight = np.empty((V, d), dtype=np.uint16)
+    scale = np.float32(w.sigma / np.sqrt(max(1, d - 1)))
+    step = 4096
+
+    def fill(v0: int) -> None:
+        rng = np.random.default_rng([900] + key + [v0])
+        blk = rng.standard_normal((min(step, V - v0), d), dtype=np.float32) * scale
+        if w.exact:
+            blk = _grid(blk, 1.0 / 256, 127)
+        blk[:, d - 1] = prior[v0:v0 + blk.shape[0]]
+        weight[v0:v0 + blk.shape[0]] = f32_to_bf16_bits(blk)
+
+    threads = min(16, len(os.sched_getaffinity(0)))
+    with ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+        list(ex.map(fill, range(0, V, step)))
+    if w.ragged:
+        lens = np.random.default_rng([905] + key).integers(1, K + 1, size=B).astype(np.int32)
+    else:
+        lens = np.full(B, K, dtype=np.int32)
+    h = np.random.default_rng([901] + key).standard_normal((B, K + 1, d), dtype=np.float32)
+    hd = h[:, :K] + np.float32(w.sigma_d) * np.random.default_rng([902] + key).standard_normal(
+        (B, K, d), dtype=np.float32)
+    if w.exact:
+        h, hd = _grid(h, 1.0 / 8, 31), _grid(hd, 1.0 / 8, 31)
+    h[..., d - 1] = 1.0
+    hd[..., d - 1] = 1.0
+    ht_bits, hd_bits = f32_to_bf16_bits(h), f32_to_bf16_bits(hd)
+    del h
+    rng_x = np.random.default_rng([903] + key)
+    tok = np.zeros((B, K), dtype=np.int32)
+    Wf = bf16_bits_to_f32(weight) if w.drafter == "head" else None
+    T = w.temperature if w.mode == "stochastic" else 1.0
+    for b in range(B):
+        L = int(lens[b])
+        if w.drafter == "head":
+            zd = bf16_bits_to_f32(hd_bits[b, :L]) @ Wf.T
+        else:
+            zd = np.broadcast_to(prior, (L, V))
+        for i in range(L):
+            z = zd[i].astype(np.float64)
+            if w.mode == "greedy":
+                tok[b, i] = int(np.argmax(z))
+            else:
+                tok[b, i] = int(np.argmax(z / T + rng_x.gumbel(size=V)))
+        ht_bits[b, L + 1:] = BF16_NAN
+        hd_bits[b, L:] = BF16_NAN
+    uni = np.random.default_rng(0 if offset == 0 else [0, offset]).random((B, K + 1),
+                                                                           dtype=np.float32)
+    return {"workload": w, "hidden_target": ht_bits, "hidden_draft": hd_bits, "weight": weight,
+            "draft_tokens": tok, "draft_lens": lens, "uniforms": uni}

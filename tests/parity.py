@@ -43,8 +43,10 @@ def _close(a: float, b: float) -> bool:
         abs(a - b) <= REL_TOL * abs(b) + 1e-30
 
 
-def compare(results, seqs, gpu_acc, gpu_tok, gpu_topf=None, dbg=None, x=None) -> Report:
-    """results: oracle SeqResults for sequences ``seqs``; gpu_*: numpy arrays over all B."""
+def compare(results, seqs, gpu_acc, gpu_tok, gpu_topf=None, dbg=None, x=None,
+            margin: float = O.MARGIN) -> Report:
+    """results: oracle SeqResults for sequences ``seqs``; gpu_*: numpy arrays over all B.
+    ``margin``: decisions closer than this are flagged (1e-6 unless the inputs call for more)."""
     rep = Report()
     for r, b in zip(results, seqs):
         rep.sequences += 1
@@ -54,7 +56,7 @@ def compare(results, seqs, gpu_acc, gpu_tok, gpu_topf=None, dbg=None, x=None) ->
             if ga != -1 or (gt != -1).any():
                 rep.mismatches.append((b, "invalid", r.accept_len, ga))
             continue
-        j = r.first_flag()
+        j = r.first_flag(margin)
         if j is None:
             if ga != r.accept_len or not np.array_equal(gt, r.tokens):
                 rep.mismatches.append((b, "tokens", r.accept_len, ga, r.tokens.tolist(),

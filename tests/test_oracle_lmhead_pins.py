@@ -84,7 +84,7 @@ def test_fraction_exact_sum_on_bf16_values():
 
 
 # ----------------------------------------------------------------------------------------------
-# softmax statistics (speculative sampling page, "Algorithm")
+# softmax statistics (Kangaroo guide, section 3: the accept ratio p(x) / q(x))
 # ----------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("T", [1.0, 0.8, 2.5])
 def test_lse_closed_forms(T):
@@ -162,3 +162,36 @@ def test_error_bound_covers_float32_summation_orders():
                 pw = (pw[0::2] + pw[1::2]).astype(np.float32)
             assert abs(float(pw[0]) - z[r, v]) <= bound[r, v]
     assert np.all(bound > 0)
+
+
+# ----------------------------------------------------------------------------------------------
+# the verify step from hidden states (Kangaroo guide, section 3)
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", ["stochastic", "greedy"])
+def test_identity_head_reduces_to_the_verify_step(mode):
+    """With W = I (V = d) the logits are the hidden states, so the outcome must be the verify
+    step's on those rows read as logits (a transposed or shifted head, or rows scored at the
+    wrong position, would change it)."""
+    from oracle import verify as O
+    rng = np.random.default_rng(9)
+    B, K, d = 6, 3, 7
+    ht = rng.normal(0.0, 1.5, size=(B, K + 1, d))
+    hd = ht[:, :K] + rng.normal(0.0, 0.6, size=(B, K, d))
+    W = np.eye(d)
+    lens = np.array([3, 1, 2, 3, 2, 1], np.int32)
+    x = rng.integers(0, d, size=(B, K)).astype(np.int32)
+    if mode == "greedy":
+        x[:, 0] = ht[:, 0].argmax(axis=1)  # so that some drafts are accepted
+    u = rng.random((B, K + 1)).astype(np.float32)
+    got = H.verify_hidden_batch(ht, hd if mode == "stochastic" else None, W, x, lens, u,
+                                temperature=0.9, mode=mode)
+    tgt = np.where(np.arange(K + 1)[None, :, None] <= lens[:, None, None], ht, np.nan)
+    dft = np.where(np.arange(K)[None, :, None] < lens[:, None, None], hd, np.nan)
+    want = O.verify_batch(tgt, dft if mode == "stochastic" else None, x, lens, u,
+                          temperature=0.9, mode=mode)
+    accepted = 0
+    for g, w in zip(got, want):
+        assert g.accept_len == w.accept_len
+        assert np.array_equal(g.tokens, w.tokens)
+        accepted += g.accept_len
+    assert accepted > 0

@@ -109,24 +109,20 @@ __global__ void __launch_bounds__(kScanThreads) hv_scan(int B, int K, int greedy
   }
 }
 
-// Pack the rows of sequence blockIdx.x: target 0..L, then (stochastic) draft 0..L-1, each with
-// the id it is scored at (x_i; -1 for target row L).
+// Pack row blockIdx.y of sequence blockIdx.x (target 0..L, then, stochastic, draft 0..L-1) with
+// the id it is scored at (x_i; -1 for target row L). Row slots past the sequence's rows idle.
 __global__ void __launch_bounds__(128) hv_gather(const HvProblem p, const int* off, uint16_t* A,
                                                  int32_t* ids) {
-  const int b = blockIdx.x;
+  const int b = blockIdx.x, r = blockIdx.y;
   const int L = p.lens[b];
-  const int n = rows_of(L, p.K, p.greedy);
-  if (n == 0) return;
+  if (r >= rows_of(L, p.K, p.greedy)) return;
   const int o = off[b];
-  const int nvec = p.d / 8;
-  for (int idx = threadIdx.x; idx < n * nvec; idx += blockDim.x) {
-    const int r = idx / nvec, v = idx - (idx / nvec) * nvec;
-    const uint16_t* src = r <= L ? p.ht + (static_cast<long long>(b) * (p.K + 1) + r) * p.hts
-                                 : p.hd + (static_cast<long long>(b) * p.K + (r - L - 1)) * p.hds;
-    reinterpret_cast<uint4*>(A + static_cast<long long>(o + r) * p.d)[v] =
-        reinterpret_cast<const uint4*>(src)[v];
-  }
-  for (int r = threadIdx.x; r < n; r += blockDim.x) {
+  const uint16_t* src = r <= L ? p.ht + (static_cast<long long>(b) * (p.K + 1) + r) * p.hts
+                               : p.hd + (static_cast<long long>(b) * p.K + (r - L - 1)) * p.hds;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(A + static_cast<long long>(o + r) * p.d);
+  for (int v = threadIdx.x; v < p.d / 8; v += blockDim.x) d4[v] = s4[v];
+  if (threadIdx.x == 0) {
     const int i = r <= L ? r : r - L - 1;
     ids[o + r] = (r <= L && i == L) ? -1 : p.x[static_cast<long long>(b) * p.K + i];
   }
@@ -382,7 +378,7 @@ cudaError_t hv_run(const HvProblem& p, int sms, void* ws, unsigned int* err, cud
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(p.temperature));
 
   hv_scan<<<1, kScanThreads, 0, stream>>>(p.B, p.K, p.greedy, p.lens, off, count);
-  hv_gather<<<p.B, 128, 0, stream>>>(p, off, A, ids);
+  hv_gather<<<dim3(p.B, 2 * p.K + 1), 128, 0, stream>>>(p, off, A, ids);
   HeadParams P;
   memset(&P, 0, sizeof(P));
   P.R = L.Rmax;

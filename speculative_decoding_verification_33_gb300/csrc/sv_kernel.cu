@@ -707,16 +707,27 @@ __device__ __forceinline__ float weights8(const float (&zt)[8], const float (&zd
   return s;
 }
 
+// Sum of a u64 over the 8 lanes of an aligned group of 8 (every lane gets the sum).
+__device__ __forceinline__ unsigned long long group8_sum_u64(unsigned long long v) {
+  v += __shfl_xor_sync(FULL, v, 1);
+  v += __shfl_xor_sync(FULL, v, 2);
+  v += __shfl_xor_sync(FULL, v, 4);
+  return v;
+}
+
 // The cluster draws the token at position `a` of sequence `seq`. The rows come back through
 // the ring (the producer fetches them again right after the decision; they are still in L2);
-// each consumer keeps one mass per 8-element vector in `vmass`. The CTA whose range holds the
-// draw writes out_tok. All consumers of all CTAs of the cluster call this together.
+// every 8-element vector's mass is truncated to 2^-44 units, and `gmass` keeps the sum of those
+// units per group of 8 vectors (64 elements), so shared memory holds 8 bytes per 64 elements.
+// The CTA whose range holds the draw finds the group by a prefix over `gmass`, recomputes the
+// group's 8 vector masses and walks them, then the vector's elements, and writes out_tok. All
+// consumers of all CTAs of the cluster call this together.
 template <typename T, bool GREEDY, bool BONUS>
 __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
                            uint64_t* xbar, uint32_t& xround, uint32_t rank, uint32_t C,
-                           const Ring<T, GREEDY>& R, int seq, int a, float* vmass, Cursor& cons,
-                           bool& late) {
-  const int tid = threadIdx.x;
+                           const Ring<T, GREEDY>& R, int seq, int a,
+                           unsigned long long* gmass, Cursor& cons, bool& late) {
+  const int tid = threadIdx.x, lane = tid & 31;
   const int v0 = R.v0, nv = R.nv;
   const int nvec_all = (nv + 7) >> 3;
   const bool aligned = P.use_bulk != 0;
@@ -750,21 +761,26 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
     const int n = R.chunk_len(k), nvec = (n + 7) >> 3;
     const T* rt = R.row(s, 0);
     const T* rd = R.row(s, GREEDY ? 0 : 1);
-    auto vec = [&](int g) {
-      float zt[8], zd[8], w[8];
-      Elt<T>::load8(rt, g, zt);
-      if (!BONUS) Elt<T>::load8(rd, g, zd);
-      const int e0 = k * R.CH + 8 * g;
-      const float sm = weights8<BONUS>(zt, BONUS ? zt : zd, e0, W, w);
-      vmass[e0 >> 3] = sm;
-      acc += qfix(sm);
+    // vector g of the chunk (lanes 8j .. 8j + 7 hold the 8 vectors of one group, since NC and
+    // the chunk are multiples of 64 elements); every lane of the warp takes part
+    auto vec = [&](int g, bool have) {
+      unsigned long long q = 0;
+      if (have) {
+        float zt[8], zd[8], w[8];
+        Elt<T>::load8(rt, g, zt);
+        if (!BONUS) Elt<T>::load8(rd, g, zd);
+        q = qfix(weights8<BONUS>(zt, BONUS ? zt : zd, k * R.CH + 8 * g, W, w));
+      }
+      acc += q;
+      const unsigned long long gq = group8_sum_u64(q);
+      if ((lane & 7) == 0 && have) gmass[(k * (R.CH / 8) + g) >> 3] = gq;
     };
     constexpr int VPT = Ring<T, GREEDY>::CH / 8 / NC;
     if (n == R.CH) {  // a whole chunk: exactly VPT vectors per thread
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) vec(tid + j * NC);
+      for (int j = 0; j < VPT; ++j) vec(tid + j * NC, true);
     } else {
-      for (int g = tid; g < nvec; g += NC) vec(g);
+      for (int j = 0; j * NC < nvec; ++j) vec(tid + j * NC, tid + j * NC < nvec);
     }
     release_stage(R.empty, cons);
   }
@@ -776,12 +792,18 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
       W.rho_S = 0.f;
       W.mc_d = INFINITY;  // the draft term becomes 2^-inf = 0 exactly
       acc = 0;
-      for (int g = tid; g < nvec_all; g += NC) {
-        float zt[8], w[8];
-        row8<T>(gt, 8 * g, nv, aligned, zt);
-        const float sm = weights8<BONUS>(zt, zt, 8 * g, W, w);
-        vmass[g] = sm;
-        acc += qfix(sm);
+      for (int j = 0; j * NC < nvec_all; ++j) {
+        const int g = tid + j * NC;
+        const bool have = g < nvec_all;
+        unsigned long long q = 0;
+        if (have) {
+          float zt[8], w[8];
+          row8<T>(gt, 8 * g, nv, aligned, zt);
+          q = qfix(weights8<BONUS>(zt, zt, 8 * g, W, w));
+        }
+        acc += q;
+        const unsigned long long gq = group8_sum_u64(q);
+        if ((lane & 7) == 0 && have) gmass[g >> 3] = gq;
       }
     }
     const unsigned long long Wc = block_sum_u64(acc, S);
@@ -812,25 +834,30 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
     if (late || Wtot > 0 || BONUS) break;
   }
   if (!late && S.cstar == static_cast<int>(rank)) {
-    // contiguous runs of vectors per thread, so the prefix follows ascending ids
-    const int lo = static_cast<int>((static_cast<long long>(tid) * nvec_all) / NC);
-    const int hi = static_cast<int>((static_cast<long long>(tid + 1) * nvec_all) / NC);
+    // contiguous runs of groups per thread, so the prefix follows ascending ids
+    const int ngroup = (nvec_all + 7) >> 3;
+    const int lo = static_cast<int>((static_cast<long long>(tid) * ngroup) / NC);
+    const int hi = static_cast<int>((static_cast<long long>(tid + 1) * ngroup) / NC);
     unsigned long long csum = 0;
-    for (int g = lo; g < hi; ++g) csum += qfix(vmass[g]);
+    for (int gr = lo; gr < hi; ++gr) csum += gmass[gr];
     unsigned long long pre = block_exclusive_u64(csum, S);
     const unsigned long long tl = S.t_loc;
     if (pre <= tl && tl < pre + csum) {
-      for (int g = lo; g < hi; ++g) {
-        const unsigned long long q = qfix(vmass[g]);
-        if (pre + q > tl) {
-          float zt[8], zd[8], w[8];
-          row8<T>(gt, 8 * g, nv, aligned, zt);
-          if (!BONUS && W.rho != 0.f) row8<T>(gd, 8 * g, nv, aligned, zd);
-          else {
+      int gr = lo;
+      while (gr < hi - 1 && pre + gmass[gr] <= tl) pre += gmass[gr++];
+      // the group's vectors again, with the arithmetic and truncation of the stream above
+      int g = gr * 8;
+      const int gend = min(g + 8, nvec_all);
+      for (; g < gend; ++g) {
+        float zt[8], zd[8], w[8];
+        row8<T>(gt, 8 * g, nv, aligned, zt);
+        if (!BONUS && W.rho != 0.f) row8<T>(gd, 8 * g, nv, aligned, zd);
+        else {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) zd[kk] = zt[kk];
-          }
-          weights8<BONUS>(zt, zd, 8 * g, W, w);
+          for (int kk = 0; kk < 8; ++kk) zd[kk] = zt[kk];
+        }
+        const unsigned long long q = qfix(weights8<BONUS>(zt, zd, 8 * g, W, w));
+        if (pre + q > tl || g == gend - 1) {
           float s = 0.f;
           int pick = 7;
 #pragma unroll
@@ -1155,7 +1182,8 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
   R.v0 = static_cast<int>(rank) * P.slice;
   R.nv = max(0, min(P.V - R.v0, P.slice));
   R.nchunk = (R.nv + RingT::CH - 1) / RingT::CH;
-  float* vmass = reinterpret_cast<float*>(dyn + static_cast<size_t>(NS) * RingT::kRows * kStageRowBytes);
+  unsigned long long* gmass = reinterpret_cast<unsigned long long*>(
+      dyn + static_cast<size_t>(NS) * RingT::kRows * kStageRowBytes);
   const float c = P.c;
 
   if (tid == 0) {
@@ -1333,9 +1361,9 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           a = outcome;
           if (!GREEDY) {
             if (a < L)
-              draw_token<T, GREEDY, false>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+              draw_token<T, GREEDY, false>(P, S, X, xbar, xround, rank, C, R, seq, a, gmass, cons, late);
             else
-              draw_token<T, GREEDY, true>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+              draw_token<T, GREEDY, true>(P, S, X, xbar, xround, rank, C, R, seq, a, gmass, cons, late);
             if (late) aborted = true;
           }
         }
@@ -1519,9 +1547,9 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           if (invalid) break;
           if (!GREEDY && stop >= 0) {
             if (stop < L)
-              draw_token<T, GREEDY, false>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+              draw_token<T, GREEDY, false>(P, S, X, xbar, xround, rank, C, R, seq, a, gmass, cons, late);
             else
-              draw_token<T, GREEDY, true>(P, S, X, xbar, xround, rank, C, R, seq, a, vmass, cons, late);
+              draw_token<T, GREEDY, true>(P, S, X, xbar, xround, rank, C, R, seq, a, gmass, cons, late);
             if (late) {
               aborted = true;
               break;
@@ -1633,8 +1661,8 @@ cudaError_t prepare(const void* fn, int cluster, size_t smem) {
 size_t smem_bytes(int dtype, int greedy, int slice) {
   (void)dtype;
   const size_t ring = static_cast<size_t>(NS) * (greedy ? 1 : 2) * kStageRowBytes;
-  const size_t vmass = greedy ? 0 : (static_cast<size_t>(slice) / 8 * 4 + 127) / 128 * 128;
-  return ring + vmass;
+  const size_t gmass = greedy ? 0 : (static_cast<size_t>(slice + 63) / 64 * 8 + 127) / 128 * 128;
+  return ring + gmass;
 }
 
 int max_active_clusters(int dtype, int greedy, int top8, int cluster, size_t smem) {

@@ -140,6 +140,8 @@ struct CtaState {
   int dec;           // decision of the last combined position: -1 accept, a >= 0 stop at a,
                      // -2 unusable row, -3 a wait gave up (written by consumer warp 0)
   int next;          // the sequence this cluster takes next (from the first exchange)
+  unsigned long long nxt_word;  // (epoch + 1) << 32 | next sequence, stored by rank 0 once the
+                                // current sequence of a decision-ahead walk is decided
   // reduction scratch (one slot per kind)
   float rmax[2][NW];
   float rsum[2][NW];
@@ -439,9 +441,15 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
       }
       if (exhausted && q_seq < P.B) {  // move on once the next sequence is known
         const unsigned long long nw = pub_load(&S.pub_next);
-        if ((nw >> 48) & 1ull && static_cast<int>((nw >> 32) & 0xFFFF) == (q_ep & 0xFFFF)) {
+        const unsigned long long xw = *reinterpret_cast<volatile unsigned long long*>(&S.nxt_word);
+        int nq = -1;
+        if ((nw >> 48) & 1ull && static_cast<int>((nw >> 32) & 0xFFFF) == (q_ep & 0xFFFF))
+          nq = static_cast<int>(static_cast<uint32_t>(nw));
+        else if ((xw >> 32) == static_cast<unsigned long long>(static_cast<uint32_t>(q_ep + 1)))
+          nq = static_cast<int>(static_cast<uint32_t>(xw));
+        if (nq >= 0) {
           ++q_ep;
-          q_seq = static_cast<int>(static_cast<uint32_t>(nw));
+          q_seq = nq;
           q_L = load_len(P, q_seq);
           q_ph = STATS;
           q_pos = 0;
@@ -1068,10 +1076,13 @@ __device__ __forceinline__ void stats_chunk(const Ring<T, GREEDY>& R, int s, int
 // Consumer warp 0: wait for exchange round r (posted for position `pos`), combine it and take
 // the decision into S.dec; on a stop or an unusable row tell the producer, which then stops
 // streaming the positions after it. The round of position 0 also names the next sequence.
+__device__ int lpt_seq(const Params& P, const int* cnt, int r);
+
 template <bool GREEDY>
 __device__ void resolve_open(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
-                             uint64_t* xbar, uint32_t r, uint32_t C, int seq, int ep, int pos,
-                             int L, float zx_t, float zx_d) {
+                             uint64_t* xbar, uint32_t r, uint32_t C, uint32_t rank,
+                             const int* lcnt, int seq, int ep, int pos, int L, float zx_t,
+                             float zx_d) {
   const int lane = threadIdx.x & 31;
   const bool ok = mbar_wait_cluster_bounded(&xbar[r & 1u], (r >> 1) & 1u, kWaitBudget);
   const Xchg* XX = X[r & 1u];
@@ -1079,15 +1090,6 @@ __device__ void resolve_open(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster
   if (ok)
     for (uint32_t cc = 0; cc < C; ++cc) ab |= (XX[cc].flags & XF_ABORT) != 0u;
   ab = __any_sync(FULL, ab);
-  if (pos == 0 && lane == 0) {
-    const int next = ok ? XX[0].next_seq : P.B;
-    S.next = next;
-    if (next < P.B) {
-      fetch_header(P, S, S.cur ^ 1, next, GREEDY);
-      S.n_hdr_wait = 1;
-    }
-    pub_store(&S.pub_next, pack_next(next, ep));
-  }
   int stop = -3;
   if (!ab) {
     const bool st_d = !GREEDY && pos < L;
@@ -1104,7 +1106,38 @@ __device__ void resolve_open(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster
       pub_store(&S.pub_cur, pack_cur(seq, ep, stop, 0));
     }
   }
+  // the sequence is decided: rank 0 takes the cluster's next sequence from the queue now (not
+  // when this one started), so a cluster that drew a long outcome does not hold a second
+  // sequence back, and tells every CTA of the cluster
+  if (rank == 0 && stop != -1 && stop != -3) {
+    int q = 0;
+    if (lane == 0) q = static_cast<int>(atomicAdd(&P.ws->next, 1u));
+    q = __shfl_sync(FULL, q, 0);
+    const int nxt = lpt_seq(P, lcnt, q + P.n_clusters);
+    if (lane < static_cast<int>(C)) {
+      const unsigned long long w =
+          (static_cast<unsigned long long>(static_cast<uint32_t>(ep + 1)) << 32) |
+          static_cast<uint32_t>(nxt);
+      st_cluster_u64(map_to_rank(smem_u32(&S.nxt_word), static_cast<uint32_t>(lane)), w);
+    }
+  }
   __syncwarp();
+}
+
+// The next sequence stored by rank 0 for epoch `ep` (bounded wait; P.B after a timeout, with the
+// error word raised).
+__device__ __forceinline__ int wait_next_word(const Params& P, CtaState& S, int ep) {
+  const unsigned long long want = static_cast<unsigned long long>(static_cast<uint32_t>(ep + 1));
+  const long long t0 = clock64();
+  while (true) {
+    const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(&S.nxt_word);
+    if ((w >> 32) == want) return static_cast<int>(static_cast<uint32_t>(w));
+    if (clock64() - t0 > kWaitBudget) {
+      atomicOr(&P.ws->error, 1u);
+      return P.B;
+    }
+    sleep_ns(64);
+  }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1197,6 +1230,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     S.cur = 0;
     S.n_hdr_wait = 0;
     S.cons_final = 0;
+    S.nxt_word = 0ull;
   }
   // the draft-length counts of the longest-first order (every CTA its own copy)
   if (P.lpt) {
@@ -1231,7 +1265,8 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     while (seq < P.B) {
       cons.ep = ep;
       int next_local = 0;
-      if (rank == 0 && warp == 0) {  // this cluster's next sequence, named in the first exchange
+      const bool ahead = !TOP8 && !P.debug_all && S.hdr[S.cur].ok && P.use_bulk;
+      if (!ahead && rank == 0 && warp == 0) {  // the next sequence, named in the first exchange
         int q = 0;
         if (tid == 0) q = static_cast<int>(atomicAdd(&P.ws->next, 1u));
         q = __shfl_sync(FULL, q, 0);
@@ -1250,7 +1285,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
       bool first = true;
       int a = -1;
       int next = P.B;
-      if (!TOP8 && !P.debug_all && !invalid && P.use_bulk) {
+      if (ahead) {
         // ---- decisions taken while the next position streams: position i is read while
         // consumer warp 0 combines the round of position i - 1 (polled between chunks, else
         // waited for at the end of position i); a stop makes the producer switch to the draw,
@@ -1278,7 +1313,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
               const int ready = __shfl_sync(
                   FULL, tid == 0 ? static_cast<int>(mbar_test_cluster(&xbar[pend_round & 1u], (pend_round >> 1) & 1u)) : 0, 0);
               if (ready) {
-                resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, seq, ep, pend, L, pzx_t, pzx_d);
+                resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, rank, lcnt, seq, ep, pend, L, pzx_t, pzx_d);
                 resolved = true;
               }
             }
@@ -1315,7 +1350,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           }
           // the previous position's decision, at the latest now
           if (warp == 0 && !resolved) {
-            resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, seq, ep, pend, L, pzx_t, pzx_d);
+            resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, rank, lcnt, seq, ep, pend, L, pzx_t, pzx_d);
             resolved = true;
           }
           cbar();
@@ -1341,7 +1376,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           pzx_d = zx_d;
           if (i == L) {  // nothing after this position: its decision now
             if (warp == 0) {
-              resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, seq, ep, pend, L, pzx_t, pzx_d);
+              resolve_open<GREEDY>(P, S, X, xbar, pend_round, C, rank, lcnt, seq, ep, pend, L, pzx_t, pzx_d);
               resolved = true;
             }
             cbar();
@@ -1350,7 +1385,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
           }
         }
         cbar();
-        next = S.next;
+        next = P.B;
         if (late || outcome == -3 || outcome == -1) {
           aborted = true;
         } else if (outcome == -2) {
@@ -1598,17 +1633,26 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
       }
       // ---- move on to the next sequence of the queue ----
       if (tid == 0) {
+        int nxs = next;
+        if (ahead) {  // rank 0 stored it when this sequence was decided
+          nxs = wait_next_word(P, S, ep);
+          if (nxs < P.B) {
+            fetch_header(P, S, S.cur ^ 1, nxs, GREEDY);
+            S.n_hdr_wait = 1;
+          }
+        }
+        S.next = nxs;
         if (S.n_hdr_wait) {
           cp_async_wait_all();
           S.n_hdr_wait = 0;
         }
         const int nx = S.cur ^ 1;
-        if (next < P.B) S.hdr[nx].ok = header_ok(P, S.hdr[nx], GREEDY);
+        if (nxs < P.B) S.hdr[nx].ok = header_ok(P, S.hdr[nx], GREEDY);
         S.cur = nx;
-        pub_store(&S.pub_cur, pack_cur(next, ep + 1, (next < P.B && S.hdr[nx].ok) ? -1 : -2, 0));
+        pub_store(&S.pub_cur, pack_cur(nxs, ep + 1, (nxs < P.B && S.hdr[nx].ok) ? -1 : -2, 0));
       }
       cbar();
-      seq = next;
+      seq = S.next;
       ++ep;
     }
     if (tid == 0) {

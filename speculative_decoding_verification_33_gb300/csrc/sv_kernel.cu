@@ -1078,6 +1078,11 @@ __device__ __forceinline__ void stats_chunk(const Ring<T, GREEDY>& R, int s, int
 // streaming the positions after it. The round of position 0 also names the next sequence.
 __device__ int lpt_seq(const Params& P, const int* cnt, int r);
 
+// A 64-bit store into the shared memory of a CTA of the cluster (a mapped address).
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
 template <bool GREEDY>
 __device__ void resolve_open(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
                              uint64_t* xbar, uint32_t r, uint32_t C, uint32_t rank,

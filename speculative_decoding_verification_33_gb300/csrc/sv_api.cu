@@ -236,7 +236,7 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
               const int32_t* lens, const float* uni, float T, float beta, int mode,
               int32_t* out_acc, int32_t* out_tok, int32_t* out_topf, float* lse_t,
               float* lse_d, float* px, float* qx, int debug_all, Workspace* ws_user,
-              size_t ws_user_bytes, cudaStream_t stream) {
+              size_t ws_user_bytes, cudaStream_t stream, bool zero_copy = false) {
   Checked c;
   sv_status st = check_args(p, tgt, dft, tok, uni, T, beta, mode, out_acc, out_tok, out_topf, &c);
   if (st != SV_OK || p->B == 0) return st;
@@ -275,7 +275,9 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   const uintptr_t a_d = reinterpret_cast<uintptr_t>(dft);
   bool aligned = (a_t % 16 == 0) && ((p->target_row_stride * c.elt) % 16 == 0);
   if (!c.greedy) aligned = aligned && (a_d % 16 == 0) && ((p->draft_row_stride * c.elt) % 16 == 0);
-  P.use_bulk = aligned ? 1 : 0;
+  // rows read in place from pinned host memory go through the consumers' own loads
+  P.use_bulk = (aligned && !zero_copy) ? 1 : 0;
+  P.vec_fill = aligned ? 1 : 0;
 
   // The draft rows' top 8 (bias set, top-F ids) come from a prepass over the draft rows when the
   // workspace has room for its keys; otherwise (the fixed workspace of spec_verify_noalloc, or
@@ -483,6 +485,20 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
   int32_t* d_otok = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_acc) + b_acc);
   int32_t* d_topf = c.fmax > 0 ? reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_otok) + b_otok) : nullptr;
 
+  // Rows in pinned (page-locked, mapped) host memory are read in place by the verify kernel:
+  // only the rows a sequence's outcome needs cross the host link, once. Not with a top-8 prepass
+  // (its bulk copies stage device rows).
+  auto mapped = [](const void* ptr) -> const void* {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return (a.type == cudaMemoryTypeHost && a.devicePointer) ? a.devicePointer : nullptr;
+  };
+  const void* zt = needs_top8(prob, c) ? nullptr : mapped(target_logits);
+  const void* zd = (zt && !c.greedy) ? mapped(draft_logits) : nullptr;
+  const bool zero_copy = zt && (c.greedy || zd);
   // rows each sequence has: target 0..L_b, draft 0..L_b-1 (one contiguous block each)
   long long need = 0;
   for (int b = 0; b < B; ++b) need += draft_lens ? std::clamp(draft_lens[b], 0, K) : K;
@@ -491,7 +507,9 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
     return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
   };
   bool ok = true;
-  if (per_seq) {
+  if (zero_copy) {
+    // nothing to stage: the kernel reads the rows where they are
+  } else if (per_seq) {
     for (int b = 0; b < B && ok; ++b) {
       const int Lb = std::clamp(draft_lens[b], 0, K);
       const size_t ot = static_cast<size_t>(b) * (K + 1) * t_row;
@@ -510,8 +528,9 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
   if (!c.greedy) ok = ok && cp(d_uni, uniforms, static_cast<size_t>(B) * (K + 1) * 4);
   if (!ok) return SV_ERR_CUDA;
   // (the stream's own workspace, sized by run for this problem)
-  st = run(prob, d_t, c.greedy ? nullptr : d_d, d_tok, d_len, d_uni, temperature, beta, mode,
-           d_acc, d_otok, d_topf, nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0, s);
+  st = run(prob, zero_copy ? zt : d_t, c.greedy ? nullptr : (zero_copy ? zd : d_d), d_tok, d_len,
+           d_uni, temperature, beta, mode, d_acc, d_otok, d_topf, nullptr, nullptr, nullptr,
+           nullptr, 0, nullptr, 0, s, zero_copy);
   if (st != SV_OK) return st;
   Workspace* ws = nullptr;  // the workspace run used (it may have grown it)
   {

@@ -52,6 +52,8 @@ struct Params {
   int debug_all;  // read every row a sequence has and fill the diagnostics
   int slice;      // elements of a row owned by one CTA (multiple of 8)
   int use_bulk;   // rows and strides are 16-byte aligned: stage rows with bulk async copies
+  int vec_fill;   // without bulk copies, rows 16-byte aligned: consumers fill chunks with 16-byte
+                  // loads (rows read in place from pinned host memory)
   int n_clusters;
   int lpt;         // take sequences longest draft first
   const unsigned long long* keys;  // top-8 keys of every draft row from the prepass, or NULL

@@ -554,7 +554,24 @@ __device__ int fill_unaligned(const Params& P, const Ring<T, GREEDY>& R, int s, 
       if (!(rows & (1 << r))) continue;
       const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + k * R.CH;
       T* dst = R.row(s, r);
-      for (int e = threadIdx.x; e < npad; e += NC) dst[e] = e < n ? src[e] : Elt<T>::neg_inf();
+      int e0 = 0;
+      if (P.vec_fill) {  // whole 16-byte pieces, four loads in flight per thread
+        constexpr int kPer16 = 16 / static_cast<int>(sizeof(T));
+        const int n16 = n / kPer16;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        int e = threadIdx.x;
+        for (; e + 3 * NC < n16; e += 4 * NC) {
+          const uint4 a0 = s4[e], a1 = s4[e + NC], a2 = s4[e + 2 * NC], a3 = s4[e + 3 * NC];
+          d4[e] = a0;
+          d4[e + NC] = a1;
+          d4[e + 2 * NC] = a2;
+          d4[e + 3 * NC] = a3;
+        }
+        for (; e < n16; e += NC) d4[e] = s4[e];
+        e0 = n16 * kPer16;
+      }
+      for (int e = e0 + threadIdx.x; e < npad; e += NC) dst[e] = e < n ? src[e] : Elt<T>::neg_inf();
     }
   }
   late = cbar_or(late || s < 0);

@@ -222,3 +222,37 @@ def test_workspace_and_host_entry_points():
     assert np.array_equal(h_tok, ref["tokens"])
     assert np.array_equal(h_topf, ref["topf"])
     assert api.device_error() == 0
+
+
+@pytest.mark.parametrize("cfg", [5, 2, 1])
+def test_host_rows_read_in_place(cfg):
+    """Rows in pinned host memory are read in place by the kernel (no staging copy); the outcome
+    equals the device-buffer call and the oracle's."""
+    w = W.WORKLOADS[cfg] if cfg != 5 else W.small_variant(W.WORKLOADS[5], B=48)
+    d = W.make_inputs(w)
+    greedy = w.mode == "greedy"
+
+    def pinned(a):
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+    hT = pinned(d["target"])
+    hD = None if greedy else pinned(d["draft"])
+    h_acc = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h_tok = torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory()
+    api.verify_host(hT, hD, torch.from_numpy(d["draft_tokens"]).pin_memory(),
+                    torch.from_numpy(d["draft_lens"]).pin_memory(),
+                    torch.from_numpy(d["uniforms"]).pin_memory(), h_acc, h_tok,
+                    dtype=w.dtype, temperature=w.temperature, mode=w.mode)
+    T = api.to_device_logits(d["target"])
+    D = None if greedy else api.to_device_logits(d["draft"])
+    out = api.verify(T, D, torch.from_numpy(d["draft_tokens"]).cuda(),
+                     torch.from_numpy(d["draft_lens"]).cuda(),
+                     torch.from_numpy(d["uniforms"]).cuda(), temperature=w.temperature,
+                     mode=w.mode)
+    torch.cuda.synchronize()
+    assert np.array_equal(h_acc.numpy(), out["accept_len"].cpu().numpy())
+    assert np.array_equal(h_tok.numpy(), out["tokens"].cpu().numpy())
+    res = O.verify_batch(d["target"], None if greedy else d["draft"], d["draft_tokens"],
+                         d["draft_lens"], d["uniforms"], temperature=w.temperature, mode=w.mode)
+    rep = compare(res, range(w.B), h_acc.numpy(), h_tok.numpy())
+    assert rep.ok(), (rep.summary(), rep.mismatches[:3])
+    assert api.device_error() == 0

@@ -268,7 +268,7 @@ sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long lon
  * 0..L_b-1); each row is reduced on the tensor cores to its maximum, softmax sum, logit at the
  * draft id and argmax, and the two rows of the decided position are scored again for the draw,
  * so no row of logits is written to memory. Logits are accumulated in fp32 from bf16 products.
- * d must be a multiple of 64, K <= 8, V <= 2^24; hidden states and head 16-byte aligned, with
+ * d must be a multiple of 64, K <= 8, V <= 2^18; hidden states and head 16-byte aligned, with
  * row strides that are multiples of 8 elements. Asynchronous on `stream`, on the stream's
  * workspace (grown on demand: about B (2K+1) d 2 bytes for the packed rows plus 16 bytes per
  * sequence and 16 ids for the residual masses); device-side failures are read with

@@ -743,7 +743,9 @@ sv_status spec_verify_hidden(int B, int K, int V, int d, const void* hidden_targ
                              const int32_t* draft_lens, const float* uniforms, float temperature,
                              int mode, int32_t* out_accept_len, int32_t* out_tokens,
                              void* stream) {
-  if (B < 0 || K < 1 || K > 8 || V < 1 || V > (1 << 24) || d < 64 || d % 64 != 0)
+  // V <= 2^18 as for spec_verify: the draw's masses (each at most 1 in 2^-44 units per id) then
+  // sum below 2^63 even for a flat row
+  if (B < 0 || K < 1 || K > 8 || V < 1 || V > (1 << 18) || d < 64 || d % 64 != 0)
     return SV_ERR_INVALID_ARG;
   if (mode != SV_MODE_GREEDY && mode != SV_MODE_STOCHASTIC) return SV_ERR_INVALID_ARG;
   const bool greedy = mode == SV_MODE_GREEDY;

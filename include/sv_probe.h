@@ -26,6 +26,16 @@ extern "C" {
 sv_status sv_hbm_read_probe(const void* buf, size_t bytes, unsigned long long* out_checksum,
                             void* stream);
 
+/*
+ * Failure-detection check of the bounded waits, with no GPU fault: one thread waits on an
+ * mbarrier that nothing ever arrives at, using the same bounded wait as the verify, row and
+ * LM-head kernels, for about budget_us microseconds of SM clock (1 .. 1000000), then raises the
+ * error word of `stream`'s workspace and returns, as a kernel whose copy or peer never came
+ * does. spec_verify_device_error(stream) then reports SV_ERR_DEVICE_TIMEOUT once and clears it;
+ * the context stays usable. Asynchronous on `stream`.
+ */
+sv_status sv_wait_probe(unsigned int budget_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -323,6 +323,13 @@ def hbm_read_probe(buf: torch.Tensor, out: torch.Tensor, stream=None) -> None:
                 "sv_hbm_read_probe")
 
 
+def wait_probe(budget_us: int, stream=None) -> None:
+    """Run one bounded wait that nothing satisfies (``sv_wait_probe``): it gives up after about
+    ``budget_us`` microseconds and raises the stream's device error word."""
+    _lib._check(_lib.load().sv_wait_probe(int(budget_us), _stream_handle(stream)),
+                "sv_wait_probe")
+
+
 def to_device_logits(a: np.ndarray, device="cuda") -> torch.Tensor:
     """Upload stored logits (uint16 bf16 bit patterns or float32) as a bf16/f32 tensor."""
     if a.dtype == np.uint16:

@@ -803,6 +803,21 @@ const char* spec_verify_status_string(sv_status status) {
   return "unknown status";
 }
 
+sv_status sv_wait_probe(unsigned int budget_us, void* stream) {
+  if (budget_us == 0 || budget_us > 1000000u) return SV_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0, khz = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0)
+    khz = 2000000;
+  std::lock_guard<std::mutex> lock(g_mu);
+  sv_status st = SV_OK;
+  StreamRes* r = resources(dev, s, sizeof(Workspace), &st);
+  if (!r) return st;
+  const long long cycles = static_cast<long long>(budget_us) * (khz / 1000);
+  return sv::launch_wait_probe(cycles, &r->ws->error, s) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 sv_status sv_hbm_read_probe(const void* buf, size_t bytes, unsigned long long* out_checksum,
                             void* stream) {
   if (!buf || !out_checksum || bytes == 0 || bytes % 16 != 0 ||

@@ -81,5 +81,7 @@ cudaError_t launch(const Launch& L, cudaStream_t stream);
 
 cudaError_t launch_probe(const void* buf, size_t bytes, unsigned long long* out,
                          cudaStream_t stream);
+// A bounded wait that runs out after `budget_cycles` clock cycles and raises *err bit 0.
+cudaError_t launch_wait_probe(long long budget_cycles, unsigned int* err, cudaStream_t stream);
 
 }  // namespace sv

@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include "sv_internal.h"
+#include "sv_ptx.cuh"
 
 namespace sv {
 namespace {
@@ -28,7 +29,23 @@ __global__ void __launch_bounds__(256) probe_kernel(const uint4* __restrict__ p,
   if ((threadIdx.x & 31) == 0) atomicAdd(out, static_cast<unsigned long long>(acc));
 }
 
+// One thread waits on an mbarrier that nothing arrives at, with the same bounded wait the
+// kernels use, for `budget` clock cycles; when the wait gives up it raises bit 0 of the error
+// word, as a kernel whose copy or peer never came would, and returns.
+__global__ void wait_probe_kernel(long long budget, unsigned int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait_bounded(&bar, 0, budget)) atomicOr(err, 1u);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(long long budget_cycles, unsigned int* err, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(budget_cycles, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_probe(const void* buf, size_t bytes, unsigned long long* out,
                          cudaStream_t stream) {

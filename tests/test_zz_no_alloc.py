@@ -61,3 +61,23 @@ def test_no_alloc_rejects_batches_above_its_array():
     st = _lib.call("spec_verify_noalloc", prob, p, 0, p, 0, 0, 0.0, 1.0, _lib.SV_MODE_GREEDY,
                    p, p, 0, torch.cuda.current_stream().cuda_stream)
     assert st == _lib.SV_ERR_UNSUPPORTED
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """Failure detection without a GPU fault: a bounded wait that nothing satisfies runs out,
+    raises the error word, the host reads SV_ERR_DEVICE_TIMEOUT once, and the context stays
+    usable for a normal call."""
+    from speculative_decoding_verification_33_gb300._lib import SV_ERR_DEVICE_TIMEOUT
+    assert api.device_error() == 0
+    api.wait_probe(2000)
+    assert api.device_error() == SV_ERR_DEVICE_TIMEOUT
+    assert api.device_error() == 0
+    w = W.small_variant(W.WORKLOADS[3], B=4, V=4096)
+    d = W.make_inputs(w)
+    out = api.verify(api.to_device_logits(d["target"]), api.to_device_logits(d["draft"]),
+                     torch.from_numpy(d["draft_tokens"]).cuda(),
+                     torch.from_numpy(d["draft_lens"]).cuda(),
+                     torch.from_numpy(d["uniforms"]).cuda(), temperature=w.temperature)
+    torch.cuda.synchronize()
+    assert (out["accept_len"].cpu().numpy() >= 0).all()
+    assert api.device_error() == 0

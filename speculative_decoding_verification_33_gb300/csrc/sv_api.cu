@@ -18,6 +18,7 @@
 #include "sv_rows.h"
 #include "sv_lmhead.h"
 #include "sv_hverify.h"
+#include "sv_greedy.h"
 #include "sv_probe.h"
 
 namespace {
@@ -278,6 +279,43 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   // rows read in place from pinned host memory go through the consumers' own loads
   P.use_bulk = (aligned && !zero_copy) ? 1 : 0;
   P.vec_fill = aligned ? 1 : 0;
+
+  // Greedy verification of a small batch (the padded target rows fit in 16 MB): every target row
+  // in flight at once, argmax per row slice, then one warp per sequence walks the positions.
+  // The chained cluster walk would spend its time on the latency of position after position.
+  if (c.greedy && !debug_all && c.fmax == 0 && static_cast<long long>(p->B) * (p->K + 1) <= 65535 &&
+      static_cast<long long>(p->B) * (p->K + 1) * p->target_row_stride * c.elt <= (16LL << 20)) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    sv::GreedyParams G;
+    G.tgt = tgt;
+    G.stride = p->target_row_stride;
+    G.lens = lens;
+    G.tokens = tok;
+    G.B = p->B;
+    G.K = p->K;
+    G.V = p->V;
+    G.aligned = aligned ? 1 : 0;
+    G.out_acc = out_acc;
+    G.out_tok = out_tok;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return SV_ERR_CUDA;
+    sv::greedy_plan(p->B, p->K, p->V, sms, &G.nslice, &G.slice);
+    const size_t kb2 = sv::greedy_keys_bytes(p->B, p->K, G.nslice);
+    Workspace* w = nullptr;
+    if (ws_user) {
+      if (ws_user_bytes >= sizeof(Workspace) + kb2) w = ws_user;
+    } else {
+      StreamRes* r = resources(dev, stream, sizeof(Workspace) + kb2, &st);
+      if (!r) return st;
+      w = r->ws;
+    }
+    if (w) {  // (a caller's workspace too small for the keys takes the cluster walk)
+      G.keys = reinterpret_cast<unsigned long long*>(w + 1);
+      return sv::launch_greedy(G, p->dtype == SV_DTYPE_BF16 ? 1 : 0, stream) == cudaSuccess
+                 ? SV_OK
+                 : SV_ERR_CUDA;
+    }
+  }
 
   // The draft rows' top 8 (bias set, top-F ids) come from a prepass over the draft rows when the
   // workspace has room for its keys; otherwise (the fixed workspace of spec_verify_noalloc, or

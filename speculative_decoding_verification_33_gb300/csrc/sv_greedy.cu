@@ -28,6 +28,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr unsigned long long kBad = ~0ull;  // a slice with a NaN or +inf
+constexpr int kMaxGreedyK = 8;              // positions per sequence (K <= 8)
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) greedy_rows(const GreedyParams P) {
@@ -71,29 +72,37 @@ __global__ void __launch_bounds__(kThreads) greedy_rows(const GreedyParams P) {
 }
 
 __global__ void greedy_decide(const GreedyParams P) {
-  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  __shared__ unsigned long long pm[4][kMaxGreedyK + 1];
+  const int wib = threadIdx.x >> 5;
+  const int b = blockIdx.x * (blockDim.x >> 5) + wib;
   const int lane = threadIdx.x & 31;
-  if (b >= P.B) return;
+  if (b >= P.B) return;  // whole warps
   const int K = P.K;
   const int L = P.lens ? P.lens[b] : K;
   const int32_t* x = P.tokens + static_cast<long long>(b) * K;
   bool ok = L >= 1 && L <= K;
-  for (int i = 0; ok && i < L; ++i) ok = x[i] >= 0 && x[i] < P.V;
+  const int xi = (ok && lane < L) ? x[lane] : 0;
+  ok = ok && __all_sync(FULL, lane >= L || (xi >= 0 && xi < P.V));
   int a = -1, last = -1;
-  for (int i = 0; ok && i <= L; ++i) {
-    const unsigned long long* k = P.keys + (static_cast<long long>(b) * (K + 1) + i) * P.nslice;
-    unsigned long long m = 0;
-    for (int s = lane; s < P.nslice; s += 32) m = k[s] > m ? k[s] : m;
-    m = warp_max_u64(m);
-    if (m == kBad || key_value(m) == -INFINITY) {  // NaN / +inf, or nothing but -inf
-      ok = false;
+  if (ok) {
+    // every slice key of rows 0..L in one round of loads, folded per row in shared memory
+    if (lane <= L) pm[wib][lane] = 0ull;
+    __syncwarp();
+    const unsigned long long* k = P.keys + static_cast<long long>(b) * (K + 1) * P.nslice;
+    for (int j = lane; j < (L + 1) * P.nslice; j += 32) atomicMax(&pm[wib][j / P.nslice], k[j]);
+    __syncwarp();
+    for (int i = 0; i <= L; ++i) {  // the oracle's order: a bad row counts only up to the stop
+      const unsigned long long m = pm[wib][i];
+      if (m == kBad || key_value(m) == -INFINITY) {  // NaN / +inf, or nothing but -inf
+        ok = false;
+        break;
+      }
+      const int g = key_id(m);
+      if (i < L && __shfl_sync(FULL, xi, i) == g) continue;
+      a = i;
+      last = g;
       break;
     }
-    const int g = key_id(m);
-    if (i < L && x[i] == g) continue;
-    a = i;
-    last = g;
-    break;
   }
   int32_t* tok = P.out_tok + static_cast<long long>(b) * (K + 1);
   for (int j = lane; j <= K; j += 32) tok[j] = (ok && j < a) ? x[j] : ((ok && j == a) ? last : -1);

@@ -105,8 +105,9 @@ def input_bytes(w, lens) -> int:
 def host_copy_bytes(w, lens, acc=None, pinned=True):
     """Bytes spec_verify_host moves per call. With pinned rows and no top-8 prepass the kernel
     reads the rows in place: the rows the outcome needs (target 0..a_b, draft 0..min(a_b,
-    L_b-1)), counted twice for the decided position (the draw reads it again), plus the staged
-    ids, lengths and uniforms. Otherwise it mirrors the per-sequence / whole-buffer staging."""
+    L_b-1)) cross the host link once (the draw reads the decided position back from a device
+    copy), plus the staged ids, lengths and uniforms. Otherwise it mirrors the per-sequence /
+    whole-buffer staging."""
     B, K = w.B, w.K
     top8 = w.mode == "stochastic" and (w.fanout or (w.beta < 1.0 and w.bias_k > 0))
     if pinned and not top8 and acc is not None:
@@ -115,8 +116,6 @@ def host_copy_bytes(w, lens, acc=None, pinned=True):
             if a < 0:
                 continue
             rows += a + 1 + (min(a, L - 1) + 1 if w.mode == "stochastic" else 0)
-            if w.mode == "stochastic":
-                rows += 1 + (1 if a < L else 0)
         h2d = rows * w.V * w.elem_bytes + B * K * 4 + B * 4
         if w.mode == "stochastic":
             h2d += B * (K + 1) * 4

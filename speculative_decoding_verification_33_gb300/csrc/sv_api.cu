@@ -32,6 +32,8 @@ struct StreamRes {
   size_t ws_bytes = 0;
   void* stage = nullptr;  // device staging for spec_verify_host
   size_t stage_bytes = 0;
+  void* scr = nullptr;    // rows read in place from host memory: the draw's device copies
+  size_t scr_bytes = 0;
 };
 
 // Workspace of spec_verify_noalloc: the queue counters and error word the kernel needs (256
@@ -325,6 +327,28 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   std::lock_guard<std::mutex> lock(g_mu);
   st = plan(p, c, dev, &L, prepass);
   if (st != SV_OK) return st;
+  if (zero_copy) {  // the draw reads the decided position back from device copies
+    const size_t need = static_cast<size_t>(P.n_clusters) * static_cast<size_t>(L.cluster) * 2 *
+                        static_cast<size_t>(P.slice) * c.elt;
+    StreamRes& r = g_res[{dev, stream}];
+    if (r.scr_bytes < need) {
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+        return SV_ERR_UNSUPPORTED;
+      if (r.scr) {
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return SV_ERR_CUDA;
+        cudaFree(r.scr);
+        r.scr = nullptr;
+        r.scr_bytes = 0;
+      }
+      if (cudaMalloc(&r.scr, need) != cudaSuccess) {
+        r.scr = nullptr;
+        return SV_ERR_CUDA;
+      }
+      r.scr_bytes = need;
+    }
+    P.scratch = r.scr;
+  }
 
   if (ws_user) {
     P.ws = ws_user;

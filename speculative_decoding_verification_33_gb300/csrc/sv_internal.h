@@ -54,6 +54,8 @@ struct Params {
   int use_bulk;   // rows and strides are 16-byte aligned: stage rows with bulk async copies
   int vec_fill;   // without bulk copies, rows 16-byte aligned: consumers fill chunks with 16-byte
                   // loads (rows read in place from pinned host memory)
+  void* scratch;  // rows read in place from host memory: per CTA, a device copy of its slices of
+                  // the position last streamed, for the draw ([clusters][C][2][slice]), or NULL
   int n_clusters;
   int lpt;         // take sequences longest draft first
   const unsigned long long* keys;  // top-8 keys of every draft row from the prepass, or NULL

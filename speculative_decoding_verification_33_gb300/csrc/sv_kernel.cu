@@ -317,6 +317,8 @@ struct Ring {
   int nchunk;  // chunks per row of this CTA's slice
   int nv;      // elements of this CTA's slice
   int v0;      // first element of the slice
+  T* scr;      // rows read in place from host memory: this CTA's copy of the slices of the
+               // position last streamed (2 rows of `slice` elements), which the draw reads back
 
   __device__ __forceinline__ T* row(int s, int r) const {
     return reinterpret_cast<T*>(base + (static_cast<size_t>(s) * kRows + r) * kStageRowBytes);
@@ -546,13 +548,19 @@ __device__ __forceinline__ int acquire_open(const Ring<T, GREEDY>& R, int seq, i
 // share of the chunk, then the consumers synchronise. All consumers call this, `late` or not.
 template <typename T, bool GREEDY>
 __device__ int fill_unaligned(const Params& P, const Ring<T, GREEDY>& R, int s, int seq,
-                              int pos, int k, bool& late) {
+                              int pos, int k, bool& late, bool draw = false) {
   if (s >= 0) {
     const int rows = tag_rows(R.desc[s]);
     const int n = R.chunk_len(k), npad = (n + 7) & ~7;
     for (int r = 0; r < Ring<T, GREEDY>::kRows; ++r) {
       if (!(rows & (1 << r))) continue;
-      const T* src = static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) + R.v0 + k * R.CH;
+      // the draw reads the decided position back from this CTA's copy when it has one
+      T* keep = R.scr ? R.scr + static_cast<size_t>(r) * P.slice + static_cast<size_t>(k) * R.CH
+                      : nullptr;
+      const T* src = (draw && keep) ? keep
+                                    : static_cast<const T*>(row_ptr(P, r == 1, seq, pos, sizeof(T))) +
+                                          R.v0 + k * R.CH;
+      if (draw) keep = nullptr;
       T* dst = R.row(s, r);
       int e0 = 0;
       if (P.vec_fill) {  // whole 16-byte pieces, four loads in flight per thread
@@ -560,6 +568,7 @@ __device__ int fill_unaligned(const Params& P, const Ring<T, GREEDY>& R, int s, 
         const int n16 = n / kPer16;
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         uint4* d4 = reinterpret_cast<uint4*>(dst);
+        uint4* k4 = reinterpret_cast<uint4*>(keep);
         int e = threadIdx.x;
         for (; e + 3 * NC < n16; e += 4 * NC) {
           const uint4 a0 = s4[e], a1 = s4[e + NC], a2 = s4[e + 2 * NC], a3 = s4[e + 3 * NC];
@@ -567,11 +576,25 @@ __device__ int fill_unaligned(const Params& P, const Ring<T, GREEDY>& R, int s, 
           d4[e + NC] = a1;
           d4[e + 2 * NC] = a2;
           d4[e + 3 * NC] = a3;
+          if (k4) {
+            k4[e] = a0;
+            k4[e + NC] = a1;
+            k4[e + 2 * NC] = a2;
+            k4[e + 3 * NC] = a3;
+          }
         }
-        for (; e < n16; e += NC) d4[e] = s4[e];
+        for (; e < n16; e += NC) {
+          const uint4 a0 = s4[e];
+          d4[e] = a0;
+          if (k4) k4[e] = a0;
+        }
         e0 = n16 * kPer16;
       }
-      for (int e = e0 + threadIdx.x; e < npad; e += NC) dst[e] = e < n ? src[e] : Elt<T>::neg_inf();
+      for (int e = e0 + threadIdx.x; e < npad; e += NC) {
+        const T v = e < n ? src[e] : Elt<T>::neg_inf();
+        dst[e] = v;
+        if (keep && e < n) keep[e] = v;
+      }
     }
   }
   late = cbar_or(late || s < 0);
@@ -781,7 +804,7 @@ __device__ void draw_token(const Params& P, CtaState& S, Xchg (*X)[kMaxCluster],
   unsigned long long acc = 0;
   for (int k = 0; k < R.nchunk; ++k) {
     int s = acquire<T, GREEDY>(R, seq, -1 - a, k, cons, late);
-    if (!P.use_bulk) s = fill_unaligned<T, GREEDY>(P, R, s, seq, a, k, late);
+    if (!P.use_bulk) s = fill_unaligned<T, GREEDY>(P, R, s, seq, a, k, late, true);
     if (s < 0) break;
     const int n = R.chunk_len(k), nvec = (n + 7) >> 3;
     const T* rt = R.row(s, 0);
@@ -1237,6 +1260,10 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
   R.v0 = static_cast<int>(rank) * P.slice;
   R.nv = max(0, min(P.V - R.v0, P.slice));
   R.nchunk = (R.nv + RingT::CH - 1) / RingT::CH;
+  R.scr = P.scratch ? static_cast<T*>(P.scratch) +
+                          static_cast<size_t>(cid * static_cast<int>(C) + static_cast<int>(rank)) * 2 *
+                              P.slice
+                    : nullptr;
   unsigned long long* gmass = reinterpret_cast<unsigned long long*>(
       dyn + static_cast<size_t>(NS) * RingT::kRows * kStageRowBytes);
   const float c = P.c;

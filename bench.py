@@ -89,11 +89,15 @@ def algorithmic_bytes(w, lens, acc) -> int:
     return rows * w.V * w.elem_bytes + small
 
 
-def launches_per_step(w) -> int:
-    """Kernels one verify call launches: a bias set or top-F ids add the top-8 prepass over the
-    draft rows before the verify kernel."""
-    top8 = w.mode == "stochastic" and (w.fanout or (w.beta < 1.0 and w.bias_k > 0))
-    return 2 if top8 else 1
+def top8_prepass(w) -> bool:
+    """A bias set or top-F ids add the top-8 prepass over the draft rows before the verify
+    kernel (the host entry point then stages the rows instead of reading them in place)."""
+    return bool(w.mode == "stochastic" and (w.fanout or (w.beta < 1.0 and w.bias_k > 0)))
+
+
+# the kernels of each route spec_verify can take (spec_verify_route), by build source key
+ROUTE_NAMES = {0: "cluster walk", 1: "greedy rows", 2: "small batch, every row at once"}
+ROUTE_SOURCES = {0: "verify", 1: "greedy", 2: "small"}
 
 
 def input_bytes(w, lens) -> int:
@@ -652,6 +656,7 @@ def run_ours(args):
                                     cluster_hint=args.cluster)
     plan_c, plan_n, plan_smem = _lib.plan(
         prob, _lib.SV_MODE_GREEDY if greedy else _lib.SV_MODE_STOCHASTIC)
+    route, launches = _lib.route(prob, _lib.SV_MODE_GREEDY if greedy else _lib.SV_MODE_STOCHASTIC)
 
     def step():
         api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, acc, otok, otopf,
@@ -695,7 +700,7 @@ def run_ours(args):
     b_in = input_bytes(w, lens)
     peak, peak_src = measured_peak()
     achieved = b_alg / (mean_ms * 1e-3) / 1e9
-    digest = build.kernel_digest("verify")
+    digest = build.kernel_digest(ROUTE_SOURCES[route])
     traffic, traffic_src = recorded_traffic(w.name, digest)
 
     # read-only streaming probe (2 GiB), for context
@@ -727,7 +732,8 @@ def run_ours(args):
                        "verified_tokens_per_rank": toks_local,
                        "l2": ("warm: no flush between steps" if args.l2_warm else
                               "flushed before each step (256 MiB write, outside the events)"),
-                       "cluster_hint": args.cluster, "ctas_per_cluster": plan_c,
+                       "cluster_hint": args.cluster, "route": ROUTE_NAMES[route],
+                       "ctas_per_cluster": plan_c,
                        "clusters": plan_n, "smem_per_cta": plan_smem,
                        "wall_ms_per_step_incl_flush": wall / args.steps * 1e3},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -738,7 +744,7 @@ def run_ours(args):
                          "all_rows_gbs": b_in / (mean_ms * 1e-3) / 1e9,
                          "read_probe_gbs": probe_gbs,
                          "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms)},
-            "gpu_launches": args.steps * launches_per_step(w), "clocks": clk}
+            "gpu_launches": args.steps * launches, "clocks": clk}
 
     # end to end through the host-buffer entry point (pinned host memory)
     if not args.no_e2e:
@@ -773,7 +779,7 @@ def run_ours(args):
         line["e2e"] = {"value": toks_all / t_e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e_max * 1e3,
                        "host_rows": "read in place by the kernel from pinned host memory"
-                       if launches_per_step(w) == 1 else "staged with one copy per sequence",
+                       if not top8_prepass(w) else "staged with one copy per sequence",
                        "matches_device_call": bool(np.array_equal(h_acc.numpy(), g_acc) and
                                                    np.array_equal(h_out.numpy(), g_tok))}
 

@@ -81,7 +81,10 @@ typedef struct {
   int bias_k;                   /* size of the beta-down-weighted set, 0..8 (0 = none)        */
   const int* fanout;            /* host array of K entries F_i in 0..8, or NULL = no top-F    */
   int cluster_hint;             /* CTAs that share one sequence's rows: 0 = chosen by the
-                                   library, else 1, 2, 4, 8 or 16                             */
+                                   library, else 1, 2, 4, 8 or 16. With 0 the library may also
+                                   take a small batch without clusters (every row in flight
+                                   at once; see spec_verify_route); a nonzero hint always
+                                   walks the positions with clusters of that size             */
 } sv_problem;
 
 /*
@@ -118,6 +121,23 @@ sv_status spec_verify(const sv_problem* prob, const void* target_logits,
  */
 sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* clusters,
                            size_t* smem_bytes);
+
+/*
+ * Which kernels spec_verify takes for this problem on the current device (*route) and how many
+ * launches one call makes (*launches). Routes: SV_ROUTE_WALK, the chained cluster walk (one
+ * launch, two with the top-8 prepass over the draft rows for a bias set or top-F ids);
+ * SV_ROUTE_GREEDY_ROWS, greedy batches whose padded target rows fit in 16 MB (an argmax per row
+ * slice of every target row, then one warp per sequence: two launches); SV_ROUTE_SMALL,
+ * stochastic batches without a bias set or top-F ids whose rows fit in 168 MiB (every row's
+ * statistics, the draw's slice masses, one pick per sequence: three launches). A nonzero
+ * cluster_hint always walks. spec_verify_ws takes the walk as well when its workspace has no
+ * room for the other routes' partials. Host-side query; either output may be NULL; the same
+ * errors as spec_verify_plan.
+ */
+#define SV_ROUTE_WALK 0
+#define SV_ROUTE_GREEDY_ROWS 1
+#define SV_ROUTE_SMALL 2
+sv_status spec_verify_route(const sv_problem* prob, int mode, int* route, int* launches);
 
 /* Bytes of device workspace spec_verify_ws needs for this problem (256: the sequence queue and
  * the error word; the size does not depend on the problem). */

@@ -18,7 +18,7 @@ SV_MODE_GREEDY, SV_MODE_STOCHASTIC = 0, 1
 # every entry point the header declares (checked by the tests against include/*.h)
 EXPORTS = ("spec_verify", "spec_verify_workspace_bytes", "spec_verify_ws", "spec_verify_debug",
            "spec_verify_host", "spec_verify_device_error", "spec_verify_status_string",
-           "spec_verify_plan", "spec_verify_noalloc", "spec_draft_sample", "spec_residual_topf",
+           "spec_verify_plan", "spec_verify_route", "spec_verify_noalloc", "spec_draft_sample", "spec_residual_topf",
            "spec_lmhead_stats", "spec_verify_hidden", "sv_hbm_read_probe", "sv_wait_probe")
 
 
@@ -67,6 +67,7 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.sv_hbm_read_probe.argtypes = [_P, _SZ, _P, _P]
         lib.sv_wait_probe.argtypes = [ctypes.c_uint, _P]
         lib.spec_verify_plan.argtypes = [_PROB, _I, _P, _P, _P]
+        lib.spec_verify_route.argtypes = [_PROB, _I, _P, _P]
         lib.spec_draft_sample.argtypes = [_I, _I, _I, ctypes.c_longlong, _P, _P, _F, _F, _I,
                                           _F, _P, _P, _P, _P]
         lib.spec_residual_topf.argtypes = [_PROB, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P, _P]
@@ -111,6 +112,17 @@ def plan(prob: SvProblem, mode: int):
     _check(load().spec_verify_plan(ctypes.byref(prob), int(mode), ctypes.addressof(c),
                                    ctypes.addressof(n), ctypes.addressof(sm)), "spec_verify_plan")
     return c.value, n.value, sm.value
+
+
+SV_ROUTE_WALK, SV_ROUTE_GREEDY_ROWS, SV_ROUTE_SMALL = 0, 1, 2
+
+
+def route(prob: SvProblem, mode: int):
+    """(route, kernel launches per call) spec_verify takes for this problem."""
+    r, n = ctypes.c_int(), ctypes.c_int()
+    _check(load().spec_verify_route(ctypes.byref(prob), int(mode), ctypes.addressof(r),
+                                    ctypes.addressof(n)), "spec_verify_route")
+    return r.value, n.value
 
 
 def call(name: str, prob: SvProblem, *args) -> int:

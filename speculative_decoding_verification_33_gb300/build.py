@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspecverify.so"
 SOURCES = ["sv_kernel.cu", "sv_api.cu", "sv_probe.cu", "sv_rows.cu", "sv_lmhead.cu",
-           "sv_hverify.cu", "sv_greedy.cu"]
+           "sv_hverify.cu", "sv_greedy.cu", "sv_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
@@ -55,6 +55,7 @@ KERNEL_SOURCES = {
     "rows": ("sv_rows.cu", "sv_rows.h", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h"),
     "lmhead": ("sv_lmhead.cu", "sv_lmhead.h", "sv_tc.cuh", "sv_math.cuh", "sv_ptx.cuh"),
     "greedy": ("sv_greedy.cu", "sv_greedy.h", "sv_math.cuh", "sv_ptx.cuh"),
+    "small": ("sv_small.cu", "sv_small.h", "sv_math.cuh", "sv_ptx.cuh"),
     "hverify": ("sv_hverify.cu", "sv_hverify.h", "sv_lmhead.cu", "sv_lmhead.h", "sv_tc.cuh",
                 "sv_math.cuh", "sv_ptx.cuh"),
 }

@@ -19,6 +19,7 @@
 #include "sv_lmhead.h"
 #include "sv_hverify.h"
 #include "sv_greedy.h"
+#include "sv_small.h"
 #include "sv_probe.h"
 
 namespace {
@@ -235,6 +236,43 @@ sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L,
   return SV_OK;
 }
 
+// The kernels a call takes. The chained cluster walk serves every problem; two paths read every
+// row a sequence has at once when that costs less than the walk's latency of position after
+// position: greedy batches whose padded target rows fit in 16 MB (argmax per row slice, then one
+// warp per sequence), and stochastic batches without a bias set or top-F ids whose rows fit in
+// 168 MiB (row statistics, the draw's slice masses, one pick per sequence). A nonzero
+// cluster_hint, the diagnostics entry point and rows read in place from host memory always take
+// the walk.
+enum Route { ROUTE_WALK = 0, ROUTE_GREEDY_ROWS = 1, ROUTE_SMALL = 2 };
+
+// Row-statistics CTAs of the small-batch route resident per multiprocessor (cached per device
+// and dtype; call under g_mu).
+int small_rows_per_sm(int dev, int dtype) {
+  static std::map<std::pair<int, int>, int> cache;
+  auto it = cache.find({dev, dtype});
+  if (it != cache.end()) return it->second;
+  const int n = sv::small_rows_per_sm(dtype);
+  cache[{dev, dtype}] = n;
+  return n;
+}
+
+Route route_of(const sv_problem* p, const Checked& c, int dev, int sms, int bias_k,
+               bool debug_all, bool zero_copy, sv::SmallParams* sp) {
+  if (debug_all || p->cluster_hint != 0 || c.fmax != 0 || sms <= 0) return ROUTE_WALK;
+  const long long B = p->B, K = p->K;
+  if (c.greedy)
+    return (B * (K + 1) <= 65535 && B * (K + 1) * p->target_row_stride * c.elt <= (16LL << 20))
+               ? ROUTE_GREEDY_ROWS
+               : ROUTE_WALK;
+  if (zero_copy || bias_k != 0 || B * (2 * K + 1) > 65535 ||
+      B * (2 * K + 1) * std::max(p->target_row_stride, p->draft_row_stride) * c.elt >
+          (168LL << 20))
+    return ROUTE_WALK;
+  const int dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
+  return sv::small_plan(p->B, p->K, p->V, sms, small_rows_per_sm(dev, dtype), sp) ? ROUTE_SMALL
+                                                                                : ROUTE_WALK;
+}
+
 sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32_t* tok,
               const int32_t* lens, const float* uni, float T, float beta, int mode,
               int32_t* out_acc, int32_t* out_tok, int32_t* out_topf, float* lse_t,
@@ -282,11 +320,16 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   P.use_bulk = (aligned && !zero_copy) ? 1 : 0;
   P.vec_fill = aligned ? 1 : 0;
 
-  // Greedy verification of a small batch (the padded target rows fit in 16 MB): every target row
-  // in flight at once, argmax per row slice, then one warp per sequence walks the positions.
-  // The chained cluster walk would spend its time on the latency of position after position.
-  if (c.greedy && !debug_all && c.fmax == 0 && static_cast<long long>(p->B) * (p->K + 1) <= 65535 &&
-      static_cast<long long>(p->B) * (p->K + 1) * p->target_row_stride * c.elt <= (16LL << 20)) {
+  sv::SmallParams G2;
+  memset(&G2, 0, sizeof(G2));
+  Route route;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    route = route_of(p, c, dev, sm_count(dev), P.bias_k, debug_all != 0, zero_copy, &G2);
+  }
+  // Greedy verification of a small batch: every target row in flight at once, argmax per row
+  // slice, then one warp per sequence walks the positions.
+  if (route == ROUTE_GREEDY_ROWS) {
     std::lock_guard<std::mutex> lock(g_mu);
     sv::GreedyParams G;
     G.tgt = tgt;
@@ -314,6 +357,43 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
     if (w) {  // (a caller's workspace too small for the keys takes the cluster walk)
       G.keys = reinterpret_cast<unsigned long long*>(w + 1);
       return sv::launch_greedy(G, p->dtype == SV_DTYPE_BF16 ? 1 : 0, stream) == cudaSuccess
+                 ? SV_OK
+                 : SV_ERR_CUDA;
+    }
+  }
+
+  // Stochastic verification of a small batch: every row's statistics at once, then the draw's
+  // slice masses of the decided rows, then one CTA per sequence picks the token.
+  if (route == ROUTE_SMALL) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    sv::SmallParams& G = G2;  // layout filled by the route's plan
+    G.tgt = tgt;
+    G.dft = dft;
+    G.t_stride = p->target_row_stride;
+    G.d_stride = p->draft_row_stride;
+    G.lens = lens;
+    G.tokens = tok;
+    G.uni = uni;
+    G.B = p->B;
+    G.K = p->K;
+    G.V = p->V;
+    G.c = P.c;
+    G.aligned = aligned ? 1 : 0;
+    G.out_acc = out_acc;
+    G.out_tok = out_tok;
+    const size_t need = sv::small_ws_bytes(G);
+    Workspace* w = nullptr;
+    if (ws_user) {
+      if (ws_user_bytes >= sizeof(Workspace) + need) w = ws_user;
+    } else {
+      StreamRes* r = resources(dev, stream, sizeof(Workspace) + need, &st);
+      if (!r) return st;
+      w = r->ws;
+    }
+    if (w) {  // (a caller's workspace too small for the partials takes the cluster walk)
+      sv::small_carve(G, reinterpret_cast<char*>(w + 1));
+      G.err = &w->error;
+      return sv::launch_small(G, p->dtype == SV_DTYPE_BF16 ? 1 : 0, stream) == cudaSuccess
                  ? SV_OK
                  : SV_ERR_CUDA;
     }
@@ -425,6 +505,31 @@ sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* 
   if (cluster) *cluster = L.cluster;
   if (clusters) *clusters = L.p.n_clusters;
   if (smem_bytes) *smem_bytes = L.smem;
+  return SV_OK;
+}
+
+sv_status spec_verify_route(const sv_problem* prob, int mode, int* route, int* launches) {
+  Checked c;
+  const int one = 1;
+  const float u = 0.5f;
+  const float beta = prob && prob->bias_k > 0 ? 0.5f : 1.f;  // a bias set implies beta < 1
+  sv_status st = check_args(prob, &one, &one, &one, &u, 1.f, beta, mode, &one, &one,
+                            prob && prob->fanout ? &one : nullptr, &c);
+  if (st != SV_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  sv::SmallParams sp;
+  memset(&sp, 0, sizeof(sp));
+  Route r;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const int sms = sm_count(dev);
+    if (sms <= 0) return SV_ERR_CUDA;
+    r = route_of(prob, c, dev, sms, c.greedy ? 0 : prob->bias_k, false, false, &sp);
+  }
+  if (route) *route = static_cast<int>(r);
+  if (launches)
+    *launches = r == ROUTE_SMALL ? 3 : (r == ROUTE_GREEDY_ROWS || needs_top8(prob, c)) ? 2 : 1;
   return SV_OK;
 }
 

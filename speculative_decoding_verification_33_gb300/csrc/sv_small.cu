@@ -1,0 +1,607 @@
+// Stochastic verification of small batches with every row in flight at once (Kangaroo guide,
+// section 3: accept x_i while u_i < p_i(x_i) / q_i(x_i), then draw from max(p_a - q_a, 0), or from
+// p_L when every draft is accepted; SSD summary, "Method").
+//
+// The chained cluster walk takes a position's decision before it streams the next one, so a
+// batch of few sequences spends its time on the latency of position after position, and it
+// reads only the rows the outcome needs. When the rows a sequence has are few enough that
+// reading all of them at full bandwidth costs less than that latency, three launches do it,
+// each started early (programmatic dependent launch) and waiting for its predecessor's writes:
+//  1. small_rows: one CTA per (row, slice of the vocabulary) for every row a sequence has
+//     (target 0..L_b, draft 0..L_b-1) reduces its slice to (max, sum of 2^(z c - fl(max c)));
+//  2. small_mass: one CTA per (sequence, slice of the vocabulary) combines the sequence's
+//     partials, takes the accept tests in order (every CTA of the sequence reaches the same
+//     decision) and sums its slice of the draw's weights: per 8-element vector the sequential
+//     float sum of max(e_t - rho e_d, 0), truncated to an integer of 2^-44, both for the
+//     residual and for p (the draw falls back to p when the residual has no mass left);
+//  3. small_pick: one CTA per sequence finds the slice that holds floor(u W) from the slices'
+//     masses, then the vector inside it by a block prefix of the vectors' integers, walks that
+//     vector and writes the outcome.
+// The integer masses make the prefix exact and independent of the order of the sums. No bias
+// set and no top-F ids on this path (those take the cluster walk).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "sv_math.cuh"
+#include "sv_ptx.cuh"
+#include "sv_small.h"
+
+namespace sv {
+namespace {
+
+constexpr int kRowThreads = 128;
+constexpr int kMassThreads = 128;
+constexpr int kPickThreads = 256;
+constexpr int kPickVecs = 4;  // vectors of a slice per pick thread: slice_d <= 8192 ids
+constexpr float kLn2 = 0.69314718055994531f;
+
+// Programmatic dependent launch: let the next launch on the stream start its CTAs, and wait
+// until the previous launch has finished and its writes are visible.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// row slot r of sequence b: target 0..K, then draft 0..K-1
+__device__ __forceinline__ const void* small_row(const SmallParams& P, int b, int slot,
+                                                 size_t elt) {
+  const bool draft = slot > P.K;
+  const int i = draft ? slot - P.K - 1 : slot;
+  const char* base = static_cast<const char*>(draft ? P.dft : P.tgt);
+  const long long rows = draft ? P.K : P.K + 1;
+  const long long stride = draft ? P.d_stride : P.t_stride;
+  return base + ((static_cast<long long>(b) * rows + i) * stride) * static_cast<long long>(elt);
+}
+
+// 8 elements as they sit in memory: one 16-byte word for bf16, two for float
+template <typename T>
+struct Raw8 {
+  uint4 w[sizeof(T) / 2];
+};
+
+template <typename T>
+__device__ __forceinline__ void raw_load(const T* p, Raw8<T>& r) {
+#pragma unroll
+  for (int k = 0; k < static_cast<int>(sizeof(T) / 2); ++k)
+    r.w[k] = ldg_nc_v4(reinterpret_cast<const char*>(p) + 16 * k);
+}
+
+__device__ __forceinline__ void raw_unpack(const Raw8<uint16_t>& r, float (&z)[8]) {
+  Elt<uint16_t>::unpack(r.w[0], z);
+}
+__device__ __forceinline__ void raw_unpack(const Raw8<float>& r, float (&z)[8]) {
+  z[0] = __uint_as_float(r.w[0].x); z[1] = __uint_as_float(r.w[0].y);
+  z[2] = __uint_as_float(r.w[0].z); z[3] = __uint_as_float(r.w[0].w);
+  z[4] = __uint_as_float(r.w[1].x); z[5] = __uint_as_float(r.w[1].y);
+  z[6] = __uint_as_float(r.w[1].z); z[7] = __uint_as_float(r.w[1].w);
+}
+
+// elements e..e+7 of a row of V ids, -inf past the end (one by one when not a whole vector)
+template <typename T>
+__device__ __forceinline__ void load8_at(const T* row, int e, int V, bool aligned, float (&z)[8]) {
+  if (aligned && e + 8 <= V) {
+    Raw8<T> r;
+    raw_load(row + e, r);
+    raw_unpack(r, z);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) z[k] = (e + k < V) ? Elt<T>::val(row[e + k]) : -INFINITY;
+  }
+}
+
+constexpr int kStages = 4;                      // bulk-copy ring of the row kernel
+constexpr int kChunk = 8192;                    // bytes per stage
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per barrier wait
+
+// Fold 8 logits into the running (max, sum).
+__device__ __forceinline__ void fold8(RowAcc& acc, const float (&z)[8], float c) {
+  float vm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) vm = max_nan(vm, z[j]);
+  acc.rescale(vm, c);
+  if (acc.m > -INFINITY) acc.sum8(z, c);
+}
+
+// A 16-byte aligned row slice [e0, e1) streamed through a ring of bulk copies into shared
+// memory (up to kStages * kChunk bytes in flight per CTA, whatever the register budget); the
+// ids past the last whole 16 bytes are read directly. False when a copy did not land within
+// the wait budget (the CTA then waits, bounded again, for the copies it issued and returns).
+template <typename T>
+__device__ bool rows_bulk(const T* row, int e0, int e1, float c, RowAcc& acc) {
+  __shared__ __align__(128) unsigned char ring[kStages][kChunk];
+  __shared__ uint64_t bar[kStages];
+  constexpr int per = kChunk / static_cast<int>(sizeof(T));  // ids per stage
+  constexpr int q16 = 16 / static_cast<int>(sizeof(T));      // ids per 16 bytes
+  const int tid = threadIdx.x;
+  const int eb = e0 + (e1 - e0) / q16 * q16;
+  const int nch = (eb - e0 + per - 1) / per;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int j) {
+    const int s = j % kStages;
+    const int ids = min(per, eb - (e0 + j * per));
+    const uint32_t bytes = static_cast<uint32_t>(ids) * sizeof(T);
+    mbar_arrive_expect_tx(&bar[s], bytes);
+    bulk_g2s(ring[s], row + e0 + j * per, bytes, &bar[s]);
+  };
+  if (tid == 0)
+    for (int j = 0; j < min(kStages, nch); ++j) issue(j);
+  int j = 0;
+  bool ok = true;
+  for (; j < nch; ++j) {
+    const int s = j % kStages;
+    const bool landed = mbar_wait_bounded(&bar[s], (j / kStages) & 1, kWaitBudget);
+    if (__syncthreads_or(!landed)) {
+      ok = false;
+      break;
+    }
+    const T* sp = reinterpret_cast<const T*>(ring[s]);
+    const int n = min(per, eb - (e0 + j * per));
+    for (int v = tid; 8 * v < n; v += kRowThreads) {
+      float z[8];
+      if (8 * v + 8 <= n) {
+        Elt<T>::load8(sp, v, z);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) z[k] = 8 * v + k < n ? Elt<T>::val(sp[8 * v + k]) : -INFINITY;
+      }
+      fold8(acc, z, c);
+    }
+    __syncthreads();  // every thread is done with stage s before it is refilled
+    if (tid == 0 && j + kStages < nch) issue(j + kStages);
+  }
+  if (!ok) {
+    if (tid == 0)
+      for (int k = j; k < min(nch, j + kStages); ++k)
+        mbar_wait_bounded(&bar[k % kStages], (k / kStages) & 1, kWaitBudget);
+    __syncthreads();
+    return false;
+  }
+  if (tid == 0 && eb < e1) {  // fewer than 16 bytes left
+    float z[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) z[k] = eb + k < e1 ? Elt<T>::val(row[eb + k]) : -INFINITY;
+    fold8(acc, z, c);
+  }
+  return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) small_rows(const SmallParams P) {
+  pdl_trigger();
+  __shared__ float sm[kRowThreads / 32], ss[kRowThreads / 32];
+  const int sl = blockIdx.x, r = blockIdx.y;
+  const int b = r / (2 * P.K + 1), slot = r - b * (2 * P.K + 1);
+  const int L = P.lens ? P.lens[b] : P.K;
+  if (L < 1 || L > P.K) return;
+  if (slot <= P.K ? slot > L : slot - P.K - 1 >= L) return;  // rows the decision never reads
+  const T* row = static_cast<const T*>(small_row(P, b, slot, sizeof(T)));
+  const float c = P.c;
+  const int e0 = sl * P.slice, e1 = min(P.V, e0 + P.slice);
+  RowAcc acc;
+  acc.init();
+  bool ok = true;
+  if (P.aligned) {
+    ok = rows_bulk(row, e0, e1, c, acc);
+  } else {  // element by element, a batch of loads in flight per thread
+    const int nv = (e1 - e0 + 7) >> 3;
+    constexpr int U = 4;
+    for (int g0 = threadIdx.x; g0 < nv; g0 += U * kRowThreads) {
+      float z[U][8];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int e = e0 + 8 * (g0 + k * kRowThreads);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) z[k][q] = e + q < e1 ? Elt<T>::val(row[e + q]) : -INFINITY;
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+        if (g0 + k * kRowThreads < nv) fold8(acc, z[k], c);
+    }
+  }
+  if (!ok) {  // a copy that never landed: the row reads as NaN and the error word is raised
+    if (threadIdx.x == 0) {
+      atomicOr(P.err, 1u);
+      P.part[static_cast<long long>(r) * P.nslice + sl] = make_float2(__int_as_float(0x7fffffff), 0.f);
+    }
+    return;
+  }
+  // the CTA's (max, sum relative to fl(max c)), with the rounding of max c folded back
+  const float m = warp_max_nan(acc.m);
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float M = sm[0];
+  for (int w = 1; w < kRowThreads / 32; ++w) M = max_nan(M, sm[w]);
+  const float Mc = __fmul_rn(M, c);
+  const float t = (!row_bad(M) && acc.m > -INFINITY) ? acc.total() * exp2f(acc.mc - Mc) : 0.f;
+  const float s = warp_sum(t);
+  if ((threadIdx.x & 31) == 0) ss[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float S = 0.f;
+    for (int w = 0; w < kRowThreads / 32; ++w) S += ss[w];
+    if (!row_bad(M)) S *= fmaf(-fmaf(M, c, -Mc), kLn2, 1.f);
+    P.part[static_cast<long long>(r) * P.nslice + sl] = make_float2(M, S);
+  }
+}
+
+constexpr int kMaxSmallK = 8;   // positions per sequence
+constexpr int kMaxSlices = 32;  // vocabulary slices per row, and per draw
+
+// (M, S) of a row from its slices: the largest maximum, and the sum rescaled to it. Warp-wide.
+__device__ __forceinline__ float2 combine_row(const float2* part, int nslice, float c) {
+  const int lane = threadIdx.x & 31;
+  const float2 p = lane < nslice ? part[lane] : make_float2(-INFINITY, 0.f);
+  const float M = warp_max_nan(p.x);
+  const float t = (!row_bad(M) && p.x > -INFINITY) ? p.y * exp2f((p.x - M) * c) : 0.f;
+  return make_float2(M, warp_sum(t));
+}
+
+// The decision of sequence b from the row partials, block-wide (every thread returns it): the
+// accept tests in order; at a rejection the residual draw's constants (fl(M_t c), fl(M_d c) and
+// rho = the ratio of the draft's scale to the target's), after every acceptance the bonus draw
+// from p_L (rho = 0). A sequence is invalid (ok = 0) for a length outside 1..K, an id outside the
+// vocabulary, a uniform outside [0, 1), or a row read before the stop that is NaN, +inf or all
+// -inf.
+template <typename T>
+__device__ SmallDecision decide(const SmallParams& P, int b) {
+  __shared__ float2 s_ms[2 * kMaxSmallK + 1];
+  __shared__ float s_zx[2][kMaxSmallK];
+  __shared__ int s_x[kMaxSmallK];
+  __shared__ float s_u[kMaxSmallK + 1];
+  __shared__ SmallDecision s_dec;
+  const int tid = threadIdx.x, warp = tid >> 5, K = P.K;
+  const int L = P.lens ? P.lens[b] : K;
+  const int32_t* x = P.tokens + static_cast<long long>(b) * K;
+  const float* u = P.uni + static_cast<long long>(b) * (K + 1);
+  const float c = P.c;
+  const bool lok = L >= 1 && L <= K;
+  // the inputs first (no earlier launch writes them): ids, uniforms, the logits at the ids
+  if (tid < K) s_x[tid] = x[tid];
+  if (tid <= K) s_u[tid] = u[tid];
+  if (lok && tid < 2 * L) {
+    const int i = tid < L ? tid : tid - L, d = tid < L ? 0 : 1;
+    const int xi = x[i];
+    s_zx[d][i] = (xi >= 0 && xi < P.V)
+                     ? Elt<T>::val(static_cast<const T*>(
+                           small_row(P, b, d ? K + 1 + i : i, sizeof(T)))[xi])
+                     : 0.f;
+  }
+  pdl_wait();  // the row partials come from the statistics launch
+  if (lok) {
+    for (int r = warp; r < 2 * L + 1; r += blockDim.x >> 5) {  // one warp per row
+      const int slot = r <= L ? r : K + 1 + (r - L - 1);
+      const float2 ms =
+          combine_row(P.part + (static_cast<long long>(b) * (2 * K + 1) + slot) * P.nslice,
+                      P.nslice, c);
+      if ((tid & 31) == 0) s_ms[slot] = ms;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    bool ok = lok;
+    for (int i = 0; ok && i < L; ++i)
+      ok = s_x[i] >= 0 && s_x[i] < P.V && s_u[i] >= 0.f && s_u[i] < 1.f;
+    ok = ok && s_u[K] >= 0.f && s_u[K] < 1.f;
+    SmallDecision d;
+    d.a = L;
+    d.mct = d.mcd = d.rho = 0.f;
+    for (int i = 0; ok && i <= L; ++i) {
+      const float2 t = s_ms[i];
+      if (row_bad(t.x)) {
+        ok = false;
+        break;
+      }
+      if (i == L) {  // every draft accepted: the bonus draw from p_L
+        d.mct = __fmul_rn(t.x, c);
+        break;
+      }
+      const float2 q = s_ms[K + 1 + i];
+      if (row_bad(q.x)) {
+        ok = false;
+        break;
+      }
+      const float zt = s_zx[0][i], zd = s_zx[1][i];
+      float ratio;
+      if (zt == -INFINITY) ratio = 0.f;
+      else if (zd == -INFINITY) ratio = INFINITY;
+      else ratio = exp2f(((zt - zd) - (t.x - q.x)) * c) * (q.y / t.y);
+      if (s_u[i] < ratio) continue;
+      d.a = i;  // the residual draw: rho = q scale / p scale
+      d.mct = __fmul_rn(t.x, c);
+      d.mcd = __fmul_rn(q.x, c);
+      const float ft = fmaf(-fmaf(t.x, c, -d.mct), kLn2, 1.f);
+      const float fd = fmaf(-fmaf(q.x, c, -d.mcd), kLn2, 1.f);
+      d.rho = (fd * t.y) / (ft * q.y);
+      break;
+    }
+    d.ok = ok ? 1 : 0;
+    if (!ok) d.a = -1;
+    s_dec = d;
+  }
+  __syncthreads();
+  return s_dec;
+}
+
+// The draw's weights of 8 elements: w = max(e_t - rho e_d, 0) with e = 2^(z c - fl(M c)), and the
+// sequential float sums of w (residual) and of e_t (p). With rho = 0 both are e_t.
+__device__ __forceinline__ void weights8(const float (&zt)[8], const float (&zd)[8], float c,
+                                         float mc_t, float mc_d, float rho, float (&w)[8],
+                                         float& s_res, float& s_p) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float et = ex2_fast(fmaf(zt[k], c, -mc_t));
+    const float ed = rho != 0.f ? ex2_fast(fmaf(zd[k], c, -mc_d)) : 0.f;
+    w[k] = fmaxf(fmaf(-rho, ed, et), 0.f);
+    s_res = k ? __fadd_rn(s_res, w[k]) : w[0];
+    s_p = k ? __fadd_rn(s_p, et) : et;
+  }
+}
+
+// Vectors (of each of the two rows) a mass thread keeps in flight: 64 bytes of each row.
+template <typename T>
+constexpr int kMassUnroll = 8 / static_cast<int>(sizeof(T));
+
+template <typename T>
+__global__ void __launch_bounds__(kMassThreads) small_mass(const SmallParams P) {
+  pdl_trigger();
+  __shared__ unsigned long long s_r[kMassThreads / 32], s_p[kMassThreads / 32];
+  const int sl = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const SmallDecision d = decide<T>(P, b);
+  if (sl == 0 && tid == 0) P.dec[b] = d;
+  if (!d.ok) return;
+  const int K = P.K;
+  const int L = P.lens ? P.lens[b] : K;
+  const T* gt = static_cast<const T*>(small_row(P, b, d.a, sizeof(T)));
+  const T* gd = d.a < L ? static_cast<const T*>(small_row(P, b, K + 1 + d.a, sizeof(T))) : gt;
+  const bool al = P.aligned != 0;
+  const bool two = d.rho != 0.f;
+  const float c = P.c;
+  const int e0 = sl * P.slice_d, e1 = min(P.V, e0 + P.slice_d);
+  const int nv = (e1 - e0 + 7) >> 3;
+  constexpr int U = kMassUnroll<T>;
+  unsigned long long own_r = 0, own_p = 0;
+  for (int g0 = tid; g0 < nv; g0 += U * kMassThreads) {
+    Raw8<T> vt[U], vd[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int e = e0 + 8 * (g0 + k * kMassThreads);
+      if (al && e + 8 <= e1) {
+        raw_load(gt + e, vt[k]);
+        if (two) raw_load(gd + e, vd[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int g = g0 + k * kMassThreads;
+      if (g >= nv) break;
+      const int e = e0 + 8 * g;
+      float zt[8], zd[8], w[8], sr, sp;
+      if (al && e + 8 <= e1) {
+        raw_unpack(vt[k], zt);
+        if (two) raw_unpack(vd[k], zd);
+      } else {
+        load8_at(gt, e, e1, al, zt);
+        if (two) load8_at(gd, e, e1, al, zd);
+      }
+      weights8(zt, zd, c, d.mct, d.mcd, d.rho, w, sr, sp);
+      own_r += qfix(sr);
+      own_p += qfix(sp);
+    }
+  }
+  own_r = warp_sum_u64(own_r);
+  own_p = warp_sum_u64(own_p);
+  if ((tid & 31) == 0) {
+    s_r[tid >> 5] = own_r;
+    s_p[tid >> 5] = own_p;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long R = 0, Q = 0;
+    for (int w = 0; w < kMassThreads / 32; ++w) {
+      R += s_r[w];
+      Q += s_p[w];
+    }
+    P.mass[(static_cast<long long>(b) * P.nslice_d + sl) * 2] = R;
+    P.mass[(static_cast<long long>(b) * P.nslice_d + sl) * 2 + 1] = Q;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) {
+  __shared__ unsigned long long s_w[kPickThreads / 32];
+  __shared__ int s_slice, s_tok;
+  __shared__ unsigned long long s_tt;
+  __shared__ float s_rho;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const int K = P.K;
+  int32_t* tok = P.out_tok + static_cast<long long>(b) * (K + 1);
+  const int32_t* x = P.tokens + static_cast<long long>(b) * K;
+  // inputs before the wait: the ids this thread may write out, the draw's uniform
+  const int xj = tid < K ? x[tid] : -1;
+  const float uK = P.uni[static_cast<long long>(b) * (K + 1) + K];
+  pdl_wait();  // decisions and slice masses come from the mass launch
+  const SmallDecision d = P.dec[b];
+  unsigned long long mr = 0, mp = 0;  // slice masses, one slice per lane of warp 0
+  if (tid < 32 && lane < P.nslice_d) {
+    const unsigned long long* m = P.mass + (static_cast<long long>(b) * P.nslice_d + lane) * 2;
+    mr = m[0];
+    mp = m[1];
+  }
+  if (!d.ok) {
+    for (int j = tid; j <= K; j += kPickThreads) tok[j] = -1;
+    if (tid == 0) P.out_acc[b] = -1;
+    return;
+  }
+  const int a = d.a;
+  if (tid < 32) {
+    // the slice that holds floor(u W): the residual's masses, or p's when the residual has none
+    const bool use_p = d.rho != 0.f && warp_sum_u64(mr) == 0ull;
+    const unsigned long long own = use_p ? mp : mr;
+    unsigned long long inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const unsigned long long W = __shfl_sync(FULL, inc, 31);
+    const unsigned long long tt = scale_floor(uK, W);
+    const bool here = W > 0 && tt >= inc - own && tt < inc;
+    const unsigned hit = __ballot_sync(FULL, here);
+    if (lane == 0) {
+      s_slice = hit ? __ffs(hit) - 1 : -1;
+      s_rho = use_p ? 0.f : d.rho;
+      s_tok = -1;
+    }
+    if (here) s_tt = tt - (inc - own);
+  }
+  __syncthreads();
+  const int sl = s_slice;
+  if (sl >= 0) {
+    // inside the slice: each thread's run of up to kPickVecs vectors, in id order
+    const int L = P.lens ? P.lens[b] : K;
+    const T* gt = static_cast<const T*>(small_row(P, b, a, sizeof(T)));
+    const T* gd = a < L ? static_cast<const T*>(small_row(P, b, K + 1 + a, sizeof(T))) : gt;
+    const float rho = s_rho, c = P.c;
+    const bool al = P.aligned != 0;
+    const int e0 = sl * P.slice_d, e1 = min(P.V, e0 + P.slice_d);
+    const int nv = (e1 - e0 + 7) >> 3;
+    const int per = (nv + kPickThreads - 1) / kPickThreads;  // <= kPickVecs
+    const int v0 = tid * per;
+    float w[kPickVecs][8];
+    unsigned long long q[kPickVecs];
+    unsigned long long own = 0;
+#pragma unroll
+    for (int j = 0; j < kPickVecs; ++j) {
+      q[j] = 0;
+      if (j < per && v0 + j < nv) {
+        float zt[8], zd[8], sr, sp;
+        load8_at(gt, e0 + 8 * (v0 + j), e1, al, zt);
+        if (rho != 0.f) load8_at(gd, e0 + 8 * (v0 + j), e1, al, zd);
+        weights8(zt, zd, c, d.mct, d.mcd, rho, w[j], sr, sp);
+        q[j] = qfix(sr);
+        own += q[j];
+      }
+    }
+    // block exclusive prefix of the threads' totals (ascending ids)
+    unsigned long long inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) s_w[tid >> 5] = inc;
+    __syncthreads();
+    unsigned long long pre = inc - own;
+    for (int k = 0; k < (tid >> 5); ++k) pre += s_w[k];
+    const unsigned long long tt = s_tt;
+    if (tt >= pre && tt < pre + own) {
+      // the first of the thread's vectors whose end passes tt, then the id inside it
+      int js = 0;
+      unsigned long long ps = pre;
+      bool found = false;
+#pragma unroll
+      for (int j = 0; j < kPickVecs; ++j) {
+        if (!found && pre + q[j] > tt) {
+          js = j;
+          ps = pre;
+          found = true;
+        }
+        pre += q[j];
+      }
+      float ws[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ws[k] = w[0][k];
+#pragma unroll
+        for (int j = 1; j < kPickVecs; ++j) ws[k] = js == j ? w[j][k] : ws[k];
+      }
+      float s = 0.f;
+      int pick = 7;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        s = k ? __fadd_rn(s, ws[k]) : ws[0];
+        if (pick == 7 && ps + qfix(s) > tt) pick = k;
+      }
+      s_tok = e0 + 8 * (v0 + js) + pick;
+    }
+  }
+  __syncthreads();
+  if (tid <= K) tok[tid] = tid < a ? xj : (tid == a ? s_tok : -1);
+  if (tid == 0) P.out_acc[b] = a;
+}
+
+template <typename Kern>
+cudaError_t launch_pdl(Kern kernel, dim3 grid, int threads, cudaStream_t stream,
+                       const SmallParams& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
+template <typename T>
+cudaError_t launch_small_t(const SmallParams& P, cudaStream_t stream) {
+  small_rows<T><<<dim3(static_cast<unsigned>(P.nslice), static_cast<unsigned>(P.B * (2 * P.K + 1))),
+                  kRowThreads, 0, stream>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(small_mass<T>, dim3(static_cast<unsigned>(P.nslice_d), static_cast<unsigned>(P.B)),
+                 kMassThreads, stream, P);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(small_pick<T>, dim3(static_cast<unsigned>(P.B)), kPickThreads, stream, P);
+}
+
+}  // namespace
+
+int small_rows_per_sm(int dtype) {
+  int n = 0;
+  const cudaError_t e =
+      dtype == 1
+          ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, small_rows<uint16_t>, kRowThreads, 0)
+          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, small_rows<float>, kRowThreads, 0);
+  return e == cudaSuccess ? n : 0;
+}
+
+bool small_plan(int B, int K, int V, int sms, int rows_per_sm, SmallParams* P) {
+  if (B <= 0 || K < 1 || K > kMaxSmallK || V < 1 || sms <= 0 || rows_per_sm <= 0) return false;
+  const long long rows = static_cast<long long>(B) * (2 * K + 1);
+  // statistics: about one resident CTA per (row, slice), slices of >= 1024 ids
+  long long ns = (static_cast<long long>(rows_per_sm) * sms) / rows;
+  ns = std::max<long long>(1, std::min<long long>({ns, (V + 1023) / 1024, kMaxSlices}));
+  const long long sl = ((V + ns - 1) / ns + 7) / 8 * 8;
+  // the draw: about 4 CTAs per multiprocessor, slices of <= kPickThreads * kPickVecs * 8 ids
+  const long long cap = static_cast<long long>(kPickThreads) * kPickVecs * 8;
+  long long nd = (4LL * sms + B - 1) / B;
+  nd = std::max<long long>({1, (V + cap - 1) / cap,
+                            std::min<long long>({nd, (V + 1023) / 1024, kMaxSlices})});
+  if (nd > kMaxSlices) return false;
+  const long long sd = ((V + nd - 1) / nd + 7) / 8 * 8;
+  if (sd > cap) return false;
+  P->B = B;
+  P->K = K;
+  P->slice = static_cast<int>(sl);
+  P->nslice = static_cast<int>((V + sl - 1) / sl);
+  P->slice_d = static_cast<int>(sd);
+  P->nslice_d = static_cast<int>((V + sd - 1) / sd);
+  return true;
+}
+
+cudaError_t launch_small(const SmallParams& P, int dtype, cudaStream_t stream) {
+  return dtype == 1 ? launch_small_t<uint16_t>(P, stream) : launch_small_t<float>(P, stream);
+}
+
+}  // namespace sv

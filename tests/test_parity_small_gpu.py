@@ -1,0 +1,147 @@
+"""GPU parity of stochastic verification for small batches (every row a sequence has read at
+once: row statistics, the draw's slice masses, one pick per sequence), against the float64
+oracle. The library takes that route for a stochastic batch without a bias set or top-F ids
+whose padded rows fit in 168 MiB, when the caller leaves the cluster size to it
+(cluster_hint 0) and asks for no diagnostics; each case here also runs the chained cluster walk
+(cluster_hint 4) on the same inputs, so both routes face the same bar."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from speculative_decoding_verification_33_gb300 import _lib  # noqa: E402
+from speculative_decoding_verification_33_gb300 import workloads as W  # noqa: E402
+from tests.test_parity_gpu import check, oracle, run_gpu  # noqa: E402
+
+
+def both_paths(d, w, **kw):
+    reps = []
+    for hint in (0, 4):
+        g = run_gpu(d, w, cluster_hint=hint, debug=False, **kw)
+        reps.append((check(d, w, g), g))
+    return reps
+
+
+def route_of(w, hint=0):
+    prob, _keep = _lib.make_problem(w.B, w.K, w.V, _lib.SV_DTYPE_BF16 if w.dtype == "bf16"
+                                    else _lib.SV_DTYPE_F32, w.V, w.V, w.bias_k, w.fanout,
+                                    cluster_hint=hint)
+    return _lib.route(prob, _lib.SV_MODE_GREEDY if w.mode == "greedy"
+                      else _lib.SV_MODE_STOCHASTIC)
+
+
+def test_routes_of_the_workloads():
+    R = _lib
+    assert route_of(W.WORKLOADS[1]) == (R.SV_ROUTE_SMALL, 3)
+    assert route_of(W.WORKLOADS[2]) == (R.SV_ROUTE_GREEDY_ROWS, 2)
+    assert route_of(W.WORKLOADS[3]) == (R.SV_ROUTE_WALK, 1)             # 180 MB of rows
+    assert route_of(W.small_variant(W.WORKLOADS[3], B=32)) == (R.SV_ROUTE_SMALL, 3)
+    assert route_of(W.WORKLOADS[4]) == (R.SV_ROUTE_WALK, 2)             # top-8 prepass
+    assert route_of(W.WORKLOADS[5]) == (R.SV_ROUTE_WALK, 1)
+    assert route_of(W.WORKLOADS[1], hint=4) == (R.SV_ROUTE_WALK, 1)
+
+
+@pytest.mark.parametrize("w", [W.WORKLOADS[1], W.small_variant(W.WORKLOADS[3], B=32),
+                               W.small_variant(W.WORKLOADS[5], B=24)],
+                         ids=["B1_K4_V32000_f32", "B32_K5_V128256_bf16", "B24_K8_V152064_ragged"])
+def test_small_path_workloads(w):
+    assert route_of(w)[0] == _lib.SV_ROUTE_SMALL
+    d = W.make_inputs(w)
+    (rep, g), (_, g4) = both_paths(d, w)
+    print(w.name, rep.summary())
+    assert (g["accept_len"] >= 0).all()
+
+
+@pytest.mark.parametrize("B,K,V,dtype", [
+    (1, 1, 7, "f32"),          # one partial vector per row
+    (3, 8, 50001, "bf16"),     # K at its maximum, a ragged last vector
+    (17, 3, 4099, "f32"),
+    (2, 5, 200000, "bf16"),    # 32 draw slices
+    (40, 6, 10000, "bf16"),
+])
+def test_small_path_shapes(B, K, V, dtype):
+    base = W.WORKLOADS[3] if dtype == "bf16" else W.WORKLOADS[1]
+    w = W.small_variant(base, B=B, V=V).replace(K=K, ragged=True)
+    d = W.make_inputs(w)
+    both_paths(d, w)
+
+
+def test_small_path_unaligned_rows():
+    """Row stride V + 1: no 16-byte vectors, every element loaded on its own."""
+    w = W.small_variant(W.WORKLOADS[3], B=5, V=3001)
+    d = W.make_inputs(w)
+    both_paths(d, w, stride_pad=1)
+
+
+def test_small_path_bonus_draws():
+    """u = 0 accepts every draft with p(x) > 0: the draw is from p_L."""
+    w = W.small_variant(W.WORKLOADS[3], B=9, V=6000).replace(ragged=True)
+    d = W.make_inputs(w)
+    d["uniforms"][:, : w.K] = 0.0
+    for rep, g in both_paths(d, w):
+        assert (g["accept_len"] == d["draft_lens"]).all()
+
+
+def test_small_path_invalid_sequences():
+    w = W.small_variant(W.WORKLOADS[3], B=8, V=600)
+    d = W.make_inputs(w)
+    d["draft_lens"][0] = 0                    # length out of range
+    d["draft_lens"][7] = w.K + 1
+    d["draft_tokens"][1, 2] = w.V             # draft id out of range
+    d["uniforms"][2, w.K] = 1.0               # final uniform out of range
+    d["target"][3, 0, 17] = W.BF16_NAN        # NaN in a needed row
+    d["draft"][4, 0, :] = 0xFF80              # draft row of -inf only
+    d["target"][5, 0, 5] = 0x7F80             # +inf
+    d["target"][6, 0, 3] = 0xFF80             # a single -inf is legal
+    for rep, g in both_paths(d, w):
+        assert (g["accept_len"][[0, 1, 2, 3, 4, 5, 7]] == -1).all()
+        assert (g["tokens"][[0, 1, 2, 3, 4, 5, 7]] == -1).all()
+        assert g["accept_len"][6] >= 0
+
+
+def test_small_path_nan_after_the_stop():
+    """Rows after the decided position hold NaN: the statistics read them, the decision must
+    not."""
+    w = W.small_variant(W.WORKLOADS[3], B=6, V=700)
+    d = W.make_inputs(w)
+    res = oracle(d, w, all_rows=False)
+    for b, r in enumerate(res):
+        a = r.accept_len
+        if a < w.K:
+            d["target"][b, a + 1:] = W.BF16_NAN
+            d["draft"][b, a + 1:] = W.BF16_NAN
+    for rep, g in both_paths(d, w):
+        assert (g["accept_len"] >= 0).all()
+
+
+def test_small_path_zero_draft_probability_and_ties():
+    V, K, B = 64, 3, 4
+    w = W.Workload(0, "crafted", B=B, K=K, V=V, dtype="f32", mode="stochastic",
+                   temperature=1.0, sigma_t=1, sigma_d=1, zipf=False)
+    rng = np.random.default_rng(0)
+    tgt = rng.integers(-2, 2, (B, K + 1, V)).astype(np.float32)   # many ties
+    dft = rng.integers(-2, 2, (B, K, V)).astype(np.float32)
+    dft[0, 0, 5] = -np.inf                                          # q(x) = 0 < p(x)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    tok[0, 0] = 5
+    d = {"target": tgt, "draft": dft, "draft_tokens": tok,
+         "draft_lens": np.full(B, K, np.int32),
+         "uniforms": rng.random((B, K + 1), dtype=np.float32)}
+    both_paths(d, w)
+
+
+def test_small_path_repeated_calls_agree():
+    """The workspace's partials, decisions and masses are rewritten each call: repeated calls
+    (and a call of another shape in between) give the same outcome."""
+    w = W.small_variant(W.WORKLOADS[3], B=12, V=9000).replace(ragged=True)
+    d = W.make_inputs(w)
+    g1 = run_gpu(d, w, debug=False)
+    w2 = W.small_variant(W.WORKLOADS[1], B=3, V=1000)
+    run_gpu(W.make_inputs(w2), w2, debug=False)
+    g2 = run_gpu(d, w, debug=False)
+    assert (g1["accept_len"] == g2["accept_len"]).all()
+    assert (g1["tokens"] == g2["tokens"]).all()

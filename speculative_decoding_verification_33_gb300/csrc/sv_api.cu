@@ -240,7 +240,7 @@ sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L,
 // row a sequence has at once when that costs less than the walk's latency of position after
 // position: greedy batches whose padded target rows fit in 16 MB (argmax per row slice, then one
 // warp per sequence), and stochastic batches without a bias set or top-F ids whose rows fit in
-// 168 MiB (row statistics, the draw's slice masses, one pick per sequence). A nonzero
+// 256 MiB (row statistics, the draw's slice masses, one pick per sequence). A nonzero
 // cluster_hint, the diagnostics entry point and rows read in place from host memory always take
 // the walk.
 enum Route { ROUTE_WALK = 0, ROUTE_GREEDY_ROWS = 1, ROUTE_SMALL = 2 };
@@ -266,7 +266,7 @@ Route route_of(const sv_problem* p, const Checked& c, int dev, int sms, int bias
                : ROUTE_WALK;
   if (zero_copy || bias_k != 0 || B * (2 * K + 1) > 65535 ||
       B * (2 * K + 1) * std::max(p->target_row_stride, p->draft_row_stride) * c.elt >
-          (168LL << 20))
+          (256LL << 20))
     return ROUTE_WALK;
   const int dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
   return sv::small_plan(p->B, p->K, p->V, sms, small_rows_per_sm(dev, dtype), sp) ? ROUTE_SMALL

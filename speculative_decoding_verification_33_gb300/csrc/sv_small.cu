@@ -92,7 +92,67 @@ __device__ __forceinline__ void load8_at(const T* row, int e, int V, bool aligne
   }
 }
 
-constexpr int kStages = 4;                      // bulk-copy ring of the row kernel
+// One thread's vectors of a staged chunk of n ids (vectors tid, tid + kRowThreads, ...), -inf
+// past n: their maximum (NaN sticks) and the values.
+template <typename T, int VPT>
+struct Staged;
+
+template <int VPT>
+struct Staged<uint16_t, VPT> {
+  static constexpr int kVecs = VPT;
+  uint4 v[VPT];
+  __device__ __forceinline__ void load(const uint16_t* s, int n) {  // n: a multiple of 8
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int g = threadIdx.x + j * kRowThreads;
+      v[j] = 8 * g + 8 <= n ? reinterpret_cast<const uint4*>(s)[g]
+                            : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+  }
+  __device__ __forceinline__ float vmax() const {
+    uint32_t m = max_nan_bf16x2(max_nan_bf16x2(v[0].x, v[0].y), max_nan_bf16x2(v[0].z, v[0].w));
+#pragma unroll
+    for (int j = 1; j < VPT; ++j)
+      m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(v[j].x, v[j].y),
+                                           max_nan_bf16x2(v[j].z, v[j].w)));
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
+  __device__ __forceinline__ void get(int j, float (&z)[8]) const {
+    Elt<uint16_t>::unpack(v[j], z);
+  }
+};
+
+template <int VPT>
+struct Staged<float, VPT> {
+  static constexpr int kVecs = VPT;
+  float z[VPT][8];
+  __device__ __forceinline__ void load(const float* s, int n) {  // n: a multiple of 4
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int g = threadIdx.x + j * kRowThreads;
+      const float4 a = 8 * g + 4 <= n ? reinterpret_cast<const float4*>(s)[2 * g]
+                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      const float4 b = 8 * g + 8 <= n ? reinterpret_cast<const float4*>(s)[2 * g + 1]
+                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      z[j][0] = a.x; z[j][1] = a.y; z[j][2] = a.z; z[j][3] = a.w;
+      z[j][4] = b.x; z[j][5] = b.y; z[j][6] = b.z; z[j][7] = b.w;
+    }
+  }
+  __device__ __forceinline__ float vmax() const {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m = max_nan(m, z[j][k]);
+    return m;
+  }
+  __device__ __forceinline__ void get(int j, float (&out)[8]) const {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) out[k] = z[j][k];
+  }
+};
+
+constexpr int kStages = 2;                      // bulk-copy ring of the row kernel
 constexpr int kChunk = 8192;                    // bytes per stage
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per barrier wait
 
@@ -141,17 +201,17 @@ __device__ bool rows_bulk(const T* row, int e0, int e1, float c, RowAcc& acc) {
       ok = false;
       break;
     }
-    const T* sp = reinterpret_cast<const T*>(ring[s]);
-    const int n = min(per, eb - (e0 + j * per));
-    for (int v = tid; 8 * v < n; v += kRowThreads) {
-      float z[8];
-      if (8 * v + 8 <= n) {
-        Elt<T>::load8(sp, v, z);
-      } else {
+    // the thread's vectors of the chunk: their maximum first, one rescale, then the sums
+    Staged<T, kChunk / static_cast<int>(sizeof(T)) / 8 / kRowThreads> st;
+    st.load(reinterpret_cast<const T*>(ring[s]), min(per, eb - (e0 + j * per)));
+    acc.rescale(st.vmax(), c);
+    if (acc.m > -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) z[k] = 8 * v + k < n ? Elt<T>::val(sp[8 * v + k]) : -INFINITY;
+      for (int v = 0; v < st.kVecs; ++v) {
+        float z[8];
+        st.get(v, z);
+        acc.sum8(z, c);
       }
-      fold8(acc, z, c);
     }
     __syncthreads();  // every thread is done with stage s before it is refilled
     if (tid == 0 && j + kStages < nch) issue(j + kStages);
@@ -349,7 +409,7 @@ template <typename T>
 constexpr int kMassUnroll = 8 / static_cast<int>(sizeof(T));
 
 template <typename T>
-__global__ void __launch_bounds__(kMassThreads) small_mass(const SmallParams P) {
+__global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams P) {
   pdl_trigger();
   __shared__ unsigned long long s_r[kMassThreads / 32], s_p[kMassThreads / 32];
   const int sl = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;

@@ -1,7 +1,7 @@
 """GPU parity of stochastic verification for small batches (every row a sequence has read at
 once: row statistics, the draw's slice masses, one pick per sequence), against the float64
 oracle. The library takes that route for a stochastic batch without a bias set or top-F ids
-whose padded rows fit in 168 MiB, when the caller leaves the cluster size to it
+whose padded rows fit in 256 MiB, when the caller leaves the cluster size to it
 (cluster_hint 0) and asks for no diagnostics; each case here also runs the chained cluster walk
 (cluster_hint 4) on the same inputs, so both routes face the same bar."""
 import numpy as np
@@ -38,16 +38,16 @@ def test_routes_of_the_workloads():
     R = _lib
     assert route_of(W.WORKLOADS[1]) == (R.SV_ROUTE_SMALL, 3)
     assert route_of(W.WORKLOADS[2]) == (R.SV_ROUTE_GREEDY_ROWS, 2)
-    assert route_of(W.WORKLOADS[3]) == (R.SV_ROUTE_WALK, 1)             # 180 MB of rows
-    assert route_of(W.small_variant(W.WORKLOADS[3], B=32)) == (R.SV_ROUTE_SMALL, 3)
+    assert route_of(W.WORKLOADS[3]) == (R.SV_ROUTE_SMALL, 3)            # 181 MB of rows
+    assert route_of(W.small_variant(W.WORKLOADS[3], B=96)) == (R.SV_ROUTE_WALK, 1)  # 271 MB
     assert route_of(W.WORKLOADS[4]) == (R.SV_ROUTE_WALK, 2)             # top-8 prepass
     assert route_of(W.WORKLOADS[5]) == (R.SV_ROUTE_WALK, 1)
     assert route_of(W.WORKLOADS[1], hint=4) == (R.SV_ROUTE_WALK, 1)
 
 
-@pytest.mark.parametrize("w", [W.WORKLOADS[1], W.small_variant(W.WORKLOADS[3], B=32),
+@pytest.mark.parametrize("w", [W.WORKLOADS[1], W.WORKLOADS[3],
                                W.small_variant(W.WORKLOADS[5], B=24)],
-                         ids=["B1_K4_V32000_f32", "B32_K5_V128256_bf16", "B24_K8_V152064_ragged"])
+                         ids=["B1_K4_V32000_f32", "B64_K5_V128256_bf16", "B24_K8_V152064_ragged"])
 def test_small_path_workloads(w):
     assert route_of(w)[0] == _lib.SV_ROUTE_SMALL
     d = W.make_inputs(w)

@@ -126,7 +126,7 @@ sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* 
  * Which kernels spec_verify takes for this problem on the current device (*route) and how many
  * launches one call makes (*launches). Routes: SV_ROUTE_WALK, the chained cluster walk (one
  * launch, two with the top-8 prepass over the draft rows for a bias set or top-F ids);
- * SV_ROUTE_GREEDY_ROWS, greedy batches whose padded target rows fit in 16 MB (an argmax per row
+ * SV_ROUTE_GREEDY_ROWS, greedy batches whose padded target rows fit in 64 MiB (an argmax per row
  * slice of every target row, then one warp per sequence: two launches); SV_ROUTE_SMALL,
  * stochastic batches without a bias set or top-F ids whose rows fit in 256 MiB (every row's
  * statistics, the draw's slice masses, one pick per sequence: three launches). A nonzero

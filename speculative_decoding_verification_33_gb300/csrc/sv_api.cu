@@ -238,7 +238,7 @@ sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L,
 
 // The kernels a call takes. The chained cluster walk serves every problem; two paths read every
 // row a sequence has at once when that costs less than the walk's latency of position after
-// position: greedy batches whose padded target rows fit in 16 MB (argmax per row slice, then one
+// position: greedy batches whose padded target rows fit in 64 MiB (argmax per row slice, then one
 // warp per sequence), and stochastic batches without a bias set or top-F ids whose rows fit in
 // 256 MiB (row statistics, the draw's slice masses, one pick per sequence). A nonzero
 // cluster_hint, the diagnostics entry point and rows read in place from host memory always take
@@ -261,7 +261,7 @@ Route route_of(const sv_problem* p, const Checked& c, int dev, int sms, int bias
   if (debug_all || p->cluster_hint != 0 || c.fmax != 0 || sms <= 0) return ROUTE_WALK;
   const long long B = p->B, K = p->K;
   if (c.greedy)
-    return (B * (K + 1) <= 65535 && B * (K + 1) * p->target_row_stride * c.elt <= (16LL << 20))
+    return (B * (K + 1) <= 65535 && B * (K + 1) * p->target_row_stride * c.elt <= (64LL << 20))
                ? ROUTE_GREEDY_ROWS
                : ROUTE_WALK;
   if (zero_copy || bias_k != 0 || B * (2 * K + 1) > 65535 ||

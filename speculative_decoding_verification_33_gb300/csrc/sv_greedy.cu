@@ -30,8 +30,16 @@ constexpr int kThreads = 256;
 constexpr unsigned long long kBad = ~0ull;  // a slice with a NaN or +inf
 constexpr int kMaxGreedyK = 8;              // positions per sequence (K <= 8)
 
+// Programmatic dependent launch: let the next launch on the stream start its CTAs, and wait
+// until the previous launch has finished and its writes are visible.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) greedy_rows(const GreedyParams P) {
+  pdl_trigger();
   __shared__ unsigned long long wk[kThreads / 32];
   const int sl = blockIdx.x, r = blockIdx.y;
   const int b = r / (P.K + 1), i = r - b * (P.K + 1);
@@ -84,6 +92,7 @@ __global__ void greedy_decide(const GreedyParams P) {
   const int xi = (ok && lane < L) ? x[lane] : 0;
   ok = ok && __all_sync(FULL, lane >= L || (xi >= 0 && xi < P.V));
   int a = -1, last = -1;
+  pdl_wait();  // the slice keys come from the row launch (the ids and lengths are inputs)
   if (ok) {
     // every slice key of rows 0..L in one round of loads, folded per row in shared memory
     if (lane <= L) pm[wib][lane] = 0ull;
@@ -129,8 +138,16 @@ cudaError_t launch_greedy(const GreedyParams& P, int dtype, cudaStream_t stream)
     greedy_rows<float><<<grid, kThreads, 0, stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  greedy_decide<<<(P.B + 3) / 4, 128, 0, stream>>>(P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((P.B + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, greedy_decide, P);
 }
 
 }  // namespace sv

@@ -391,6 +391,7 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
   enum { STATS = 0, DRAW = 1, POST = 2 };
   int q_ep = 0, q_seq = S.seq0, q_L = load_len(P, S.seq0);
   int q_ph = STATS, q_pos = 0, q_k = 0;
+  int q_mark = -1;  // greedy: the stop whose marker stage is still to be issued
   Cursor cur;
   int base_seq = -1, base_pos = -1;
   const char* src_t = nullptr;
@@ -416,19 +417,40 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
       q_ph = STATS;
       q_pos = 0;
       q_k = 0;
+      q_mark = -1;  // nobody waits on the earlier sequence any more
     }
     int rows = 0;
     bool exhausted = q_seq >= P.B;
     if (!exhausted && lag >= 0) {  // the consumers' current sequence
       const int stop = pub.stop;
+      if (stop != -1 && q_ph == STATS) {
+        if (stop == -2) {  // an invalid sequence: nothing more to stream
+          q_ph = POST;
+          q_pos = P.K + 1;
+          q_mark = 0;
+        } else {  // the decision has landed
+          q_ph = GREEDY ? POST : DRAW;
+          q_pos = GREEDY ? stop + 1 : stop;
+          if (GREEDY) q_mark = stop;
+        }
+        q_k = 0;
+      }
+      if (q_mark >= 0) {
+        // Without a draw pass (a greedy stop, an invalid sequence) no chunk would tell the
+        // consumers still waiting on a chunk of the position being streamed that the producer
+        // has moved on: one stage without data, tagged like a draw chunk, does (consumers that
+        // are not waiting hand it back).
+        if (cur.n >= NS && !mbar_try_wait_hint(&R.empty[cur.s], cur.ph ^ 1u, 1000)) continue;
+        R.desc[cur.s] = stage_tag(q_seq, q_ep, -1 - q_mark, 0);
+        mbar_arrive(&R.full[cur.s]);
+        cur.advance();
+        q_mark = -1;
+        idle0 = clock64();
+        continue;
+      }
       if (stop == -2) {
         exhausted = true;
       } else {
-        if (stop >= 0 && q_ph == STATS) {  // the decision has landed
-          q_ph = GREEDY ? POST : DRAW;
-          q_pos = GREEDY ? stop + 1 : stop;
-          q_k = 0;
-        }
         if (q_ph == STATS) {
           if (q_pos <= q_L) rows = (!GREEDY && q_pos < q_L) ? (ROW_T | ROW_D) : ROW_T;
         } else if (q_ph == DRAW) {

@@ -152,6 +152,45 @@ def test_invalid_sequences():
     assert g["accept_len"][6] >= 0
 
 
+@pytest.mark.parametrize("cluster", [4, 8])
+def test_greedy_walk_long_rows(cluster):
+    """Greedy rows of 152064 ids take several ring chunks per CTA, and with 8 sequences no
+    cluster has a second one: a stop that lands while the next position streams must still end
+    the sequence (the producer marks the stage after a stop) instead of leaving the consumers
+    waiting for chunks that will not come."""
+    w = W.small_variant(W.WORKLOADS[5], B=8).replace(mode="greedy", temperature=0.0)
+    d = W.make_inputs(w)
+    g = run_gpu(d, w, cluster_hint=cluster, debug=False)
+    assert api.device_error() == 0
+    check(d, w, g)
+    assert (g["accept_len"] >= 0).all()
+
+
+def test_invalid_row_mid_walk_long_rows():
+    """A NaN in the second position's target row, read after the first draft is accepted, makes
+    the sequence invalid while the third position streams; with one sequence per cluster and
+    rows of several chunks the walk must end it without waiting out its bounded waits."""
+    w = W.small_variant(W.WORKLOADS[5], B=6).replace(ragged=False)
+    d = W.make_inputs(w)
+    d["uniforms"][:, 0] = 0.0                  # u = 0 accepts the first draft when p(x) > 0
+    d["target"][:, 1, 17] = W.BF16_NAN
+    for cluster in (4, 8):
+        g = run_gpu(d, w, cluster_hint=cluster, debug=False)
+        assert api.device_error() == 0
+        check(d, w, g)
+        assert (g["accept_len"] == -1).all()
+
+
+def test_greedy_walk_many_short_sequences():
+    """Many greedy sequences of one chunk per position on the walk: a stop's marker stage
+    that the consumers no longer wait for is dropped when they move to the next sequence."""
+    w = W.small_variant(W.WORKLOADS[2], B=256)
+    d = W.make_inputs(w)
+    g = run_gpu(d, w, cluster_hint=4, debug=False)
+    assert api.device_error() == 0
+    check(d, w, g)
+
+
 def test_nan_after_rejection_is_not_read():
     w = W.small_variant(W.WORKLOADS[3], B=6, V=700)
     d = W.make_inputs(w)

@@ -128,8 +128,8 @@ sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* 
  * launch, two with the top-8 prepass over the draft rows for a bias set or top-F ids);
  * SV_ROUTE_GREEDY_ROWS, greedy batches whose padded target rows fit in 64 MiB (an argmax per row
  * slice of every target row, then one warp per sequence: two launches); SV_ROUTE_SMALL,
- * stochastic batches without a bias set or top-F ids whose rows fit in 256 MiB (every row's
- * statistics, the draw's slice masses, one pick per sequence: three launches). A nonzero
+ * stochastic batches whose padded rows fit in 256 MiB (every row's statistics, the draw's slice
+ * masses, one pick per sequence: three launches, four with the top-8 prepass). A nonzero
  * cluster_hint always walks. spec_verify_ws takes the walk as well when its workspace has no
  * room for the other routes' partials. Host-side query; either output may be NULL; the same
  * errors as spec_verify_plan.

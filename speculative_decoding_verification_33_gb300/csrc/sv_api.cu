@@ -239,10 +239,10 @@ sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L,
 // The kernels a call takes. The chained cluster walk serves every problem; two paths read every
 // row a sequence has at once when that costs less than the walk's latency of position after
 // position: greedy batches whose padded target rows fit in 64 MiB (argmax per row slice, then one
-// warp per sequence), and stochastic batches without a bias set or top-F ids whose rows fit in
-// 256 MiB (row statistics, the draw's slice masses, one pick per sequence). A nonzero
-// cluster_hint, the diagnostics entry point and rows read in place from host memory always take
-// the walk.
+// warp per sequence), and stochastic batches whose rows fit in 256 MiB (row statistics, the
+// draw's slice masses, one pick per sequence; after the top-8 prepass for a bias set or top-F
+// ids). A nonzero cluster_hint, the diagnostics entry point and rows read in place from host
+// memory always take the walk.
 enum Route { ROUTE_WALK = 0, ROUTE_GREEDY_ROWS = 1, ROUTE_SMALL = 2 };
 
 // Row-statistics CTAs of the small-batch route resident per multiprocessor (cached per device
@@ -256,21 +256,55 @@ int small_rows_per_sm(int dev, int dtype) {
   return n;
 }
 
-Route route_of(const sv_problem* p, const Checked& c, int dev, int sms, int bias_k,
-               bool debug_all, bool zero_copy, sv::SmallParams* sp) {
-  if (debug_all || p->cluster_hint != 0 || c.fmax != 0 || sms <= 0) return ROUTE_WALK;
+Route route_of(const sv_problem* p, const Checked& c, int dev, int sms, bool debug_all,
+               bool zero_copy, sv::SmallParams* sp) {
+  if (debug_all || p->cluster_hint != 0 || sms <= 0) return ROUTE_WALK;
   const long long B = p->B, K = p->K;
   if (c.greedy)
     return (B * (K + 1) <= 65535 && B * (K + 1) * p->target_row_stride * c.elt <= (64LL << 20))
                ? ROUTE_GREEDY_ROWS
                : ROUTE_WALK;
-  if (zero_copy || bias_k != 0 || B * (2 * K + 1) > 65535 ||
+  if (zero_copy || B * (2 * K + 1) > 65535 ||
       B * (2 * K + 1) * std::max(p->target_row_stride, p->draft_row_stride) * c.elt >
           (256LL << 20))
     return ROUTE_WALK;
   const int dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
   return sv::small_plan(p->B, p->K, p->V, sms, small_rows_per_sm(dev, dtype), sp) ? ROUTE_SMALL
                                                                                 : ROUTE_WALK;
+}
+
+// The top-8 prepass over the draft rows (bias set, top-F ids): 8 keys per draft row into `keys`,
+// and the top-F ids of the rows below L into out_topf.
+sv_status launch_prepass(const sv_problem* p, const Checked& c, int dev, int dtype,
+                         const void* dft, const int32_t* lens, float cc,
+                         unsigned long long* keys, int32_t* out_topf, Workspace* ws,
+                         cudaStream_t stream) {
+  sv::RowParams R;
+  memset(&R, 0, sizeof(R));
+  R.dft = dft;
+  R.d_stride = p->draft_row_stride;
+  R.V = p->V;
+  R.K = p->K;
+  R.B = p->B;
+  R.lens = lens;
+  R.c = cc;
+  R.fmax = c.fmax;
+  for (int i = 0; i < sv::kMaxK; ++i) R.fan[i] = c.fan[i];
+  R.use_vec = (reinterpret_cast<uintptr_t>(dft) % 16 == 0 &&
+               (p->draft_row_stride * static_cast<long long>(c.elt)) % 16 == 0)
+                  ? 1
+                  : 0;
+  R.out_keys = keys;
+  R.out_topf = c.fmax > 0 ? out_topf : nullptr;
+  R.ws = ws;
+  const std::pair<int, int> rc = row_config(dev, 2, dtype, false, p->V);
+  if (rc.first < 2 || rc.second < 1) return SV_ERR_UNSUPPORTED;
+  R.nstages = rc.first;
+  const int units = p->B * p->K;
+  const int ctas = std::min(units, rc.second * sm_count(dev));
+  return sv::launch_rows(R, 2, dtype, ctas, nullptr, nullptr, nullptr, stream) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
 }
 
 sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32_t* tok,
@@ -325,7 +359,7 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   Route route;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    route = route_of(p, c, dev, sm_count(dev), P.bias_k, debug_all != 0, zero_copy, &G2);
+    route = route_of(p, c, dev, sm_count(dev), debug_all != 0, zero_copy, &G2);
   }
   // Greedy verification of a small batch: every target row in flight at once, argmax per row
   // slice, then one warp per sequence walks the positions.
@@ -381,7 +415,10 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
     G.aligned = aligned ? 1 : 0;
     G.out_acc = out_acc;
     G.out_tok = out_tok;
-    const size_t need = sv::small_ws_bytes(G);
+    // a bias set or top-F ids: the top-8 prepass's keys first in the workspace
+    const bool top8 = needs_top8(p, c);
+    const size_t kb = top8 ? (keys_bytes(p) + 255) / 256 * 256 : 0;
+    const size_t need = kb + sv::small_ws_bytes(G);
     Workspace* w = nullptr;
     if (ws_user) {
       if (ws_user_bytes >= sizeof(Workspace) + need) w = ws_user;
@@ -391,11 +428,20 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
       w = r->ws;
     }
     if (w) {  // (a caller's workspace too small for the partials takes the cluster walk)
-      sv::small_carve(G, reinterpret_cast<char*>(w + 1));
+      const int dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
+      sv::small_carve(G, reinterpret_cast<char*>(w + 1) + kb);
       G.err = &w->error;
-      return sv::launch_small(G, p->dtype == SV_DTYPE_BF16 ? 1 : 0, stream) == cudaSuccess
-                 ? SV_OK
-                 : SV_ERR_CUDA;
+      G.bias_k = P.bias_k;
+      G.beta = P.beta;
+      G.fmax = c.fmax;
+      G.out_topf = c.fmax > 0 ? out_topf : nullptr;
+      if (top8) {
+        unsigned long long* keys = reinterpret_cast<unsigned long long*>(w + 1);
+        G.keys = keys;
+        st = launch_prepass(p, c, dev, dtype, dft, lens, P.c, keys, out_topf, w, stream);
+        if (st != SV_OK) return st;
+      }
+      return sv::launch_small(G, dtype, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
   }
 
@@ -441,31 +487,8 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
   if (prepass) {
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(P.ws + 1);
     P.keys = keys;
-    sv::RowParams R;
-    memset(&R, 0, sizeof(R));
-    R.dft = dft;
-    R.d_stride = p->draft_row_stride;
-    R.V = p->V;
-    R.K = p->K;
-    R.B = p->B;
-    R.lens = lens;
-    R.c = P.c;
-    R.fmax = c.fmax;
-    for (int i = 0; i < sv::kMaxK; ++i) R.fan[i] = c.fan[i];
-    R.use_vec = (reinterpret_cast<uintptr_t>(dft) % 16 == 0 &&
-                 (p->draft_row_stride * static_cast<long long>(c.elt)) % 16 == 0)
-                    ? 1
-                    : 0;
-    R.out_keys = keys;
-    R.out_topf = c.fmax > 0 ? out_topf : nullptr;
-    R.ws = P.ws;
-    const std::pair<int, int> rc = row_config(dev, 2, L.dtype, false, p->V);
-    if (rc.first < 2 || rc.second < 1) return SV_ERR_UNSUPPORTED;
-    R.nstages = rc.first;
-    const int units = p->B * p->K;
-    const int ctas = std::min(units, rc.second * sm_count(dev));
-    if (sv::launch_rows(R, 2, L.dtype, ctas, nullptr, nullptr, nullptr, stream) != cudaSuccess)
-      return SV_ERR_CUDA;
+    st = launch_prepass(p, c, dev, L.dtype, dft, lens, P.c, keys, out_topf, P.ws, stream);
+    if (st != SV_OK) return st;
   }
   return sv::launch(L, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -525,11 +548,12 @@ sv_status spec_verify_route(const sv_problem* prob, int mode, int* route, int* l
     std::lock_guard<std::mutex> lock(g_mu);
     const int sms = sm_count(dev);
     if (sms <= 0) return SV_ERR_CUDA;
-    r = route_of(prob, c, dev, sms, c.greedy ? 0 : prob->bias_k, false, false, &sp);
+    r = route_of(prob, c, dev, sms, false, false, &sp);
   }
   if (route) *route = static_cast<int>(r);
   if (launches)
-    *launches = r == ROUTE_SMALL ? 3 : (r == ROUTE_GREEDY_ROWS || needs_top8(prob, c)) ? 2 : 1;
+    *launches = r == ROUTE_SMALL ? 3 + (needs_top8(prob, c) ? 1 : 0)
+                                 : (r == ROUTE_GREEDY_ROWS || needs_top8(prob, c)) ? 2 : 1;
   return SV_OK;
 }
 

@@ -315,6 +315,7 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
   __shared__ float s_zx[2][kMaxSmallK];
   __shared__ int s_x[kMaxSmallK];
   __shared__ float s_u[kMaxSmallK + 1];
+  __shared__ unsigned long long s_key[kMaxSmallK][8];
   __shared__ SmallDecision s_dec;
   const int tid = threadIdx.x, warp = tid >> 5, K = P.K;
   const int L = P.lens ? P.lens[b] : K;
@@ -333,6 +334,9 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
                            small_row(P, b, d ? K + 1 + i : i, sizeof(T)))[xi])
                      : 0.f;
   }
+  const bool bias = P.bias_k > 0 && P.keys != nullptr;
+  if (bias && lok && tid < 8 * L)  // the draft rows' top 8, written by the prepass launch
+    s_key[tid >> 3][tid & 7] = P.keys[(static_cast<long long>(b) * K + (tid >> 3)) * 8 + (tid & 7)];
   pdl_wait();  // the row partials come from the statistics launch
   if (lok) {
     for (int r = warp; r < 2 * L + 1; r += blockDim.x >> 5) {  // one warp per row
@@ -351,7 +355,8 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
     ok = ok && s_u[K] >= 0.f && s_u[K] < 1.f;
     SmallDecision d;
     d.a = L;
-    d.mct = d.mcd = d.rho = 0.f;
+    d.mct = d.mcd = d.rho = d.rho_s = 0.f;
+    d.nS = 0;
     for (int i = 0; ok && i <= L; ++i) {
       const float2 t = s_ms[i];
       if (row_bad(t.x)) {
@@ -367,18 +372,35 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
         ok = false;
         break;
       }
+      // Saguaro bias set: the bias_k most likely draft ids get weight beta, and q' is q
+      // reweighted and renormalised by N = 1 - (1 - beta) * q(set)
+      float N = 1.f, f = 1.f;
+      int nS = 0;
+      if (bias) {
+        float sq = 0.f;
+        for (int j = 0; j < P.bias_k; ++j) {
+          const unsigned long long kj = s_key[i][j];
+          if (kj == 0ull) break;
+          sq += exp2f((key_value(kj) - q.x) * c) / q.y;
+          d.ids[nS++] = key_id(kj);
+          if (key_id(kj) == s_x[i]) f = P.beta;
+        }
+        N = fmaf(-(1.f - P.beta), sq, 1.f);
+      }
       const float zt = s_zx[0][i], zd = s_zx[1][i];
       float ratio;
       if (zt == -INFINITY) ratio = 0.f;
       else if (zd == -INFINITY) ratio = INFINITY;
-      else ratio = exp2f(((zt - zd) - (t.x - q.x)) * c) * (q.y / t.y);
+      else ratio = exp2f(((zt - zd) - (t.x - q.x)) * c) * (q.y / t.y) * (N / f);
       if (s_u[i] < ratio) continue;
-      d.a = i;  // the residual draw: rho = q scale / p scale
+      d.a = i;  // the residual draw: rho = q' scale / p scale
       d.mct = __fmul_rn(t.x, c);
       d.mcd = __fmul_rn(q.x, c);
       const float ft = fmaf(-fmaf(t.x, c, -d.mct), kLn2, 1.f);
       const float fd = fmaf(-fmaf(q.x, c, -d.mcd), kLn2, 1.f);
-      d.rho = (fd * t.y) / (ft * q.y);
+      d.rho = (fd * t.y) / (ft * (q.y * N));
+      d.rho_s = d.rho * P.beta;
+      d.nS = nS;
       break;
     }
     d.ok = ok ? 1 : 0;
@@ -392,15 +414,34 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
 // The draw's weights of 8 elements: w = max(e_t - rho e_d, 0) with e = 2^(z c - fl(M c)), and the
 // sequential float sums of w (residual) and of e_t (p). With rho = 0 both are e_t.
 __device__ __forceinline__ void weights8(const float (&zt)[8], const float (&zd)[8], float c,
-                                         float mc_t, float mc_d, float rho, float (&w)[8],
-                                         float& s_res, float& s_p) {
+                                         float mc_t, float mc_d, const float (&rk)[8], bool two,
+                                         float (&w)[8], float& s_res, float& s_p) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const float et = ex2_fast(fmaf(zt[k], c, -mc_t));
-    const float ed = rho != 0.f ? ex2_fast(fmaf(zd[k], c, -mc_d)) : 0.f;
-    w[k] = fmaxf(fmaf(-rho, ed, et), 0.f);
+    const float ed = two ? ex2_fast(fmaf(zd[k], c, -mc_d)) : 0.f;
+    w[k] = fmaxf(fmaf(-rk[k], ed, et), 0.f);
     s_res = k ? __fadd_rn(s_res, w[k]) : w[0];
     s_p = k ? __fadd_rn(s_p, et) : et;
+  }
+}
+
+// The draft weight's factor for ids e..e+7: rho, or rho * beta on the bias set of the decided
+// draft row (rho = 0: a draw from p).
+__device__ __forceinline__ void rho8(const SmallDecision& d, float rho, int e, float (&rk)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) rk[k] = rho;
+  if (rho == 0.f || d.nS == 0) return;
+  bool any = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) any |= j < d.nS && static_cast<unsigned>(d.ids[j] - e) < 8u;
+  if (!any) return;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int off = j < d.nS ? d.ids[j] - e : -1;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k == off) rk[k] = d.rho_s;
   }
 }
 
@@ -450,7 +491,9 @@ __global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams 
         load8_at(gt, e, e1, al, zt);
         if (two) load8_at(gd, e, e1, al, zd);
       }
-      weights8(zt, zd, c, d.mct, d.mcd, d.rho, w, sr, sp);
+      float rk[8];
+      rho8(d, d.rho, e, rk);
+      weights8(zt, zd, c, d.mct, d.mcd, rk, two, w, sr, sp);
       own_r += qfix(sr);
       own_p += qfix(sp);
     }
@@ -493,6 +536,12 @@ __global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) 
     const unsigned long long* m = P.mass + (static_cast<long long>(b) * P.nslice_d + lane) * 2;
     mr = m[0];
     mp = m[1];
+  }
+  if (P.fmax > 0) {  // the prepass wrote the top-F ids of rows below L; the rest reads -1
+    const int L = P.lens ? P.lens[b] : K;
+    int32_t* tf = P.out_topf + static_cast<long long>(b) * K * P.fmax;
+    for (int e = tid; e < K * P.fmax; e += kPickThreads)
+      if (!d.ok || e / P.fmax >= L) tf[e] = -1;
   }
   if (!d.ok) {
     for (int j = tid; j <= K; j += kPickThreads) tok[j] = -1;
@@ -544,7 +593,9 @@ __global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) 
         float zt[8], zd[8], sr, sp;
         load8_at(gt, e0 + 8 * (v0 + j), e1, al, zt);
         if (rho != 0.f) load8_at(gd, e0 + 8 * (v0 + j), e1, al, zd);
-        weights8(zt, zd, c, d.mct, d.mcd, rho, w[j], sr, sp);
+        float rk[8];
+        rho8(d, rho, e0 + 8 * (v0 + j), rk);
+        weights8(zt, zd, c, d.mct, d.mcd, rk, rho != 0.f, w[j], sr, sp);
         q[j] = qfix(sr);
         own += q[j];
       }

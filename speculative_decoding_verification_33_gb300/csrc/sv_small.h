@@ -13,8 +13,11 @@ struct SmallDecision {
   int ok;       // 1 = valid
   float mct;    // fl(M_t c) of the target row at a
   float mcd;    // fl(M_d c) of the draft row at a (residual draws)
-  float rho;    // draft scale / target scale; 0 = draw from p
-  int pad[3];
+  float rho;    // q' scale / p scale off the bias set; 0 = draw from p
+  float rho_s;  // the same on the bias set (rho * beta)
+  int nS;       // ids in the bias set of the draft row at a
+  int ids[8];   // those ids
+  int pad;
 };
 
 struct SmallParams {
@@ -29,6 +32,11 @@ struct SmallParams {
   int slice, nslice;         // row statistics: ids per CTA (multiple of 8), slices per row
   int slice_d, nslice_d;     // the draw: ids per CTA (multiple of 8), slices per row
   int aligned;               // rows 16-byte aligned: bulk copies and vector loads
+  const unsigned long long* keys;  // [B][K][8] the draft rows' top 8 from the prepass, or NULL
+  int bias_k;                // size of the bias set (0: none)
+  float beta;                // its weight
+  int fmax;                  // top-F ids per position (written by the prepass), 0: none
+  int32_t* out_topf;         // [B][K][fmax]: -1 where the sequence is invalid or i >= L
   float2* part;              // [B][2K+1][nslice] per slice (max, sum)
   SmallDecision* dec;        // [B]
   unsigned long long* mass;  // [B][nslice_d][2] the draw's residual and p masses per slice
@@ -42,6 +50,7 @@ int small_rows_per_sm(int dtype);
 
 // Fills B, K and the slice fields of P for a batch of B sequences on `sms` multiprocessors;
 // false when the problem does not fit this path (K > 8, or V above 32 draw slices of 8192 ids).
+// A bias set or top-F ids need the draft rows' top 8 from the prepass (P.keys).
 bool small_plan(int B, int K, int V, int sms, int rows_per_sm, SmallParams* P);
 
 // Workspace bytes after the fixed header: partials, decisions, masses (each 256-byte aligned),

@@ -40,7 +40,8 @@ def test_routes_of_the_workloads():
     assert route_of(W.WORKLOADS[2]) == (R.SV_ROUTE_GREEDY_ROWS, 2)
     assert route_of(W.WORKLOADS[3]) == (R.SV_ROUTE_SMALL, 3)            # 181 MB of rows
     assert route_of(W.small_variant(W.WORKLOADS[3], B=96)) == (R.SV_ROUTE_WALK, 1)  # 271 MB
-    assert route_of(W.WORKLOADS[4]) == (R.SV_ROUTE_WALK, 2)             # top-8 prepass
+    assert route_of(W.WORKLOADS[4]) == (R.SV_ROUTE_SMALL, 4)            # after the top-8 prepass
+    assert route_of(W.WORKLOADS[4], hint=4) == (R.SV_ROUTE_WALK, 2)
     assert route_of(W.WORKLOADS[5]) == (R.SV_ROUTE_WALK, 1)
     assert route_of(W.WORKLOADS[1], hint=4) == (R.SV_ROUTE_WALK, 1)
 
@@ -54,6 +55,27 @@ def test_small_path_workloads(w):
     (rep, g), (_, g4) = both_paths(d, w)
     print(w.name, rep.summary())
     assert (g["accept_len"] >= 0).all()
+
+
+@pytest.mark.parametrize("fanout,beta,bias_k", [
+    ((8, 4, 2, 1, 1), 0.5, 8),     # workload 4: bias set and top-F ids
+    (None, 0.5, 8),                # bias set only
+    ((3, 3, 3, 3, 3), 1.0, 0),     # top-F ids only
+    (None, 0.25, 1),               # a bias set of one id
+])
+def test_small_path_bias_and_topf(fanout, beta, bias_k):
+    """The draft rows' top 8 from the prepass drive the bias set (q' = q reweighted by beta on
+    the bias_k most likely draft ids, renormalised) in the accept tests and the residual draw,
+    and the prepass's top-F ids are kept for rows below L (-1 elsewhere and for invalid
+    sequences)."""
+    w = W.WORKLOADS[4].replace(fanout=fanout, beta=beta, bias_k=bias_k, ragged=True)
+    assert route_of(w)[0] == _lib.SV_ROUTE_SMALL
+    d = W.make_inputs(w)
+    d["draft_tokens"][3, 1] = w.V                # an invalid sequence
+    for rep, g in both_paths(d, w):
+        assert g["accept_len"][3] == -1
+        if fanout is not None:
+            assert (g["topf"][3] == -1).all()
 
 
 @pytest.mark.parametrize("B,K,V,dtype", [

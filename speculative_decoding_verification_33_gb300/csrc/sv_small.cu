@@ -309,7 +309,7 @@ __device__ __forceinline__ float2 combine_row(const float2* part, int nslice, fl
 // from p_L (rho = 0). A sequence is invalid (ok = 0) for a length outside 1..K, an id outside the
 // vocabulary, a uniform outside [0, 1), or a row read before the stop that is NaN, +inf or all
 // -inf.
-template <typename T>
+template <typename T, bool BIAS>
 __device__ SmallDecision decide(const SmallParams& P, int b) {
   __shared__ float2 s_ms[2 * kMaxSmallK + 1];
   __shared__ float s_zx[2][kMaxSmallK];
@@ -334,7 +334,7 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
                            small_row(P, b, d ? K + 1 + i : i, sizeof(T)))[xi])
                      : 0.f;
   }
-  const bool bias = P.bias_k > 0 && P.keys != nullptr;
+  const bool bias = BIAS && P.bias_k > 0 && P.keys != nullptr;
   if (bias && lok && tid < 8 * L)  // the draft rows' top 8, written by the prepass launch
     s_key[tid >> 3][tid & 7] = P.keys[(static_cast<long long>(b) * K + (tid >> 3)) * 8 + (tid & 7)];
   pdl_wait();  // the row partials come from the statistics launch
@@ -428,10 +428,11 @@ __device__ __forceinline__ void weights8(const float (&zt)[8], const float (&zd)
 
 // The draft weight's factor for ids e..e+7: rho, or rho * beta on the bias set of the decided
 // draft row (rho = 0: a draw from p).
+template <bool BIAS>
 __device__ __forceinline__ void rho8(const SmallDecision& d, float rho, int e, float (&rk)[8]) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) rk[k] = rho;
-  if (rho == 0.f || d.nS == 0) return;
+  if (!BIAS || rho == 0.f || d.nS == 0) return;
   bool any = false;
 #pragma unroll
   for (int j = 0; j < 8; ++j) any |= j < d.nS && static_cast<unsigned>(d.ids[j] - e) < 8u;
@@ -449,12 +450,12 @@ __device__ __forceinline__ void rho8(const SmallDecision& d, float rho, int e, f
 template <typename T>
 constexpr int kMassUnroll = 8 / static_cast<int>(sizeof(T));
 
-template <typename T>
+template <typename T, bool BIAS>
 __global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams P) {
   pdl_trigger();
   __shared__ unsigned long long s_r[kMassThreads / 32], s_p[kMassThreads / 32];
   const int sl = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const SmallDecision d = decide<T>(P, b);
+  const SmallDecision d = decide<T, BIAS>(P, b);
   if (sl == 0 && tid == 0) P.dec[b] = d;
   if (!d.ok) return;
   const int K = P.K;
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams 
         if (two) load8_at(gd, e, e1, al, zd);
       }
       float rk[8];
-      rho8(d, d.rho, e, rk);
+      rho8<BIAS>(d, d.rho, e, rk);
       weights8(zt, zd, c, d.mct, d.mcd, rk, two, w, sr, sp);
       own_r += qfix(sr);
       own_p += qfix(sp);
@@ -516,7 +517,7 @@ __global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams 
   }
 }
 
-template <typename T>
+template <typename T, bool BIAS>
 __global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) {
   __shared__ unsigned long long s_w[kPickThreads / 32];
   __shared__ int s_slice, s_tok;
@@ -594,7 +595,7 @@ __global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) 
         load8_at(gt, e0 + 8 * (v0 + j), e1, al, zt);
         if (rho != 0.f) load8_at(gd, e0 + 8 * (v0 + j), e1, al, zd);
         float rk[8];
-        rho8(d, rho, e0 + 8 * (v0 + j), rk);
+        rho8<BIAS>(d, rho, e0 + 8 * (v0 + j), rk);
         weights8(zt, zd, c, d.mct, d.mcd, rk, rho != 0.f, w[j], sr, sp);
         q[j] = qfix(sr);
         own += q[j];
@@ -670,10 +671,15 @@ cudaError_t launch_small_t(const SmallParams& P, cudaStream_t stream) {
                   kRowThreads, 0, stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(small_mass<T>, dim3(static_cast<unsigned>(P.nslice_d), static_cast<unsigned>(P.B)),
-                 kMassThreads, stream, P);
+  // the bias set's per-id factor only in the variants that have one
+  const bool bias = P.bias_k > 0 && P.keys != nullptr;
+  const dim3 gm(static_cast<unsigned>(P.nslice_d), static_cast<unsigned>(P.B));
+  e = bias ? launch_pdl(small_mass<T, true>, gm, kMassThreads, stream, P)
+           : launch_pdl(small_mass<T, false>, gm, kMassThreads, stream, P);
   if (e != cudaSuccess) return e;
-  return launch_pdl(small_pick<T>, dim3(static_cast<unsigned>(P.B)), kPickThreads, stream, P);
+  const dim3 gp(static_cast<unsigned>(P.B));
+  return bias ? launch_pdl(small_pick<T, true>, gp, kPickThreads, stream, P)
+              : launch_pdl(small_pick<T, false>, gp, kPickThreads, stream, P);
 }
 
 }  // namespace

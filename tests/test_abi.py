@@ -116,3 +116,20 @@ def test_binding_refuses_host_tensors():
     t = torch.zeros(1, 3, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         api.verify(t, None, torch.zeros(1, 2, dtype=torch.int32), mode="greedy")
+
+
+@pytest.mark.parametrize("kw", BAD_PROBLEMS[:6])
+def test_route_query_checks_the_problem(kw):
+    """spec_verify_route validates the problem on the host before it asks the device anything."""
+    base = dict(B=2, K=4, V=1000, dtype=_lib.SV_DTYPE_BF16, target_row_stride=1000,
+                draft_row_stride=1000)
+    base.update(kw)
+    prob, keep = _lib.make_problem(**base)
+    r, n = ctypes.c_int(-7), ctypes.c_int(-7)
+    st = _lib.load().spec_verify_route(ctypes.byref(prob), _lib.SV_MODE_STOCHASTIC,
+                                       ctypes.addressof(r), ctypes.addressof(n))
+    del keep
+    assert st == _lib.SV_ERR_INVALID_ARG
+    assert r.value == -7 and n.value == -7  # outputs untouched on an error
+    assert _lib.load().spec_verify_route(None, _lib.SV_MODE_STOCHASTIC, None, None) == \
+        _lib.SV_ERR_INVALID_ARG

@@ -59,11 +59,6 @@ def draft_sample(row, u: float, *, temperature: float, beta: float = 1.0, bias_k
     return DraftDraw(int(tok), float(margin), conf, ex)
 
 
-def draft_sample_rows(rows, uniforms, **kw):
-    """``draft_sample`` over the rows of a [R, V] array."""
-    return [draft_sample(rows[r], float(uniforms[r]), **kw) for r in range(rows.shape[0])]
-
-
 def residual_order(target_row, draft_row, *, temperature: float, beta: float = 1.0,
                    bias_k: int = 0):
     """(r, ids): the exact residual max(p - q', 0) of one position and its positive ids ordered

@@ -325,14 +325,6 @@ def verify_batch(target, draft, draft_tokens, draft_lens, uniforms, *, temperatu
     return out
 
 
-def stack_outputs(results: Sequence[SeqResult]):
-    """(accept_len [n], tokens [n, K+1], topf [n, K, F]) arrays from a list of results."""
-    acc = np.array([r.accept_len for r in results], dtype=np.int32)
-    tok = np.stack([r.tokens for r in results]).astype(np.int32)
-    topf = np.stack([r.topf for r in results]).astype(np.int32)
-    return acc, tok, topf
-
-
 def expected_accept_len(alphas: Sequence[float]) -> float:
     """Closed form E[a] = sum_{j=1..L} prod_{i<j} alpha_i for per-position acceptance alpha_i.
 

@@ -195,3 +195,23 @@ def test_identity_head_reduces_to_the_verify_step(mode):
         assert np.array_equal(g.tokens, w.tokens)
         accepted += g.accept_len
     assert accepted > 0
+
+
+def test_head_stats_of_a_one_hot_head():
+    """A head whose row v is the unit vector e_pi(v) scores z[r, v] = h[r, pi(v)], so the row
+    statistics are those of the selected hidden units: max, ln sum exp(h / T) term by term, and
+    the logit of the requested id (a transposed head or a dropped temperature changes them)."""
+    rng = np.random.default_rng(11)
+    R, d, V, T = 3, 6, 5, 0.6
+    h = rng.integers(-16, 17, size=(R, d)).astype(np.float64) / 8.0
+    pi = np.array([5, 1, 1, 3, 0])
+    W = np.zeros((V, d))
+    W[np.arange(V), pi] = 1.0
+    ids = np.array([2, 4, 7])
+    st = H.head_stats(h, W, T, ids)
+    for r in range(R):
+        sel = [h[r, pi[v]] for v in range(V)]
+        assert st.max[r] == max(sel)
+        assert st.lse[r] == pytest.approx(math.log(math.fsum(math.exp(s / T) for s in sel)),
+                                          rel=1e-14)
+    assert st.zx[0] == h[0, pi[2]] and st.zx[1] == h[1, pi[4]] and math.isnan(st.zx[2])

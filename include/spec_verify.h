@@ -147,7 +147,8 @@ size_t spec_verify_workspace_bytes(const sv_problem* prob);
  * spec_verify with a caller-owned workspace of spec_verify_workspace_bytes() bytes of device
  * memory, 16-byte aligned and zero-filled before its first use; the kernel leaves it ready for
  * the next call. Calls that may overlap on the GPU must use different workspaces. Same
- * arguments and errors as spec_verify otherwise.
+ * arguments and errors as spec_verify otherwise. A device-side bounded wait that gives up
+ * raises the error word inside this workspace; spec_verify_workspace_error reads it.
  */
 sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
                          const void* draft_logits, const int32_t* draft_tokens,
@@ -158,17 +159,21 @@ sv_status spec_verify_ws(const sv_problem* prob, const void* target_logits,
 
 /*
  * spec_verify for callers that cannot allocate device memory. This entry point has no
- * counterpart in the method; it exists for the integration. Code that runs inside CUDA graph
- * capture, under an allocator that forbids cudaMalloc (a serving loop that reserved all device
- * memory up front, or a runtime whose allocations go through its own pool), or on a path where
- * a cudaMalloc would synchronise the device cannot let the library create its workspace. This
- * variant allocates nothing: its workspace is a fixed array inside the library's device code
- * (256 bytes on every GPU that loads the library, held until the process exits); it accepts at
+ * counterpart in the method; it exists for the integration. Code running under an allocator
+ * that forbids cudaMalloc (a serving loop that reserved all device memory up front, or a
+ * runtime whose allocations must go through its own pool), or on a path where a cudaMalloc
+ * would synchronise the device, cannot let the library create its workspace. This variant
+ * allocates nothing: its workspace is a fixed array inside the library's device code (256
+ * bytes on every GPU that loads the library, held until the process exits); it accepts at
  * most 65536 sequences, a larger B returns SV_ERR_UNSUPPORTED. Inputs and outputs are the
- * caller's device buffers, exactly as for spec_verify, and the results are identical.
+ * caller's device buffers, exactly as for spec_verify, and the results are identical. With
+ * only that fixed array it always takes the cluster walk (route 0 of spec_verify_route): the
+ * small-batch routes and the top-8 prepass need a larger workspace, so small batches run
+ * slower than through spec_verify (greedy B=8, V=32000: about 15 us instead of 11 us).
  * The first call on a device (with that device current) looks the array up with
  * cudaGetSymbolAddress; make that first call before any stream capture. Each call clears the
- * array's counters with an asynchronous memset on `stream`, then launches. Every call shares
+ * array's queue counters with an asynchronous memset on `stream`, then launches; the array's
+ * error word is kept until spec_verify_device_error reads and clears it. Every call shares
  * the one array, so calls that may overlap on the GPU (different streams, or different host
  * threads) race and must not be issued.
  */
@@ -211,11 +216,23 @@ sv_status spec_verify_host(const sv_problem* prob, const void* target_logits,
                            int32_t* out_residual_topF, void* stream);
 
 /*
- * Synchronises `stream` and reports whether any spec_verify call on it since the last check
- * had a device-side bounded wait give up (SV_ERR_DEVICE_TIMEOUT; those sequences read -2).
- * Clears the flag. SV_OK otherwise.
+ * Synchronises `stream` and reports whether a device-side bounded wait gave up since the last
+ * check (SV_ERR_DEVICE_TIMEOUT; the sequences it gave up on read -2) in a call that used the
+ * library's own workspaces on the current device: spec_verify, spec_verify_debug and
+ * spec_verify_host on `stream` (their per-stream workspace), and spec_verify_noalloc on any
+ * stream (its fixed array, shared by every stream of the device). Clears both error words.
+ * SV_OK otherwise. A call with a caller-owned workspace (spec_verify_ws) reports through
+ * spec_verify_workspace_error instead.
  */
 sv_status spec_verify_device_error(void* stream);
+
+/*
+ * The same report for a caller-owned workspace of spec_verify_ws: synchronises `stream`, reads
+ * the workspace's error word (device memory, 16-byte aligned), clears it, and returns
+ * SV_ERR_DEVICE_TIMEOUT if a bounded wait of a call that used it gave up, SV_OK if not,
+ * SV_ERR_INVALID_ARG for a null or misaligned pointer.
+ */
+sv_status spec_verify_workspace_error(void* workspace, void* stream);
 
 /*
  * The draft generator's step, for `rows` independent rows of draft-head logits (row r at element

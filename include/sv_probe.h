@@ -36,6 +36,19 @@ sv_status sv_hbm_read_probe(const void* buf, size_t bytes, unsigned long long* o
  */
 sv_status sv_wait_probe(unsigned int budget_us, void* stream);
 
+/*
+ * The same bounded wait, raising the error word of another workspace, so that the reports of
+ * the entry points with their own workspaces can be checked: target SV_PROBE_NOALLOC raises the
+ * fixed array of spec_verify_noalloc on the current device (looked up on first use, like that
+ * entry point's first call; `workspace` is ignored), and spec_verify_device_error then reports
+ * it once; target SV_PROBE_WORKSPACE raises the word of `workspace`, a caller-owned workspace
+ * of spec_verify_ws (device memory, 16-byte aligned), and spec_verify_workspace_error reports
+ * it once. SV_ERR_INVALID_ARG for another target, a budget outside 1 .. 1000000 us, or a null or
+ * misaligned caller workspace. Asynchronous on `stream`.
+ */
+enum { SV_PROBE_NOALLOC = 1, SV_PROBE_WORKSPACE = 2 };
+sv_status sv_wait_probe_at(unsigned int budget_us, int target, void* workspace, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,9 @@ SV_MODE_GREEDY, SV_MODE_STOCHASTIC = 0, 1
 EXPORTS = ("spec_verify", "spec_verify_workspace_bytes", "spec_verify_ws", "spec_verify_debug",
            "spec_verify_host", "spec_verify_device_error", "spec_verify_status_string",
            "spec_verify_plan", "spec_verify_route", "spec_verify_noalloc", "spec_draft_sample", "spec_residual_topf",
-           "spec_lmhead_stats", "spec_verify_hidden", "sv_hbm_read_probe", "sv_wait_probe")
+           "spec_lmhead_stats", "spec_verify_hidden", "sv_hbm_read_probe", "sv_wait_probe",
+           "spec_verify_workspace_error", "sv_wait_probe_at")
+SV_PROBE_NOALLOC, SV_PROBE_WORKSPACE = 1, 2
 
 
 class SvProblem(ctypes.Structure):
@@ -66,6 +68,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.spec_verify_status_string.restype = ctypes.c_char_p
         lib.sv_hbm_read_probe.argtypes = [_P, _SZ, _P, _P]
         lib.sv_wait_probe.argtypes = [ctypes.c_uint, _P]
+        lib.sv_wait_probe_at.argtypes = [ctypes.c_uint, _I, _P, _P]
+        lib.spec_verify_workspace_error.argtypes = [_P, _P]
         lib.spec_verify_plan.argtypes = [_PROB, _I, _P, _P, _P]
         lib.spec_verify_route.argtypes = [_PROB, _I, _P, _P]
         lib.spec_draft_sample.argtypes = [_I, _I, _I, ctypes.c_longlong, _P, _P, _F, _F, _I,

@@ -313,8 +313,14 @@ def workspace_bytes(B: int) -> int:
 
 
 def device_error(stream=None) -> int:
-    """Status of the device-side bounded waits on ``stream`` since the last check."""
+    """Status of the device-side bounded waits since the last check, in calls on ``stream``
+    that used the library's workspaces, and in no-alloc calls on any stream of the device."""
     return _lib.load().spec_verify_device_error(_stream_handle(stream))
+
+
+def workspace_error(workspace: torch.Tensor, stream=None) -> int:
+    """The same status for a caller-owned workspace of ``spec_verify_ws``."""
+    return _lib.load().spec_verify_workspace_error(workspace.data_ptr(), _stream_handle(stream))
 
 
 def hbm_read_probe(buf: torch.Tensor, out: torch.Tensor, stream=None) -> None:
@@ -323,11 +329,19 @@ def hbm_read_probe(buf: torch.Tensor, out: torch.Tensor, stream=None) -> None:
                 "sv_hbm_read_probe")
 
 
-def wait_probe(budget_us: int, stream=None) -> None:
+def wait_probe(budget_us: int, stream=None, target: Optional[str] = None,
+               workspace: Optional[torch.Tensor] = None) -> None:
     """Run one bounded wait that nothing satisfies (``sv_wait_probe``): it gives up after about
-    ``budget_us`` microseconds and raises the stream's device error word."""
-    _lib._check(_lib.load().sv_wait_probe(int(budget_us), _stream_handle(stream)),
-                "sv_wait_probe")
+    ``budget_us`` microseconds and raises the stream's device error word, or with ``target``
+    "noalloc" the no-alloc array's, or with "workspace" that of the caller's ``workspace``."""
+    lib = _lib.load()
+    if target is None:
+        _lib._check(lib.sv_wait_probe(int(budget_us), _stream_handle(stream)), "sv_wait_probe")
+        return
+    t = {"noalloc": _lib.SV_PROBE_NOALLOC, "workspace": _lib.SV_PROBE_WORKSPACE}[target]
+    ptr = workspace.data_ptr() if workspace is not None else None
+    _lib._check(lib.sv_wait_probe_at(int(budget_us), t, ptr, _stream_handle(stream)),
+                "sv_wait_probe_at")
 
 
 def to_device_logits(a: np.ndarray, device="cuda") -> torch.Tensor:

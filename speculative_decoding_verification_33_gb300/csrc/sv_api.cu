@@ -2,6 +2,7 @@
 // cluster size, and the launch. Everything here is host code; every step of the verify path
 // runs in the kernels of sv_kernel.cu.
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -45,6 +46,35 @@ struct StreamRes {
 constexpr int kNoAllocMaxB = 65536;
 static __device__ __align__(256) unsigned char g_noalloc_ws[sv::workspace_bytes_for(kNoAllocMaxB)];
 std::map<int, void*> g_noalloc_ptr;  // device ordinal -> address of g_noalloc_ws there
+
+// Device address of g_noalloc_ws on device `dev` (the current device). The first request with
+// `create` looks the array up with cudaGetSymbolAddress and keeps the address; without
+// `create`, *ws stays NULL until then. Caller holds g_mu.
+sv_status noalloc_array(int dev, bool create, void** ws) {
+  *ws = nullptr;
+  auto it = g_noalloc_ptr.find(dev);
+  if (it != g_noalloc_ptr.end()) {
+    *ws = it->second;
+    return SV_OK;
+  }
+  if (!create) return SV_OK;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || !p) return SV_ERR_CUDA;
+  g_noalloc_ptr[dev] = p;
+  *ws = p;
+  return SV_OK;
+}
+
+// Reads the error word of a workspace (after the caller synchronised its stream) and clears it.
+// Returns SV_ERR_DEVICE_TIMEOUT if it was raised.
+sv_status take_error(Workspace* ws) {
+  unsigned int err = 0;
+  if (cudaMemcpy(&err, &ws->error, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (!err) return SV_OK;
+  if (cudaMemset(&ws->error, 0, sizeof(err)) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_ERR_DEVICE_TIMEOUT;
+}
 
 std::mutex g_mu;
 std::map<std::pair<int, cudaStream_t>, StreamRes> g_res;
@@ -596,17 +626,13 @@ sv_status spec_verify_noalloc(const sv_problem* prob, const void* target_logits,
   void* ws = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    auto it = g_noalloc_ptr.find(dev);
-    if (it != g_noalloc_ptr.end()) {
-      ws = it->second;
-    } else {  // first call on this device (with it current): look the array up once
-      if (cudaGetSymbolAddress(&ws, g_noalloc_ws) != cudaSuccess || !ws) return SV_ERR_CUDA;
-      g_noalloc_ptr[dev] = ws;
-    }
+    st = noalloc_array(dev, true, &ws);
+    if (st != SV_OK) return st;
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the queue counters and the order-ready flag must start at zero for every call
-  if (cudaMemsetAsync(ws, 0, sizeof(Workspace), s) != cudaSuccess) return SV_ERR_CUDA;
+  // the queue counters must start at zero for every call (a call cut short by a bounded wait
+  // leaves them set); the error word is left alone, for spec_verify_device_error to report
+  if (cudaMemsetAsync(ws, 0, offsetof(Workspace, error), s) != cudaSuccess) return SV_ERR_CUDA;
   return run(prob, target_logits, draft_logits, draft_tokens, draft_lens, uniforms, temperature,
              beta, mode, out_accept_len, out_tokens, out_residual_topF, nullptr, nullptr, nullptr,
              nullptr, 0, static_cast<Workspace*>(ws), sizeof(Workspace), s);
@@ -754,19 +780,28 @@ sv_status spec_verify_device_error(void* stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
   Workspace* ws = nullptr;
+  void* fixed = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = g_res.find({dev, s});
     if (it != g_res.end()) ws = it->second.ws;
+    const sv_status st = noalloc_array(dev, false, &fixed);
+    if (st != SV_OK) return st;
   }
   if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
-  if (!ws) return SV_OK;
-  unsigned int err = 0;
-  if (cudaMemcpy(&err, &ws->error, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+  // both words are read and cleared, so one report covers both
+  const sv_status a = ws ? take_error(ws) : SV_OK;
+  const sv_status b = fixed ? take_error(static_cast<Workspace*>(fixed)) : SV_OK;
+  if (a == SV_ERR_CUDA || b == SV_ERR_CUDA) return SV_ERR_CUDA;
+  return (a == SV_ERR_DEVICE_TIMEOUT || b == SV_ERR_DEVICE_TIMEOUT) ? SV_ERR_DEVICE_TIMEOUT
+                                                                    : SV_OK;
+}
+
+sv_status spec_verify_workspace_error(void* workspace, void* stream) {
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SV_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SV_ERR_CUDA;
-  if (!err) return SV_OK;
-  if (cudaMemset(&ws->error, 0, sizeof(err)) != cudaSuccess) return SV_ERR_CUDA;
-  return SV_ERR_DEVICE_TIMEOUT;
+  return take_error(static_cast<Workspace*>(workspace));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1007,6 +1042,29 @@ sv_status sv_wait_probe(unsigned int budget_us, void* stream) {
   if (!r) return st;
   const long long cycles = static_cast<long long>(budget_us) * (khz / 1000);
   return sv::launch_wait_probe(cycles, &r->ws->error, s) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_wait_probe_at(unsigned int budget_us, int target, void* workspace, void* stream) {
+  if (budget_us == 0 || budget_us > 1000000u) return SV_ERR_INVALID_ARG;
+  if (target != SV_PROBE_NOALLOC && target != SV_PROBE_WORKSPACE) return SV_ERR_INVALID_ARG;
+  if (target == SV_PROBE_WORKSPACE &&
+      (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+    return SV_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0, khz = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0)
+    khz = 2000000;
+  Workspace* ws = static_cast<Workspace*>(workspace);
+  if (target == SV_PROBE_NOALLOC) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    void* p = nullptr;
+    const sv_status st = noalloc_array(dev, true, &p);
+    if (st != SV_OK) return st;
+    ws = static_cast<Workspace*>(p);
+  }
+  const long long cycles = static_cast<long long>(budget_us) * (khz / 1000);
+  return sv::launch_wait_probe(cycles, &ws->error, s) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 sv_status sv_hbm_read_probe(const void* buf, size_t bytes, unsigned long long* out_checksum,

@@ -104,6 +104,16 @@ def test_workspace_entry_checks_workspace():
     assert _status("spec_verify_ws", B=64, extra=(16, 240)) == _lib.SV_ERR_INVALID_ARG
 
 
+def test_error_readers_and_targeted_probe_check_arguments():
+    lib = _lib.load()
+    assert lib.spec_verify_workspace_error(None, None) == _lib.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_workspace_error(8, None) == _lib.SV_ERR_INVALID_ARG  # misaligned
+    assert lib.sv_wait_probe_at(1000, 0, None, None) == _lib.SV_ERR_INVALID_ARG  # bad target
+    assert lib.sv_wait_probe_at(0, _lib.SV_PROBE_NOALLOC, None, None) == _lib.SV_ERR_INVALID_ARG
+    assert lib.sv_wait_probe_at(1000, _lib.SV_PROBE_WORKSPACE, None, None) == _lib.SV_ERR_INVALID_ARG
+    assert lib.sv_wait_probe_at(1000, _lib.SV_PROBE_WORKSPACE, 8, None) == _lib.SV_ERR_INVALID_ARG
+
+
 def test_probe_checks_arguments():
     lib = _lib.load()
     assert lib.sv_hbm_read_probe(None, 16, 16, None) == _lib.SV_ERR_INVALID_ARG

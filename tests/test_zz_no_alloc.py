@@ -1,8 +1,8 @@
 """The allocation-free entry point (spec_verify_noalloc) gives the same outputs as spec_verify.
 
-Callers that cannot allocate device memory (graph capture, a serving loop that reserved all
-device memory up front, a runtime whose allocations must go through its own pool) use this
-variant; its workspace is a fixed array inside the library. This file is collected last so that
+Callers that cannot allocate device memory (a serving loop that reserved all device memory up
+front, a runtime whose allocations must go through its own pool) use this variant; its workspace
+is a fixed array inside the library. This file is collected last so that
 a failure here does not hide the other GPU tests; it must also pass on its own.
 """
 import numpy as np
@@ -80,4 +80,39 @@ def test_bounded_wait_gives_up_and_reports():
                      torch.from_numpy(d["uniforms"]).cuda(), temperature=w.temperature)
     torch.cuda.synchronize()
     assert (out["accept_len"].cpu().numpy() >= 0).all()
+    assert api.device_error() == 0
+
+
+def test_timeout_in_the_fixed_array_is_reported_once():
+    """A bounded wait that gives up inside the no-alloc array is reported by
+    spec_verify_device_error exactly once, and the next no-alloc call does not erase it first."""
+    from speculative_decoding_verification_33_gb300._lib import SV_ERR_DEVICE_TIMEOUT
+    assert api.device_error() == 0
+    api.wait_probe(2000, target="noalloc")
+    w = W.small_variant(W.WORKLOADS[3], B=6, V=4096)
+    T, D, tok, ln, uni = _inputs(w)
+    got = _outputs(w)
+    api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, *got, no_alloc=True)
+    torch.cuda.synchronize()
+    assert (got[0].cpu().numpy() >= 0).all()
+    assert api.device_error() == SV_ERR_DEVICE_TIMEOUT
+    assert api.device_error() == 0
+
+
+def test_timeout_in_a_caller_workspace_is_reported_once():
+    """The same for a caller-owned workspace: spec_verify_workspace_error reports it once, and
+    a verify call through that workspace still gives valid outcomes."""
+    from speculative_decoding_verification_33_gb300._lib import SV_ERR_DEVICE_TIMEOUT
+    w = W.small_variant(W.WORKLOADS[3], B=6, V=4096)
+    ws = torch.zeros(api.workspace_bytes(w.B) // 4, dtype=torch.int32, device="cuda")
+    assert api.workspace_error(ws) == 0
+    api.wait_probe(2000, target="workspace", workspace=ws)
+    assert api.workspace_error(ws) == SV_ERR_DEVICE_TIMEOUT
+    assert api.workspace_error(ws) == 0
+    T, D, tok, ln, uni = _inputs(w)
+    got = _outputs(w)
+    api.spec_verify(T, D, tok, ln, uni, w.temperature, w.beta, w.mode, *got, workspace=ws)
+    torch.cuda.synchronize()
+    assert (got[0].cpu().numpy() >= 0).all()
+    assert api.workspace_error(ws) == 0
     assert api.device_error() == 0

@@ -63,6 +63,9 @@ def parse_args(argv=None):
                          "verify_hidden: the verify step from hidden states through that head")
     ap.add_argument("--head", default="head_B256_K8_V152064_d3584",
                     help="LM-head workload of --kernel lmhead")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="default run: skip the row-kernel, LM-head and hidden-state legs that "
+                         "are attached to the verify line")
     return ap.parse_args(argv)
 
 
@@ -339,7 +342,7 @@ def row_workload(W, args):
                      temperature=w.temperature or 1.0)
 
 
-def run_rows(args):
+def run_rows(args, quiet=False):
     import torch
 
     from speculative_decoding_verification_33_gb300 import api, build
@@ -445,7 +448,35 @@ def run_rows(args):
                                          for i in range(int(lens[seqs[j]]))))}
         line["cpu_baseline"] = {"value": n / dt, "unit": unit, "cores": 1, "kind": "oracle",
                                 "sample": f"first {n} {'rows' if args.kernel == 'draft_sample' else 'positions'}"}
-    print(json.dumps(line), flush=True)
+    if args.kernel == "residual_topf":
+        line["cache_hit"] = cache_hit_rates(w, vo, res)
+    if not quiet:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+def cache_hit_rates(w, vo, res):
+    """How often the token the verify step drew after a rejection at a_b < L_b is among the ids a
+    speculation cache would have prepared for that outcome: R1, the first F_a ids of the draft
+    row by logit (spec_verify's top-F output, the kernel's hit flags), and R2, the first F_a ids
+    of the exact residual max(p - q', 0) (spec_residual_topf). Over every rejected sequence of
+    the batch."""
+    hit = res["hit"].cpu().numpy()
+    acc = vo["accept_len"].cpu().numpy()
+    tok = vo["tokens"].cpu().numpy()
+    r2 = res["r2"].cpu().numpy()
+    rej = [b for b in range(w.B) if hit[b] >= 0]
+    h2 = 0
+    for b in rej:
+        a = int(acc[b])
+        f = min(int(w.fanout[a]), r2.shape[2])
+        h2 += int(tok[b, a] in r2[b, a, :f].tolist())
+    n = max(1, len(rej))
+    return {"rejected_sequences": len(rej), "r1_draft_topf_rate": int(np.sum(hit[rej] == 1)) / n,
+            "r2_exact_residual_topf_rate": h2 / n, "fanout": list(w.fanout),
+            "beta": w.beta, "bias_k": w.bias_k,
+            "context": "SSD summary, Key claims: the speculation cache predicts the bonus token "
+                       "from the draft logits, up to about 90% (other hardware, real models)"}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -461,7 +492,7 @@ def measured_tensor_peak():
         return 1900.0, "fallback (1.9 PFLOP/s bf16 burst)"
 
 
-def run_lmhead(args):
+def run_lmhead(args, quiet=False):
     import torch
 
     from speculative_decoding_verification_33_gb300 import api, build
@@ -530,10 +561,12 @@ def run_lmhead(args):
                                 "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                                 "sample": f"{len(rows)} rows of {w.R} (float64 numpy matmul, "
                                           "BLAS threads on the host cores)"}
-    print(json.dumps(line), flush=True)
+    if not quiet:
+        print(json.dumps(line), flush=True)
+    return line
 
 
-def run_hidden(args):
+def run_hidden(args, quiet=False, oracle_seqs=8):
     """The verify step from hidden states: every row each sequence has goes through the
     tensor-core head (statistics only), the decided rows again for the draw."""
     import torch
@@ -603,9 +636,10 @@ def run_hidden(args):
                          "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms)},
             "gpu_launches": args.steps * 7, "clocks": clk}
     if not args.no_cpu:  # the oracle on a bounded sample of sequences
-        seqs = list(range(0, w.B, 32))
+        seqs = list(range(0, w.B, w.B // oracle_seqs))[:oracle_seqs]
         t0 = time.perf_counter()
-        res = HO.verify_hidden_batch(x["hidden_target"], x["hidden_draft"], x["weight"],
+        w64 = HO.bf16_to_f64(x["weight"])  # the head in float64 once for the sampled sequences
+        res = HO.verify_hidden_batch(x["hidden_target"], x["hidden_draft"], w64,
                                      x["draft_tokens"], lens, x["uniforms"],
                                      temperature=w.temperature, mode=w.mode, seqs=seqs)
         dt = time.perf_counter() - t0
@@ -617,7 +651,37 @@ def run_hidden(args):
                                 "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                                 "sample": f"{len(seqs)} of {w.B} sequences (float64 numpy "
                                           "matmul for the logits, BLAS threads)"}
-    print(json.dumps(line), flush=True)
+    if not quiet:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+LEG_KEYS = ("metric", "value", "unit", "ms_per_step", "dtype", "config", "roofline", "clocks",
+            "gpu_launches", "parity_sample", "cpu_baseline", "cache_hit")
+
+
+def run_legs(args):
+    """The row kernels (draft sampling, exact-residual top-F with the cache-hit rates) on the
+    headline batch with a Saguaro bias, the tensor-core LM head, and the verify step from hidden
+    states, each timed like the verify step (L2 flushed, CUDA events, clocks sampled), for the
+    default line."""
+    import copy
+    legs = {}
+    for kernel, fn in (("draft_sample", run_rows), ("residual_topf", run_rows),
+                       ("lmhead", run_lmhead), ("verify_hidden", run_hidden)):
+        sub = copy.copy(args)
+        sub.kernel = kernel
+        sub.steps = min(args.steps, 10)
+        sub.warmup = 3
+        t0 = time.perf_counter()
+        line = fn(sub, quiet=True, **({"oracle_seqs": 2} if kernel == "verify_hidden" else {}))
+        leg = {k: line[k] for k in LEG_KEYS if k in line}
+        leg["steps"] = sub.steps
+        leg["wall_s"] = time.perf_counter() - t0
+        legs[kernel] = leg
+        import torch
+        torch.cuda.empty_cache()
+    return legs
 
 
 # ---------------------------------------------------------------------------------------------
@@ -808,6 +872,10 @@ def run_ours(args):
                                             "kind": "oracle, sequences sharded over processes"}
         line["parity"] = {"sequences": rep.sequences, "flagged": rep.flagged,
                           "mismatches": len(rep.mismatches), "invalid": rep.invalid}
+    if rank == 0 and world == 1 and args.workload == 5 and args.cluster == 0 and not args.no_legs:
+        del d
+        torch.cuda.empty_cache()
+        line["legs"] = run_legs(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

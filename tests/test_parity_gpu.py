@@ -288,10 +288,16 @@ def test_host_rows_read_in_place(cfg):
                      torch.from_numpy(d["uniforms"]).cuda(), temperature=w.temperature,
                      mode=w.mode)
     torch.cuda.synchronize()
-    assert np.array_equal(h_acc.numpy(), out["accept_len"].cpu().numpy())
-    assert np.array_equal(h_tok.numpy(), out["tokens"].cpu().numpy())
     res = O.verify_batch(d["target"], None if greedy else d["draft"], d["draft_tokens"],
                          d["draft_lens"], d["uniforms"], temperature=w.temperature, mode=w.mode)
     rep = compare(res, range(w.B), h_acc.numpy(), h_tok.numpy())
     assert rep.ok(), (rep.summary(), rep.mismatches[:3])
+    # the device call may take another route than the in-place host rows (the walk):
+    # both calls equal the oracle, and each other wherever no decision is flagged
+    d_acc, d_tok = out["accept_len"].cpu().numpy(), out["tokens"].cpu().numpy()
+    rep_d = compare(res, range(w.B), d_acc, d_tok)
+    assert rep_d.ok(), (rep_d.summary(), rep_d.mismatches[:3])
+    for b, r in enumerate(res):
+        if r.first_flag(O.MARGIN) is None:
+            assert h_acc.numpy()[b] == d_acc[b] and np.array_equal(h_tok.numpy()[b], d_tok[b])
     assert api.device_error() == 0

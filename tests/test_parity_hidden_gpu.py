@@ -47,12 +47,13 @@ def run_gpu(x, w):
     return out["accept_len"].cpu().numpy(), out["tokens"].cpu().numpy()
 
 
-def check(x, w, margin, seqs=None):
+def check(x, w, margin, seqs=None, weight64=None):
     greedy = w.mode == "greedy"
     acc, tok = run_gpu(x, w)
     seqs = list(range(w.B)) if seqs is None else list(seqs)
     res = HO.verify_hidden_batch(x["hidden_target"], None if greedy else x["hidden_draft"],
-                                 x["weight"], x["draft_tokens"], x["draft_lens"], x["uniforms"],
+                                 x["weight"] if weight64 is None else weight64,
+                                 x["draft_tokens"], x["draft_lens"], x["uniforms"],
                                  temperature=w.temperature, mode=w.mode, seqs=seqs)
     rep = parity.compare(res, seqs, acc, tok, margin=margin)
     assert rep.ok(), (rep.summary(), rep.mismatches[:4])
@@ -71,6 +72,22 @@ def test_hidden_exact(B, K, V, d, T, mode):
     x = W.hidden_inputs(w)
     rep, res = check(x, w, margin=1e-6)
     assert sum(r.accept_len for r in res if r.valid) > 0  # accept and reject paths both ran
+    assert rep.flagged <= max(1, B // 20)
+
+
+@pytest.mark.parametrize("mode,B", [("stochastic", 64), ("greedy", 32)])
+def test_hidden_exact_full_vocabulary(mode, B):
+    """Exact-grid inputs at the bench's vocabulary (V = 152064: the whole split of the vocabulary
+    over column tiles, with its ragged last tile) and the deepest K loop the exact grid allows
+    (d = 1024), ragged K = 8: every draw is compared at the 1e-6 margin, so a wrong token at full
+    size shows here."""
+    w = W.HiddenWorkload(f"exact_full_{mode}", B=B, K=8, V=152064, d=1024, mode=mode,
+                         exact=True, drafter="prior")
+    x = W.hidden_inputs(w)
+    weight64 = HO.bf16_to_f64(x["weight"])  # converted once for the oracle's B head products
+    rep, res = check(x, w, margin=1e-6, weight64=weight64)
+    print(w.name, rep.summary())
+    assert sum(r.accept_len for r in res if r.valid) > 0
     assert rep.flagged <= max(1, B // 20)
 
 
@@ -104,7 +121,12 @@ def test_hidden_full_size_sampled():
     x = W.hidden_inputs(w)
     seqs = list(range(0, w.B, 16)) + [w.B - 1]
     rep, res = check(x, w, margin=CONTINUOUS_MARGIN, seqs=seqs)
+    # At this margin a draw's relative CDF gap (about 1 / V) is almost always below it, so the
+    # draws here are flagged and only the accept decisions, lengths and accepted ids are compared;
+    # test_hidden_exact_full_vocabulary compares the draws at this vocabulary.
+    print(w.name, rep.summary())
     assert sum(r.accept_len for r in res) > 0
+    assert rep.flagged <= len(seqs)
 
 
 def test_hidden_rejects_bad_arguments():

@@ -270,8 +270,8 @@ sv_status plan(const sv_problem* p, const Checked& c, int dev, sv::Launch* L,
 // row a sequence has at once when that costs less than the walk's latency of position after
 // position: greedy batches whose padded target rows fit in 64 MiB (argmax per row slice, then one
 // warp per sequence), and stochastic batches whose rows fit in 256 MiB (row statistics, the
-// draw's slice masses, one pick per sequence; after the top-8 prepass for a bias set or top-F
-// ids). A nonzero cluster_hint, the diagnostics entry point and rows read in place from host
+// draw's slice masses, one pick per sequence; the statistics launch keeps the draft rows' top 8
+// for a bias set or top-F ids). A nonzero cluster_hint, the diagnostics entry point and rows read in place from host
 // memory always take the walk.
 enum Route { ROUTE_WALK = 0, ROUTE_GREEDY_ROWS = 1, ROUTE_SMALL = 2 };
 
@@ -445,10 +445,9 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
     G.aligned = aligned ? 1 : 0;
     G.out_acc = out_acc;
     G.out_tok = out_tok;
-    // a bias set or top-F ids: the top-8 prepass's keys first in the workspace
-    const bool top8 = needs_top8(p, c);
-    const size_t kb = top8 ? (keys_bytes(p) + 255) / 256 * 256 : 0;
-    const size_t need = kb + sv::small_ws_bytes(G);
+    // a bias set or top-F ids: the statistics launch keeps the draft rows' top 8 per slice
+    G.top8 = needs_top8(p, c) ? 1 : 0;
+    const size_t need = sv::small_ws_bytes(G);
     Workspace* w = nullptr;
     if (ws_user) {
       if (ws_user_bytes >= sizeof(Workspace) + need) w = ws_user;
@@ -459,18 +458,13 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
     }
     if (w) {  // (a caller's workspace too small for the partials takes the cluster walk)
       const int dtype = p->dtype == SV_DTYPE_BF16 ? 1 : 0;
-      sv::small_carve(G, reinterpret_cast<char*>(w + 1) + kb);
+      sv::small_carve(G, reinterpret_cast<char*>(w + 1));
       G.err = &w->error;
       G.bias_k = P.bias_k;
       G.beta = P.beta;
       G.fmax = c.fmax;
+      for (int i = 0; i < sv::kMaxK; ++i) G.fan[i] = c.fan[i];
       G.out_topf = c.fmax > 0 ? out_topf : nullptr;
-      if (top8) {
-        unsigned long long* keys = reinterpret_cast<unsigned long long*>(w + 1);
-        G.keys = keys;
-        st = launch_prepass(p, c, dev, dtype, dft, lens, P.c, keys, out_topf, w, stream);
-        if (st != SV_OK) return st;
-      }
       return sv::launch_small(G, dtype, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
   }
@@ -582,7 +576,7 @@ sv_status spec_verify_route(const sv_problem* prob, int mode, int* route, int* l
   }
   if (route) *route = static_cast<int>(r);
   if (launches)
-    *launches = r == ROUTE_SMALL ? 3 + (needs_top8(prob, c) ? 1 : 0)
+    *launches = r == ROUTE_SMALL ? 3
                                  : (r == ROUTE_GREEDY_ROWS || needs_top8(prob, c)) ? 2 : 1;
   return SV_OK;
 }

@@ -116,9 +116,10 @@ __device__ __forceinline__ bool row_bad(float m) {
   return isnan(m) || m == INFINITY || m == -INFINITY;
 }
 
-// Sort key of a logit: larger value first, then lower id. 0 means "empty".
+// Sort key of a logit: larger value first, then lower id (-0 and +0 are one value). 0 means
+// "empty".
 __device__ __forceinline__ unsigned long long make_key(float z, uint32_t id) {
-  const uint32_t b = __float_as_uint(z);
+  const uint32_t b = __float_as_uint(z == 0.f ? 0.f : z);
   const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
   return (static_cast<unsigned long long>(ord) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - id);
 }

@@ -17,8 +17,12 @@
 //  3. small_pick: one CTA per sequence finds the slice that holds floor(u W) from the slices'
 //     masses, then the vector inside it by a block prefix of the vectors' integers, walks that
 //     vector and writes the outcome.
-// The integer masses make the prefix exact and independent of the order of the sums. No bias
-// set and no top-F ids on this path (those take the cluster walk).
+// The integer masses make the prefix exact and independent of the order of the sums.
+//
+// A Saguaro bias set (the bias_k most likely draft ids reweighted by beta; Saguaro summary,
+// "Method") and the top-F ids need the 8 largest logits of each draft row: small_rows keeps them
+// per slice while it streams (a warp's 8 largest keys, offered only what can still enter), and
+// small_mass merges the slices' lists of each row before the accept tests.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -152,6 +156,42 @@ struct Staged<float, VPT> {
   }
 };
 
+// ------------------------------------------------------------------------------------------
+// The 8 largest logits of a draft row slice (keys: larger value first, then lower id)
+// ------------------------------------------------------------------------------------------
+// The largest key over the warp (keys are distinct unless 0): the upper halves first, then the
+// lower halves of the lanes that hold the largest upper half.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k) {
+  const uint32_t hi = static_cast<uint32_t>(k >> 32);
+  const uint32_t mh = __reduce_max_sync(FULL, hi);
+  const uint32_t ml = __reduce_max_sync(FULL, hi == mh ? static_cast<uint32_t>(k) : 0u);
+  return (static_cast<unsigned long long>(mh) << 32) | ml;
+}
+
+// Order-preserving 32 bits of a float, 0 for NaN (absent).
+__device__ __forceinline__ uint32_t float_ord(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return isnan(v) ? 0u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
+}
+__device__ __forceinline__ float ord_value(uint32_t m) {
+  return m == 0u ? -INFINITY : __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
+}
+
+// The 8 largest of the lanes' order-preserving integers, with repeats (0 = absent): lane q < 8
+// returns the q-th, 0 past those there are. Warp-wide.
+__device__ __forceinline__ uint32_t warp_top8_u32(uint32_t o) {
+  const int lane = threadIdx.x & 31;
+  uint32_t mine = 0u;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const uint32_t m = __reduce_max_sync(FULL, o);
+    if (lane == r) mine = m;
+    const unsigned who = __ballot_sync(FULL, o == m && m != 0u);
+    if (who && lane == __ffs(who) - 1) o = 0u;
+  }
+  return mine;
+}
+
 constexpr int kStages = 2;                      // bulk-copy ring of the row kernel
 constexpr int kChunk = 8192;                    // bytes per stage
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per barrier wait
@@ -167,8 +207,10 @@ __device__ __forceinline__ void fold8(RowAcc& acc, const float (&z)[8], float c)
 
 // A 16-byte aligned row slice [e0, e1) streamed through a ring of bulk copies into shared
 // memory (up to kStages * kChunk bytes in flight per CTA, whatever the register budget); the
-// ids past the last whole 16 bytes are read directly. False when a copy did not land within
-// the wait budget (the CTA then waits, bounded again, for the copies it issued and returns).
+// ids past the last whole 16 bytes are read directly, by thread 0. Thread t folds the slice's
+// vectors t, t + kRowThreads, ... (8 ids each, counted from e0). False when a copy did not land
+// within the wait budget (the CTA then waits, bounded again, for the copies it issued and
+// returns).
 template <typename T>
 __device__ bool rows_bulk(const T* row, int e0, int e1, float c, RowAcc& acc) {
   __shared__ __align__(128) unsigned char ring[kStages][kChunk];
@@ -232,6 +274,138 @@ __device__ bool rows_bulk(const T* row, int e0, int e1, float c, RowAcc& acc) {
   return true;
 }
 
+// A row slice [e0, e1) that is not 16-byte aligned, element by element, a batch of loads in
+// flight per thread; thread t folds vectors t, t + kRowThreads, ... as in rows_bulk.
+template <typename T>
+__device__ void rows_plain(const T* row, int e0, int e1, float c, RowAcc& acc) {
+  const int nv = (e1 - e0 + 7) >> 3;
+  constexpr int U = 4;
+  for (int g0 = threadIdx.x; g0 < nv; g0 += U * kRowThreads) {
+    float z[U][8];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int e = e0 + 8 * (g0 + k * kRowThreads);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) z[k][q] = e + q < e1 ? Elt<T>::val(row[e + q]) : -INFINITY;
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (g0 + k * kRowThreads < nv) fold8(acc, z[k], c);
+  }
+}
+
+// The 8 largest keys of a draft row slice [e0, e1) without NaN or +inf, after the stream
+// (block-wide; lane q < 8 of warp 0 returns the q-th, 0 where the slice has fewer ids).
+// Thread t has folded vectors t (mod kRowThreads) of the slice (and thread 0 the ids past the
+// last whole 16 bytes, which lie in the slice's last vector); tmax is its running maximum. The
+// 8th largest tmax, theta, is a value that 8 of the slice's elements reach: an element below
+// theta is not among the 8 largest, and neither is any element of a thread whose tmax is below
+// theta. The vectors of the other threads (and the last vector) are read again, from L2, and
+// their elements at or above theta collected as keys in shared memory (up to kCand), of which
+// the 8 largest are taken. Should more than kCand elements tie at or above theta, the 8 are
+// found by 8 passes over those vectors instead, each taking the largest key below the one
+// before.
+constexpr int kCand = 256;
+constexpr int kItemsInFlight = 2;  // vectors a thread reads again at once
+template <typename T>
+__device__ unsigned long long slice_top8(const T* row, int e0, int e1, bool aligned, float tmax,
+                                         unsigned long long* cand, uint32_t* s_top, int* s_list,
+                                         int* s_n) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kRowThreads / 32;
+  static_assert(kRowThreads == 128, "four warps' 8 largest fill one warp");
+  const uint32_t wt = warp_top8_u32(float_ord(tmax));  // each warp's 8 largest, then the block's
+  if (lane < 8) s_top[warp * 8 + lane] = wt;
+  if (tid == 0) s_n[0] = s_n[1] = 0;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t8 = __shfl_sync(FULL, warp_top8_u32(s_top[lane]), 7);
+    if (lane == 0) s_top[32] = t8;
+  }
+  __syncthreads();
+  const float th = ord_value(s_top[32]);
+  const int nvec = (e1 - e0 + 7) >> 3;
+  const int glast = nvec - 1;
+  if (tmax >= th) s_list[atomicAdd(&s_n[1], 1)] = tid;  // this thread's vectors may hold one
+  __syncthreads();
+  const int ncand = s_n[1];
+  // work items: (candidate thread c, its k-th vector), then the last vector unless its owner
+  // is a candidate
+  bool owner_in = false;
+  for (int q = 0; q < ncand; ++q) owner_in |= s_list[q] == glast % kRowThreads;
+  const int per_c = (nvec + kRowThreads - 1) / kRowThreads;
+  const int items = ncand * per_c + (owner_in ? 0 : 1);
+  auto each = [&](auto&& f) {  // f(z, id) for every element at or above theta
+    for (int i0 = tid; i0 < items; i0 += kItemsInFlight * kRowThreads) {
+      float z[kItemsInFlight][8];
+      int g[kItemsInFlight];
+#pragma unroll
+      for (int u = 0; u < kItemsInFlight; ++u) {
+        const int it = i0 + u * kRowThreads;
+        g[u] = -1;
+        if (it < items) {
+          g[u] = it == ncand * per_c ? glast : s_list[it / per_c] + kRowThreads * (it % per_c);
+          if (g[u] >= nvec) g[u] = -1;
+        }
+        if (g[u] >= 0) load8_at(row, e0 + 8 * g[u], e1, aligned, z[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kItemsInFlight; ++u) {
+        if (g[u] < 0) continue;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (e0 + 8 * g[u] + k < e1 && z[u][k] >= th) f(z[u][k], e0 + 8 * g[u] + k);
+      }
+    }
+  };
+  each([&](float z, int id) {
+    const int at = atomicAdd(&s_n[0], 1);
+    if (at < kCand) cand[at] = make_key(z, static_cast<uint32_t>(id));
+  });
+  __syncthreads();
+  const int n = s_n[0];
+  unsigned long long mine_key = 0ull;
+  if (n <= kCand) {
+    if (warp == 0) {
+      unsigned long long a[kCand / 32];
+#pragma unroll
+      for (int q = 0; q < kCand / 32; ++q) a[q] = lane + 32 * q < n ? cand[lane + 32 * q] : 0ull;
+#pragma unroll 1
+      for (int r = 0; r < 8; ++r) {
+        unsigned long long best = 0ull;
+#pragma unroll
+        for (int q = 0; q < kCand / 32; ++q) best = a[q] > best ? a[q] : best;
+        const unsigned long long m = warp_max_key(best);
+        if (lane == r) mine_key = m;
+#pragma unroll
+        for (int q = 0; q < kCand / 32; ++q)
+          if (a[q] == m) a[q] = 0ull;
+      }
+    }
+  } else {
+    unsigned long long prev = ~0ull;
+#pragma unroll 1
+    for (int r = 0; r < 8; ++r) {
+      unsigned long long best = 0ull;
+      each([&](float z, int id) {
+        const unsigned long long k = make_key(z, static_cast<uint32_t>(id));
+        if (k < prev && k > best) best = k;
+      });
+      best = warp_max_key(best);
+      __syncthreads();  // the previous pass's reads of cand are done
+      if (lane == 0) cand[warp] = best;
+      __syncthreads();
+      unsigned long long m = cand[0];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) m = cand[w] > m ? cand[w] : m;
+      if (lane == r) mine_key = m;
+      prev = m;
+      if (m == 0ull) break;  // fewer than 8 keys below the last one: the rest stay 0
+    }
+  }
+  return mine_key;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) small_rows(const SmallParams P) {
   pdl_trigger();
@@ -247,24 +421,10 @@ __global__ void __launch_bounds__(kRowThreads) small_rows(const SmallParams P) {
   RowAcc acc;
   acc.init();
   bool ok = true;
-  if (P.aligned) {
+  if (P.aligned)
     ok = rows_bulk(row, e0, e1, c, acc);
-  } else {  // element by element, a batch of loads in flight per thread
-    const int nv = (e1 - e0 + 7) >> 3;
-    constexpr int U = 4;
-    for (int g0 = threadIdx.x; g0 < nv; g0 += U * kRowThreads) {
-      float z[U][8];
-#pragma unroll
-      for (int k = 0; k < U; ++k) {
-        const int e = e0 + 8 * (g0 + k * kRowThreads);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) z[k][q] = e + q < e1 ? Elt<T>::val(row[e + q]) : -INFINITY;
-      }
-#pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (g0 + k * kRowThreads < nv) fold8(acc, z[k], c);
-    }
-  }
+  else
+    rows_plain(row, e0, e1, c, acc);
   if (!ok) {  // a copy that never landed: the row reads as NaN and the error word is raised
     if (threadIdx.x == 0) {
       atomicOr(P.err, 1u);
@@ -289,6 +449,20 @@ __global__ void __launch_bounds__(kRowThreads) small_rows(const SmallParams P) {
     if (!row_bad(M)) S *= fmaf(-fmaf(M, c, -Mc), kLn2, 1.f);
     P.part[static_cast<long long>(r) * P.nslice + sl] = make_float2(M, S);
   }
+  if (P.top8 && slot > P.K) {
+    // a draft row's slice: its 8 largest keys (none for a row with NaN or +inf; a slice of -inf
+    // only still has keys, of its lowest ids)
+    __shared__ unsigned long long s_cand[kCand];
+    __shared__ uint32_t s_top[33];
+    __shared__ int s_list[kRowThreads], s_n[2];
+    const unsigned long long k =
+        (isnan(M) || M == INFINITY)
+            ? 0ull
+            : slice_top8(row, e0, e1, P.aligned != 0, acc.m, s_cand, s_top, s_list, s_n);
+    if (threadIdx.x < 8)
+      P.keys[((static_cast<long long>(b) * P.K + (slot - P.K - 1)) * P.nslice + sl) * 8 +
+             threadIdx.x] = k;
+  }
 }
 
 constexpr int kMaxSmallK = 8;   // positions per sequence
@@ -303,12 +477,45 @@ __device__ __forceinline__ float2 combine_row(const float2* part, int nslice, fl
   return make_float2(M, warp_sum(t));
 }
 
+// The 8 largest keys of a draft row from its slices' lists (each descending; one slice per
+// lane, nslice <= 32): lane q < 8 returns the q-th. Warp-wide.
+__device__ __forceinline__ unsigned long long merge_slices(const unsigned long long* lists,
+                                                          int nslice) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long a[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) a[q] = 0ull;
+  if (lane < nslice) {
+    const ulonglong2* p = reinterpret_cast<const ulonglong2*>(lists + lane * 8);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const ulonglong2 v = p[q];
+      a[2 * q] = v.x;
+      a[2 * q + 1] = v.y;
+    }
+  }
+  unsigned long long mine = 0ull;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const unsigned long long m = warp_max_key(a[0]);
+    if (lane == q) mine = m;
+    if (m != 0ull && a[0] == m) {
+#pragma unroll
+      for (int j = 0; j < 7; ++j) a[j] = a[j + 1];
+      a[7] = 0ull;
+    }
+  }
+  return mine;
+}
+
 // The decision of sequence b from the row partials, block-wide (every thread returns it): the
 // accept tests in order; at a rejection the residual draw's constants (fl(M_t c), fl(M_d c) and
 // rho = the ratio of the draft's scale to the target's), after every acceptance the bonus draw
 // from p_L (rho = 0). A sequence is invalid (ok = 0) for a length outside 1..K, an id outside the
 // vocabulary, a uniform outside [0, 1), or a row read before the stop that is NaN, +inf or all
-// -inf.
+// -inf; with top-F ids, also a draft row below L that is NaN, +inf or all -inf. The first CTA
+// of the sequence writes its top-F ids: for i < L the first F_i ids of draft row i (-1 past
+// them), -1 for i >= L and for an invalid sequence.
 template <typename T, bool BIAS>
 __device__ SmallDecision decide(const SmallParams& P, int b) {
   __shared__ float2 s_ms[2 * kMaxSmallK + 1];
@@ -316,6 +523,8 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
   __shared__ int s_x[kMaxSmallK];
   __shared__ float s_u[kMaxSmallK + 1];
   __shared__ unsigned long long s_key[kMaxSmallK][8];
+  __shared__ float s_N[kMaxSmallK], s_f[kMaxSmallK];
+  __shared__ int s_nS[kMaxSmallK];
   __shared__ SmallDecision s_dec;
   const int tid = threadIdx.x, warp = tid >> 5, K = P.K;
   const int L = P.lens ? P.lens[b] : K;
@@ -334,25 +543,56 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
                            small_row(P, b, d ? K + 1 + i : i, sizeof(T)))[xi])
                      : 0.f;
   }
-  const bool bias = BIAS && P.bias_k > 0 && P.keys != nullptr;
-  if (bias && lok && tid < 8 * L)  // the draft rows' top 8, written by the prepass launch
-    s_key[tid >> 3][tid & 7] = P.keys[(static_cast<long long>(b) * K + (tid >> 3)) * 8 + (tid & 7)];
-  pdl_wait();  // the row partials come from the statistics launch
+  const bool bias = BIAS && P.bias_k > 0 && P.top8;
+  pdl_wait();  // the row partials and the slices' keys come from the statistics launch
   if (lok) {
-    for (int r = warp; r < 2 * L + 1; r += blockDim.x >> 5) {  // one warp per row
+    const int nw = blockDim.x >> 5;
+    for (int r = warp; r < 2 * L + 1; r += nw) {  // one warp per row
       const int slot = r <= L ? r : K + 1 + (r - L - 1);
       const float2 ms =
           combine_row(P.part + (static_cast<long long>(b) * (2 * K + 1) + slot) * P.nslice,
                       P.nslice, c);
       if ((tid & 31) == 0) s_ms[slot] = ms;
     }
+    if (P.top8)  // the draft rows' top 8: one warp per row merges its slices
+      for (int i = (warp + 2 * L + 1) % nw; i < L; i += nw) {
+        const unsigned long long k =
+            merge_slices(P.keys + (static_cast<long long>(b) * K + i) * P.nslice * 8, P.nslice);
+        if ((tid & 31) < 8) s_key[i][tid & 31] = k;
+      }
   }
   __syncthreads();
+  if (bias && lok) {
+    // per draft row i < L, one warp: the bias set (its first bias_k keys), q(set) summed in key
+    // order, N = 1 - (1 - beta) q(set), and whether the draft id is in the set
+    const int lane = tid & 31, nw = blockDim.x >> 5;
+    for (int i = warp; i < L; i += nw) {
+      const float2 q = s_ms[K + 1 + i];
+      const unsigned long long kj = lane < 8 ? s_key[i][lane] : 0ull;
+      const bool in = lane < P.bias_k && kj != 0ull;
+      const float term = in ? exp2f((key_value(kj) - q.x) * c) / q.y : 0.f;
+      const unsigned hit = __ballot_sync(FULL, in && key_id(kj) == s_x[i]);
+      const unsigned n = __popc(__ballot_sync(FULL, in));
+      float sq = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float tj = __shfl_sync(FULL, term, j);
+        if (j < static_cast<int>(n)) sq += tj;
+      }
+      if (lane == 0) {
+        s_N[i] = fmaf(-(1.f - P.beta), sq, 1.f);
+        s_f[i] = hit ? P.beta : 1.f;
+        s_nS[i] = static_cast<int>(n);
+      }
+    }
+    __syncthreads();
+  }
   if (tid == 0) {
     bool ok = lok;
     for (int i = 0; ok && i < L; ++i)
       ok = s_x[i] >= 0 && s_x[i] < P.V && s_u[i] >= 0.f && s_u[i] < 1.f;
     ok = ok && s_u[K] >= 0.f && s_u[K] < 1.f;
+    for (int i = 0; ok && P.fmax > 0 && i < L; ++i) ok = !row_bad(s_ms[K + 1 + i].x);
     SmallDecision d;
     d.a = L;
     d.mct = d.mcd = d.rho = d.rho_s = 0.f;
@@ -377,15 +617,11 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
       float N = 1.f, f = 1.f;
       int nS = 0;
       if (bias) {
-        float sq = 0.f;
-        for (int j = 0; j < P.bias_k; ++j) {
-          const unsigned long long kj = s_key[i][j];
-          if (kj == 0ull) break;
-          sq += exp2f((key_value(kj) - q.x) * c) / q.y;
-          d.ids[nS++] = key_id(kj);
-          if (key_id(kj) == s_x[i]) f = P.beta;
-        }
-        N = fmaf(-(1.f - P.beta), sq, 1.f);
+        N = s_N[i];
+        f = s_f[i];
+        nS = s_nS[i];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d.ids[j] = j < nS ? key_id(s_key[i][j]) : -1;
       }
       const float zt = s_zx[0][i], zd = s_zx[1][i];
       float ratio;
@@ -408,6 +644,15 @@ __device__ SmallDecision decide(const SmallParams& P, int b) {
     s_dec = d;
   }
   __syncthreads();
+  if (P.fmax > 0 && blockIdx.x == 0) {
+    int32_t* tf = P.out_topf + static_cast<long long>(b) * K * P.fmax;
+    const bool ok = s_dec.ok != 0;
+    for (int e = tid; e < K * P.fmax; e += blockDim.x) {
+      const int i = e / P.fmax, f = e - i * P.fmax;
+      const unsigned long long k = (ok && i < L && f < P.fan[i] && f < 8) ? s_key[i][f] : 0ull;
+      tf[e] = k ? key_id(k) : -1;
+    }
+  }
   return s_dec;
 }
 
@@ -429,10 +674,11 @@ __device__ __forceinline__ void weights8(const float (&zt)[8], const float (&zd)
 // The draft weight's factor for ids e..e+7: rho, or rho * beta on the bias set of the decided
 // draft row (rho = 0: a draw from p).
 template <bool BIAS>
-__device__ __forceinline__ void rho8(const SmallDecision& d, float rho, int e, float (&rk)[8]) {
+__device__ __forceinline__ void rho8(const SmallDecision& d, float rho, int e, float (&rk)[8],
+                                     bool maybe = true) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) rk[k] = rho;
-  if (!BIAS || rho == 0.f || d.nS == 0) return;
+  if (!BIAS || !maybe || rho == 0.f || d.nS == 0) return;
   bool any = false;
 #pragma unroll
   for (int j = 0; j < 8; ++j) any |= j < d.nS && static_cast<unsigned>(d.ids[j] - e) < 8u;
@@ -468,6 +714,14 @@ __global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams 
   const int e0 = sl * P.slice_d, e1 = min(P.V, e0 + P.slice_d);
   const int nv = (e1 - e0 + 7) >> 3;
   constexpr int U = kMassUnroll<T>;
+  // a bias-set id in one of this thread's vectors (g = tid mod kMassThreads)?
+  bool maybe = false;
+  if (BIAS && two)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int o = d.ids[j] - e0;
+      maybe |= j < d.nS && o >= 0 && d.ids[j] < e1 && ((o >> 3) % kMassThreads) == tid;
+    }
   unsigned long long own_r = 0, own_p = 0;
   for (int g0 = tid; g0 < nv; g0 += U * kMassThreads) {
     Raw8<T> vt[U], vd[U];
@@ -493,7 +747,7 @@ __global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams 
         if (two) load8_at(gd, e, e1, al, zd);
       }
       float rk[8];
-      rho8<BIAS>(d, d.rho, e, rk);
+      rho8<BIAS>(d, d.rho, e, rk, maybe);
       weights8(zt, zd, c, d.mct, d.mcd, rk, two, w, sr, sp);
       own_r += qfix(sr);
       own_p += qfix(sp);
@@ -537,12 +791,6 @@ __global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) 
     const unsigned long long* m = P.mass + (static_cast<long long>(b) * P.nslice_d + lane) * 2;
     mr = m[0];
     mp = m[1];
-  }
-  if (P.fmax > 0) {  // the prepass wrote the top-F ids of rows below L; the rest reads -1
-    const int L = P.lens ? P.lens[b] : K;
-    int32_t* tf = P.out_topf + static_cast<long long>(b) * K * P.fmax;
-    for (int e = tid; e < K * P.fmax; e += kPickThreads)
-      if (!d.ok || e / P.fmax >= L) tf[e] = -1;
   }
   if (!d.ok) {
     for (int j = tid; j <= K; j += kPickThreads) tok[j] = -1;
@@ -672,7 +920,7 @@ cudaError_t launch_small_t(const SmallParams& P, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the bias set's per-id factor only in the variants that have one
-  const bool bias = P.bias_k > 0 && P.keys != nullptr;
+  const bool bias = P.bias_k > 0 && P.top8;
   const dim3 gm(static_cast<unsigned>(P.nslice_d), static_cast<unsigned>(P.B));
   e = bias ? launch_pdl(small_mass<T, true>, gm, kMassThreads, stream, P)
            : launch_pdl(small_mass<T, false>, gm, kMassThreads, stream, P);

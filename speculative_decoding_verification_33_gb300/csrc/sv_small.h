@@ -32,12 +32,14 @@ struct SmallParams {
   int slice, nslice;         // row statistics: ids per CTA (multiple of 8), slices per row
   int slice_d, nslice_d;     // the draw: ids per CTA (multiple of 8), slices per row
   int aligned;               // rows 16-byte aligned: bulk copies and vector loads
-  const unsigned long long* keys;  // [B][K][8] the draft rows' top 8 from the prepass, or NULL
+  int top8;                  // 1: the draft rows' top 8 are kept (bias set or top-F ids)
   int bias_k;                // size of the bias set (0: none)
   float beta;                // its weight
-  int fmax;                  // top-F ids per position (written by the prepass), 0: none
+  int fmax;                  // top-F ids per position, 0: none
+  int fan[8];                // F_i of position i (at most 8)
   int32_t* out_topf;         // [B][K][fmax]: -1 where the sequence is invalid or i >= L
   float2* part;              // [B][2K+1][nslice] per slice (max, sum)
+  unsigned long long* keys;  // [B][K][nslice][8] per slice of a draft row: its 8 largest keys
   SmallDecision* dec;        // [B]
   unsigned long long* mass;  // [B][nslice_d][2] the draw's residual and p masses per slice
   unsigned int* err;         // error word: bit 0 = a bounded wait gave up
@@ -50,16 +52,19 @@ int small_rows_per_sm(int dtype);
 
 // Fills B, K and the slice fields of P for a batch of B sequences on `sms` multiprocessors;
 // false when the problem does not fit this path (K > 8, or V above 32 draw slices of 8192 ids).
-// A bias set or top-F ids need the draft rows' top 8 from the prepass (P.keys).
 bool small_plan(int B, int K, int V, int sms, int rows_per_sm, SmallParams* P);
 
-// Workspace bytes after the fixed header: partials, decisions, masses (each 256-byte aligned),
-// and the pointers into it.
+// Workspace bytes after the fixed header: partials, decisions, masses and, with top8 set, the
+// slices' keys (each 256-byte aligned), and the pointers into it.
 inline size_t small_align(size_t n) { return (n + 255) / 256 * 256; }
+inline size_t small_keys_bytes(const SmallParams& P) {
+  return P.top8 ? static_cast<size_t>(P.B) * P.K * P.nslice * 8 * 8 : 0;
+}
 inline size_t small_ws_bytes(const SmallParams& P) {
   return small_align(static_cast<size_t>(P.B) * (2 * P.K + 1) * P.nslice * 8) +
          small_align(static_cast<size_t>(P.B) * sizeof(SmallDecision)) +
-         small_align(static_cast<size_t>(P.B) * P.nslice_d * 16);
+         small_align(static_cast<size_t>(P.B) * P.nslice_d * 16) +
+         small_align(small_keys_bytes(P));
 }
 inline void small_carve(SmallParams& P, char* base) {
   P.part = reinterpret_cast<float2*>(base);
@@ -67,6 +72,8 @@ inline void small_carve(SmallParams& P, char* base) {
   P.dec = reinterpret_cast<SmallDecision*>(base);
   base += small_align(static_cast<size_t>(P.B) * sizeof(SmallDecision));
   P.mass = reinterpret_cast<unsigned long long*>(base);
+  base += small_align(static_cast<size_t>(P.B) * P.nslice_d * 16);
+  P.keys = P.top8 ? reinterpret_cast<unsigned long long*>(base) : nullptr;
 }
 
 // The three launches (row slices; the draw's slice masses; one pick CTA per sequence) on

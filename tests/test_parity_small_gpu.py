@@ -1,9 +1,10 @@
 """GPU parity of stochastic verification for small batches (every row a sequence has read at
 once: row statistics, the draw's slice masses, one pick per sequence), against the float64
-oracle. The library takes that route for a stochastic batch without a bias set or top-F ids
-whose padded rows fit in 256 MiB, when the caller leaves the cluster size to it
-(cluster_hint 0) and asks for no diagnostics; each case here also runs the chained cluster walk
-(cluster_hint 4) on the same inputs, so both routes face the same bar."""
+oracle. The library takes that route for a stochastic batch whose padded rows fit in 256 MiB,
+when the caller leaves the cluster size to it (cluster_hint 0) and asks for no diagnostics; with
+a bias set or top-F ids the statistics launch also keeps each draft row slice's 8 largest
+logits. Each case here also runs the chained cluster walk (cluster_hint 4) on the same inputs,
+so both routes face the same bar."""
 import numpy as np
 import pytest
 
@@ -40,7 +41,7 @@ def test_routes_of_the_workloads():
     assert route_of(W.WORKLOADS[2]) == (R.SV_ROUTE_GREEDY_ROWS, 2)
     assert route_of(W.WORKLOADS[3]) == (R.SV_ROUTE_SMALL, 3)            # 181 MB of rows
     assert route_of(W.small_variant(W.WORKLOADS[3], B=96)) == (R.SV_ROUTE_WALK, 1)  # 271 MB
-    assert route_of(W.WORKLOADS[4]) == (R.SV_ROUTE_SMALL, 4)            # after the top-8 prepass
+    assert route_of(W.WORKLOADS[4]) == (R.SV_ROUTE_SMALL, 3)            # top 8 kept per slice
     assert route_of(W.WORKLOADS[4], hint=4) == (R.SV_ROUTE_WALK, 2)
     assert route_of(W.WORKLOADS[5]) == (R.SV_ROUTE_WALK, 1)
     assert route_of(W.WORKLOADS[1], hint=4) == (R.SV_ROUTE_WALK, 1)
@@ -64,9 +65,9 @@ def test_small_path_workloads(w):
     (None, 0.25, 1),               # a bias set of one id
 ])
 def test_small_path_bias_and_topf(fanout, beta, bias_k):
-    """The draft rows' top 8 from the prepass drive the bias set (q' = q reweighted by beta on
-    the bias_k most likely draft ids, renormalised) in the accept tests and the residual draw,
-    and the prepass's top-F ids are kept for rows below L (-1 elsewhere and for invalid
+    """The draft rows' top 8 (merged from the slices' lists) drive the bias set (q' = q
+    reweighted by beta on the bias_k most likely draft ids, renormalised) in the accept tests and
+    the residual draw, and give the top-F ids of rows below L (-1 elsewhere and for invalid
     sequences)."""
     w = W.WORKLOADS[4].replace(fanout=fanout, beta=beta, bias_k=bias_k, ragged=True)
     assert route_of(w)[0] == _lib.SV_ROUTE_SMALL
@@ -76,6 +77,70 @@ def test_small_path_bias_and_topf(fanout, beta, bias_k):
         assert g["accept_len"][3] == -1
         if fanout is not None:
             assert (g["topf"][3] == -1).all()
+
+
+@pytest.mark.parametrize("V", [1, 3, 7, 9, 1000, 70001])
+def test_small_path_top8_vocabularies(V):
+    """Vocabularies below 8 ids (the missing keys read as no id), one partial vector, and
+    several slices per row."""
+    w = W.small_variant(W.WORKLOADS[4], B=5, V=V).replace(ragged=True)
+    w = w.replace(bias_k=min(w.bias_k, V))
+    assert route_of(w)[0] == _lib.SV_ROUTE_SMALL
+    d = W.make_inputs(w)
+    both_paths(d, w)
+
+
+def test_small_path_top8_ties_zeros_and_sparse_rows():
+    """Draft rows that stress the per-slice top 8: every logit equal (ties go to the lower id),
+    -0 and +0 as the largest value (one value), -inf but for 5 ids (fewer finite ids than the
+    list holds), logits that grow along the row (every later element enters), and a row whose 8
+    largest sit in its last 8 ids (a whole vector and the 3-id tail that the bulk copies leave
+    to plain loads: row stride V + 5)."""
+    w = W.small_variant(W.WORKLOADS[4], B=6, V=20011).replace(ragged=False)
+    assert route_of(w)[0] == _lib.SV_ROUTE_SMALL
+    d = W.make_inputs(w)
+    V, K = w.V, w.K
+    dr = d["draft"]
+    rng = np.random.default_rng(7)
+    dr[0] = 0x3F80                                                   # all 1.0
+    dr[1] = rng.choice(np.array([0x8000, 0x0000, 0xBF80], np.uint16), size=dr[1].shape)
+    dr[2] = 0xFF80                                                   # -inf ...
+    for i in range(K):
+        dr[2, i, rng.choice(V, 5, replace=False)] = rng.integers(0x3F00, 0x4000, 5)
+    dr[3] = (0x3F80 + np.arange(V) // 4).astype(np.uint16)         # nondecreasing
+    dr[4, :, V - 8:] = 0x4100                                        # 8.0 in the last 8 ids
+    for b in range(5):                       # drafts the rows can have drawn (q(x) > 0)
+        for i in range(K):
+            d["draft_tokens"][b, i] = int(np.argmax(W.bf16_bits_to_f32(dr[b, i])))
+    for fanout, beta, bias_k in (((8, 4, 2, 1, 1), 0.5, 8), ((8, 8, 8, 8, 8), 1.0, 0)):
+        w2 = w.replace(fanout=fanout, beta=beta, bias_k=bias_k)
+        for rep, g in both_paths(d, w2, stride_pad=5):
+            assert (g["accept_len"] >= 0).all()
+
+
+@pytest.mark.parametrize("fanout", [(8, 4, 2, 1, 1), None])
+def test_small_path_bad_draft_row_below_L(fanout):
+    """With top-F ids every draft row below L is needed, so a NaN in the last draft row makes
+    the sequence invalid even when the decision stops before it; with a bias set alone it
+    matters only where the decision reads the row."""
+    w = W.small_variant(W.WORKLOADS[4], B=8, V=3000).replace(ragged=False, fanout=fanout)
+    d = W.make_inputs(w)
+    d["draft"][:, w.K - 1, 11] = W.BF16_NAN
+    for rep, g in both_paths(d, w):
+        if fanout is not None:
+            assert (g["accept_len"] == -1).all()
+            assert (g["topf"] == -1).all()
+
+
+def test_small_path_top8_unaligned_and_f32():
+    """Top 8 kept by the element-by-element path (bf16 rows of stride V + 1, fp32 rows of odd
+    stride) and by the bulk copies of fp32 rows with a 3-id tail (stride V + 1 = 5004)."""
+    w = W.small_variant(W.WORKLOADS[4], B=5, V=3001).replace(ragged=True)
+    both_paths(W.make_inputs(w), w, stride_pad=1)
+    w = w.replace(dtype="f32", V=5003)
+    d = W.make_inputs(w)
+    both_paths(d, w)
+    both_paths(d, w, stride_pad=1)
 
 
 @pytest.mark.parametrize("B,K,V,dtype", [

@@ -17,7 +17,8 @@ shares no code with that path.
 
 * The verify step from hidden states (Kangaroo guide, section 3, with the logits of "Exit 1";
   LayerSkip guide, "Verification Phase": the early-exit draft and the full model share the
-  head): the logits of each sequence's rows are ``h W^T`` as above, and the outcome is the one
+  head): the logits of each sequence's rows are ``h W^T`` as above, and the outcome (with the
+  Saguaro bias set and the top-F draft ids when asked for) is the one
   ``oracle.verify.verify_sequence`` gives for those float64 rows.
 
 Parity pins: ``tests/test_oracle_lmhead_pins.py`` (one-hot heads, closed-form sums, shift and
@@ -90,12 +91,15 @@ def logit_error_bound(hidden, weight) -> np.ndarray:
 
 
 def verify_hidden_batch(hidden_target, hidden_draft, weight, draft_tokens, draft_lens, uniforms,
-                        *, temperature: float, mode: str,
+                        *, temperature: float, mode: str, beta: float = 1.0, bias_k: int = 0,
+                        fanout: Optional[Sequence[int]] = None,
                         seqs: Optional[Sequence[int]] = None):
     """The verify step on logits computed from hidden states: ``hidden_target`` [B, K+1, d],
     ``hidden_draft`` [B, K, d] (None in greedy mode) and ``weight`` [V, d], bf16 bits or floats.
     Only rows 0..L_b (target) and 0..L_b-1 (draft) are scored; the others are NaN rows the verify
-    step never reads. Returns a list of ``oracle.verify.SeqResult``."""
+    step never reads. ``beta``, ``bias_k`` (the Saguaro bias set of the draft rows) and ``fanout``
+    (top-F draft ids) mean what they mean for ``oracle.verify.verify_sequence``, on those logits.
+    Returns a list of ``oracle.verify.SeqResult``."""
     B, K = np.asarray(draft_tokens).shape
     V = np.asarray(weight).shape[0]
     out = []
@@ -108,5 +112,6 @@ def verify_hidden_batch(hidden_target, hidden_draft, weight, draft_tokens, draft
             if zd is not None:
                 zd[:L] = head_logits(np.asarray(hidden_draft)[b, :L], weight)
         out.append(_v.verify_sequence(zt, zd, draft_tokens[b], L, uniforms[b],
-                                      temperature=temperature, mode=mode))
+                                      temperature=temperature, mode=mode, beta=beta,
+                                      bias_k=bias_k, fanout=fanout))
     return out

@@ -197,6 +197,38 @@ def test_identity_head_reduces_to_the_verify_step(mode):
     assert accepted > 0
 
 
+def test_identity_head_carries_the_bias_set_and_top_f():
+    """With W = I the bias set and the top-F ids of the verify step from hidden states are those
+    of the verify step on the hidden states read as logits: the ids of the largest draft hidden
+    units (a head that scored the target rows, or transposed ids, would give others)."""
+    from oracle import verify as O
+    rng = np.random.default_rng(11)
+    B, K, d = 8, 4, 24
+    ht = rng.normal(0.0, 1.0, size=(B, K + 1, d))
+    hd = ht[:, :K] + rng.normal(0.0, 0.8, size=(B, K, d))
+    lens = np.array([4, 1, 2, 3, 4, 2, 1, 3], np.int32)
+    x = rng.integers(0, d, size=(B, K)).astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    fan = (5, 3, 2, 1)
+    got = H.verify_hidden_batch(ht, hd, np.eye(d), x, lens, u, temperature=1.1, mode="stochastic",
+                                beta=0.4, bias_k=6, fanout=fan)
+    tgt = np.where(np.arange(K + 1)[None, :, None] <= lens[:, None, None], ht, np.nan)
+    dft = np.where(np.arange(K)[None, :, None] < lens[:, None, None], hd, np.nan)
+    want = O.verify_batch(tgt, dft, x, lens, u, temperature=1.1, mode="stochastic", beta=0.4,
+                          bias_k=6, fanout=fan)
+    for b, (g, w) in enumerate(zip(got, want)):
+        assert g.accept_len == w.accept_len
+        assert np.array_equal(g.tokens, w.tokens)
+        assert np.array_equal(g.topf, w.topf)
+        for i in range(lens[b]):  # the top-F ids are the largest draft hidden units of row i
+            f = fan[i]
+            assert list(g.topf[i, :f]) == list(np.argsort(-hd[b, i], kind="stable")[:f])
+    base = H.verify_hidden_batch(ht, hd, np.eye(d), x, lens, u, temperature=1.1,
+                                 mode="stochastic")
+    assert any(g.accept_len != h.accept_len or not np.array_equal(g.tokens, h.tokens)
+               for g, h in zip(got, base))  # the bias set changes some outcome
+
+
 def test_head_stats_of_a_one_hot_head():
     """A head whose row v is the unit vector e_pi(v) scores z[r, v] = h[r, pi(v)], so the row
     statistics are those of the selected hidden units: max, ln sum exp(h / T) term by term, and

@@ -299,12 +299,16 @@ sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long lon
  * one LM head). The logits of every row are z = h W^T with the head W [V][d] (bf16, row stride
  * weight_stride), for the target hidden states [B][K+1] rows (bf16, target_row_stride elements
  * apart) and the draft hidden states [B][K] rows (draft_row_stride apart; unused and may be NULL
- * in greedy mode). The outcome is the one spec_verify gives for those logits (beta = 1, no bias
- * set, no top-F ids): out_accept_len [B] and out_tokens [B][K+1], the same layout, validity
- * rules and uniforms. Only the rows each sequence has are scored (target 0..L_b, draft
- * 0..L_b-1); each row is reduced on the tensor cores to its maximum, softmax sum, logit at the
- * draft id and argmax, and the two rows of the decided position are scored again for the draw,
- * so no row of logits is written to memory. Logits are accumulated in fp32 from bf16 products.
+ * in greedy mode). The outcome is the one spec_verify gives for those logits with the same
+ * beta, bias set size (bias_k, 0..8) and top-F widths (fanout: a host array of K entries in
+ * 0..8, or NULL; stochastic mode only): out_accept_len [B], out_tokens [B][K+1] and, iff fanout
+ * is given, out_residual_topF [B][K][max_i F_i], in the same layout, with the same validity
+ * rules and uniforms (with top-F ids every draft row below L_b is needed). Only the rows each
+ * sequence has are scored (target 0..L_b, draft 0..L_b-1); each row is reduced on the tensor
+ * cores to its maximum, softmax sum, logit at the draft id and argmax (with a bias set or top-F
+ * ids also to its 8 largest logits per vocabulary range, merged per draft row before the
+ * decision), and the two rows of the decided position are scored again for the draw, so no row
+ * of logits is written to memory. Logits are accumulated in fp32 from bf16 products.
  * d must be a multiple of 64, K <= 8, V <= 2^18; hidden states and head 16-byte aligned, with
  * row strides that are multiples of 8 elements. Asynchronous on `stream`, on the stream's
  * workspace (grown on demand: about B (2K+1) d 2 bytes for the packed rows plus 16 bytes per
@@ -316,8 +320,9 @@ sv_status spec_verify_hidden(int B, int K, int V, int d, const void* hidden_targ
                              long long draft_row_stride, const void* weight,
                              long long weight_stride, const int32_t* draft_tokens,
                              const int32_t* draft_lens, const float* uniforms, float temperature,
-                             int mode, int32_t* out_accept_len, int32_t* out_tokens,
-                             void* stream);
+                             float beta, int bias_k, const int* fanout, int mode,
+                             int32_t* out_accept_len, int32_t* out_tokens,
+                             int32_t* out_residual_topF, void* stream);
 
 /* A static, human-readable name for a status code. */
 const char* spec_verify_status_string(sv_status status);

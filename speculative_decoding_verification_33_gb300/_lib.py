@@ -79,7 +79,7 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                           _F, _P, _P, _P, _P, _P, _P, _P]
         _LL = ctypes.c_longlong
         lib.spec_verify_hidden.argtypes = [_I, _I, _I, _I, _P, _LL, _P, _LL, _P, _LL, _P, _P, _P,
-                                           _F, _I, _P, _P, _P]
+                                           _F, _F, _I, _P, _I, _P, _P, _P, _P]
         for name in EXPORTS:
             if name not in ("spec_verify_workspace_bytes", "spec_verify_status_string"):
                 getattr(lib, name).restype = _I

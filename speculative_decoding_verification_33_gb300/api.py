@@ -8,6 +8,7 @@ allocates the outputs and returns them. ``verify_host`` is the end-to-end form o
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Optional, Sequence
 
 import numpy as np
@@ -233,13 +234,15 @@ def verify_hidden(hidden_target: torch.Tensor, hidden_draft: Optional[torch.Tens
                   weight: torch.Tensor, draft_tokens: torch.Tensor,
                   draft_lens: Optional[torch.Tensor] = None,
                   uniforms: Optional[torch.Tensor] = None, *, temperature: float = 1.0,
+                  beta: float = 1.0, bias_k: int = 0, fanout=None,
                   mode="stochastic", stream=None, out=None):
     """The verify step from hidden states (``spec_verify_hidden`` in include/spec_verify.h).
 
     ``hidden_target`` [B, K+1, d] and ``hidden_draft`` [B, K, d] (None in greedy mode) are bf16
     CUDA tensors whose rows are contiguous (any row stride that is a multiple of 8 elements, the
-    same between positions and sequences); ``weight`` [V, d] bf16. Returns
-    {"accept_len" [B], "tokens" [B, K+1]} (int32)."""
+    same between positions and sequences); ``weight`` [V, d] bf16. ``beta`` and ``bias_k`` give
+    the Saguaro bias set, ``fanout`` (K widths, or None) the top-F draft ids. Returns
+    {"accept_len" [B], "tokens" [B, K+1]} (int32), and "topf" [B, K, max F] with a fanout."""
     B, K = draft_tokens.shape
     d = hidden_target.shape[-1]
     V = weight.shape[0]
@@ -260,16 +263,27 @@ def verify_hidden(hidden_target: torch.Tensor, hidden_draft: Optional[torch.Tens
             weight.shape[1] != d:
         raise ValueError("weight must be a bf16 [V, d] tensor with contiguous rows")
     dev = hidden_target.device
+    fan = None
+    if fanout is not None:
+        if len(fanout) != K:
+            raise ValueError(f"fanout needs {K} entries")
+        fan = (ctypes.c_int * K)(*[int(f) for f in fanout])
     if out is None:
         out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
                "tokens": torch.empty(B, K + 1, dtype=torch.int32, device=dev)}
+        if fanout is not None:
+            out["topf"] = torch.empty(B, K, max(fanout), dtype=torch.int32, device=dev)
     st = _lib.load().spec_verify_hidden(
         int(B), int(K), int(V), int(d), _ptr(hidden_target, "hidden_target"), int(ts),
         _ptr(hidden_draft, "hidden_draft"), int(ds), _ptr(weight, "weight"),
         int(weight.stride(0) if V > 1 else d), _ptr(draft_tokens, "draft_tokens", torch.int32),
         _ptr(draft_lens, "draft_lens", torch.int32), _ptr(uniforms, "uniforms", torch.float32),
-        float(temperature), m, _ptr(out["accept_len"], "accept_len", torch.int32),
-        _ptr(out["tokens"], "tokens", torch.int32), _stream_handle(stream))
+        float(temperature), float(beta), int(bias_k),
+        ctypes.cast(fan, ctypes.c_void_p).value if fan is not None else 0, m,
+        _ptr(out["accept_len"], "accept_len", torch.int32),
+        _ptr(out["tokens"], "tokens", torch.int32),
+        _ptr(out.get("topf"), "topf", torch.int32) if fanout is not None else 0,
+        _stream_handle(stream))
     _lib._check(st, "spec_verify_hidden")
     return out
 

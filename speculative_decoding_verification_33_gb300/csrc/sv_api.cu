@@ -961,8 +961,9 @@ sv_status spec_verify_hidden(int B, int K, int V, int d, const void* hidden_targ
                              long long draft_row_stride, const void* weight,
                              long long weight_stride, const int32_t* draft_tokens,
                              const int32_t* draft_lens, const float* uniforms, float temperature,
-                             int mode, int32_t* out_accept_len, int32_t* out_tokens,
-                             void* stream) {
+                             float beta, int bias_k, const int* fanout, int mode,
+                             int32_t* out_accept_len, int32_t* out_tokens,
+                             int32_t* out_residual_topF, void* stream) {
   // V <= 2^18 as for spec_verify: the draw's masses (each at most 1 in 2^-44 units per id) then
   // sum below 2^63 even for a flat row
   if (B < 0 || K < 1 || K > 8 || V < 1 || V > (1 << 18) || d < 64 || d % 64 != 0)
@@ -970,6 +971,20 @@ sv_status spec_verify_hidden(int B, int K, int V, int d, const void* hidden_targ
   if (mode != SV_MODE_GREEDY && mode != SV_MODE_STOCHASTIC) return SV_ERR_INVALID_ARG;
   const bool greedy = mode == SV_MODE_GREEDY;
   if (!greedy && !finite_in(temperature, 1e-4f, 1e4f)) return SV_ERR_INVALID_ARG;
+  if (!greedy && (!(std::isfinite(beta) && beta > 0.f && beta <= 1.f) || bias_k < 0 || bias_k > 8))
+    return SV_ERR_INVALID_ARG;
+  int fan[sv::kMaxK] = {0};
+  int fmax = 0;
+  if (fanout) {
+    if (greedy) return SV_ERR_INVALID_ARG;
+    for (int i = 0; i < K; ++i) {
+      if (fanout[i] < 0 || fanout[i] > 8) return SV_ERR_INVALID_ARG;
+      fan[i] = fanout[i];
+      fmax = std::max(fmax, fan[i]);
+    }
+  }
+  if ((fmax > 0 && !out_residual_topF) || (!fanout && out_residual_topF))
+    return SV_ERR_INVALID_ARG;
   if (B == 0) return SV_OK;
   if (!hidden_target || !weight || !draft_tokens || !draft_lens || !out_accept_len ||
       !out_tokens)
@@ -1002,8 +1017,13 @@ sv_status spec_verify_hidden(int B, int K, int V, int d, const void* hidden_targ
   p.lens = draft_lens;
   p.uni = greedy ? nullptr : uniforms;
   p.temperature = greedy ? 1.f : temperature;
+  p.beta = greedy ? 1.f : beta;
+  p.bias_k = (greedy || beta >= 1.f) ? 0 : bias_k;
+  p.fmax = fmax;
+  for (int i = 0; i < 8; ++i) p.fan[i] = i < sv::kMaxK ? fan[i] : 0;
   p.out_acc = out_accept_len;
   p.out_tok = out_tokens;
+  p.out_topf = fmax > 0 ? out_residual_topF : nullptr;
   sv_status st = SV_OK;
   StreamRes* r = resources(dev, s, sizeof(Workspace) + sv::hv_workspace_bytes(p, sms), &st);
   if (!r) return st;

@@ -7,10 +7,12 @@
 //  1. hv_scan / hv_gather: the rows each sequence has (target 0..L_b, draft 0..L_b-1) packed
 //     into one bf16 matrix, with the draft id each row is scored at;
 //  2. the head GEMM with its statistics epilogue and the combine: per row the maximum, the sum
-//     of 2^(z c - fl(m c)), the logit at the draft id and the lowest id of the maximum;
-//  3. hv_decide: per sequence the accept tests u_i < p_i(x_i) / q_i(x_i) in order (greedy:
-//     x_i == argmax), the first rejection a_b, the accepted ids; it copies the hidden states of
-//     position a_b (target, and draft unless every draft was accepted) into pair slots;
+//     of 2^(z c - fl(m c)), the logit at the draft id and the lowest id of the maximum (with a
+//     Saguaro bias set or top-F ids, also each row's 8 largest logits per vocabulary range);
+//  3. hv_decide: per sequence the accept tests u_i < p_i(x_i) / q'_i(x_i) in order (greedy:
+//     x_i == argmax), the first rejection a_b, the accepted ids, the top-F ids; it copies the
+//     hidden states of position a_b (target, and draft unless every draft was accepted) into
+//     pair slots;
 //  4. the head GEMM again over those pairs with the residual epilogue: per sequence and per 16
 //     ids the masses of max(p - q, 0) (or of p for the bonus draw) in 2^-44 units;
 //  5. hv_pick: per sequence the inverse CDF over ascending ids: the 16-id block that holds
@@ -33,9 +35,11 @@ namespace {
 constexpr int kScanThreads = 1024;
 constexpr int kPickThreads = 256;
 
+constexpr int kMaxRanges = 64;  // vocabulary ranges of the statistics GEMM when the top 8 are kept
+
 struct HvLayout {
   int Rmax, npairs, nsplit, tps, ntiles, nh, rsplit, rtps;
-  size_t off, count, ids, rows, part, A, Ad, pairs, seqa, mass, massp, total;
+  size_t off, count, ids, rows, part, keys, A, Ad, pairs, seqa, mass, massp, total;
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -44,7 +48,7 @@ HvLayout layout(const HvProblem& p, int sms) {
   HvLayout L;
   L.Rmax = p.B * ((p.K + 1) + (p.greedy ? 0 : p.K));
   L.npairs = p.greedy ? 0 : (p.B + 63) / 64 * 64;
-  head_split(L.Rmax, p.V, sms, &L.nsplit, &L.tps, &L.ntiles);
+  head_split(L.Rmax, p.V, sms, &L.nsplit, &L.tps, &L.ntiles, hv_top8(p) ? kMaxRanges : 0);
   L.nh = L.ntiles * kHeadHalves;
   int nt2 = 0;
   head_split(std::max(1, 2 * L.npairs), p.V, sms, &L.rsplit, &L.rtps, &nt2);
@@ -54,6 +58,7 @@ HvLayout layout(const HvProblem& p, int sms) {
   L.ids = o;   o += up256(sizeof(int32_t) * L.Rmax);
   L.rows = o;  o += up256(sizeof(HeadRow) * L.Rmax);
   L.part = o;  o += up256(head_part_bytes(L.Rmax, L.nsplit));
+  L.keys = o;  o += hv_top8(p) ? up256(static_cast<size_t>(L.Rmax) * L.nsplit * 64) : 0;
   L.A = o;     o += up256(static_cast<size_t>(L.Rmax) * p.d * 2);
   L.Ad = o;    o += up256(static_cast<size_t>(2 * L.npairs) * p.d * 2);
   L.pairs = o; o += up256(sizeof(HeadPair) * L.npairs);
@@ -128,33 +133,113 @@ __global__ void __launch_bounds__(128) hv_gather(const HvProblem p, const int* o
   }
 }
 
-// Decisions of sequence blockIdx.x (thread 0), then the copy of the decided position's hidden
-// states into its pair slot. Blocks past B only mark their pair slot as unused.
+// The 8 largest keys of a row from its vocabulary ranges' lists (each descending; list r at
+// keys + (r * Rmax + row) * 8, nsplit <= 64): lane q < 8 returns the q-th. Warp-wide.
+__device__ __forceinline__ unsigned long long merge_ranges(const unsigned long long* keys,
+                                                          int nsplit, int Rmax, int row) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long a[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) a[q] = 0ull;
+  float thr = -INFINITY;
+  for (int r = lane; r < nsplit; r += 32) {  // the lane's lists into one
+    const unsigned long long* kr = keys + (static_cast<long long>(r) * Rmax + row) * 8;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const unsigned long long k = kr[q];
+      if (k != 0ull) top8_insert(a, thr, key_value(k), static_cast<uint32_t>(key_id(k)));
+    }
+  }
+  unsigned long long mine = 0ull;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const unsigned long long m = warp_max_key(a[0]);
+    if (lane == q) mine = m;
+    if (m != 0ull && a[0] == m) {
+#pragma unroll
+      for (int j = 0; j < 7; ++j) a[j] = a[j + 1];
+      a[7] = 0ull;
+    }
+  }
+  return mine;
+}
+
+// Decisions of sequence blockIdx.x, then the copy of the decided position's hidden states into
+// its pair slot. Blocks past B only mark their pair slot as unused. With a bias set or top-F ids
+// the draft rows' 8 largest logits are merged from the ranges' lists first (one warp per row);
+// the bias set is the first bias_k of them, q' = q f / N with f = beta on the set and
+// N = 1 - (1 - beta) q(set), so the accept ratio gains N / f and the residual's draft weight is
+// rho = S_t / (S_d N) off the set and rho beta on it (Saguaro summary, "Method"). With top-F ids
+// every draft row below L is needed.
 __global__ void __launch_bounds__(128) hv_decide(const HvProblem p, float c, const int* off,
                                                  const uint16_t* A, const HeadRow* rows,
-                                                 uint16_t* Ad, HeadPair* pairs, int* seq_a) {
+                                                 const unsigned long long* keys, int nsplit,
+                                                 int Rmax, uint16_t* Ad, HeadPair* pairs,
+                                                 int* seq_a) {
   __shared__ int s_src_t, s_src_d;  // packed rows to copy (-1: none / zeros)
-  const int b = blockIdx.x;
-  if (threadIdx.x == 0) {
+  __shared__ unsigned long long s_key[8][8];
+  __shared__ float s_N[8], s_f[8];
+  __shared__ int s_nS[8], s_ok;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = p.K;
+  const bool top8 = hv_top8(p);
+  const bool bias = top8 && p.bias_k > 0 && p.beta < 1.f;
+  const int L = b < p.B ? p.lens[b] : 0;
+  const bool lok = b < p.B && L >= 1 && L <= K;
+  const int o = lok ? off[b] : 0;
+  if (top8 && lok) {
+    for (int i = warp; i < L; i += blockDim.x >> 5) {
+      const unsigned long long k = merge_ranges(keys, nsplit, Rmax, o + L + 1 + i);
+      if (lane < 8) s_key[i][lane] = k;
+    }
+    __syncthreads();
+    if (bias) {  // per draft row: q(set) summed in key order, N, and whether x_i is in the set
+      for (int i = warp; i < L; i += blockDim.x >> 5) {
+        const HeadRow rd = rows[o + L + 1 + i];
+        const unsigned long long kj = lane < 8 ? s_key[i][lane] : 0ull;
+        const bool in = lane < p.bias_k && kj != 0ull;
+        const float term = in ? exp2f(fmaf(key_value(kj), c, -rd.mc)) / rd.sum : 0.f;
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, in && key_id(kj) == p.x[static_cast<long long>(b) * K + i]);
+        const int n = __popc(__ballot_sync(0xffffffffu, in));
+        float sq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float tj = __shfl_sync(0xffffffffu, term, j);
+          if (j < n) sq += tj;
+        }
+        if (lane == 0) {
+          s_N[i] = fmaf(-(1.f - p.beta), sq, 1.f);
+          s_f[i] = hit ? p.beta : 1.f;
+          s_nS[i] = n;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
     s_src_t = -1;
     s_src_d = -1;
+    s_ok = 0;
     HeadPair pp;
-    pp.mc_t = pp.mc_d = pp.rho = 0.f;
+    pp.mc_t = pp.mc_d = pp.rho = pp.rho_s = 0.f;
     pp.skip = 1;
+    pp.nS = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pp.ids[j] = -1;
     if (b < p.B) {
-      const int K = p.K, L = p.lens[b];
       const int32_t* x = p.x + static_cast<long long>(b) * K;
       const float* u = p.uni ? p.uni + static_cast<long long>(b) * (K + 1) : nullptr;
       int32_t* tok = p.out_tok + static_cast<long long>(b) * (K + 1);
-      bool ok = L >= 1 && L <= K;
+      bool ok = lok;
       for (int i = 0; ok && i < L; ++i) ok = x[i] >= 0 && x[i] < p.V;
       if (ok && !p.greedy) {
         for (int i = 0; ok && i < L; ++i) ok = u[i] >= 0.f && u[i] < 1.f;
         ok = ok && u[K] >= 0.f && u[K] < 1.f;
       }
+      for (int i = 0; ok && p.fmax > 0 && i < L; ++i) ok = !row_bad(rows[o + L + 1 + i].max);
       int a = -1, last = -1, draw = 0;
       if (ok) {
-        const int o = off[b];
         if (p.greedy) {
           for (int i = 0; i <= L; ++i) {
             const HeadRow rt = rows[o + i];
@@ -175,14 +260,21 @@ __global__ void __launch_bounds__(128) hv_decide(const HvProblem p, float c, con
               ok = false;
               break;
             }
-            // p(x) / q(x) = 2^(z_t c - mc_t) S_d / (2^(z_d c - mc_d) S_t)
+            const float N = bias ? s_N[i] : 1.f, f = bias ? s_f[i] : 1.f;
+            // p(x) / q'(x) = 2^(z_t c - mc_t) S_d N / (2^(z_d c - mc_d) S_t f)
             const float lr = fmaf(rt.zx, c, -rt.mc) - fmaf(rd.zx, c, -rd.mc);
-            const float ratio = exp2f(lr) * (rd.sum / rt.sum);
+            const float ratio = exp2f(lr) * (rd.sum / rt.sum) * (N / f);
             if (u[i] < ratio) continue;
             a = i;
             pp.mc_t = rt.mc;
             pp.mc_d = rd.mc;
-            pp.rho = rt.sum / rd.sum;
+            pp.rho = rt.sum / (rd.sum * N);
+            pp.rho_s = pp.rho * p.beta;
+            if (bias) {
+              pp.nS = s_nS[i];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) pp.ids[j] = j < pp.nS ? key_id(s_key[i][j]) : -1;
+            }
             break;
           }
           if (ok && a == L) {
@@ -204,8 +296,10 @@ __global__ void __launch_bounds__(128) hv_decide(const HvProblem p, float c, con
         a = -1;
         draw = 0;
         pp.skip = 1;
+        pp.nS = 0;
         s_src_t = -1;
       }
+      s_ok = ok ? 1 : 0;
       p.out_acc[b] = a;
       for (int i = 0; i <= K; ++i)
         tok[i] = (ok && i < a) ? x[i] : ((ok && i == a && p.greedy) ? last : -1);
@@ -214,6 +308,15 @@ __global__ void __launch_bounds__(128) hv_decide(const HvProblem p, float c, con
     if (!p.greedy) pairs[b] = pp;
   }
   __syncthreads();
+  if (p.fmax > 0 && b < p.B) {  // the first F_i draft ids of rows below L; -1 elsewhere
+    int32_t* tf = p.out_topf + static_cast<long long>(b) * K * p.fmax;
+    const bool ok = s_ok != 0;
+    for (int e = tid; e < K * p.fmax; e += blockDim.x) {
+      const int i = e / p.fmax, f = e - i * p.fmax;
+      const unsigned long long k = (ok && i < L && f < p.fan[i] && f < 8) ? s_key[i][f] : 0ull;
+      tf[e] = k ? key_id(k) : -1;
+    }
+  }
   if (p.greedy || s_src_t < 0) return;
   const int nvec = p.d / 8;
   uint4* dt = reinterpret_cast<uint4*>(Ad + static_cast<long long>(head_pair_row(b, 0)) * p.d);
@@ -344,7 +447,9 @@ __global__ void __launch_bounds__(kPickThreads) hv_pick(const HvProblem p, float
     if (v0 + j >= p.V) break;
     const float et = ex2_fast(fmaf(zt[j], c, -pp.mc_t));
     const float ed = ex2_fast(fmaf(zd[j], c, -pp.mc_d));
-    const float w = use_p ? et : fmaxf(fmaf(-pp.rho, ed, et), 0.f);
+    float rk = pp.rho;
+    for (int k = 0; k < pp.nS; ++k) rk = pp.ids[k] == v0 + j ? pp.rho_s : rk;
+    const float w = use_p ? et : fmaxf(fmaf(-rk, ed, et), 0.f);
     cs += w;
     if (w > 0.f) lastpos = j;
     if (qfix(cs) > s_t) {
@@ -393,11 +498,16 @@ cudaError_t hv_run(const HvProblem& p, int sms, void* ws, unsigned int* err, cud
   P.tiles_per_split = L.tps;
   P.ntiles = L.ntiles;
   P.err = err;
-  cudaError_t e = launch_head_gemm(HEAD_STATS, A, p.d, p.W, p.ws, P, head_ctas(sms), stream);
+  const bool top8 = hv_top8(p);
+  unsigned long long* keys = top8 ? reinterpret_cast<unsigned long long*>(w + L.keys) : nullptr;
+  P.keys = keys;
+  cudaError_t e = launch_head_gemm(top8 ? HEAD_STATS_TOP8 : HEAD_STATS, A, p.d, p.W, p.ws, P,
+                                   head_ctas(sms), stream);
   if (e != cudaSuccess) return e;
   e = launch_head_combine(P, nullptr, nullptr, nullptr, nullptr, rows, stream);
   if (e != cudaSuccess) return e;
-  hv_decide<<<p.greedy ? p.B : L.npairs, 128, 0, stream>>>(p, c, off, A, rows, Ad, pairs, seqa);
+  hv_decide<<<p.greedy ? p.B : L.npairs, 128, 0, stream>>>(p, c, off, A, rows, keys, L.nsplit,
+                                                            L.Rmax, Ad, pairs, seqa);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.greedy) return e;
   HeadParams Q = P;
@@ -405,6 +515,7 @@ cudaError_t hv_run(const HvProblem& p, int sms, void* ws, unsigned int* err, cud
   Q.R_dev = nullptr;
   Q.ids = nullptr;
   Q.part = nullptr;
+  Q.keys = nullptr;
   Q.pair = pairs;
   Q.mass = mr;
   Q.mass_p = mp;

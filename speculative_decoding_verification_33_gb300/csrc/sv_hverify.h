@@ -23,9 +23,19 @@ struct HvProblem {
   const int32_t* lens;    // [B] draft lengths
   const float* uni;       // [B][K+1] uniforms (stochastic)
   float temperature;
+  float beta;             // weight of the Saguaro bias set (stochastic; 1 = none)
+  int bias_k;             // its size, 0..8 (0 = none)
+  int fmax;               // top-F ids per position (0 = none)
+  int fan[8];             // F_i of position i
   int32_t* out_acc;       // [B]
   int32_t* out_tok;       // [B][K+1]
+  int32_t* out_topf;      // [B][K][fmax] (fmax > 0)
 };
+
+// The draft rows' 8 largest logits are needed (a bias set or top-F ids).
+__host__ __device__ inline bool hv_top8(const HvProblem& p) {
+  return !p.greedy && ((p.bias_k > 0 && p.beta < 1.f) || p.fmax > 0);
+}
 
 // Bytes of device workspace the call needs beyond the 256-byte header.
 size_t hv_workspace_bytes(const HvProblem& p, int sms);

@@ -15,10 +15,13 @@
 //    tensor cores fill the other one:
 //      HEAD_STATS: the row's running maximum m (and the lowest id holding it), the sum
 //        2^(z c - fl(m c)) rescaled when m rises, and the logit at a requested id; one partial
-//        per (range, row), combined by a second kernel;
+//        per (range, row), combined by a second kernel; HEAD_STATS_TOP8 keeps besides the row's
+//        8 largest logits in the range (as keys: larger value first, then lower id), offered
+//        only the chunks whose maximum reaches the 8th so far;
 //      HEAD_RESID: rows come in (target, draft) pairs 16 lanes apart; each thread takes 16 of a
 //        chunk's 32 ids, gets the other row's logits by a lane exchange, and writes the mass of
-//        max(2^(z_t c - mc_t) - rho 2^(z_d c - mc_d), 0) over those 16 ids in 2^-44 units.
+//        max(2^(z_t c - mc_t) - rho 2^(z_d c - mc_d), 0) over those 16 ids in 2^-44 units (rho
+//        times beta on the ids of a Saguaro bias set).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -80,8 +83,9 @@ struct StatsState {
   int arg;
 };
 
-__device__ __forceinline__ void stats_chunk(StatsState& st, const float (&v)[32], int col0,
-                                            int nvalid, int x, float c, float* logits_row) {
+// Returns the chunk's maximum.
+__device__ __forceinline__ float stats_chunk(StatsState& st, const float (&v)[32], int col0,
+                                             int nvalid, int x, float c, float* logits_row) {
   float cm = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j)
@@ -117,15 +121,36 @@ __device__ __forceinline__ void stats_chunk(StatsState& st, const float (&v)[32]
     }
     st.s += acc.x + acc.y;
   }
+  return cm;
+}
+
+// The chunk's logits that reach the row's 8th largest so far, into its 8 largest (keys, ids
+// col0 + j); cm is the chunk's maximum.
+__device__ __forceinline__ void top8_chunk(unsigned long long (&keys)[8], float& thr,
+                                           const float (&v)[32], float cm, int col0, int nvalid) {
+  if (!(cm >= thr)) return;
+  unsigned mask = 0u;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) mask |= (j < nvalid && v[j] >= thr) ? (1u << j) : 0u;
+  while (mask) {
+    const int j = __ffs(mask) - 1;
+    mask &= mask - 1;
+    top8_insert(keys, thr, pick32(v, j), static_cast<uint32_t>(col0 + j));
+  }
 }
 
 // Residual mass (and target mass) of this thread's 16 ids of a chunk. Lane l < 16 holds the
 // target row of its pair and takes ids col0 .. col0 + 15; lane l + 16 holds the draft row and
 // takes the other 16. Both sums run in id order, one addition per id.
-__device__ __forceinline__ float2 resid_chunk(const float (&v)[32], bool is_d, int nvalid,
-                                              float c, const HeadPair& pp) {
+__device__ __forceinline__ float2 resid_chunk(const float (&v)[32], bool is_d, int col0,
+                                              int nvalid, float c, const HeadPair& pp) {
   float acc = 0.f, accp = 0.f;
   const int base = is_d ? 16 : 0;
+  // an id of the bias set among this thread's 16 (then each id is checked)
+  bool hb = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    hb |= k < pp.nS && static_cast<unsigned>(pp.ids[k] - (col0 + base)) < 16u;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float send = is_d ? v[j] : v[16 + j];
@@ -134,7 +159,13 @@ __device__ __forceinline__ float2 resid_chunk(const float (&v)[32], bool is_d, i
     const float zd = is_d ? v[16 + j] : got;
     const float et = ex2_fast(fmaf(zt, c, -pp.mc_t));
     const float ed = ex2_fast(fmaf(zd, c, -pp.mc_d));
-    const float w = fmaxf(fmaf(-pp.rho, ed, et), 0.f);
+    float rk = pp.rho;
+    if (hb) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        rk = (k < pp.nS && pp.ids[k] == col0 + base + j) ? pp.rho_s : rk;
+    }
+    const float w = fmaxf(fmaf(-rk, ed, et), 0.f);
     acc += (base + j < nvalid) ? w : 0.f;
     accp += (base + j < nvalid) ? et : 0.f;
   }
@@ -269,11 +300,16 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       int x = -1;
       float* lrow = nullptr;
       HeadPair pp;
-      pp.mc_t = pp.mc_d = pp.rho = 0.f;
+      pp.mc_t = pp.mc_d = pp.rho = pp.rho_s = 0.f;
       pp.skip = 1;
+      pp.nS = 0;
+      unsigned long long keys[8];
+      float kthr = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) keys[k] = 0ull;
       const bool is_d = lane >= 16;
       const int pr = (I.m0 >> 1) + 16 * q + (lane & 15);
-      if (MODE == HEAD_STATS) {
+      if (MODE != HEAD_RESID) {
         x = (P.ids && row < R) ? P.ids[row] : -1;
         lrow = (P.out_logits && row < R) ? P.out_logits + static_cast<long long>(row) * P.V
                                          : nullptr;
@@ -299,10 +335,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     v);
           const int col0 = n0 + ch * 32;
           const int nvalid = min(32, P.V - col0);
-          if (MODE == HEAD_STATS) {
-            stats_chunk(st, v, col0, nvalid, x, c, lrow);
+          if (MODE != HEAD_RESID) {
+            const float cm = stats_chunk(st, v, col0, nvalid, x, c, lrow);
+            if (MODE == HEAD_STATS_TOP8) top8_chunk(keys, kthr, v, cm, col0, nvalid);
           } else {
-            const float2 s = resid_chunk(v, is_d, nvalid, c, pp);
+            const float2 s = resid_chunk(v, is_d, col0, nvalid, c, pp);
             if (row < R) {
               const long long at = static_cast<long long>(pr) * P.nh + col0 / 16 + (is_d ? 1 : 0);
               P.mass[at] = pp.skip ? 0ull : qfix(s.x);
@@ -314,9 +351,15 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce[b]);
       }
-      if (MODE == HEAD_STATS && ok && row < R)
+      if (MODE != HEAD_RESID && ok && row < R)
         P.part[static_cast<long long>(I.split) * P.R + row] =
             make_float4(st.m, st.s, st.zx, __int_as_float(st.arg));
+      if (MODE == HEAD_STATS_TOP8 && ok && row < R) {
+        ulonglong2* kp = reinterpret_cast<ulonglong2*>(
+            P.keys + (static_cast<long long>(I.split) * P.R + row) * 8);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) kp[k] = make_ulonglong2(keys[2 * k], keys[2 * k + 1]);
+      }
     }
   }
   tc_fence_before();
@@ -436,10 +479,28 @@ bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, l
 
 int head_ctas(int sms) { return std::max(1, sms); }
 
-void head_split(int R, int V, int sms, int* nsplit, int* tiles_per_split, int* ntiles) {
+void head_split(int R, int V, int sms, int* nsplit, int* tiles_per_split, int* ntiles,
+                int max_ranges) {
   const int mt = std::max(1, (R + BM - 1) / BM);
   const int nt = (V + BN - 1) / BN;
   const int ctas = head_ctas(sms);
+  if (max_ranges > 0) {  // any range length that keeps the ranges at most max_ranges
+    long long best = -1;
+    int best_tps = nt;
+    for (int tps = (nt + max_ranges - 1) / max_ranges; tps <= nt; ++tps) {
+      const int ns = (nt + tps - 1) / tps;
+      const long long items = static_cast<long long>(mt) * ns;
+      const long long cost = (items + ctas - 1) / ctas * tps;
+      if (best < 0 || cost <= best) {
+        best = cost;
+        best_tps = tps;
+      }
+    }
+    *tiles_per_split = best_tps;
+    *nsplit = (nt + best_tps - 1) / best_tps;
+    *ntiles = nt;
+    return;
+  }
   // the range length (in tiles) with the fewest tile-times on the busiest CTA; longer ranges
   // win ties (fewer partial statistics)
   long long best = -1;
@@ -468,7 +529,9 @@ cudaError_t launch_head_gemm(int mode, const void* A, long long as, const void* 
       !make_map(&tb, weight, P.V, P.d, ws, BN))
     return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(kStages) * kStageBytes + 1024;
-  auto kern = mode == HEAD_STATS ? lmhead_kernel<HEAD_STATS> : lmhead_kernel<HEAD_RESID>;
+  auto kern = mode == HEAD_STATS        ? lmhead_kernel<HEAD_STATS>
+              : mode == HEAD_STATS_TOP8 ? lmhead_kernel<HEAD_STATS_TOP8>
+                                        : lmhead_kernel<HEAD_RESID>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;

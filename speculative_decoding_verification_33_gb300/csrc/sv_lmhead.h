@@ -17,6 +17,7 @@ enum HeadMode : int {
   HEAD_STATS = 0,  // per row: maximum, sum of 2^(z c - fl(m c)), logit at an id, first argmax
   HEAD_RESID = 1,  // per pair of rows (target, draft): masses of max(e_t - rho e_d, 0) and of e_t
                    // per 16 ids
+  HEAD_STATS_TOP8 = 2,  // HEAD_STATS, and per row and range the 8 largest logits as keys
 };
 
 // Per-row statistics after the combine (HEAD_STATS).
@@ -30,11 +31,15 @@ struct HeadRow {
 };
 
 // Per-pair inputs of HEAD_RESID: the residual weight of id v is
-// max(2^(z_t c - mc_t) - rho 2^(z_d c - mc_d), 0); rho = 0 gives the bonus weights of p alone.
-// A pair with skip != 0 produces zero masses.
+// max(2^(z_t c - mc_t) - rho_v 2^(z_d c - mc_d), 0) with rho_v = rho_s for the nS ids of the
+// bias set and rho for the others; rho = 0 gives the bonus weights of p alone. A pair with
+// skip != 0 produces zero masses.
 struct HeadPair {
   float mc_t, mc_d, rho;
   int skip;
+  float rho_s;
+  int nS;
+  int ids[8];
 };
 
 struct HeadParams {
@@ -48,6 +53,8 @@ struct HeadParams {
   const HeadPair* pair;      // resid: [R / 2] pair inputs
   unsigned long long* mass;  // resid: [R / 2][nh] residual masses in 2^-44 units
   unsigned long long* mass_p;  // resid: [R / 2][nh] masses of 2^(z_t c - mc_t) alone
+  unsigned long long* keys;  // stats with top 8: [nsplit][R][8] each row's 8 largest keys per
+                             // range (larger value first, then lower id; 0 = none)
   int nh;                    // resid: masses per pair (ntiles * kHeadHalves)
   int nsplit;                // vocabulary ranges
   int tiles_per_split;       // 256-column tiles per range
@@ -68,8 +75,10 @@ inline size_t head_part_bytes(int R, int nsplit) {
 }
 
 // The split of the vocabulary into ranges for up to R rows: ranges of whole 256-column tiles,
-// small enough that row tiles x ranges give every SM several work items.
-void head_split(int R, int V, int sms, int* nsplit, int* tiles_per_split, int* ntiles);
+// small enough that row tiles x ranges give every SM several work items; with max_ranges > 0,
+// no more than that many ranges (each row's per-range top 8 are merged over the ranges).
+void head_split(int R, int V, int sms, int* nsplit, int* tiles_per_split, int* ntiles,
+                int max_ranges = 0);
 
 // Persistent CTAs for the head GEMM on a device with `sms` multiprocessors.
 int head_ctas(int sms);

@@ -207,6 +207,15 @@ __device__ __forceinline__ void top8_insert(unsigned long long (&keys)[8], float
 }
 
 
+// The largest key over the warp (keys are distinct unless 0): the upper halves first, then the
+// lower halves of the lanes that hold the largest upper half.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k) {
+  const uint32_t hi = static_cast<uint32_t>(k >> 32);
+  const uint32_t mh = __reduce_max_sync(FULL, hi);
+  const uint32_t ml = __reduce_max_sync(FULL, hi == mh ? static_cast<uint32_t>(k) : 0u);
+  return (static_cast<unsigned long long>(mh) << 32) | ml;
+}
+
 // Merge every lane's descending list of 8 keys into the warp's top 8 (the result on every
 // lane); the lanes' lists are consumed.
 __device__ __forceinline__ void warp_top8(unsigned long long (&keys)[8],

@@ -159,15 +159,6 @@ struct Staged<float, VPT> {
 // ------------------------------------------------------------------------------------------
 // The 8 largest logits of a draft row slice (keys: larger value first, then lower id)
 // ------------------------------------------------------------------------------------------
-// The largest key over the warp (keys are distinct unless 0): the upper halves first, then the
-// lower halves of the lanes that hold the largest upper half.
-__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k) {
-  const uint32_t hi = static_cast<uint32_t>(k >> 32);
-  const uint32_t mh = __reduce_max_sync(FULL, hi);
-  const uint32_t ml = __reduce_max_sync(FULL, hi == mh ? static_cast<uint32_t>(k) : 0u);
-  return (static_cast<unsigned long long>(mh) << 32) | ml;
-}
-
 // Order-preserving 32 bits of a float, 0 for NaN (absent).
 __device__ __forceinline__ uint32_t float_ord(float v) {
   const uint32_t b = __float_as_uint(v);

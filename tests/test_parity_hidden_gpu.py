@@ -35,29 +35,33 @@ def bf16(bits: np.ndarray) -> "torch.Tensor":
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
 
-def run_gpu(x, w):
+def run_gpu(x, w, beta=1.0, bias_k=0, fanout=None):
     greedy = w.mode == "greedy"
     out = api.verify_hidden(bf16(x["hidden_target"]),
                             None if greedy else bf16(x["hidden_draft"]), bf16(x["weight"]),
                             torch.from_numpy(x["draft_tokens"]).cuda(),
                             torch.from_numpy(x["draft_lens"]).cuda(),
                             None if greedy else torch.from_numpy(x["uniforms"]).cuda(),
-                            temperature=w.temperature, mode=w.mode)
+                            temperature=w.temperature, beta=beta, bias_k=bias_k, fanout=fanout,
+                            mode=w.mode)
     torch.cuda.synchronize()
-    return out["accept_len"].cpu().numpy(), out["tokens"].cpu().numpy()
+    return (out["accept_len"].cpu().numpy(), out["tokens"].cpu().numpy(),
+            out["topf"].cpu().numpy() if fanout is not None else None)
 
 
-def check(x, w, margin, seqs=None, weight64=None):
+def check(x, w, margin, seqs=None, weight64=None, beta=1.0, bias_k=0, fanout=None,
+          topf_exact=True):
     greedy = w.mode == "greedy"
-    acc, tok = run_gpu(x, w)
+    acc, tok, topf = run_gpu(x, w, beta, bias_k, fanout)
     seqs = list(range(w.B)) if seqs is None else list(seqs)
     res = HO.verify_hidden_batch(x["hidden_target"], None if greedy else x["hidden_draft"],
                                  x["weight"] if weight64 is None else weight64,
                                  x["draft_tokens"], x["draft_lens"], x["uniforms"],
-                                 temperature=w.temperature, mode=w.mode, seqs=seqs)
-    rep = parity.compare(res, seqs, acc, tok, margin=margin)
+                                 temperature=w.temperature, mode=w.mode, beta=beta,
+                                 bias_k=bias_k, fanout=fanout, seqs=seqs)
+    rep = parity.compare(res, seqs, acc, tok, topf if topf_exact else None, margin=margin)
     assert rep.ok(), (rep.summary(), rep.mismatches[:4])
-    return rep, res
+    return rep, res, topf
 
 
 @pytest.mark.parametrize("B,K,V,d,T,mode", [
@@ -70,7 +74,7 @@ def test_hidden_exact(B, K, V, d, T, mode):
     w = W.HiddenWorkload(f"exact_{B}_{K}_{V}_{d}", B=B, K=K, V=V, d=d, mode=mode, temperature=T,
                          exact=True)
     x = W.hidden_inputs(w)
-    rep, res = check(x, w, margin=1e-6)
+    rep, res, _ = check(x, w, margin=1e-6)
     assert sum(r.accept_len for r in res if r.valid) > 0  # accept and reject paths both ran
     assert rep.flagged <= max(1, B // 20)
 
@@ -85,10 +89,70 @@ def test_hidden_exact_full_vocabulary(mode, B):
                          exact=True, drafter="prior")
     x = W.hidden_inputs(w)
     weight64 = HO.bf16_to_f64(x["weight"])  # converted once for the oracle's B head products
-    rep, res = check(x, w, margin=1e-6, weight64=weight64)
+    rep, res, _ = check(x, w, margin=1e-6, weight64=weight64)
     print(w.name, rep.summary())
     assert sum(r.accept_len for r in res if r.valid) > 0
     assert rep.flagged <= max(1, B // 20)
+
+
+@pytest.mark.parametrize("fanout,beta,bias_k", [
+    ((8, 4, 2, 1, 1), 0.5, 8),     # the Saguaro workload's options
+    (None, 0.3, 3),                # bias set only
+    ((3, 3, 3, 3, 3), 1.0, 0),     # top-F ids only
+])
+def test_hidden_exact_bias_set_and_top_f(fanout, beta, bias_k):
+    """The bias set (the bias_k largest draft logits, merged from the head GEMM's vocabulary
+    ranges) in the accept tests and the residual draw, and the top-F draft ids, on exact-grid
+    inputs: ids, lengths and tokens equal the oracle's."""
+    w = W.HiddenWorkload("exact_bias", B=40, K=5, V=3000, d=256, exact=True)
+    x = W.hidden_inputs(w)
+    x["draft_tokens"][3, 1] = w.V  # an invalid sequence: -1 everywhere, top-F ids included
+    rep, res, topf = check(x, w, margin=1e-6, beta=beta, bias_k=bias_k, fanout=fanout)
+    assert sum(r.accept_len for r in res if r.valid) > 0
+    assert rep.flagged <= max(1, w.B // 20)
+    if fanout is not None:
+        assert (topf[3] == -1).all()
+        assert (topf >= 0).sum() > 0
+
+
+def test_hidden_exact_bias_set_full_vocabulary():
+    """The bias set and top-F ids at the bench's vocabulary (V = 152064 over many ranges of the
+    head GEMM, K = 8 ragged): the merge over ranges must find each draft row's 8 largest."""
+    w = W.HiddenWorkload("exact_full_bias", B=48, K=8, V=152064, d=1024, exact=True,
+                         drafter="prior")
+    x = W.hidden_inputs(w)
+    weight64 = HO.bf16_to_f64(x["weight"])
+    rep, res, topf = check(x, w, margin=1e-6, weight64=weight64, beta=0.5, bias_k=8,
+                           fanout=(8, 4, 2, 1, 1, 1, 1, 1))
+    print(w.name, rep.summary())
+    assert sum(r.accept_len for r in res if r.valid) > 0
+    assert rep.flagged <= max(1, w.B // 20)
+
+
+def test_hidden_continuous_bias_set_and_top_f():
+    """Continuous inputs: the accept decisions at the float32 margin, and every top-F id within
+    the logits' rounding of the oracle's id at that rank (near ties may swap)."""
+    w = W.HiddenWorkload("cont_bias", B=32, K=5, V=4000, d=512, temperature=0.9)
+    x = W.hidden_inputs(w)
+    fan = (6, 3, 2, 1, 1)
+    rep, res, topf = check(x, w, margin=CONTINUOUS_MARGIN, beta=0.5, bias_k=8, fanout=fan,
+                           topf_exact=False)
+    assert sum(r.accept_len for r in res) > 0
+    swaps = 0
+    for b, r in enumerate(res):
+        if not r.valid:
+            assert (topf[b] == -1).all()
+            continue
+        L = int(x["draft_lens"][b])
+        z = HO.head_logits(x["hidden_draft"][b, :L], x["weight"])
+        err = HO.logit_error_bound(x["hidden_draft"][b, :L], x["weight"])
+        for i in range(L):
+            for f in range(fan[i]):
+                g, o = int(topf[b, i, f]), int(r.topf[i, f])
+                if g != o:
+                    swaps += 1
+                    assert abs(z[i, g] - z[i, o]) <= 2 * (err[i, g] + err[i, o])
+    assert swaps <= 2
 
 
 def test_hidden_every_draft_accepted_and_invalid_rows():
@@ -102,7 +166,7 @@ def test_hidden_every_draft_accepted_and_invalid_rows():
     x["draft_lens"][8] = 4
     x["draft_tokens"][9, 1] = 1500
     x["uniforms"][10, 3] = 1.0
-    rep, res = check(x, w, margin=1e-6)
+    rep, res, _ = check(x, w, margin=1e-6)
     assert all(res[b].accept_len == 3 for b in range(6))
     assert rep.invalid == 4
 
@@ -110,7 +174,7 @@ def test_hidden_every_draft_accepted_and_invalid_rows():
 def test_hidden_continuous():
     w = W.HiddenWorkload("cont", B=48, K=5, V=4000, d=512, temperature=0.9)
     x = W.hidden_inputs(w)
-    rep, res = check(x, w, margin=CONTINUOUS_MARGIN)
+    rep, res, _ = check(x, w, margin=CONTINUOUS_MARGIN)
     assert rep.flagged < rep.sequences
     assert sum(r.accept_len for r in res) > 0
 
@@ -120,7 +184,7 @@ def test_hidden_full_size_sampled():
     w = W.HIDDEN_WORKLOADS["hv_B256_K8_V152064_d3584"]
     x = W.hidden_inputs(w)
     seqs = list(range(0, w.B, 16)) + [w.B - 1]
-    rep, res = check(x, w, margin=CONTINUOUS_MARGIN, seqs=seqs)
+    rep, res, _ = check(x, w, margin=CONTINUOUS_MARGIN, seqs=seqs)
     # At this margin a draw's relative CDF gap (about 1 / V) is almost always below it, so the
     # draws here are flagged and only the accept decisions, lengths and accepted ids are compared;
     # test_hidden_exact_full_vocabulary compares the draws at this vocabulary.

@@ -116,6 +116,15 @@ __device__ __forceinline__ bool row_bad(float m) {
   return isnan(m) || m == INFINITY || m == -INFINITY;
 }
 
+// Order-preserving 32 bits of a float (a larger float gives a larger integer), and back.
+__device__ __forceinline__ uint32_t float_to_ord(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord_to_float(uint32_t m) {
+  return __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
+}
+
 // Sort key of a logit: larger value first, then lower id (-0 and +0 are one value). 0 means
 // "empty".
 __device__ __forceinline__ unsigned long long make_key(float z, uint32_t id) {

@@ -57,6 +57,7 @@ constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per
 constexpr int MODE_SAMPLE = 0, MODE_RESID = 1, MODE_TOP8 = 2;
 constexpr int kEnd = -1;  // unit tag after the last unit
 constexpr int kBatch = 4;  // candidate groups whose loads an epilogue warp keeps in flight
+constexpr int kCandCap = 64;  // sampling: candidate groups of the bias set kept in shared memory
 
 static_assert(RT == CT + ET + 32, "chunk warps, epilogue warps, one producer warp");
 static_assert(kStage % (8 * kGroup) == 0, "whole groups per stage");
@@ -78,6 +79,13 @@ struct RowShared {
   int S_ids[8];
   float S_z[8];
   unsigned long long t_loc;
+  // sampling with a bias set: the candidate groups of the 8 largest, and the corrections of the
+  // groups that hold ids of the set
+  unsigned long long cand[kCandCap];
+  int ncand;
+  int dg[8];
+  long long dq[8];
+  uint32_t tm8[NEW * 8];
 };
 
 // The epilogue team: thread t of ET, warp t / 32.
@@ -87,18 +95,6 @@ __device__ __forceinline__ void esync() { named_sync(kBarE, ET); }
 // ------------------------------------------------------------------------------------------
 // epilogue team reductions
 // ------------------------------------------------------------------------------------------
-__device__ unsigned long long team_sum_u64(unsigned long long v, RowShared& S) {
-  const int lane = threadIdx.x & 31, warp = et() >> 5;
-  v = warp_sum_u64(v);
-  if (lane == 0) S.ru[warp] = v;
-  esync();
-  unsigned long long r = 0;
-#pragma unroll
-  for (int w = 0; w < NEW; ++w) r += S.ru[w];
-  esync();
-  return r;
-}
-
 __device__ __forceinline__ unsigned long long warp_inclusive_u64(unsigned long long v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -109,14 +105,19 @@ __device__ __forceinline__ unsigned long long warp_inclusive_u64(unsigned long l
   return v;
 }
 
-__device__ unsigned long long team_exclusive_u64(unsigned long long v, RowShared& S) {
+__device__ unsigned long long team_exclusive_u64(unsigned long long v, RowShared& S,
+                                                 unsigned long long* total = nullptr) {
   const int lane = threadIdx.x & 31, warp = et() >> 5;
   const unsigned long long inc = warp_inclusive_u64(v);
   if (lane == 31) S.ru[warp] = inc;
   esync();
-  unsigned long long base = 0;
-  for (int w = 0; w < warp; ++w) base += S.ru[w];
+  unsigned long long base = 0, all = 0;
+  for (int w = 0; w < NEW; ++w) {
+    if (w < warp) base += S.ru[w];
+    all += S.ru[w];
+  }
   esync();
+  if (total) *total = all;
   return base + inc - v;
 }
 
@@ -390,10 +391,11 @@ __device__ __forceinline__ float group_sum(float v) {
 }
 
 // Group maxima and masses of one staged chunk (n valid elements) into gmax / gmass at the
-// chunk's first group; the groups also go into the thread's running row stats.
+// chunk's first group; the groups also go into the thread's running row stats. Returns the
+// lane's group maximum (every lane of the group holds it).
 template <typename T>
-__device__ __forceinline__ void chunk_groups(const T* stage, int n, float c, float* gmax,
-                                             float* gmass, RowRun& run) {
+__device__ __forceinline__ float chunk_groups(const T* stage, int n, float c, float* gmax,
+                                              float* gmass, RowRun& run) {
   using G = Lanes<T>;
   const int tid = threadIdx.x, lane = tid & 31;
   uint4 q[G::PPL];
@@ -406,6 +408,7 @@ __device__ __forceinline__ void chunk_groups(const T* stage, int n, float c, flo
     gmass[tid / G::LPG] = sm;
     run.add(g, gc, sm);
   }
+  return g;
 }
 
 // Group maxima only (the top-8 prepass), and the row maximum in the thread's running stats.
@@ -504,13 +507,21 @@ __device__ void chunk_row_stats(const RowRun& run, float c, RowShared& S, float*
   named_sync(kBarC, CT);  // the scratch is free again
 }
 
-// The row's top-8 elements (the bias set's candidates) into S.top. They lie in the 8 groups with
-// the largest maxima (ties to the lower group): an element outside them is beaten by those 8
-// maxima. The groups are found from the group maxima alone (only those at or above a lower bound
-// of the 8th are offered), then read again, two per epilogue warp, and their elements offered.
+// The row's top-8 elements (the bias set's candidates) into S.top, in two steps so that the
+// group reads can overlap other work. They lie in the 8 groups with the largest maxima (ties to
+// the lower group): an element outside them is beaten by those 8 maxima.
+//  - top8_groups: the 8 groups from the group maxima alone (only those at or above a lower bound
+//    of the 8th are offered); each epilogue warp then starts reading its two of them (G8);
+//  - top8_elements: their elements offered, from the 8th group maximum up (nothing below it can
+//    be among the 8 largest: the 8 groups' maxima reach it).
+struct G8 {
+  int g0, g1;
+  float a0, b0, a1, b1;
+  float thr;
+};
+
 template <typename T>
-__device__ void row_top8(const T* row, int V, bool vec, const float* gmax, int ng,
-                         RowShared& S) {
+__device__ G8 top8_groups(const T* row, int V, bool vec, const float* gmax, int ng, RowShared& S) {
   const int t = et(), lane = t & 31, warp = t >> 5;
   float m = -INFINITY;
   for (int g = t; g < ng; g += ET) m = fmaxf(m, gmax[g]);
@@ -525,38 +536,137 @@ __device__ void row_top8(const T* row, int V, bool vec, const float* gmax, int n
   }
   team_top8(gtop, S);
   static_assert(NEW * 2 == 8, "two groups per epilogue warp");
-  const unsigned long long k0 = S.top[2 * warp], k1 = S.top[2 * warp + 1];
+  const unsigned long long k0 = S.top[2 * warp], k1 = S.top[2 * warp + 1], k7 = S.top[7];
   esync();  // S.top is read by every warp before it is rewritten
-  const int g0 = k0 ? key_id(k0) : -1, g1 = k1 ? key_id(k1) : -1;
-  float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;
-  if (g0 >= 0) ld2<T>(row, kGroup * g0 + 2 * lane, V, vec, a0, b0);
-  if (g1 >= 0) ld2<T>(row, kGroup * g1 + 2 * lane, V, vec, a1, b1);
+  G8 r;
+  r.g0 = k0 ? key_id(k0) : -1;
+  r.g1 = k1 ? key_id(k1) : -1;
+  r.thr = k7 ? key_value(k7) : -INFINITY;
+  r.a0 = r.b0 = r.a1 = r.b1 = -INFINITY;
+  if (r.g0 >= 0) ld2<T>(row, kGroup * r.g0 + 2 * lane, V, vec, r.a0, r.b0);
+  if (r.g1 >= 0) ld2<T>(row, kGroup * r.g1 + 2 * lane, V, vec, r.a1, r.b1);
+  return r;
+}
+
+__device__ void top8_elements(const G8& r, int V, RowShared& S) {
+  const int lane = threadIdx.x & 31;
   WarpTop8 top;
-  top.init(-INFINITY);
-  const int e0 = kGroup * g0 + 2 * lane, e1 = kGroup * g1 + 2 * lane;
-  top.offer(g0 >= 0 && e0 < V, a0, static_cast<uint32_t>(e0));
-  top.offer(g0 >= 0 && e0 + 1 < V, b0, static_cast<uint32_t>(e0 + 1));
-  top.offer(g1 >= 0 && e1 < V, a1, static_cast<uint32_t>(e1));
-  top.offer(g1 >= 0 && e1 + 1 < V, b1, static_cast<uint32_t>(e1 + 1));
+  top.init(r.thr);
+  const int e0 = kGroup * r.g0 + 2 * lane, e1 = kGroup * r.g1 + 2 * lane;
+  top.offer(r.g0 >= 0 && e0 < V, r.a0, static_cast<uint32_t>(e0));
+  top.offer(r.g0 >= 0 && e0 + 1 < V, r.b0, static_cast<uint32_t>(e0 + 1));
+  top.offer(r.g1 >= 0 && e1 < V, r.a1, static_cast<uint32_t>(e1));
+  top.offer(r.g1 >= 0 && e1 + 1 < V, r.b1, static_cast<uint32_t>(e1 + 1));
   team_top8(top, S);
 }
 
-// Epilogue thread 0: the Saguaro bias set (the bias_k largest draft logits, from S.top) and the
-// renormalisation N = 1 - (1 - beta) sum_S q.
-__device__ void bias_set(const RowParams& P, RowShared& S, float Md, float Sd) {
-  if (et() != 0) return;
-  float sq = 0.f;
-  int nS = 0;
-  for (int j = 0; j < P.bias_k; ++j) {
-    const unsigned long long k = S.top[j];
-    if (k == 0ull) break;
-    const float z = key_value(k);
-    sq += exp2f((z - Md) * P.c) / Sd;
-    S.S_z[nS] = z;
-    S.S_ids[nS++] = key_id(k);
+template <typename T>
+__device__ void row_top8(const T* row, int V, bool vec, const float* gmax, int ng,
+                         RowShared& S) {
+  top8_elements(top8_groups<T>(row, V, vec, gmax, ng, S), V, S);
+}
+
+// top8_groups for the sampling epilogue, from the threads' contiguous runs of groups [lo, hi)
+// (tmax: the run's largest group maximum): the 8th largest run maximum, theta, is reached by 8
+// groups, so only runs whose maximum reaches it can hold one of the 8 largest groups, and only
+// their groups at or above theta are collected as keys (S.cand), of which warp 0 keeps the 8
+// largest. More than kCandCap such groups (ties at theta) take top8_groups instead.
+template <typename T>
+__device__ G8 run_top8_groups(const float* gmax, int lo, int hi, float tmax, int ng, const T* row,
+                              int V, bool vec, RowShared& S) {
+  const int t = et(), lane = t & 31, warp = t >> 5;
+  // the 8 largest run maxima of each warp (with repeats), then of the team
+  uint32_t o = float_to_ord(tmax), mine = 0u;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const uint32_t m = __reduce_max_sync(FULL, o);
+    if (lane == r) mine = m;
+    const unsigned who = __ballot_sync(FULL, o == m && m != 0u);
+    if (who && lane == __ffs(who) - 1) o = 0u;
   }
-  S.nS = nS;
-  S.N = fmaf(-(1.f - P.beta), sq, 1.f);
+  if (lane < 8) S.tm8[warp * 8 + lane] = mine;
+  if (t == 0) S.ncand = 0;
+  esync();
+  if (warp == 0) {
+    static_assert(NEW * 8 == 32, "the warps' 8 largest fill one warp");
+    uint32_t q = S.tm8[lane], m = 0u;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      m = __reduce_max_sync(FULL, q);
+      const unsigned who = __ballot_sync(FULL, q == m && m != 0u);
+      if (who && lane == __ffs(who) - 1) q = 0u;
+    }
+    if (lane == 0) S.rb[0] = m ? ord_to_float(m) : -INFINITY;
+  }
+  esync();
+  const float th = S.rb[0];
+  if (tmax >= th)
+    for (int g = lo; g < hi; ++g)
+      if (gmax[g] >= th) {
+        const int i = atomicAdd(&S.ncand, 1);
+        if (i < kCandCap) S.cand[i] = make_key(gmax[g], static_cast<uint32_t>(g));
+      }
+  esync();
+  const int n = S.ncand;
+  if (n > kCandCap) return top8_groups<T>(row, V, vec, gmax, ng, S);
+  if (warp == 0) {
+    static_assert(kCandCap == 64, "two candidates per lane");
+    unsigned long long a = lane < n ? S.cand[lane] : 0ull;
+    unsigned long long c = lane + 32 < n ? S.cand[lane + 32] : 0ull;
+    if (c > a) {
+      const unsigned long long x = a;
+      a = c;
+      c = x;
+    }
+    unsigned long long k = 0ull;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const unsigned long long m = warp_max_key(a);
+      if (lane == r) k = m;
+      if (m != 0ull && a == m) {
+        a = c;
+        c = 0ull;
+      }
+    }
+    if (lane < 8) S.top[lane] = k;
+  }
+  esync();
+  const unsigned long long k0 = S.top[2 * warp], k1 = S.top[2 * warp + 1], k7 = S.top[7];
+  esync();  // S.top is read by every warp before it is rewritten
+  G8 r;
+  r.g0 = k0 ? key_id(k0) : -1;
+  r.g1 = k1 ? key_id(k1) : -1;
+  r.thr = k7 ? key_value(k7) : -INFINITY;
+  r.a0 = r.b0 = r.a1 = r.b1 = -INFINITY;
+  if (r.g0 >= 0) ld2<T>(row, kGroup * r.g0 + 2 * lane, V, vec, r.a0, r.b0);
+  if (r.g1 >= 0) ld2<T>(row, kGroup * r.g1 + 2 * lane, V, vec, r.a1, r.b1);
+  return r;
+}
+
+// The Saguaro bias set (the bias_k largest draft logits, from S.top) and the renormalisation
+// N = 1 - (1 - beta) sum_S q, the terms summed in key order. Epilogue warp 0.
+__device__ void bias_set(const RowParams& P, RowShared& S, float Md, float Sd) {
+  if (et() >= 32) return;
+  const int lane = et();
+  const unsigned long long k = lane < 8 ? S.top[lane] : 0ull;
+  const bool in = lane < P.bias_k && k != 0ull;
+  const float z = in ? key_value(k) : 0.f;
+  const float term = in ? exp2f((z - Md) * P.c) / Sd : 0.f;
+  const int nS = __popc(__ballot_sync(FULL, in));
+  float sq = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float tj = __shfl_sync(FULL, term, j);
+    if (j < nS) sq += tj;
+  }
+  if (in) {
+    S.S_z[lane] = z;
+    S.S_ids[lane] = key_id(k);
+  }
+  if (lane == 0) {
+    S.nS = nS;
+    S.N = fmaf(-(1.f - P.beta), sq, 1.f);
+  }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -767,36 +877,71 @@ __device__ void sample_epilogue(const RowParams& P, RowShared& S, int u, float* 
     return;
   }
   int nS = 0;
-  if (BIAS) {
-    row_top8<T>(row, V, vec, gmax, ng, S);
-    bias_set(P, S, M, Sd);
-    esync();
-    nS = S.nS;
-  }
-
-  // group masses relative to the row maximum, the biased ids corrected; fixed-point total
+  // group masses relative to the row maximum, over contiguous runs of groups per thread (so that
+  // the prefix of the inverse CDF follows the ids): fixed-point run totals, the run's largest
+  // group maximum
   const float Mdc = __fmul_rn(M, c);
-  unsigned long long acc = 0;
-  for (int g = t; g < ng; g += ET) {
-    const float gm = gmax[g];
-    float w = gm > -INFINITY ? gmass[g] * exp2f(__fmul_rn(gm, c) - Mdc) : 0.f;
-    for (int j = 0; j < nS; ++j)
-      if (S.S_ids[j] / kGroup == g)
-        w = fmaxf(fmaf(P.beta - 1.f, ex2_fast(fmaf(S.S_z[j], c, -Mdc)), w), 0.f);
-    gmass[g] = w;
-    acc += qfix(w);
-  }
-  const unsigned long long W = team_sum_u64(acc, S);  // (its barriers publish gmass)
-  const float uu = P.uni[u];
-  const bool uok = uu >= 0.f && uu < 1.f;
-  const unsigned long long tt = scale_floor(uu, W);
-
-  // the group holding tt: contiguous runs of groups per thread, so the prefix follows the ids
   const int lo = static_cast<int>((static_cast<long long>(t) * ng) / ET);
   const int hi = static_cast<int>((static_cast<long long>(t + 1) * ng) / ET);
   unsigned long long csum = 0;
-  for (int g = lo; g < hi; ++g) csum += qfix(gmass[g]);
-  unsigned long long pre = team_exclusive_u64(csum, S);
+  float tmax = -INFINITY;
+  for (int g = lo; g < hi; ++g) {
+    const float gm = gmax[g];
+    tmax = fmaxf(tmax, gm);
+    const float w = gm > -INFINITY ? gmass[g] * exp2f(__fmul_rn(gm, c) - Mdc) : 0.f;
+    gmass[g] = w;
+    csum += qfix(w);
+  }
+  // the bias set's 8 candidate groups, their reads started (they land during the prefix)
+  G8 cand;
+  if (BIAS) cand = run_top8_groups<T>(gmax, lo, hi, tmax, ng, row, V, vec, S);
+  unsigned long long W = 0;
+  unsigned long long pre = team_exclusive_u64(csum, S, &W);  // (its barriers publish gmass)
+  if (BIAS) {
+    // the bias set, then (warp 0, lane j for the first id of each group in set order) the
+    // weights of its ids scaled by beta in the groups holding them: the change of each such
+    // group's fixed-point mass moves the totals and prefixes after it
+    top8_elements(cand, V, S);
+    bias_set(P, S, M, Sd);
+    if (t < 32) __syncwarp();  // warp 0 wrote the set
+    if (t < 8) {
+      const int ns = S.nS;
+      int g = -1;
+      long long dq = 0;
+      if (t < ns) {
+        g = S.S_ids[t] / kGroup;
+        bool first = true;
+        for (int i = 0; i < t; ++i) first = first && S.S_ids[i] / kGroup != g;
+        if (first) {
+          float w = gmass[g];
+          const unsigned long long before = qfix(w);
+          for (int i = t; i < ns; ++i)
+            if (S.S_ids[i] / kGroup == g)
+              w = fmaxf(fmaf(P.beta - 1.f, ex2_fast(fmaf(S.S_z[i], c, -Mdc)), w), 0.f);
+          gmass[g] = w;
+          dq = static_cast<long long>(qfix(w) - before);
+        } else {
+          g = -1;
+        }
+      }
+      S.dg[t] = g;
+      S.dq[t] = dq;
+    }
+    esync();
+    nS = S.nS;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int g = S.dg[j];
+      if (g < 0) continue;
+      const unsigned long long d = static_cast<unsigned long long>(S.dq[j]);
+      W += d;
+      if (g < lo) pre += d;
+      else if (g < hi) csum += d;
+    }
+  }
+  const float uu = P.uni[u];
+  const bool uok = uu >= 0.f && uu < 1.f;
+  const unsigned long long tt = scale_floor(uu, W);
   if (t == 0) S.gstar = -1;
   esync();
   if (uok && pre <= tt && tt < pre + csum) {

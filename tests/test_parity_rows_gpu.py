@@ -95,6 +95,45 @@ def test_draft_draw_bad_uniforms_and_rows():
     check_draws(rows, uni, T=0.8, beta=1.0, bias_k=0, tau=0.5)
 
 
+def _planted_rows(V, dtype):
+    """Draft rows whose bias set decides the draws (bf16 bit patterns or float32): (a) 12 large,
+    close logits over N(0, 1) noise (most of the mass, the 8th and 9th close); (b) groups of 4
+    ever larger logits planted in chunks 2, 5, 8, ... of the stream, so the kept candidate groups
+    fill up and are compacted; (c) a decreasing row (the first chunk holds the 8 largest); (d) an
+    increasing row (every later group reaches the kept bound: the store runs over and the groups
+    are read again); (e) a row of equal values."""
+    rng = np.random.default_rng(21)
+    base = rng.standard_normal((5, V)).astype(np.float32)
+    ids = rng.choice(V, 12, replace=False)
+    base[0, ids] = 14.0 + 0.05 * np.arange(12)
+    chunk = 8192 if dtype == "bf16" else 4096
+    for j, ch in enumerate(range(2, (V + chunk - 1) // chunk, 3)):
+        lo = ch * chunk
+        at = lo + rng.choice(min(chunk, V - lo), 4, replace=False)
+        base[1, at] = 12.0 + j + 0.1 * np.arange(4)
+    base[2] = np.linspace(8.0, -8.0, V)
+    base[3] = np.linspace(-8.0, 8.0, V)
+    base[4] = 1.0
+    return W.f32_to_bf16_bits(base) if dtype == "bf16" else base
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_draft_draw_bias_set_decides_the_draws(dtype):
+    """Each planted row drawn at 96 evenly spaced uniforms: the tokens sweep the inverse CDF of
+    q' = q reweighted by beta on the 8 largest logits, so a wrong bias set (kept groups missing
+    one of the 8, a compaction that drops one, a fallback that does not read the groups again)
+    moves tokens across the CDF."""
+    V = 152064 if dtype == "bf16" else 70001
+    base = _planted_rows(V, dtype)
+    n = 96
+    rows = np.repeat(base, n, axis=0)
+    uni = np.tile((np.arange(n, dtype=np.float64) + 0.5) / n, base.shape[0]).astype(np.float32)
+    checked, flagged = check_draws(rows, uni, T=1.0, beta=0.3, bias_k=8, tau=0.1,
+                                   seqs=range(2 * n))  # the planted rows, where the set decides
+    assert flagged <= checked // 20
+    check_draws(rows, uni, T=1.0, beta=0.3, bias_k=8, tau=0.1, seqs=range(2 * n, rows.shape[0]))
+
+
 def test_draft_draw_frequencies_follow_biased_draft():
     """Many draws of one row: token frequencies match q' (chi-square style bound)."""
     V, n = 64, 1 << 16

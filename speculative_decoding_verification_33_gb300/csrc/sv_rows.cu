@@ -58,6 +58,7 @@ constexpr int MODE_SAMPLE = 0, MODE_RESID = 1, MODE_TOP8 = 2;
 constexpr int kEnd = -1;  // unit tag after the last unit
 constexpr int kBatch = 4;  // candidate groups whose loads an epilogue warp keeps in flight
 constexpr int kCandCap = 64;  // sampling: candidate groups of the bias set kept in shared memory
+constexpr int kTierCap = 256;  // residual: groups of one tier listed in shared memory at once
 
 static_assert(RT == CT + ET + 32, "chunk warps, epilogue warps, one producer warp");
 static_assert(kStage % (8 * kGroup) == 0, "whole groups per stage");
@@ -86,6 +87,9 @@ struct RowShared {
   int dg[8];
   long long dq[8];
   uint32_t tm8[NEW * 8];
+  // residual: the groups of the current tier
+  int tl[kTierCap];
+  int ntl;
 };
 
 // The epilogue team: thread t of ET, warp t / 32.
@@ -1022,6 +1026,8 @@ __device__ __forceinline__ void offer_groups(WarpTop8& top, const T* zt, const T
       ld2<T>(zd, e, V, vec, da[k], db[k]);
     }
   }
+  float wa[kBatch], wb[kBatch];
+  float lm = -INFINITY;  // the lane's largest residual of the batch
 #pragma unroll
   for (int k = 0; k < kBatch; ++k) {
     const int e = kGroup * gs[k] + 2 * lane;
@@ -1031,26 +1037,18 @@ __device__ __forceinline__ void offer_groups(WarpTop8& top, const T* zt, const T
         ra = S.S_ids[j] == e ? rhoS : ra;
         rb = S.S_ids[j] == e + 1 ? rhoS : rb;
       }
-    const float wa =
-        fmaxf(fmaf(-ra, ex2_fast(fmaf(da[k], c, -Mdc)), ex2_fast(fmaf(ta[k], c, -Mtc))), 0.f);
-    const float wb =
-        fmaxf(fmaf(-rb, ex2_fast(fmaf(db[k], c, -Mdc)), ex2_fast(fmaf(tb[k], c, -Mtc))), 0.f);
-    top.offer(gs[k] >= 0 && e < V && wa > 0.f, wa, static_cast<uint32_t>(e));
-    top.offer(gs[k] >= 0 && e + 1 < V && wb > 0.f, wb, static_cast<uint32_t>(e + 1));
+    wa[k] = fmaxf(fmaf(-ra, ex2_fast(fmaf(da[k], c, -Mdc)), ex2_fast(fmaf(ta[k], c, -Mtc))), 0.f);
+    wb[k] = fmaxf(fmaf(-rb, ex2_fast(fmaf(db[k], c, -Mdc)), ex2_fast(fmaf(tb[k], c, -Mtc))), 0.f);
+    if (gs[k] >= 0 && e < V && wa[k] > 0.f) lm = fmaxf(lm, wa[k]);
+    if (gs[k] >= 0 && e + 1 < V && wb[k] > 0.f) lm = fmaxf(lm, wb[k]);
   }
-}
-
-// A warp's candidate groups (bits of the ballot over groups base + lane) in batches of kBatch.
-template <typename Body>
-__device__ __forceinline__ void batches(unsigned bits, int base, Body body) {
-  while (bits) {
-    int gs[kBatch];
+  // 8 lanes hold a residual at least the 8th largest lane maximum: nothing below it can enter
+  top.thr = fmaxf(top.thr, warp_8th_largest(lm));
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      gs[k] = bits ? base + __ffs(bits) - 1 : -1;
-      bits &= bits - 1;
-    }
-    body(gs);
+  for (int k = 0; k < kBatch; ++k) {
+    const int e = kGroup * gs[k] + 2 * lane;
+    top.offer(gs[k] >= 0 && e < V && wa[k] > 0.f, wa[k], static_cast<uint32_t>(e));
+    top.offer(gs[k] >= 0 && e + 1 < V && wb[k] > 0.f, wb[k], static_cast<uint32_t>(e + 1));
   }
 }
 
@@ -1076,8 +1074,12 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const fl
   }
   int nS = 0;
   float N = 1.f;
-  if (BIAS) {
-    row_top8<T>(zd, V, vec, gmax_d, ng, S);
+  if (BIAS) {  // the bias set: the draft row's 8 largest, from contiguous runs of its groups
+    const int lo = static_cast<int>((static_cast<long long>(t) * ng) / ET);
+    const int hi = static_cast<int>((static_cast<long long>(t + 1) * ng) / ET);
+    float tmax = -INFINITY;
+    for (int g = lo; g < hi; ++g) tmax = fmaxf(tmax, gmax_d[g]);
+    top8_elements(run_top8_groups<T>(gmax_d, lo, hi, tmax, ng, zd, V, vec, S), V, S);
     bias_set(P, S, D2.x, D2.y);
     esync();
     nS = S.nS;
@@ -1096,25 +1098,38 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const fl
   // rounding of both sides. Stored over the log-ratio maxima.
   const float kappa = __log2f(BIAS ? rhoS : rho) + Mtc - Mdc;
   float bm = -INFINITY;
+  int gbest = -1;
   for (int g = t; g < ng; g += ET) {
     const float x = fmaf(gdel[g], c, -kappa) + 1e-4f;
     const float et = ex2_fast(fmaf(gmax_t[g], c, -Mtc));
     const float f = x <= 0.f ? 0.f : (x < 0.25f ? x * 0.69314718f : 1.f - ex2_fast(-x) + 1e-6f);
     const float bnd = gmax_t[g] > -INFINITY ? et * fminf(f, 1.f) * 1.001f + 1e-30f : 0.f;
     gdel[g] = bnd;
+    if (bnd > bm) gbest = g;
     bm = fmaxf(bm, bnd);
+  }
+  // The rows streamed long ago are out of L2 by now: the group of the largest bound of each
+  // thread (those the tiers below read first) is fetched into L2 at once, both rows, so that the
+  // tiers' reads find it there instead of queueing behind the stream one tier after another.
+  if (gbest >= 0 && bm > 0.f) {
+    const int e0 = kGroup * gbest, e1 = min(V, e0 + kGroup) - 1;
+    prefetch_l2(zt + e0);
+    prefetch_l2(zt + e1);
+    prefetch_l2(zd + e0);
+    prefetch_l2(zd + e1);
   }
   // Tiers of groups in decreasing bound: each tier is the groups (not yet visited) whose bound
   // reaches both the 8th best residual so far and a lower bound of the 8th largest remaining
   // bound; a visited group's bound is set to -1. It ends when no group's bound reaches the 8th
-  // best residual; after kTiers tiers, every group that still could is visited at once.
+  // best residual; after kTiers tiers, every group that still could is visited at once. A tier's
+  // groups are listed first (up to kTierCap; the rest wait for the next round), then taken four
+  // at a time per warp, so that a warp's reads of a tier are a round trip or two, not one per
+  // group.
   constexpr int kTiers = 6;
   WarpTop8 top;
   top.init(-INFINITY);
   const int per = (ng + ET - 1) / ET;
-  auto offer_batch = [&](const int (&gs)[kBatch]) {
-    offer_groups<T, BIAS>(top, zt, zd, gs, V, vec, c, Mtc, Mdc, rho, rhoS, S, nS);
-  };
+  const int warp = t >> 5;
   float thr = 0.f;  // the team's 8th best residual so far (0 until 8 are known)
   for (int tier = 0;; ++tier) {
     float bt = -INFINITY;
@@ -1124,24 +1139,39 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const fl
         const float bg = gdel[g];
         if (bg > 0.f && bg >= thr) bm2 = fmaxf(bm2, bg);
       }
-      bt = team_bound(bm2, S);
+      bt = team_bound(bm2, S);  // (its barriers also order the list's reset below)
     }
+    if (t == 0) S.ntl = 0;
+    esync();
     const float lo = fmaxf(bt, thr);
-    bool any = false;
+    bool over = false;
     for (int k = 0; k < per; ++k) {
-      const int g = t + k * ET;  // warp w of the team scans groups base .. base + 31
-      const float bg = g < ng ? gdel[g] : -1.f;
-      const bool pick = bg > 0.f && bg >= lo;
-      any |= pick;
-      batches(__ballot_sync(FULL, pick), g - (t & 31), offer_batch);
-      if (pick) gdel[g] = -1.f;
+      const int g = t + k * ET;
+      if (g < ng && gdel[g] > 0.f && gdel[g] >= lo) {
+        const int at = atomicAdd(&S.ntl, 1);
+        if (at < kTierCap) {
+          S.tl[at] = g;
+          gdel[g] = -1.f;
+        } else {
+          over = true;  // listed in a later round
+        }
+      }
     }
-    if (!named_sync_or(kBarE, ET, any)) break;  // nothing left that can reach the top 8
+    esync();
+    const int n = min(S.ntl, kTierCap);
+    if (n == 0) break;  // nothing left that can reach the top 8
+    for (int j0 = kBatch * warp; j0 < n; j0 += kBatch * NEW) {
+      int gs[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) gs[k] = j0 + k < n ? S.tl[j0 + k] : -1;
+      offer_groups<T, BIAS>(top, zt, zd, gs, V, vec, c, Mtc, Mdc, rho, rhoS, S, nS);
+    }
+    const bool more = named_sync_or(kBarE, ET, over);
     team_top8(top, S);
     const unsigned long long k8 = S.top[7];
     thr = k8 ? key_value(k8) : 0.f;
     if (thr > top.thr) top.thr = thr;
-    if (bt == -INFINITY) break;  // that tier took every group still in reach
+    if (bt == -INFINITY && !more) break;  // that tier took every group still in reach
   }
   team_top8(top, S);
   if (t < P.fmax) {

@@ -36,7 +36,9 @@ struct StreamRes {
   size_t stage_bytes = 0;
   void* scr = nullptr;    // rows read in place from host memory: the draw's device copies
   size_t scr_bytes = 0;
-};
+  void* dd = nullptr;     // deferred draws of the walk (sv::walk_draw_carve) for batches of up
+  int dd_cap = 0;         // to dd_cap sequences: order list (all zero between calls), decisions,
+};                        // masses
 
 // Workspace of spec_verify_noalloc: the queue counters and error word the kernel needs (256
 // bytes), for batches of up to kNoAllocMaxB sequences, in device memory that belongs to this
@@ -514,7 +516,58 @@ sv_status run(const sv_problem* p, const void* tgt, const void* dft, const int32
     st = launch_prepass(p, c, dev, L.dtype, dft, lens, P.c, keys, out_topf, P.ws, stream);
     if (st != SV_OK) return st;
   }
-  return sv::launch(L, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  // Deferred draws: a stochastic decision-ahead walk (no top-8, no diagnostics, rows in device
+  // memory and 16-byte aligned, the library's own workspace) publishes each decided sequence's
+  // draw constants instead of drawing; two launches chained after it take the draws, the slice
+  // masses of a sequence starting as soon as the walk has decided it.
+  sv::SmallParams D;
+  memset(&D, 0, sizeof(D));
+  bool defer = !c.greedy && !L.p.top8 && !prepass && !debug_all && P.use_bulk && !zero_copy &&
+               !ws_user && p->B <= 65535 &&
+               sv::small_plan(p->B, p->K, p->V, sm_count(dev), small_rows_per_sm(dev, L.dtype),
+                              &D);
+  if (defer) {
+    StreamRes& r = g_res[{dev, stream}];
+    if (r.dd_cap < p->B) {
+      const size_t need = sv::walk_draw_ws_bytes(p->B);
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+        return SV_ERR_UNSUPPORTED;  // the state must exist (and be large enough) before capture
+      if (r.dd) {
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return SV_ERR_CUDA;
+        cudaFree(r.dd);
+        r.dd = nullptr;
+        r.dd_cap = 0;
+      }
+      if (cudaMalloc(&r.dd, need) != cudaSuccess || cudaMemset(r.dd, 0, need) != cudaSuccess) {
+        if (r.dd) cudaFree(r.dd);
+        r.dd = nullptr;
+        return SV_ERR_CUDA;
+      }
+      r.dd_cap = p->B;
+    }
+    D.tgt = tgt;
+    D.dft = dft;
+    D.t_stride = p->target_row_stride;
+    D.d_stride = p->draft_row_stride;
+    D.lens = lens;
+    D.tokens = tok;
+    D.uni = uni;
+    D.V = p->V;
+    D.c = P.c;
+    D.aligned = 1;
+    D.beta = 1.f;
+    D.err = &P.ws->error;
+    D.out_acc = out_acc;
+    D.out_tok = out_tok;
+    sv::walk_draw_carve(D, static_cast<char*>(r.dd), r.dd_cap);
+    P.defer = 1;
+    P.ddec = D.dec;
+    P.dlist = D.dlist;
+  }
+  if (sv::launch(L, stream) != cudaSuccess) return SV_ERR_CUDA;
+  if (defer && sv::launch_walk_draws(D, L.dtype, stream) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
 }
 
 }  // namespace
@@ -576,8 +629,10 @@ sv_status spec_verify_route(const sv_problem* prob, int mode, int* route, int* l
   }
   if (route) *route = static_cast<int>(r);
   if (launches)
+    // (the stochastic walk without a top-8 prepass defers its draws to two launches)
     *launches = r == ROUTE_SMALL ? 3
-                                 : (r == ROUTE_GREEDY_ROWS || needs_top8(prob, c)) ? 2 : 1;
+                : (r == ROUTE_GREEDY_ROWS || needs_top8(prob, c)) ? 2
+                : c.greedy ? 1 : 3;
   return SV_OK;
 }
 

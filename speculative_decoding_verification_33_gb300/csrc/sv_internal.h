@@ -19,10 +19,11 @@ constexpr int kMaxSlice = 65536;  // elements of a row one CTA owns (bounds the 
 // zero when the last cluster leaves, so stream-ordered launches (and replays of a captured
 // launch) can reuse it.
 struct Workspace {
-  unsigned int next;   // dynamic sequence queue
-  unsigned int done;   // clusters that have finished
-  unsigned int error;  // bit 0: a bounded wait gave up
-  unsigned int pad[61];
+  unsigned int next;    // dynamic sequence queue
+  unsigned int done;    // clusters that have finished
+  unsigned int error;   // bit 0: a bounded wait gave up
+  unsigned int dcount;  // deferred draws: sequences decided so far
+  unsigned int pad[60];
 };
 static_assert(sizeof(Workspace) == 256, "workspace layout");
 
@@ -60,6 +61,12 @@ struct Params {
   int lpt;         // take sequences longest draft first
   const unsigned long long* keys;  // top-8 keys of every draft row from the prepass, or NULL
   Workspace* ws;
+  // Deferred draws (stochastic decision-ahead walk): instead of drawing, a decided sequence's
+  // draw constants go to ddec[seq] (a SmallDecision, sv_small.h) and seq + 1 to dlist[k] for the
+  // k-th sequence decided; the draw launches that follow the walk take them from there.
+  int defer;
+  void* ddec;
+  int* dlist;
 };
 
 constexpr int kLptMaxB = 4096;  // larger batches keep the natural order

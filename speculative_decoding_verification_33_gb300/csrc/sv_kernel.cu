@@ -31,6 +31,7 @@
 #include <stdint.h>
 
 #include "sv_internal.h"
+#include "sv_small.h"
 #include "sv_math.cuh"
 #include "sv_ptx.cuh"
 
@@ -429,9 +430,11 @@ __device__ void producer(const Params& P, CtaState& S, const Ring<T, GREEDY>& R)
           q_pos = P.K + 1;
           q_mark = 0;
         } else {  // the decision has landed
-          q_ph = GREEDY ? POST : DRAW;
-          q_pos = GREEDY ? stop + 1 : stop;
-          if (GREEDY) q_mark = stop;
+          // (a deferred draw, like a greedy stop, streams nothing more of this sequence)
+          const bool nodraw = GREEDY || P.defer;
+          q_ph = nodraw ? POST : DRAW;
+          q_pos = nodraw ? stop + 1 : stop;
+          if (nodraw) q_mark = stop;
         }
         q_k = 0;
       }
@@ -1267,6 +1270,8 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
   __shared__ unsigned long long sdesc[NS];
   __shared__ int lcnt[kMaxK + 1];
 
+  // with deferred draws, let the draw launches start (their CTAs wait per sequence)
+  if (P.defer) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using RingT = Ring<T, GREEDY>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -1465,7 +1470,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
         } else {
           decided = true;
           a = outcome;
-          if (!GREEDY) {
+          if (!GREEDY && !P.defer) {
             if (a < L)
               draw_token<T, GREEDY, false>(P, S, X, xbar, xround, rank, C, R, seq, a, gmass, cons, late);
             else
@@ -1688,6 +1693,31 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
             }
           }
         }
+        if (!GREEDY && P.defer && tid == 0) {
+          // the draw's constants for the deferred draw launches (the same as draw_token's),
+          // then the sequence's place in the order they read
+          SmallDecision d;
+          d.ok = bad ? 0 : 1;
+          d.a = aborted ? -2 : (invalid ? -1 : a);
+          d.mct = __fmul_rn(S.M_t, P.c);
+          d.mcd = 0.f;
+          d.rho = d.rho_s = 0.f;
+          d.nS = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) d.ids[j] = -1;
+          if (!bad && a < L) {  // a residual draw; at a == L the bonus draw from p_L
+            d.mcd = __fmul_rn(S.M_d, P.c);
+            const float ft = fmaf(-fmaf(S.M_t, P.c, -d.mct), kLn2, 1.f);
+            const float fd = fmaf(-fmaf(S.M_d, P.c, -d.mcd), kLn2, 1.f);
+            d.rho = (fd * S.S_t) / (ft * (S.S_d * S.N));
+            d.rho_s = d.rho * P.beta;
+          }
+          const int q = static_cast<int>(atomicAdd(&P.ws->dcount, 1u));
+          d.q = q;
+          static_cast<SmallDecision*>(P.ddec)[seq] = d;
+          __threadfence();
+          st_release_gpu_s32(P.dlist + q, seq + 1);
+        }
         if (P.dbg_lse_t && tid <= K)
           P.dbg_lse_t[static_cast<long long>(seq) * (K + 1) + tid] = S.lse_t[tid];
         if (tid < K) {
@@ -1742,6 +1772,7 @@ __global__ void __launch_bounds__(NTOT, 3) verify_kernel(const Params P) {
     if (old == static_cast<unsigned>(P.n_clusters) - 1u) {
       atomicExch(&P.ws->next, 0u);
       atomicExch(&P.ws->done, 0u);
+      atomicExch(&P.ws->dcount, 0u);
     }
   }
 }

@@ -160,6 +160,16 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p) : "memory");
 }
 
+// A 32-bit global load with acquire semantics at GPU scope, and the matching release store.
+__device__ __forceinline__ int ld_acquire_gpu_s32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu_s32(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // 16-byte read-only global load that does not allocate in L1.
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;

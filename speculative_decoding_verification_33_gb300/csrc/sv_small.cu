@@ -687,14 +687,13 @@ __device__ __forceinline__ void rho8(const SmallDecision& d, float rho, int e, f
 template <typename T>
 constexpr int kMassUnroll = 8 / static_cast<int>(sizeof(T));
 
+// The draw's weights summed over slice `sl` of sequence b's decided rows (decision d): per
+// 8-element vector the sequential float sums of the residual and of p, truncated to integers of
+// 2^-44, summed per slice into P.mass. Block-wide.
 template <typename T, bool BIAS>
-__global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams P) {
-  pdl_trigger();
+__device__ void slice_masses(const SmallParams& P, int b, const SmallDecision& d, int sl) {
   __shared__ unsigned long long s_r[kMassThreads / 32], s_p[kMassThreads / 32];
-  const int sl = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const SmallDecision d = decide<T, BIAS>(P, b);
-  if (sl == 0 && tid == 0) P.dec[b] = d;
-  if (!d.ok) return;
+  const int tid = threadIdx.x;
   const int K = P.K;
   const int L = P.lens ? P.lens[b] : K;
   const T* gt = static_cast<const T*>(small_row(P, b, d.a, sizeof(T)));
@@ -763,6 +762,51 @@ __global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams 
 }
 
 template <typename T, bool BIAS>
+__global__ void __launch_bounds__(kMassThreads, 8) small_mass(const SmallParams P) {
+  pdl_trigger();
+  const int sl = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const SmallDecision d = decide<T, BIAS>(P, b);
+  if (sl == 0 && tid == 0) P.dec[b] = d;
+  if (!d.ok) return;
+  slice_masses<T, BIAS>(P, b, d, sl);
+}
+
+// The deferred draws of the walk: CTA (sl, k) sums slice sl of the k-th sequence the walk
+// decided, once the walk has published it (seq + 1 in P.dlist[k], written after its decision;
+// a bounded wait: the walk's clusters are all running before this launch can start, and none of
+// them waits on it). CTAs start in the order the walk decides, so the sums of the sequences
+// decided first run while the walk finishes the last ones.
+template <typename T, bool BIAS>
+__global__ void __launch_bounds__(kMassThreads, 8) walk_mass(const SmallParams P) {
+  pdl_trigger();
+  __shared__ int s_b;
+  const int sl = blockIdx.x, k = blockIdx.y;
+  if (threadIdx.x == 0) {
+    int b = -1;
+    const long long t0 = clock64();
+    for (;;) {
+      const int v = ld_acquire_gpu_s32(P.dlist + k);
+      if (v > 0) {
+        b = v - 1;
+        break;
+      }
+      if (clock64() - t0 > kWaitBudget) {
+        atomicOr(P.err, 1u);
+        break;
+      }
+      __nanosleep(256);
+    }
+    s_b = b;
+  }
+  __syncthreads();
+  const int b = s_b;
+  if (b < 0 || b >= P.B) return;
+  const SmallDecision d = P.dec[b];
+  if (!d.ok || d.a < 0 || d.a > P.K) return;
+  slice_masses<T, BIAS>(P, b, d, sl);
+}
+
+template <typename T, bool BIAS>
 __global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) {
   __shared__ unsigned long long s_w[kPickThreads / 32];
   __shared__ int s_slice, s_tok;
@@ -783,9 +827,12 @@ __global__ void __launch_bounds__(kPickThreads) small_pick(const SmallParams P) 
     mr = m[0];
     mp = m[1];
   }
-  if (!d.ok) {
+  if (P.dlist && tid == 0 && d.q >= 0 && d.q < P.B)
+    P.dlist[d.q] = 0;  // the walk's order list, empty for the next call
+  if (!d.ok || d.a < 0 || d.a > K) {
     for (int j = tid; j <= K; j += kPickThreads) tok[j] = -1;
-    if (tid == 0) P.out_acc[b] = -1;
+    // -1 invalid, -2 a bounded wait gave up (the walk's record; or a record out of range)
+    if (tid == 0) P.out_acc[b] = (!d.ok && d.a == -1) ? -1 : -2;
     return;
   }
   const int a = d.a;
@@ -958,6 +1005,22 @@ bool small_plan(int B, int K, int V, int sms, int rows_per_sm, SmallParams* P) {
 
 cudaError_t launch_small(const SmallParams& P, int dtype, cudaStream_t stream) {
   return dtype == 1 ? launch_small_t<uint16_t>(P, stream) : launch_small_t<float>(P, stream);
+}
+
+namespace {
+template <typename T>
+cudaError_t launch_walk_draws_t(const SmallParams& P, cudaStream_t stream) {
+  const dim3 gm(static_cast<unsigned>(P.nslice_d), static_cast<unsigned>(P.B));
+  cudaError_t e = launch_pdl(walk_mass<T, false>, gm, kMassThreads, stream, P);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(small_pick<T, false>, dim3(static_cast<unsigned>(P.B)), kPickThreads, stream,
+                    P);
+}
+}  // namespace
+
+cudaError_t launch_walk_draws(const SmallParams& P, int dtype, cudaStream_t stream) {
+  return dtype == 1 ? launch_walk_draws_t<uint16_t>(P, stream)
+                    : launch_walk_draws_t<float>(P, stream);
 }
 
 }  // namespace sv

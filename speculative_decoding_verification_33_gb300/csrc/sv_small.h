@@ -17,7 +17,7 @@ struct SmallDecision {
   float rho_s;  // the same on the bias set (rho * beta)
   int nS;       // ids in the bias set of the draft row at a
   int ids[8];   // those ids
-  int pad;
+  int q;        // deferred draws: the place of the sequence in the order list
 };
 
 struct SmallParams {
@@ -42,6 +42,7 @@ struct SmallParams {
   unsigned long long* keys;  // [B][K][nslice][8] per slice of a draft row: its 8 largest keys
   SmallDecision* dec;        // [B]
   unsigned long long* mass;  // [B][nslice_d][2] the draw's residual and p masses per slice
+  int* dlist;                // deferred draws: seq + 1 of the k-th sequence the walk decided
   unsigned int* err;         // error word: bit 0 = a bounded wait gave up
   int32_t* out_acc;          // [B]
   int32_t* out_tok;          // [B][K+1]
@@ -59,6 +60,22 @@ bool small_plan(int B, int K, int V, int sms, int rows_per_sm, SmallParams* P);
 inline size_t small_align(size_t n) { return (n + 255) / 256 * 256; }
 inline size_t small_keys_bytes(const SmallParams& P) {
   return P.top8 ? static_cast<size_t>(P.B) * P.K * P.nslice * 8 * 8 : 0;
+}
+// Device state of the deferred draws for batches of up to `cap` sequences: the order list first
+// (it must read zero at the start of every call, so it stays where it is whatever the batch:
+// the pick clears what the walk wrote), then the decisions and the masses of up to 32 draw
+// slices per sequence (written before they are read in every call). Each part 256-byte aligned.
+inline size_t walk_draw_ws_bytes(int cap) {
+  return small_align(static_cast<size_t>(cap) * sizeof(int)) +
+         small_align(static_cast<size_t>(cap) * sizeof(SmallDecision)) +
+         small_align(static_cast<size_t>(cap) * 32 * 16);
+}
+inline void walk_draw_carve(SmallParams& P, char* base, int cap) {
+  P.dlist = reinterpret_cast<int*>(base);
+  base += small_align(static_cast<size_t>(cap) * sizeof(int));
+  P.dec = reinterpret_cast<SmallDecision*>(base);
+  base += small_align(static_cast<size_t>(cap) * sizeof(SmallDecision));
+  P.mass = reinterpret_cast<unsigned long long*>(base);
 }
 inline size_t small_ws_bytes(const SmallParams& P) {
   return small_align(static_cast<size_t>(P.B) * (2 * P.K + 1) * P.nslice * 8) +
@@ -79,5 +96,11 @@ inline void small_carve(SmallParams& P, char* base) {
 // The three launches (row slices; the draw's slice masses; one pick CTA per sequence) on
 // `stream`, the last two chained by programmatic dependent launch; dtype 1 = bf16.
 cudaError_t launch_small(const SmallParams& P, int dtype, cudaStream_t stream);
+
+// The draws the walk deferred (P.dec and P.dlist written by the walk, P.mass and the slice
+// fields as for launch_small): the slice masses of each sequence, its CTAs waiting (bounded)
+// until the walk has decided it, then the pick; both chained by programmatic dependent launch
+// after the walk on `stream`.
+cudaError_t launch_walk_draws(const SmallParams& P, int dtype, cudaStream_t stream);
 
 }  // namespace sv

@@ -51,7 +51,8 @@ def source_digest() -> str:
 
 # the files each kernel's code comes from (a recorded profile stays valid while they are unchanged)
 KERNEL_SOURCES = {
-    "verify": ("sv_kernel.cu", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h"),
+    "verify": ("sv_kernel.cu", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h", "sv_small.cu",
+               "sv_small.h"),
     "rows": ("sv_rows.cu", "sv_rows.h", "sv_math.cuh", "sv_ptx.cuh", "sv_internal.h"),
     "lmhead": ("sv_lmhead.cu", "sv_lmhead.h", "sv_tc.cuh", "sv_math.cuh", "sv_ptx.cuh"),
     "greedy": ("sv_greedy.cu", "sv_greedy.h", "sv_math.cuh", "sv_ptx.cuh"),

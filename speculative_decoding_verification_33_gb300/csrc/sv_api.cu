@@ -209,12 +209,12 @@ std::pair<int, int> row_config(int dev, int mode, int dtype, bool bias, int V) {
   if (it == g_row_occ.end()) {
     int nst = 0, per_sm = 0;
     for (int st = sv::kRowMaxStages; st >= 3 && !nst; --st)
-      if (sv::row_smem_bytes(mode, V, st) <= 112 * 1024) nst = st;
+      if (sv::row_smem_bytes(mode, dtype, V, st) <= 112 * 1024) nst = st;
     if (nst) per_sm = sv::row_ctas_per_sm(mode, dtype, bias, V, nst);
     if (per_sm < 2) {
       nst = 0;
       for (int st = sv::kRowMaxStages; st >= 2 && !nst; --st)
-        if (sv::row_smem_bytes(mode, V, st) <= sv::kRowMaxSmem) nst = st;
+        if (sv::row_smem_bytes(mode, dtype, V, st) <= sv::kRowMaxSmem) nst = st;
       per_sm = nst ? sv::row_ctas_per_sm(mode, dtype, bias, V, nst) : 0;
     }
     it = g_row_occ.emplace(key, std::make_pair(nst, per_sm)).first;

@@ -56,7 +56,7 @@ constexpr float kLn2r = 0.69314718055994531f;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per barrier wait
 constexpr int MODE_SAMPLE = 0, MODE_RESID = 1, MODE_TOP8 = 2;
 constexpr int kEnd = -1;  // unit tag after the last unit
-constexpr int kBatch = 4;  // candidate groups whose loads an epilogue warp keeps in flight
+constexpr int kBatch = 8;  // residual: groups an epilogue warp reads per round trip
 constexpr int kCandCap = 64;  // sampling: candidate groups of the bias set kept in shared memory
 constexpr int kTierCap = 256;  // residual: groups of one tier listed in shared memory at once
 
@@ -79,6 +79,7 @@ struct RowShared {
   int nS, gstar;
   int S_ids[8];
   float S_z[8];
+  int sgrp[8];  // the groups of S_ids
   unsigned long long t_loc;
   // sampling with a bias set: the candidate groups of the 8 largest, and the corrections of the
   // groups that hold ids of the set
@@ -131,6 +132,7 @@ __device__ unsigned long long team_exclusive_u64(unsigned long long v, RowShared
 struct Top8State {
   unsigned long long L;
   float thr;
+  int kth;  // the threshold follows the key of this rank (0 .. 7) once it is held
 };
 
 // The insertion behind WarpTop8::offer, out of line (its loop is long and rarely taken); state in
@@ -150,28 +152,31 @@ __device__ __noinline__ Top8State warp_top8_insert(unsigned pend, float z, uint3
       const unsigned long long up = __shfl_up_sync(FULL, st.L, 1);
       if (lane == pos) st.L = K;
       else if (lane > pos && lane < 8) st.L = up;
-      const unsigned long long l7 = __shfl_sync(FULL, st.L, 7);
-      if (l7) st.thr = key_value(l7);
+      const unsigned long long lk = __shfl_sync(FULL, st.L, st.kth);
+      if (lk) st.thr = key_value(lk);
     }
   }
   return st;
 }
 
 // A warp's running top 8: the keys, descending, in lanes 0..7 (0 = empty; the other lanes hold
-// 0), and a threshold every lane shares: nothing below it can enter (the 8th key's value once 8
-// are held, or a known lower bound of the final 8th).
+// 0), and a threshold every lane shares: nothing below it can enter. It is the value of the key
+// of rank kth once that many are held (the 8th, or the F-th when only the first F of the list
+// are wanted), or a known lower bound of that final key.
 struct WarpTop8 {
   unsigned long long L;
   float thr;
-  __device__ __forceinline__ void init(float lower) {
+  int kth;
+  __device__ __forceinline__ void init(float lower, int rank = 7) {
     L = 0ull;
     thr = lower;
+    kth = rank;
   }
   // Every lane of the warp calls this; a lane offers (z, id) when ok.
   __device__ __forceinline__ void offer(bool ok, float z, uint32_t id) {
     const unsigned pend = __ballot_sync(FULL, ok && z >= thr);
     if (!pend) return;
-    const Top8State st = warp_top8_insert(pend, z, id, Top8State{L, thr});
+    const Top8State st = warp_top8_insert(pend, z, id, Top8State{L, thr, kth});
     L = st.L;
     thr = st.thr;
   }
@@ -200,8 +205,9 @@ __device__ void team_top8(const WarpTop8& W, RowShared& S) {
   esync();
 }
 
-// The 8th largest of the warp's 32 values (on every lane): bitonic sort, descending by lane.
-__device__ __forceinline__ float warp_8th_largest(float v) {
+// The (r + 1)-th largest of the warp's 32 values (on every lane; r < 32): bitonic sort,
+// descending by lane.
+__device__ __forceinline__ float warp_rank_value(float v, int r) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
@@ -213,8 +219,9 @@ __device__ __forceinline__ float warp_8th_largest(float v) {
       v = (low == desc) ? fmaxf(v, o) : fminf(v, o);
     }
   }
-  return __shfl_sync(FULL, v, 7);
+  return __shfl_sync(FULL, v, r);
 }
+__device__ __forceinline__ float warp_8th_largest(float v) { return warp_rank_value(v, 7); }
 
 // A lower bound of the 8th largest of the elements whose per-thread maxima are m (distinct
 // elements): some warp has 8 lanes whose maxima reach the largest of the warps' 8th-largest.
@@ -256,6 +263,35 @@ __device__ __forceinline__ void ld2(const T* row, int e, int V, bool vec, float&
 template <typename T>
 __host__ __device__ constexpr int chunk_elems() {
   return kStage / static_cast<int>(sizeof(T));
+}
+
+// Per-group values in shared memory: floats, or for the residual of bf16 rows 16-bit floats (the
+// upper half of a float). A bf16 row's group maxima are bf16 values and stay exact; the log-ratio
+// maxima and the bounds that replace them are upper bounds and are rounded up.
+template <typename T, int MODE>
+struct GroupVal {
+  using type = float;
+};
+template <>
+struct GroupVal<uint16_t, MODE_RESID> {
+  using type = uint16_t;
+};
+__device__ __forceinline__ float gv_get(const float* a, int g) { return a[g]; }
+__device__ __forceinline__ float gv_get(const uint16_t* a, int g) {
+  return __uint_as_float(static_cast<uint32_t>(a[g]) << 16);
+}
+// v exactly (a 16-bit array takes only bf16 values here)
+__device__ __forceinline__ void gv_put(float* a, int g, float v) { a[g] = v; }
+__device__ __forceinline__ void gv_put(uint16_t* a, int g, float v) {
+  a[g] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
+}
+// v rounded toward +inf: a positive value with bits below the kept half goes up one unit (the
+// largest finite ones to +inf); negative values lose them, which is up too; NaN stays NaN
+__device__ __forceinline__ void gv_put_up(float* a, int g, float v) { a[g] = v; }
+__device__ __forceinline__ void gv_put_up(uint16_t* a, int g, float v) {
+  uint32_t u = __float_as_uint(v);
+  if (!(u & 0x80000000u) && (u & 0xFFFFu) && !(v != v)) u += 0x10000u;
+  a[g] = static_cast<uint16_t>(u >> 16);
 }
 
 // A thread's running maximum m and sum 2^(z c - fl(m c)) over the groups it has reduced.
@@ -433,10 +469,10 @@ __device__ __forceinline__ void chunk_maxima(const T* stage, int n, float c, flo
 // Residual chunks: the same for a target and a draft chunk at once (n valid elements each), plus
 // each group's largest log-ratio max (z_t - z_d), which bounds the group's residual from above
 // once the normalisers are known.
-template <typename T>
+template <typename T, typename GV>
 __device__ __forceinline__ void chunk_pair(const T* st_t, const T* st_d, int n, float c,
-                                           float* gmax_t, float* gmax_d, float* gdel,
-                                           RowRun& run_t, RowRun& run_d) {
+                                           GV* gmax_t, GV* gmax_d, GV* gdel, RowRun& run_t,
+                                           RowRun& run_d) {
   using G = Lanes<T>;
   const int tid = threadIdx.x, lane = tid & 31;
   uint4 qt[G::PPL], qd[G::PPL];
@@ -474,9 +510,9 @@ __device__ __forceinline__ void chunk_pair(const T* st_t, const T* st_d, int n, 
   const float smt = group_sum<G::LPG>(gt > -INFINITY ? pieces_mass<T>(qt, c, gtc) : 0.f);
   const float smd = group_sum<G::LPG>(gd > -INFINITY ? pieces_mass<T>(qd, c, gdc) : 0.f);
   if ((lane & (G::LPG - 1)) == 0 && G::EPL * tid < n) {
-    gmax_t[tid / G::LPG] = gt;
-    gmax_d[tid / G::LPG] = gd;
-    gdel[tid / G::LPG] = gl;
+    gv_put(gmax_t, tid / G::LPG, gt);
+    gv_put(gmax_d, tid / G::LPG, gd);
+    gv_put_up(gdel, tid / G::LPG, gl);
     run_t.add(gt, gtc, smt);
     run_d.add(gd, gdc, smd);
   }
@@ -524,18 +560,18 @@ struct G8 {
   float thr;
 };
 
-template <typename T>
-__device__ G8 top8_groups(const T* row, int V, bool vec, const float* gmax, int ng, RowShared& S) {
+template <typename T, typename GV>
+__device__ G8 top8_groups(const T* row, int V, bool vec, const GV* gmax, int ng, RowShared& S) {
   const int t = et(), lane = t & 31, warp = t >> 5;
   float m = -INFINITY;
-  for (int g = t; g < ng; g += ET) m = fmaxf(m, gmax[g]);
+  for (int g = t; g < ng; g += ET) m = fmaxf(m, gv_get(gmax, g));
   const float B = team_bound(m, S);
   WarpTop8 gtop;
   gtop.init(B);
   const int per = (ng + ET - 1) / ET;
   for (int k = 0; k < per; ++k) {
     const int g = t + k * ET;
-    const float v = g < ng ? gmax[g] : -INFINITY;
+    const float v = g < ng ? gv_get(gmax, g) : -INFINITY;
     gtop.offer(g < ng && v >= B, v, static_cast<uint32_t>(g));
   }
   team_top8(gtop, S);
@@ -564,9 +600,8 @@ __device__ void top8_elements(const G8& r, int V, RowShared& S) {
   team_top8(top, S);
 }
 
-template <typename T>
-__device__ void row_top8(const T* row, int V, bool vec, const float* gmax, int ng,
-                         RowShared& S) {
+template <typename T, typename GV>
+__device__ void row_top8(const T* row, int V, bool vec, const GV* gmax, int ng, RowShared& S) {
   top8_elements(top8_groups<T>(row, V, vec, gmax, ng, S), V, S);
 }
 
@@ -575,8 +610,8 @@ __device__ void row_top8(const T* row, int V, bool vec, const float* gmax, int n
 // groups, so only runs whose maximum reaches it can hold one of the 8 largest groups, and only
 // their groups at or above theta are collected as keys (S.cand), of which warp 0 keeps the 8
 // largest. More than kCandCap such groups (ties at theta) take top8_groups instead.
-template <typename T>
-__device__ G8 run_top8_groups(const float* gmax, int lo, int hi, float tmax, int ng, const T* row,
+template <typename T, typename GV>
+__device__ G8 run_top8_groups(const GV* gmax, int lo, int hi, float tmax, int ng, const T* row,
                               int V, bool vec, RowShared& S) {
   const int t = et(), lane = t & 31, warp = t >> 5;
   // the 8 largest run maxima of each warp (with repeats), then of the team
@@ -605,11 +640,13 @@ __device__ G8 run_top8_groups(const float* gmax, int lo, int hi, float tmax, int
   esync();
   const float th = S.rb[0];
   if (tmax >= th)
-    for (int g = lo; g < hi; ++g)
-      if (gmax[g] >= th) {
+    for (int g = lo; g < hi; ++g) {
+      const float v = gv_get(gmax, g);
+      if (v >= th) {
         const int i = atomicAdd(&S.ncand, 1);
-        if (i < kCandCap) S.cand[i] = make_key(gmax[g], static_cast<uint32_t>(g));
+        if (i < kCandCap) S.cand[i] = make_key(v, static_cast<uint32_t>(g));
       }
+    }
   esync();
   const int n = S.ncand;
   if (n > kCandCap) return top8_groups<T>(row, V, vec, gmax, ng, S);
@@ -666,6 +703,7 @@ __device__ void bias_set(const RowParams& P, RowShared& S, float Md, float Sd) {
   if (in) {
     S.S_z[lane] = z;
     S.S_ids[lane] = key_id(k);
+    S.sgrp[lane] = key_id(k) / kGroup;
   }
   if (lane == 0) {
     S.nS = nS;
@@ -784,8 +822,9 @@ __device__ void producer(const RowParams& P, RowShared& S, unsigned char* ring) 
 // the chunk warps: group values of every unit into the two group buffers in turn
 // ------------------------------------------------------------------------------------------
 template <typename T, int MODE>
-__device__ void chunk_warps(const RowParams& P, RowShared& S, unsigned char* ring, float* gbuf0,
-                            float* gbuf1, int ngmax) {
+__device__ void chunk_warps(const RowParams& P, RowShared& S, unsigned char* ring,
+                            unsigned char* gbuf0, unsigned char* gbuf1, int ngmax) {
+  using GV = typename GroupVal<T, MODE>::type;
   const int tid = threadIdx.x, lane = tid & 31;
   const int nst = P.nstages;
   constexpr int CE = chunk_elems<T>();
@@ -826,7 +865,8 @@ __device__ void chunk_warps(const RowParams& P, RowShared& S, unsigned char* rin
     const int u = S.tag[s0];
     if (named_sync_or(kBarC, CT, ab || u == kEnd)) break;
     const int b = take_buffer();
-    float* gb = b ? gbuf1 : gbuf0;
+    float* gb = reinterpret_cast<float*>(b ? gbuf1 : gbuf0);
+    GV* gv = reinterpret_cast<GV*>(b ? gbuf1 : gbuf0);
     RowRun run[2];
     run[0].init();
     run[1].init();
@@ -844,7 +884,7 @@ __device__ void chunk_warps(const RowParams& P, RowShared& S, unsigned char* rin
       } else {  // target maxima, draft maxima, log-ratio maxima
         const int s2 = wait_full(it + 1);
         chunk_pair<T>(st, reinterpret_cast<const T*>(ring + static_cast<size_t>(s2) * kStage), n,
-                      P.c, gb + ch * go, gb + ngmax + ch * go, gb + 2 * ngmax + ch * go, run[0],
+                      P.c, gv + ch * go, gv + ngmax + ch * go, gv + 2 * ngmax + ch * go, run[0],
                       run[1]);
         release(s);
         release(s2);
@@ -1008,53 +1048,232 @@ __device__ void sample_epilogue(const RowParams& P, RowShared& S, int u, float* 
 // ------------------------------------------------------------------------------------------
 // epilogue: exact-residual top-F
 // ------------------------------------------------------------------------------------------
-// Residual weights of groups (one warp, two elements per lane and group) offered to the warp's
-// list, for up to kBatch groups at once (g < 0: none); all loads are issued before the first use.
-template <typename T, bool BIAS>
-__device__ __forceinline__ void offer_groups(WarpTop8& top, const T* zt, const T* zd,
-                                             const int (&gs)[kBatch], int V, bool vec, float c,
-                                             float Mtc, float Mdc, float rho, float rhoS,
-                                             const RowShared& S, int nS) {
-  const int lane = threadIdx.x & 31;
-  float ta[kBatch], tb[kBatch], da[kBatch], db[kBatch];
+// The 16-byte piece of a global row at element e (a multiple of 16 / sizeof(T)): one vector load
+// when the row is 16-byte aligned and the piece lies below V, else element by element; elements
+// at or past V, and every element when e < 0, read as -inf.
+template <typename T>
+__device__ __forceinline__ uint4 row_piece(const T* row, int e, int V, bool vec) {
+  constexpr int EPP = 16 / static_cast<int>(sizeof(T));
+  if (e >= 0 && vec && e + EPP <= V) return ldg_nc_v4(row + e);
+  uint32_t w[4];
 #pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    ta[k] = tb[k] = da[k] = db[k] = -INFINITY;
-    if (gs[k] >= 0) {
-      const int e = kGroup * gs[k] + 2 * lane;
-      ld2<T>(zt, e, V, vec, ta[k], tb[k]);
-      ld2<T>(zd, e, V, vec, da[k], db[k]);
+  for (int h = 0; h < 4; ++h) {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t lo = (e >= 0 && e + 2 * h < V) ? static_cast<uint32_t>(row[e + 2 * h]) : 0xFF80u;
+      const uint32_t hi =
+          (e >= 0 && e + 2 * h + 1 < V) ? static_cast<uint32_t>(row[e + 2 * h + 1]) : 0xFF80u;
+      w[h] = lo | (hi << 16);
+    } else {
+      w[h] = (e >= 0 && e + h < V) ? __float_as_uint(row[e + h]) : __float_as_uint(-INFINITY);
     }
   }
-  float wa[kBatch], wb[kBatch];
-  float lm = -INFINITY;  // the lane's largest residual of the batch
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    const int e = kGroup * gs[k] + 2 * lane;
-    float ra = rho, rb = rho;
-    if (BIAS)
-      for (int j = 0; j < nS; ++j) {
-        ra = S.S_ids[j] == e ? rhoS : ra;
-        rb = S.S_ids[j] == e + 1 ? rhoS : rb;
-      }
-    wa[k] = fmaxf(fmaf(-ra, ex2_fast(fmaf(da[k], c, -Mdc)), ex2_fast(fmaf(ta[k], c, -Mtc))), 0.f);
-    wb[k] = fmaxf(fmaf(-rb, ex2_fast(fmaf(db[k], c, -Mdc)), ex2_fast(fmaf(tb[k], c, -Mtc))), 0.f);
-    if (gs[k] >= 0 && e < V && wa[k] > 0.f) lm = fmaxf(lm, wa[k]);
-    if (gs[k] >= 0 && e + 1 < V && wb[k] > 0.f) lm = fmaxf(lm, wb[k]);
-  }
-  // 8 lanes hold a residual at least the 8th largest lane maximum: nothing below it can enter
-  top.thr = fmaxf(top.thr, warp_8th_largest(lm));
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    const int e = kGroup * gs[k] + 2 * lane;
-    top.offer(gs[k] >= 0 && e < V && wa[k] > 0.f, wa[k], static_cast<uint32_t>(e));
-    top.offer(gs[k] >= 0 && e + 1 < V && wb[k] > 0.f, wb[k], static_cast<uint32_t>(e + 1));
-  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// How a warp reads groups of a global row: 16-byte pieces of EPP elements, PPG pieces per group,
+// GPL groups per warp-wide load; lane l takes piece l mod PPG of group slot l / PPG.
+template <typename T>
+struct GroupReads {
+  static constexpr int EPP = 16 / static_cast<int>(sizeof(T));
+  static constexpr int PPG = kGroup / EPP;
+  static constexpr int GPL = 32 / PPG;
+  static constexpr int NL = kBatch / GPL;  // loads per row and lane for kBatch groups
+  static_assert(GPL * PPG == 32 && NL * GPL == kBatch, "group reads");
+};
+
+// The bias set of a residual unit (the draft row's bias_k largest logits) and N, into S (nS, N,
+// S_ids and sgrp, the groups of those ids) for every epilogue thread. The 8 largest logits lie in
+// the 8 groups with the largest maxima (ties to the lower group), those groups in the runs (the
+// threads' contiguous stretches of groups) whose maximum reaches a lower bound of the 8th largest
+// run maximum, and there at or above that bound: the candidates. Warp 0 keeps the 8 largest
+// candidates, reads their 512 elements at once, keeps the 8 largest of them (from the 8th group
+// maximum up) and forms the set, its terms summed in key order.
+template <typename T, typename GV>
+__device__ void resid_bias_set(const RowParams& P, RowShared& S, const GV* gmax, int ng,
+                               const T* row, int V, bool vec, float Md, float Sd) {
+  const int t = et(), lane = t & 31, warp = t >> 5;
+  const int lo = static_cast<int>((static_cast<long long>(t) * ng) / ET);
+  const int hi = static_cast<int>((static_cast<long long>(t + 1) * ng) / ET);
+  float tmax = -INFINITY;
+  int gm = -1;
+  for (int g = lo; g < hi; ++g) {
+    const float v = gv_get(gmax, g);
+    if (v > tmax) {
+      tmax = v;
+      gm = g;
+    }
+  }
+  // the groups warp 0 reads below are mostly the maxima of some runs: into L2 meanwhile
+  if (gm >= 0)
+    for (int o = 0; o < kGroup && kGroup * gm + o < V; o += 128 / static_cast<int>(sizeof(T)))
+      prefetch_l2(row + kGroup * gm + o);
+  if (t == 0) S.ncand = 0;
+  const float th = team_bound(tmax, S);  // (its barriers order the reset before the adds)
+  if (tmax >= th)
+    for (int g = lo; g < hi; ++g) {
+      const float v = gv_get(gmax, g);
+      if (v >= th) {
+        const int k = atomicAdd(&S.ncand, 1);
+        if (k < kCandCap) S.cand[k] = make_key(v, static_cast<uint32_t>(g));
+      }
+    }
+  esync();
+  const int n = S.ncand;
+  if (n > kCandCap) {  // (ties beyond the list) every group offered
+    top8_elements(top8_groups<T>(row, V, vec, gmax, ng, S), V, S);
+    bias_set(P, S, Md, Sd);
+    esync();
+    return;
+  }
+  if (warp == 0) {
+    static_assert(kCandCap == 64, "two candidates per lane");
+    unsigned long long a = lane < n ? S.cand[lane] : 0ull;
+    unsigned long long b = lane + 32 < n ? S.cand[lane + 32] : 0ull;
+    if (b > a) {
+      const unsigned long long x = a;
+      a = b;
+      b = x;
+    }
+    unsigned long long gk = 0ull;  // lane r: the r-th largest group key
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const unsigned long long m = warp_max_key(a);
+      if (lane == r) gk = m;
+      if (m != 0ull && a == m) {
+        a = b;
+        b = 0ull;
+      }
+    }
+    const unsigned long long k7 = __shfl_sync(FULL, gk, 7);
+    using R = GroupReads<T>;
+    constexpr int NP = 8 * R::PPG / 32;  // pieces per lane
+    uint4 q[NP];
+    int e[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      const int p = lane + 32 * j;
+      const unsigned long long kg = __shfl_sync(FULL, gk, p / R::PPG);
+      e[j] = kg ? kGroup * key_id(kg) + R::EPP * (p % R::PPG) : -1;
+      q[j] = row_piece<T>(row, e[j], V, vec);
+    }
+    // Each of the 8 groups holds an element at or above the 8th group maximum t8 (its own
+    // maximum). When they are the only 8 such elements, the r-th largest element is the maximum
+    // of the group of rank r (groups of equal maxima rank by index, as their ids do); otherwise
+    // the elements from t8 up go through a list.
+    const float t8 = k7 ? key_value(k7) : -INFINITY;
+    float ze[NP][R::EPP];
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      unpack_piece<T>(q[j], ze[j]);
+#pragma unroll
+      for (int kk = 0; kk < R::EPP; ++kk)
+        cnt += (e[j] >= 0 && e[j] + kk < V && ze[j][kk] >= t8) ? 1 : 0;
+    }
+    unsigned long long k = 0ull;  // lanes 0..7: the 8 largest, descending; 0 elsewhere
+    if (k7 != 0ull && __reduce_add_sync(FULL, cnt) == 8) {
+#pragma unroll
+      for (int j = 0; j < NP; ++j)
+#pragma unroll
+        for (int kk = 0; kk < R::EPP; ++kk)
+          if (e[j] >= 0 && e[j] + kk < V && ze[j][kk] >= t8)
+            S.wtop[0][(lane + 32 * j) / R::PPG] =
+                make_key(ze[j][kk], static_cast<uint32_t>(e[j] + kk));
+      __syncwarp();
+      k = lane < 8 ? S.wtop[0][lane] : 0ull;
+    } else {
+      WarpTop8 top;
+      top.init(t8);
+#pragma unroll
+      for (int j = 0; j < NP; ++j)
+#pragma unroll
+        for (int kk = 0; kk < R::EPP; ++kk)
+          top.offer(e[j] >= 0 && e[j] + kk < V, ze[j][kk], static_cast<uint32_t>(e[j] + kk));
+      k = top.L;
+    }
+    const bool in = lane < P.bias_k && k != 0ull;
+    const float z = in ? key_value(k) : 0.f;
+    const float term = in ? exp2f((z - Md) * P.c) / Sd : 0.f;
+    const int nS = __popc(__ballot_sync(FULL, in));
+    float sq = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float tj = __shfl_sync(FULL, term, j);
+      if (j < nS) sq += tj;
+    }
+    if (in) {
+      S.S_z[lane] = z;
+      S.S_ids[lane] = key_id(k);
+      S.sgrp[lane] = key_id(k) / kGroup;
+    }
+    if (lane == 0) {
+      S.nS = nS;
+      S.N = fmaf(-(1.f - P.beta), sq, 1.f);
+    }
+  }
+  esync();
+}
+
+// Residual weights of up to kBatch groups, list[j0 .. min(j0 + kBatch, n)), offered to the warp's
+// list; every load is issued before the first use, so the batch costs one round trip.
 template <typename T, bool BIAS>
-__device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const float* gmax_t,
-                               const float* gmax_d, float* gdel, const float* hdr) {
+__device__ __forceinline__ void offer_groups(WarpTop8& top, const T* zt, const T* zd,
+                                             const int* list, int j0, int n, int V, bool vec,
+                                             float c, float Mtc, float Mdc, float rho, float rhoS,
+                                             const RowShared& S, int nS) {
+  using R = GroupReads<T>;
+  const int lane = threadIdx.x & 31;
+  const int slot = lane / R::PPG, piece = lane % R::PPG;
+  uint4 qt[R::NL], qd[R::NL];
+  int e[R::NL];
+#pragma unroll
+  for (int j = 0; j < R::NL; ++j) {
+    const int at = j0 + j * R::GPL + slot;
+    e[j] = at < n ? kGroup * list[at] + R::EPP * piece : -1;
+    qt[j] = row_piece<T>(zt, e[j], V, vec);
+    qd[j] = row_piece<T>(zd, e[j], V, vec);
+  }
+  uint32_t smask[R::NL];  // bit k: element e[j] + k is in the bias set
+#pragma unroll
+  for (int j = 0; j < R::NL; ++j) smask[j] = 0u;
+  if (BIAS)
+    for (int m = 0; m < nS; ++m) {
+      const int id = S.S_ids[m];
+#pragma unroll
+      for (int j = 0; j < R::NL; ++j) {
+        const uint32_t o = static_cast<uint32_t>(id - e[j]);
+        if (e[j] >= 0 && o < static_cast<uint32_t>(R::EPP)) smask[j] |= 1u << o;
+      }
+    }
+  float w[R::NL][R::EPP];
+  float lm = -INFINITY;  // the lane's largest residual of the batch
+#pragma unroll
+  for (int j = 0; j < R::NL; ++j) {
+    float ft[R::EPP], fd[R::EPP];
+    unpack_piece<T>(qt[j], ft);
+    unpack_piece<T>(qd[j], fd);
+#pragma unroll
+    for (int k = 0; k < R::EPP; ++k) {
+      const float r = (BIAS && ((smask[j] >> k) & 1u)) ? rhoS : rho;
+      w[j][k] = fmaxf(fmaf(-r, ex2_fast(fmaf(fd[k], c, -Mdc)), ex2_fast(fmaf(ft[k], c, -Mtc))),
+                      0.f);
+      if (e[j] >= 0 && e[j] + k < V && w[j][k] > 0.f) lm = fmaxf(lm, w[j][k]);
+    }
+  }
+  // kth + 1 lanes hold a residual at least the (kth + 1)-th largest lane maximum: nothing below
+  // it can be among the first kth + 1
+  top.thr = fmaxf(top.thr, warp_rank_value(lm, top.kth));
+#pragma unroll
+  for (int j = 0; j < R::NL; ++j)
+#pragma unroll
+    for (int k = 0; k < R::EPP; ++k)
+      top.offer(e[j] >= 0 && e[j] + k < V && w[j][k] > 0.f, w[j][k],
+                static_cast<uint32_t>(e[j] + k));
+}
+
+template <typename T, bool BIAS, typename GV>
+__device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const GV* gmax_t,
+                               const GV* gmax_d, GV* gdel, const float* hdr) {
   const int t = et();
   const float c = P.c;
   const int V = P.V;
@@ -1065,23 +1284,38 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const fl
   const T* zd = static_cast<const T*>(P.dft) + (static_cast<long long>(b) * P.K + i) * P.d_stride;
   int32_t* out = P.out_r2 + static_cast<long long>(u) * P.fmax;
   const bool vec = P.use_vec != 0;
+  const int F = min(P.fan[i], 8);  // only the first F of the order are written
 
   const float2 T2 = make_float2(hdr[0], hdr[1]);
   const float2 D2 = make_float2(hdr[2], hdr[3]);
-  if (row_bad(T2.x) || row_bad(D2.x)) {
+  if (F <= 0 || row_bad(T2.x) || row_bad(D2.x)) {
     if (t < P.fmax) out[t] = -1;
     return;
   }
+  // The rows streamed a while ago are leaving L2: the group of each thread whose target maximum
+  // is largest (the bounds below are close to e_t,max for most groups, so these are the groups
+  // the first round reads) is fetched into L2 at once, both rows, while the bias set and the
+  // bounds are worked out.
+  {
+    float gm = -INFINITY;
+    int gb = -1;
+    for (int g = t; g < ng; g += ET) {
+      const float v = gv_get(gmax_t, g);
+      if (v > gm) {
+        gm = v;
+        gb = g;
+      }
+    }
+    if (gb >= 0)
+      for (int o = 0; o < kGroup && kGroup * gb + o < V; o += 128 / static_cast<int>(sizeof(T))) {
+        prefetch_l2(zt + kGroup * gb + o);
+        prefetch_l2(zd + kGroup * gb + o);
+      }
+  }
   int nS = 0;
   float N = 1.f;
-  if (BIAS) {  // the bias set: the draft row's 8 largest, from contiguous runs of its groups
-    const int lo = static_cast<int>((static_cast<long long>(t) * ng) / ET);
-    const int hi = static_cast<int>((static_cast<long long>(t + 1) * ng) / ET);
-    float tmax = -INFINITY;
-    for (int g = lo; g < hi; ++g) tmax = fmaxf(tmax, gmax_d[g]);
-    top8_elements(run_top8_groups<T>(gmax_d, lo, hi, tmax, ng, zd, V, vec, S), V, S);
-    bias_set(P, S, D2.x, D2.y);
-    esync();
+  if (BIAS) {
+    resid_bias_set<T>(P, S, gmax_d, ng, zd, V, vec, D2.x, D2.y);
     nS = S.nS;
     N = S.N;
   }
@@ -1095,87 +1329,99 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const fl
   // An upper bound of each group's residual: with delta = max (z_t - z_d) c over the group,
   // w = e_t (1 - rho_v 2^((z_d - z_t) c + Mtc - Mdc)) <= e_t,max (1 - 2^-(delta - kappa)),
   // kappa = log2(min rho_v) + Mtc - Mdc; 1 - 2^-x <= min(1, x ln 2). A small margin covers the
-  // rounding of both sides. Stored over the log-ratio maxima.
-  const float kappa = __log2f(BIAS ? rhoS : rho) + Mtc - Mdc;
-  float bm = -INFINITY;
-  int gbest = -1;
-  for (int g = t; g < ng; g += ET) {
-    const float x = fmaf(gdel[g], c, -kappa) + 1e-4f;
-    const float et = ex2_fast(fmaf(gmax_t[g], c, -Mtc));
+  // rounding of both sides; the bound is stored (rounded up) over the log-ratio maximum. A group
+  // with x <= 0 gets 0: each of its residuals is below zero by a relative 7e-5 or more, far past
+  // the rounding of the weights, so none is offered (and one whose e_t,max is below the smallest
+  // normal float offers nothing either: the weights flush it to zero). min rho_v is rho except in
+  // the groups that hold ids of the bias set (rho beta there): those few bounds are taken first
+  // and put in place after the others.
+  auto bound = [&](int g, float kap) {
+    const float x = fmaf(gv_get(gdel, g), c, -kap) + 1e-4f;
+    const float gt = gv_get(gmax_t, g);
+    const float et = ex2_fast(fmaf(gt, c, -Mtc));
     const float f = x <= 0.f ? 0.f : (x < 0.25f ? x * 0.69314718f : 1.f - ex2_fast(-x) + 1e-6f);
-    const float bnd = gmax_t[g] > -INFINITY ? et * fminf(f, 1.f) * 1.001f + 1e-30f : 0.f;
-    gdel[g] = bnd;
-    if (bnd > bm) gbest = g;
+    return gt > -INFINITY ? et * fminf(f, 1.f) * 1.001f : 0.f;
+  };
+  const float kappa = __log2f(rho) + Mtc - Mdc;
+  int gS = -1;
+  float bS = 0.f;
+  if (BIAS && t < nS) {
+    gS = S.sgrp[t];
+    bS = bound(gS, __log2f(rhoS) + Mtc - Mdc);
+  }
+  if (BIAS) esync();  // the set's groups read their log-ratio maxima before they are replaced
+  float bm = -INFINITY;
+  for (int g = t; g < ng; g += ET) {
+    const float bnd = bound(g, kappa);
+    gv_put_up(gdel, g, bnd);
     bm = fmaxf(bm, bnd);
   }
-  // The rows streamed long ago are out of L2 by now: the group of the largest bound of each
-  // thread (those the tiers below read first) is fetched into L2 at once, both rows, so that the
-  // tiers' reads find it there instead of queueing behind the stream one tier after another.
-  if (gbest >= 0 && bm > 0.f) {
-    const int e0 = kGroup * gbest, e1 = min(V, e0 + kGroup) - 1;
-    prefetch_l2(zt + e0);
-    prefetch_l2(zt + e1);
-    prefetch_l2(zd + e0);
-    prefetch_l2(zd + e1);
-  }
-  // Tiers of groups in decreasing bound: each tier is the groups (not yet visited) whose bound
-  // reaches both the 8th best residual so far and a lower bound of the 8th largest remaining
-  // bound; a visited group's bound is set to -1. It ends when no group's bound reaches the 8th
-  // best residual; after kTiers tiers, every group that still could is visited at once. A tier's
-  // groups are listed first (up to kTierCap; the rest wait for the next round), then taken four
-  // at a time per warp, so that a warp's reads of a tier are a round trip or two, not one per
-  // group.
-  constexpr int kTiers = 6;
-  WarpTop8 top;
-  top.init(-INFINITY);
-  const int per = (ng + ET - 1) / ET;
-  const int warp = t >> 5;
-  float thr = 0.f;  // the team's 8th best residual so far (0 until 8 are known)
-  for (int tier = 0;; ++tier) {
-    float bt = -INFINITY;
-    if (tier < kTiers) {
-      float bm2 = -INFINITY;
-      for (int g = t; g < ng; g += ET) {
-        const float bg = gdel[g];
-        if (bg > 0.f && bg >= thr) bm2 = fmaxf(bm2, bg);
-      }
-      bt = team_bound(bm2, S);  // (its barriers also order the list's reset below)
-    }
-    if (t == 0) S.ntl = 0;
+  if (BIAS) {
     esync();
-    const float lo = fmaxf(bt, thr);
-    bool over = false;
-    for (int k = 0; k < per; ++k) {
-      const int g = t + k * ET;
-      if (g < ng && gdel[g] > 0.f && gdel[g] >= lo) {
+    if (gS >= 0) gv_put_up(gdel, gS, bS);  // (two ids of one group write the same bound)
+  }
+  // Rounds of groups in decreasing bound, a visited group's bound set to -1. Each round takes the
+  // groups left whose bound reaches both the F-th best residual found so far and a lower bound
+  // of the 8th largest bound left (some warp has 8 threads whose largest bound left reaches its
+  // 8th largest), so a round reads the next few groups in bound order (up to kTierCap; the rest
+  // stay for the next round), each warp kBatch groups per round trip. The listing pass also
+  // finds each thread's largest bound left: the rounds end when none reaches the F-th best (or
+  // none is positive while fewer than F residuals are known).
+  const int warp = t >> 5, lane = t & 31;
+  WarpTop8 top;
+  top.init(-INFINITY, F - 1);
+  if (t == 0) S.ntl = 0;
+  float lo = team_bound(bm, S);  // (its barriers publish the set's bounds and the reset)
+  float thr = 0.f;  // the team's F-th best residual so far (0 until F are known)
+  bool merged = false;  // S.top holds the team's list as it stands
+  for (int round = 0;; ++round) {
+    if (round > 0) {
+      if (t == 0) S.ntl = 0;
+      esync();
+    }
+    const float lr = fmaxf(lo, thr);
+    float rest = -INFINITY;
+    for (int g = t; g < ng; g += ET) {
+      const float bg = gv_get(gdel, g);
+      bool listed = false;
+      if (bg > 0.f && bg >= lr) {
         const int at = atomicAdd(&S.ntl, 1);
         if (at < kTierCap) {
           S.tl[at] = g;
-          gdel[g] = -1.f;
-        } else {
-          over = true;  // listed in a later round
+          gv_put(gdel, g, -1.f);
+          listed = true;
         }
       }
+      if (!listed) rest = fmaxf(rest, bg);
+    }
+    const float r8 = warp_8th_largest(rest);
+    const float rm = ord_to_float(__reduce_max_sync(FULL, float_to_ord(rest)));
+    if (lane == 0) {
+      S.rb[warp] = r8;
+      S.rmax[warp] = rm;
     }
     esync();
     const int n = min(S.ntl, kTierCap);
-    if (n == 0) break;  // nothing left that can reach the top 8
-    for (int j0 = kBatch * warp; j0 < n; j0 += kBatch * NEW) {
-      int gs[kBatch];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) gs[k] = j0 + k < n ? S.tl[j0 + k] : -1;
-      offer_groups<T, BIAS>(top, zt, zd, gs, V, vec, c, Mtc, Mdc, rho, rhoS, S, nS);
+    if (n > 0)
+      for (int j0 = kBatch * warp; j0 < n; j0 += kBatch * NEW)
+        offer_groups<T, BIAS>(top, zt, zd, S.tl, j0, n, V, vec, c, Mtc, Mdc, rho, rhoS, S, nS);
+    if (n > 0 || !merged) {
+      team_top8(top, S);
+      merged = true;
     }
-    const bool more = named_sync_or(kBarE, ET, over);
-    team_top8(top, S);
-    const unsigned long long k8 = S.top[7];
-    thr = k8 ? key_value(k8) : 0.f;
+    const unsigned long long kf = S.top[F - 1];
+    thr = kf ? key_value(kf) : 0.f;
     if (thr > top.thr) top.thr = thr;
-    if (bt == -INFINITY && !more) break;  // that tier took every group still in reach
+    float r8t = S.rb[0], rmt = S.rmax[0];
+#pragma unroll
+    for (int w = 1; w < NEW; ++w) {
+      r8t = fmaxf(r8t, S.rb[w]);
+      rmt = fmaxf(rmt, S.rmax[w]);
+    }
+    if (rmt <= 0.f || (kf && rmt < thr)) break;  // nothing left reaches the F-th best
+    lo = r8t;
   }
-  team_top8(top, S);
   if (t < P.fmax) {
-    const int F = P.fan[i];
     const unsigned long long k = t < 8 ? S.top[t] : 0ull;
     out[t] = (t < F && k != 0ull) ? key_id(k) : -1;
   }
@@ -1210,8 +1456,9 @@ __device__ void top8_epilogue(const RowParams& P, RowShared& S, int u, const flo
 }
 
 template <typename T, int MODE, bool BIAS>
-__device__ void epilogue_warps(const RowParams& P, RowShared& S, float* gbuf0, float* gbuf1,
-                               int ngmax) {
+__device__ void epilogue_warps(const RowParams& P, RowShared& S, unsigned char* gbuf0,
+                               unsigned char* gbuf1, int ngmax) {
+  using GV = typename GroupVal<T, MODE>::type;
   int k = 0;
   for (;;) {
     const int b = k & 1;
@@ -1219,13 +1466,14 @@ __device__ void epilogue_warps(const RowParams& P, RowShared& S, float* gbuf0, f
     if (!ok && et() == 0) atomicOr(&P.ws->error, 1u);
     const int u = S.gunit[b];
     if (named_sync_or(kBarE, ET, !ok || u == kEnd)) break;
-    float* gb = b ? gbuf1 : gbuf0;
+    float* gb = reinterpret_cast<float*>(b ? gbuf1 : gbuf0);
+    GV* gv = reinterpret_cast<GV*>(b ? gbuf1 : gbuf0);
     if (MODE == MODE_SAMPLE)
       sample_epilogue<T, BIAS>(P, S, u, gb, gb + ngmax, S.hdr[b]);
     else if (MODE == MODE_TOP8)
       top8_epilogue<T>(P, S, u, gb, S.hdr[b]);
     else
-      resid_epilogue<T, BIAS>(P, S, u, gb, gb + ngmax, gb + 2 * ngmax, S.hdr[b]);
+      resid_epilogue<T, BIAS>(P, S, u, gv, gv + ngmax, gv + 2 * ngmax, S.hdr[b]);
     esync();  // every epilogue thread is done with the buffer and the scratch
     if (et() == 0) mbar_arrive(&S.gfree[b]);
     ++k;
@@ -1243,8 +1491,9 @@ __global__ void __launch_bounds__(RT, 2) row_kernel(const RowParams P) {
   unsigned char* ring = smem;
   const int ngmax = (P.V + kGroup - 1) / kGroup;
   const int narr = MODE == MODE_SAMPLE ? 2 : (MODE == MODE_TOP8 ? 1 : 3);  // arrays per buffer
-  float* gbuf0 = reinterpret_cast<float*>(smem + static_cast<size_t>(nst) * kStage);
-  float* gbuf1 = gbuf0 + static_cast<size_t>(narr) * ngmax;
+  using GV = typename GroupVal<T, MODE>::type;
+  unsigned char* gbuf0 = smem + static_cast<size_t>(nst) * kStage;
+  unsigned char* gbuf1 = gbuf0 + static_cast<size_t>(narr) * ngmax * sizeof(GV);
   const int tid = threadIdx.x;
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -1297,17 +1546,19 @@ const void* pick_fn(int dtype, bool bias) {
 
 }  // namespace
 
-size_t row_smem_bytes(int mode, int V, int nstages) {
+size_t row_smem_bytes(int mode, int dtype, int V, int nstages) {
   const size_t ng = static_cast<size_t>((V + kGroup - 1) / kGroup);
+  const size_t esz = (mode == MODE_RESID && dtype == 1) ? sizeof(GroupVal<uint16_t, MODE_RESID>::type)
+                                                        : sizeof(float);
   return static_cast<size_t>(nstages) * kStage +
-         2 * ng * 4 * (mode == MODE_SAMPLE ? 2 : (mode == MODE_TOP8 ? 1 : 3));
+         2 * ng * esz * (mode == MODE_SAMPLE ? 2 : (mode == MODE_TOP8 ? 1 : 3));
 }
 
 int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages) {
   const void* fn = mode == MODE_SAMPLE ? pick_fn<MODE_SAMPLE>(dtype, bias)
                    : mode == MODE_TOP8  ? pick_fn<MODE_TOP8>(dtype, false)
                                         : pick_fn<MODE_RESID>(dtype, bias);
-  const size_t smem = row_smem_bytes(mode, V, nstages);
+  const size_t smem = row_smem_bytes(mode, dtype, V, nstages);
   if (smem > kRowMaxSmem) return 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -1324,7 +1575,7 @@ cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const
                    : mode == MODE_TOP8  ? pick_fn<MODE_TOP8>(dtype, false)
                                         : pick_fn<MODE_RESID>(dtype, bias);
   if (P.nstages < 2 || P.nstages > kRowMaxStages) return cudaErrorInvalidValue;
-  const size_t smem = row_smem_bytes(mode, P.V, P.nstages);
+  const size_t smem = row_smem_bytes(mode, dtype, P.V, P.nstages);
   if (smem > kRowMaxSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

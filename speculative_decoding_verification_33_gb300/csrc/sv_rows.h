@@ -40,8 +40,9 @@ struct RowParams {
   Workspace* ws;                 // unit queue and error word (bit 0: a bounded wait gave up)
 };
 
-// Dynamic shared memory of one CTA: the ring and two buffers of per-group values.
-size_t row_smem_bytes(int mode, int V, int nstages);
+// Dynamic shared memory of one CTA: the ring and two buffers of per-group values (dtype 1 =
+// bf16 rows, whose residual keeps 16-bit group values).
+size_t row_smem_bytes(int mode, int dtype, int V, int nstages);
 // Co-resident CTAs per SM of the kernel for this configuration (0: does not fit).
 int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages);
 

@@ -248,6 +248,39 @@ def test_residual_topf_and_hits(cfg):
     print(w.name, "near ties", near, "hits", hits)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_residual_topf_planted_bias_sets(dtype):
+    """Draft rows whose bias sets take every path of the kernel's selection of the draft's 8
+    largest: one per group (random rows), several in one group (8 groups holding two planted
+    logits each; a decreasing row), more tied candidates than the kernel lists (a row of equal
+    values); ever larger logits planted across the stream. The target rows are the draft plus
+    noise, so beta on the set's ids moves the residual order there."""
+    V = 152064 if dtype == "bf16" else 70001
+    base = _planted_rows(V, dtype)
+    zd = W.bf16_bits_to_f32(base) if dtype == "bf16" else base.copy()
+    rng = np.random.default_rng(33)
+    pair = rng.standard_normal(V).astype(np.float32)
+    groups = rng.choice(V // 64, 8, replace=False)
+    for j, g in enumerate(groups):
+        pair[64 * g + 5] = 11.0 + 0.25 * j
+        pair[64 * g + 40] = 11.1 + 0.25 * j
+    noise = rng.standard_normal((2, V)).astype(np.float32)
+    zd = np.concatenate([zd, pair[None], noise[:1]], axis=0)
+    B = zd.shape[0]
+    zt = zd + 0.7 * rng.standard_normal(zd.shape).astype(np.float32)
+    tgt = np.stack([zt, zt[::-1]], axis=1)  # position 1: the bonus row, not read here
+    if dtype == "bf16":
+        tgt, dft = W.f32_to_bf16_bits(tgt), W.f32_to_bf16_bits(zd[:, None])
+    else:
+        dft = zd[:, None].copy()
+    w = W.small_variant(W.WORKLOADS[4], B=B, V=V).replace(
+        K=1, fanout=(8,), beta=0.3, bias_k=8, temperature=1.0, dtype=dtype)
+    d = {"target": tgt, "draft": dft, "draft_lens": np.ones(B, np.int32)}
+    compare_residual(d, w, residual_gpu(d, w)["r2"], range(B))
+    w3 = w.replace(fanout=(3,))
+    compare_residual(d, w3, residual_gpu(d, w3)["r2"], range(B))
+
+
 @pytest.mark.parametrize("V", [1, 9, 3001, 50000])
 def test_residual_topf_vocab_sizes_and_stride(V):
     w = W.small_variant(W.WORKLOADS[4], B=4, V=V).replace(bias_k=min(8, V))

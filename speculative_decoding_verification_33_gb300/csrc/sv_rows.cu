@@ -605,85 +605,6 @@ __device__ void row_top8(const T* row, int V, bool vec, const GV* gmax, int ng, 
   top8_elements(top8_groups<T>(row, V, vec, gmax, ng, S), V, S);
 }
 
-// top8_groups for the sampling epilogue, from the threads' contiguous runs of groups [lo, hi)
-// (tmax: the run's largest group maximum): the 8th largest run maximum, theta, is reached by 8
-// groups, so only runs whose maximum reaches it can hold one of the 8 largest groups, and only
-// their groups at or above theta are collected as keys (S.cand), of which warp 0 keeps the 8
-// largest. More than kCandCap such groups (ties at theta) take top8_groups instead.
-template <typename T, typename GV>
-__device__ G8 run_top8_groups(const GV* gmax, int lo, int hi, float tmax, int ng, const T* row,
-                              int V, bool vec, RowShared& S) {
-  const int t = et(), lane = t & 31, warp = t >> 5;
-  // the 8 largest run maxima of each warp (with repeats), then of the team
-  uint32_t o = float_to_ord(tmax), mine = 0u;
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const uint32_t m = __reduce_max_sync(FULL, o);
-    if (lane == r) mine = m;
-    const unsigned who = __ballot_sync(FULL, o == m && m != 0u);
-    if (who && lane == __ffs(who) - 1) o = 0u;
-  }
-  if (lane < 8) S.tm8[warp * 8 + lane] = mine;
-  if (t == 0) S.ncand = 0;
-  esync();
-  if (warp == 0) {
-    static_assert(NEW * 8 == 32, "the warps' 8 largest fill one warp");
-    uint32_t q = S.tm8[lane], m = 0u;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      m = __reduce_max_sync(FULL, q);
-      const unsigned who = __ballot_sync(FULL, q == m && m != 0u);
-      if (who && lane == __ffs(who) - 1) q = 0u;
-    }
-    if (lane == 0) S.rb[0] = m ? ord_to_float(m) : -INFINITY;
-  }
-  esync();
-  const float th = S.rb[0];
-  if (tmax >= th)
-    for (int g = lo; g < hi; ++g) {
-      const float v = gv_get(gmax, g);
-      if (v >= th) {
-        const int i = atomicAdd(&S.ncand, 1);
-        if (i < kCandCap) S.cand[i] = make_key(v, static_cast<uint32_t>(g));
-      }
-    }
-  esync();
-  const int n = S.ncand;
-  if (n > kCandCap) return top8_groups<T>(row, V, vec, gmax, ng, S);
-  if (warp == 0) {
-    static_assert(kCandCap == 64, "two candidates per lane");
-    unsigned long long a = lane < n ? S.cand[lane] : 0ull;
-    unsigned long long c = lane + 32 < n ? S.cand[lane + 32] : 0ull;
-    if (c > a) {
-      const unsigned long long x = a;
-      a = c;
-      c = x;
-    }
-    unsigned long long k = 0ull;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const unsigned long long m = warp_max_key(a);
-      if (lane == r) k = m;
-      if (m != 0ull && a == m) {
-        a = c;
-        c = 0ull;
-      }
-    }
-    if (lane < 8) S.top[lane] = k;
-  }
-  esync();
-  const unsigned long long k0 = S.top[2 * warp], k1 = S.top[2 * warp + 1], k7 = S.top[7];
-  esync();  // S.top is read by every warp before it is rewritten
-  G8 r;
-  r.g0 = k0 ? key_id(k0) : -1;
-  r.g1 = k1 ? key_id(k1) : -1;
-  r.thr = k7 ? key_value(k7) : -INFINITY;
-  r.a0 = r.b0 = r.a1 = r.b1 = -INFINITY;
-  if (r.g0 >= 0) ld2<T>(row, kGroup * r.g0 + 2 * lane, V, vec, r.a0, r.b0);
-  if (r.g1 >= 0) ld2<T>(row, kGroup * r.g1 + 2 * lane, V, vec, r.a1, r.b1);
-  return r;
-}
-
 // The Saguaro bias set (the bias_k largest draft logits, from S.top) and the renormalisation
 // N = 1 - (1 - beta) sum_S q, the terms summed in key order. Epilogue warp 0.
 __device__ void bias_set(const RowParams& P, RowShared& S, float Md, float Sd) {
@@ -899,8 +820,159 @@ __device__ void chunk_warps(const RowParams& P, RowShared& S, unsigned char* rin
 }
 
 // ------------------------------------------------------------------------------------------
+// reads of whole groups of a global row
+// ------------------------------------------------------------------------------------------
+// The 16-byte piece of a global row at element e (a multiple of 16 / sizeof(T)): one vector load
+// when the row is 16-byte aligned and the piece lies below V, else element by element; elements
+// at or past V, and every element when e < 0, read as -inf.
+template <typename T>
+__device__ __forceinline__ uint4 row_piece(const T* row, int e, int V, bool vec) {
+  constexpr int EPP = 16 / static_cast<int>(sizeof(T));
+  if (e >= 0 && vec && e + EPP <= V) return ldg_nc_v4(row + e);
+  uint32_t w[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t lo = (e >= 0 && e + 2 * h < V) ? static_cast<uint32_t>(row[e + 2 * h]) : 0xFF80u;
+      const uint32_t hi =
+          (e >= 0 && e + 2 * h + 1 < V) ? static_cast<uint32_t>(row[e + 2 * h + 1]) : 0xFF80u;
+      w[h] = lo | (hi << 16);
+    } else {
+      w[h] = (e >= 0 && e + h < V) ? __float_as_uint(row[e + h]) : __float_as_uint(-INFINITY);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// How a warp reads groups of a global row: 16-byte pieces of EPP elements, PPG pieces per group,
+// GPL groups per warp-wide load; lane l takes piece l mod PPG of group slot l / PPG.
+template <typename T>
+struct GroupReads {
+  static constexpr int EPP = 16 / static_cast<int>(sizeof(T));
+  static constexpr int PPG = kGroup / EPP;
+  static constexpr int GPL = 32 / PPG;
+  static constexpr int NL = kBatch / GPL;  // loads per row and lane for kBatch groups
+  static_assert(GPL * PPG == 32 && NL * GPL == kBatch, "group reads");
+};
+
+// Warp 0: the 8 largest elements of the n (<= kCandCap) candidate groups in S.cand (keys of group
+// maxima), as keys on lanes 0..7, descending (0 where fewer; 0 on the other lanes). The 8 largest
+// groups are read at once.
+template <typename T>
+__device__ unsigned long long warp_top8_of_candidates(RowShared& S, int n, const T* row, int V,
+                                                     bool vec) {
+  const int lane = threadIdx.x & 31;
+  static_assert(kCandCap == 64, "two candidates per lane");
+  unsigned long long a = lane < n ? S.cand[lane] : 0ull;
+  unsigned long long b = lane + 32 < n ? S.cand[lane + 32] : 0ull;
+  if (b > a) {
+    const unsigned long long x = a;
+    a = b;
+    b = x;
+  }
+  unsigned long long gk = 0ull;  // lane r: the r-th largest group key
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const unsigned long long m = warp_max_key(a);
+    if (lane == r) gk = m;
+    if (m != 0ull && a == m) {
+      a = b;
+      b = 0ull;
+    }
+  }
+  const unsigned long long k7 = __shfl_sync(FULL, gk, 7);
+  using R = GroupReads<T>;
+  constexpr int NP = 8 * R::PPG / 32;  // pieces per lane
+  uint4 q[NP];
+  int e[NP];
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    const int p = lane + 32 * j;
+    const unsigned long long kg = __shfl_sync(FULL, gk, p / R::PPG);
+    e[j] = kg ? kGroup * key_id(kg) + R::EPP * (p % R::PPG) : -1;
+    q[j] = row_piece<T>(row, e[j], V, vec);
+  }
+  // Each of the 8 groups holds an element at or above the 8th group maximum t8 (its own
+  // maximum). When they are the only 8 such elements, the r-th largest element is the maximum
+  // of the group of rank r (groups of equal maxima rank by index, as their ids do); otherwise
+  // the elements from t8 up go through a list.
+  const float t8 = k7 ? key_value(k7) : -INFINITY;
+  float ze[NP][R::EPP];
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    unpack_piece<T>(q[j], ze[j]);
+#pragma unroll
+    for (int kk = 0; kk < R::EPP; ++kk)
+      cnt += (e[j] >= 0 && e[j] + kk < V && ze[j][kk] >= t8) ? 1 : 0;
+  }
+  unsigned long long k = 0ull;  // lanes 0..7: the 8 largest, descending; 0 elsewhere
+  if (k7 != 0ull && __reduce_add_sync(FULL, cnt) == 8) {
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int kk = 0; kk < R::EPP; ++kk)
+        if (e[j] >= 0 && e[j] + kk < V && ze[j][kk] >= t8)
+          S.wtop[0][(lane + 32 * j) / R::PPG] =
+              make_key(ze[j][kk], static_cast<uint32_t>(e[j] + kk));
+    __syncwarp();
+    k = lane < 8 ? S.wtop[0][lane] : 0ull;
+  } else {
+    WarpTop8 top;
+    top.init(t8);
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int kk = 0; kk < R::EPP; ++kk)
+        top.offer(e[j] >= 0 && e[j] + kk < V, ze[j][kk], static_cast<uint32_t>(e[j] + kk));
+    k = top.L;
+  }
+  return k;
+}
+
+// ------------------------------------------------------------------------------------------
 // epilogue: sampling
 // ------------------------------------------------------------------------------------------
+// Warp 0 of the sampling epilogue: the bias set (the bias_k largest of the row's 8 largest, keys k
+// on lanes 0..7) into S (nS, S_ids, S_z, sgrp), and beta applied to the masses of the groups that
+// hold its ids: the lane of the first id of each such group (in set order) rescales the group's
+// mass by its ids from there on and records the change of its fixed-point value (S.dg, S.dq).
+__device__ void sample_set(const RowParams& P, RowShared& S, unsigned long long k, float* gmass,
+                           float Mdc) {
+  const int lane = threadIdx.x & 31;
+  const bool in = lane < P.bias_k && lane < 8 && k != 0ull;
+  const int nS = __popc(__ballot_sync(FULL, in));
+  const int id = in ? key_id(k) : -1;
+  const float z = in ? key_value(k) : 0.f;
+  const int g = in ? id / kGroup : -1;
+  if (in) {
+    S.S_ids[lane] = id;
+    S.S_z[lane] = z;
+    S.sgrp[lane] = g;
+  }
+  if (lane == 0) S.nS = nS;
+  bool first = in;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int gi = __shfl_sync(FULL, g, i);
+    if (i < lane && gi == g) first = false;
+  }
+  float w = first ? gmass[g] : 0.f;
+  const unsigned long long before = qfix(w);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int gi = __shfl_sync(FULL, g, i);
+    const float zi = __shfl_sync(FULL, z, i);
+    if (first && i >= lane && i < nS && gi == g)
+      w = fmaxf(fmaf(P.beta - 1.f, ex2_fast(fmaf(zi, P.c, -Mdc)), w), 0.f);
+  }
+  if (first) gmass[g] = w;
+  if (lane < 8) {
+    S.dg[lane] = first ? g : -1;
+    S.dq[lane] = first ? static_cast<long long>(qfix(w) - before) : 0ll;
+  }
+}
+
 template <typename T, bool BIAS>
 __device__ void sample_epilogue(const RowParams& P, RowShared& S, int u, float* gmax,
                                 float* gmass, const float* hdr) {
@@ -923,53 +995,50 @@ __device__ void sample_epilogue(const RowParams& P, RowShared& S, int u, float* 
   int nS = 0;
   // group masses relative to the row maximum, over contiguous runs of groups per thread (so that
   // the prefix of the inverse CDF follows the ids): fixed-point run totals, the run's largest
-  // group maximum
+  // group maximum and its group
   const float Mdc = __fmul_rn(M, c);
   const int lo = static_cast<int>((static_cast<long long>(t) * ng) / ET);
   const int hi = static_cast<int>((static_cast<long long>(t + 1) * ng) / ET);
   unsigned long long csum = 0;
   float tmax = -INFINITY;
+  int gtop = -1;
+#pragma unroll 4
   for (int g = lo; g < hi; ++g) {
     const float gm = gmax[g];
-    tmax = fmaxf(tmax, gm);
+    if (gm > tmax) {
+      tmax = gm;
+      gtop = g;
+    }
     const float w = gm > -INFINITY ? gmass[g] * exp2f(__fmul_rn(gm, c) - Mdc) : 0.f;
     gmass[g] = w;
     csum += qfix(w);
   }
-  // the bias set's 8 candidate groups, their reads started (they land during the prefix)
-  G8 cand;
-  if (BIAS) cand = run_top8_groups<T>(gmax, lo, hi, tmax, ng, row, V, vec, S);
-  unsigned long long W = 0;
-  unsigned long long pre = team_exclusive_u64(csum, S, &W);  // (its barriers publish gmass)
+  unsigned long long W = 0, pre = 0;
   if (BIAS) {
-    // the bias set, then (warp 0, lane j for the first id of each group in set order) the
-    // weights of its ids scaled by beta in the groups holding them: the change of each such
-    // group's fixed-point mass moves the totals and prefixes after it
-    top8_elements(cand, V, S);
-    bias_set(P, S, M, Sd);
-    if (t < 32) __syncwarp();  // warp 0 wrote the set
-    if (t < 8) {
-      const int ns = S.nS;
-      int g = -1;
-      long long dq = 0;
-      if (t < ns) {
-        g = S.S_ids[t] / kGroup;
-        bool first = true;
-        for (int i = 0; i < t; ++i) first = first && S.S_ids[i] / kGroup != g;
-        if (first) {
-          float w = gmass[g];
-          const unsigned long long before = qfix(w);
-          for (int i = t; i < ns; ++i)
-            if (S.S_ids[i] / kGroup == g)
-              w = fmaxf(fmaf(P.beta - 1.f, ex2_fast(fmaf(S.S_z[i], c, -Mdc)), w), 0.f);
-          gmass[g] = w;
-          dq = static_cast<long long>(qfix(w) - before);
-        } else {
-          g = -1;
+    // The bias set: its 8 elements lie in the 8 groups with the largest maxima, those in the runs
+    // whose maximum reaches a lower bound of the 8th largest run maximum, and there at or above
+    // it (the candidates, listed while the prefix runs). Each run's largest group is fetched into
+    // L2 meanwhile; most of the 8 are among them. Warp 0 then finds the set and its corrections.
+    if (gtop >= 0)
+      for (int o = 0; o < kGroup && kGroup * gtop + o < V; o += 128 / static_cast<int>(sizeof(T)))
+        prefetch_l2(row + kGroup * gtop + o);
+    if (t == 0) S.ncand = 0;
+    const float th = team_bound(tmax, S);  // (its barriers order the reset before the adds)
+    if (tmax >= th)
+      for (int g = lo; g < hi; ++g) {
+        const float v = gmax[g];
+        if (v >= th) {
+          const int k = atomicAdd(&S.ncand, 1);
+          if (k < kCandCap) S.cand[k] = make_key(v, static_cast<uint32_t>(g));
         }
       }
-      S.dg[t] = g;
-      S.dq[t] = dq;
+    pre = team_exclusive_u64(csum, S, &W);  // (its barriers publish gmass and the candidates)
+    const int n = S.ncand;
+    if (n > kCandCap) {  // (ties beyond the list) every group offered
+      top8_elements(top8_groups<T>(row, V, vec, gmax, ng, S), V, S);
+      if (t < 32) sample_set(P, S, t < 8 ? S.top[t] : 0ull, gmass, Mdc);
+    } else if (t < 32) {
+      sample_set(P, S, warp_top8_of_candidates<T>(S, n, row, V, vec), gmass, Mdc);
     }
     esync();
     nS = S.nS;
@@ -982,6 +1051,8 @@ __device__ void sample_epilogue(const RowParams& P, RowShared& S, int u, float* 
       if (g < lo) pre += d;
       else if (g < hi) csum += d;
     }
+  } else {
+    pre = team_exclusive_u64(csum, S, &W);  // (its barriers publish gmass)
   }
   const float uu = P.uni[u];
   const bool uok = uu >= 0.f && uu < 1.f;
@@ -1048,39 +1119,6 @@ __device__ void sample_epilogue(const RowParams& P, RowShared& S, int u, float* 
 // ------------------------------------------------------------------------------------------
 // epilogue: exact-residual top-F
 // ------------------------------------------------------------------------------------------
-// The 16-byte piece of a global row at element e (a multiple of 16 / sizeof(T)): one vector load
-// when the row is 16-byte aligned and the piece lies below V, else element by element; elements
-// at or past V, and every element when e < 0, read as -inf.
-template <typename T>
-__device__ __forceinline__ uint4 row_piece(const T* row, int e, int V, bool vec) {
-  constexpr int EPP = 16 / static_cast<int>(sizeof(T));
-  if (e >= 0 && vec && e + EPP <= V) return ldg_nc_v4(row + e);
-  uint32_t w[4];
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    if constexpr (sizeof(T) == 2) {
-      const uint32_t lo = (e >= 0 && e + 2 * h < V) ? static_cast<uint32_t>(row[e + 2 * h]) : 0xFF80u;
-      const uint32_t hi =
-          (e >= 0 && e + 2 * h + 1 < V) ? static_cast<uint32_t>(row[e + 2 * h + 1]) : 0xFF80u;
-      w[h] = lo | (hi << 16);
-    } else {
-      w[h] = (e >= 0 && e + h < V) ? __float_as_uint(row[e + h]) : __float_as_uint(-INFINITY);
-    }
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// How a warp reads groups of a global row: 16-byte pieces of EPP elements, PPG pieces per group,
-// GPL groups per warp-wide load; lane l takes piece l mod PPG of group slot l / PPG.
-template <typename T>
-struct GroupReads {
-  static constexpr int EPP = 16 / static_cast<int>(sizeof(T));
-  static constexpr int PPG = kGroup / EPP;
-  static constexpr int GPL = 32 / PPG;
-  static constexpr int NL = kBatch / GPL;  // loads per row and lane for kBatch groups
-  static_assert(GPL * PPG == 32 && NL * GPL == kBatch, "group reads");
-};
-
 // The bias set of a residual unit (the draft row's bias_k largest logits) and N, into S (nS, N,
 // S_ids and sgrp, the groups of those ids) for every epilogue thread. The 8 largest logits lie in
 // the 8 groups with the largest maxima (ties to the lower group), those groups in the runs (the
@@ -1126,71 +1164,7 @@ __device__ void resid_bias_set(const RowParams& P, RowShared& S, const GV* gmax,
     return;
   }
   if (warp == 0) {
-    static_assert(kCandCap == 64, "two candidates per lane");
-    unsigned long long a = lane < n ? S.cand[lane] : 0ull;
-    unsigned long long b = lane + 32 < n ? S.cand[lane + 32] : 0ull;
-    if (b > a) {
-      const unsigned long long x = a;
-      a = b;
-      b = x;
-    }
-    unsigned long long gk = 0ull;  // lane r: the r-th largest group key
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const unsigned long long m = warp_max_key(a);
-      if (lane == r) gk = m;
-      if (m != 0ull && a == m) {
-        a = b;
-        b = 0ull;
-      }
-    }
-    const unsigned long long k7 = __shfl_sync(FULL, gk, 7);
-    using R = GroupReads<T>;
-    constexpr int NP = 8 * R::PPG / 32;  // pieces per lane
-    uint4 q[NP];
-    int e[NP];
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-      const int p = lane + 32 * j;
-      const unsigned long long kg = __shfl_sync(FULL, gk, p / R::PPG);
-      e[j] = kg ? kGroup * key_id(kg) + R::EPP * (p % R::PPG) : -1;
-      q[j] = row_piece<T>(row, e[j], V, vec);
-    }
-    // Each of the 8 groups holds an element at or above the 8th group maximum t8 (its own
-    // maximum). When they are the only 8 such elements, the r-th largest element is the maximum
-    // of the group of rank r (groups of equal maxima rank by index, as their ids do); otherwise
-    // the elements from t8 up go through a list.
-    const float t8 = k7 ? key_value(k7) : -INFINITY;
-    float ze[NP][R::EPP];
-    int cnt = 0;
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-      unpack_piece<T>(q[j], ze[j]);
-#pragma unroll
-      for (int kk = 0; kk < R::EPP; ++kk)
-        cnt += (e[j] >= 0 && e[j] + kk < V && ze[j][kk] >= t8) ? 1 : 0;
-    }
-    unsigned long long k = 0ull;  // lanes 0..7: the 8 largest, descending; 0 elsewhere
-    if (k7 != 0ull && __reduce_add_sync(FULL, cnt) == 8) {
-#pragma unroll
-      for (int j = 0; j < NP; ++j)
-#pragma unroll
-        for (int kk = 0; kk < R::EPP; ++kk)
-          if (e[j] >= 0 && e[j] + kk < V && ze[j][kk] >= t8)
-            S.wtop[0][(lane + 32 * j) / R::PPG] =
-                make_key(ze[j][kk], static_cast<uint32_t>(e[j] + kk));
-      __syncwarp();
-      k = lane < 8 ? S.wtop[0][lane] : 0ull;
-    } else {
-      WarpTop8 top;
-      top.init(t8);
-#pragma unroll
-      for (int j = 0; j < NP; ++j)
-#pragma unroll
-        for (int kk = 0; kk < R::EPP; ++kk)
-          top.offer(e[j] >= 0 && e[j] + kk < V, ze[j][kk], static_cast<uint32_t>(e[j] + kk));
-      k = top.L;
-    }
+    const unsigned long long k = warp_top8_of_candidates<T>(S, n, row, V, vec);
     const bool in = lane < P.bias_k && k != 0ull;
     const float z = in ? key_value(k) : 0.f;
     const float term = in ? exp2f((z - Md) * P.c) / Sd : 0.f;

@@ -442,7 +442,7 @@ def run_rows(args, quiet=False):
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "traffic_source": traffic_src, "algorithmic_bytes_per_launch": b_alg,
                          "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms)},
-            "gpu_launches": args.steps * (1 if args.kernel == "draft_sample" else 2),
+            "gpu_launches": args.steps,
             "clocks": clk}
     if not args.no_cpu:  # the oracle on a bounded sample, one core
         n = 32

@@ -334,7 +334,7 @@ sv_status launch_prepass(const sv_problem* p, const Checked& c, int dev, int dty
   R.nstages = rc.first;
   const int units = p->B * p->K;
   const int ctas = std::min(units, rc.second * sm_count(dev));
-  return sv::launch_rows(R, 2, dtype, ctas, nullptr, nullptr, nullptr, stream) == cudaSuccess
+  return sv::launch_rows(R, 2, dtype, ctas, stream) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
 }
@@ -868,8 +868,7 @@ bool aligned16(const void* p, long long stride, size_t elt) {
 // device, at most one per unit), on the stream's workspace (queue counters and error word). The
 // ring gets the most stages that still let two CTAs share an SM (at least 3); failing that, one
 // CTA per SM with up to kRowMaxStages.
-sv_status run_rows(sv::RowParams& P, int mode, int dtype, int units, const int32_t* acc,
-                   const int32_t* tok, const int32_t* r1, cudaStream_t stream) {
+sv_status run_rows(sv::RowParams& P, int mode, int dtype, int units, cudaStream_t stream) {
   const bool bias = P.bias_k > 0 && P.beta < 1.f;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
@@ -883,8 +882,7 @@ sv_status run_rows(sv::RowParams& P, int mode, int dtype, int units, const int32
   if (!r) return st;
   P.ws = r->ws;
   const int ctas = std::min(units, per_sm * sm_count(dev));
-  return sv::launch_rows(P, mode, dtype, ctas, acc, tok, r1, stream) == cudaSuccess ? SV_OK
-                                                                                     : SV_ERR_CUDA;
+  return sv::launch_rows(P, mode, dtype, ctas, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace
@@ -919,8 +917,7 @@ sv_status spec_draft_sample(int rows, int V, sv_dtype dtype, long long row_strid
   P.out_conf = out_conf;
   P.out_exit = out_exit;
   P.use_vec = aligned16(draft_logits, row_stride, elt) ? 1 : 0;
-  return run_rows(P, 0, dtype == SV_DTYPE_BF16 ? 1 : 0, rows, nullptr, nullptr, nullptr,
-                  static_cast<cudaStream_t>(stream));
+  return run_rows(P, 0, dtype == SV_DTYPE_BF16 ? 1 : 0, rows, static_cast<cudaStream_t>(stream));
 }
 
 sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
@@ -960,12 +957,15 @@ sv_status spec_residual_topf(const sv_problem* prob, const void* target_logits,
   for (int i = 0; i < sv::kMaxK; ++i) P.fan[i] = c.fan[i];
   P.out_r2 = out_r2;
   P.out_hit = out_hit;
+  P.acc = accept_len;
+  P.tok = out_tokens;
+  P.r1 = r1_topF;
   P.use_vec = (aligned16(target_logits, prob->target_row_stride, c.elt) &&
                aligned16(draft_logits, prob->draft_row_stride, c.elt))
                   ? 1
                   : 0;
-  return run_rows(P, 1, prob->dtype == SV_DTYPE_BF16 ? 1 : 0, prob->B * prob->K, accept_len,
-                  out_tokens, r1_topF, static_cast<cudaStream_t>(stream));
+  return run_rows(P, 1, prob->dtype == SV_DTYPE_BF16 ? 1 : 0, prob->B * prob->K,
+                  static_cast<cudaStream_t>(stream));
 }
 
 sv_status spec_lmhead_stats(int rows, int d, int V, const void* hidden, long long hidden_stride,

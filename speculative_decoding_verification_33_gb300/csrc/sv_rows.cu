@@ -650,6 +650,10 @@ __device__ void producer(const RowParams& P, RowShared& S, unsigned char* ring) 
     if (lane == 0) u = static_cast<int>(atomicAdd(&P.ws->next, 1u));
     u = __shfl_sync(FULL, u, 0);
     if (u >= nunits) break;
+    // residual units are taken position by position across the sequences: the first positions,
+    // which want the most ids (F_i falls with i) and whose epilogues read the most groups, go
+    // while the stream still hides their epilogues; the last units taken want few
+    if (MODE == MODE_RESID) u = (u % P.B) * P.K + u / P.B;
     const T* rows[2] = {nullptr, nullptr};
     int nrows = 1;
     if (MODE == MODE_SAMPLE) {
@@ -664,6 +668,8 @@ __device__ void producer(const RowParams& P, RowShared& S, unsigned char* ring) 
       const int L = P.lens ? P.lens[b] : P.K;
       if (L < 1 || L > P.K || i >= L) {  // no residual here: its ids are -1
         if (lane < P.fmax) P.out_r2[static_cast<long long>(u) * P.fmax + lane] = -1;
+        // a sequence of invalid length has no cache-hit flag (its first unit writes it)
+        if (i == 0 && P.out_hit && lane == 0) P.out_hit[b] = -1;
         continue;
       }
       rows[0] = static_cast<const T*>(P.tgt) +
@@ -1259,6 +1265,22 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const GV
   int32_t* out = P.out_r2 + static_cast<long long>(u) * P.fmax;
   const bool vec = P.use_vec != 0;
   const int F = min(P.fan[i], 8);  // only the first F of the order are written
+  // The sequence's cache-hit flag, by one lane for its first unit: 1 if the token the verify step
+  // drew at a rejected position a is among the top-F draft ids it prepared for that position, 0
+  // if not, -1 when every draft was accepted or the sequence is invalid.
+  if (P.out_hit && i == 0 && t == ET - 32) {
+    const int L = P.lens ? P.lens[b] : P.K;
+    const int a = P.acc[b];
+    int hit = -1;
+    if (a >= 0 && a < L) {
+      const int x = P.tok[static_cast<long long>(b) * (P.K + 1) + a];
+      const int Fa = min(P.fan[a], P.fmax);
+      const int32_t* r1 = P.r1 + (static_cast<long long>(b) * P.K + a) * P.fmax;
+      hit = 0;
+      for (int f = 0; f < Fa; ++f) hit |= r1[f] == x ? 1 : 0;
+    }
+    P.out_hit[b] = hit;
+  }
 
   const float2 T2 = make_float2(hdr[0], hdr[1]);
   const float2 D2 = make_float2(hdr[2], hdr[3]);
@@ -1489,26 +1511,6 @@ __global__ void __launch_bounds__(RT, 2) row_kernel(const RowParams P) {
     chunk_warps<T, MODE>(P, S, ring, gbuf0, gbuf1, ngmax);
 }
 
-// Cache-hit flags: 1 if the token the verify step drew at a rejected position is among the
-// top-F draft ids prepared for that outcome, 0 if not, -1 when every draft was accepted or the
-// sequence is invalid.
-__global__ void hit_kernel(const RowParams P, const int32_t* acc, const int32_t* tok,
-                           const int32_t* r1) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= P.B) return;
-  const int a = acc[b];
-  const int L = P.lens ? P.lens[b] : P.K;
-  int hit = -1;
-  if (a >= 0 && L >= 1 && L <= P.K && a < L) {
-    const int x = tok[static_cast<long long>(b) * (P.K + 1) + a];
-    const int F = min(P.fan[a], P.fmax);
-    hit = 0;
-    for (int f = 0; f < F; ++f)
-      if (r1[(static_cast<long long>(b) * P.K + a) * P.fmax + f] == x) hit = 1;
-  }
-  P.out_hit[b] = hit;
-}
-
 template <int MODE>
 const void* pick_fn(int dtype, bool bias) {
   if (dtype == 1)
@@ -1542,8 +1544,7 @@ int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages) {
   return n;
 }
 
-cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const int32_t* acc,
-                        const int32_t* tok, const int32_t* r1, cudaStream_t stream) {
+cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, cudaStream_t stream) {
   const bool bias = P.bias_k > 0 && P.beta < 1.f;
   const void* fn = mode == MODE_SAMPLE ? pick_fn<MODE_SAMPLE>(dtype, bias)
                    : mode == MODE_TOP8  ? pick_fn<MODE_TOP8>(dtype, false)
@@ -1557,11 +1558,6 @@ cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const
   if (ctas > 0) {
     void* args[] = {const_cast<RowParams*>(&P)};
     e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(RT), args, smem, stream);
-    if (e != cudaSuccess) return e;
-  }
-  if (mode == MODE_RESID && P.out_hit && P.B > 0) {
-    hit_kernel<<<(P.B + 127) / 128, 128, 0, stream>>>(P, acc, tok, r1);
-    e = cudaGetLastError();
   }
   return e;
 }

@@ -34,7 +34,10 @@ struct RowParams {
   float* out_conf;
   int32_t* out_exit;             // may be NULL
   int32_t* out_r2;               // residual
-  int32_t* out_hit;              // may be NULL
+  int32_t* out_hit;              // may be NULL; else the verify outputs below give the flags
+  const int32_t* acc;            // residual with out_hit: the verify step's [B] accept lengths,
+  const int32_t* tok;            //   [B][K+1] tokens
+  const int32_t* r1;             //   and [B][K][fmax] top-F ids
   unsigned long long* out_keys;  // top-8 prepass: 8 keys per (sequence, position)
   int32_t* out_topf;             // top-8 prepass: [B][K][fmax] top-F ids (may be NULL)
   Workspace* ws;                 // unit queue and error word (bit 0: a bounded wait gave up)
@@ -48,8 +51,7 @@ int row_ctas_per_sm(int mode, int dtype, bool bias, int V, int nstages);
 
 // mode 0: sampling (B rows), 1: residual top-F, 2: top-8 prepass of the verify step's draft rows
 // (both over B * K (sequence, position) pairs); `ctas` persistent CTAs. With out_hit set, the
-// residual launch is followed by the cache-hit flags.
-cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, const int32_t* acc,
-                        const int32_t* tok, const int32_t* r1, cudaStream_t stream);
+// residual launch also writes the cache-hit flags.
+cudaError_t launch_rows(const RowParams& P, int mode, int dtype, int ctas, cudaStream_t stream);
 
 }  // namespace sv

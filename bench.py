@@ -693,7 +693,7 @@ def run_legs(args):
                        ("lmhead", run_lmhead), ("verify_hidden", run_hidden)):
         sub = copy.copy(args)
         sub.kernel = kernel
-        sub.steps = min(args.steps, 10)
+        sub.steps = args.steps
         sub.warmup = 3
         t0 = time.perf_counter()
         line = fn(sub, quiet=True, **({"oracle_seqs": 2} if kernel == "verify_hidden" else {}))

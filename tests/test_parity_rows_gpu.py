@@ -281,6 +281,30 @@ def test_residual_topf_planted_bias_sets(dtype):
     compare_residual(d, w3, residual_gpu(d, w3)["r2"], range(B))
 
 
+def test_residual_topf_fewer_positive_than_wanted():
+    """Draft rows equal to the target rows: with beta = 1 every residual is zero (all ids -1);
+    with beta = 0.5 on 3 ids exactly those 3 are positive (p - beta q / N > 0 there, p - q / N < 0
+    elsewhere), fewer than the 8 or 2 ids asked for, so the search must end on having no positive
+    bound left rather than on an F-th best residual."""
+    rng = np.random.default_rng(34)
+    V, B, K = 50000, 4, 2
+    zt = rng.standard_normal((B, K + 1, V)).astype(np.float32) * 2.0
+    tgt = W.f32_to_bf16_bits(zt)
+    dft = tgt[:, :K].copy()
+    d = {"target": tgt, "draft": dft, "draft_lens": np.full(B, K, np.int32)}
+    base = W.small_variant(W.WORKLOADS[4], B=B, V=V).replace(K=K, fanout=(8, 2),
+                                                             temperature=1.0)
+    for beta, bias_k in ((1.0, 0), (0.5, 3)):
+        w = base.replace(beta=beta, bias_k=bias_k)
+        r2 = residual_gpu(d, w)["r2"]
+        compare_residual(d, w, r2, range(B))
+        want = 0 if bias_k == 0 else bias_k
+        for b in range(B):
+            for i in range(K):
+                got = [g for g in r2[b, i].tolist() if g >= 0]
+                assert len(got) == min(want, w.fanout[i]), (beta, b, i, got)
+
+
 @pytest.mark.parametrize("V", [1, 9, 3001, 50000])
 def test_residual_topf_vocab_sizes_and_stride(V):
     w = W.small_variant(W.WORKLOADS[4], B=4, V=V).replace(bias_k=min(8, V))

@@ -125,7 +125,9 @@ sv_status spec_verify_plan(const sv_problem* prob, int mode, int* cluster, int* 
 /*
  * Which kernels spec_verify takes for this problem on the current device (*route) and how many
  * launches one call makes (*launches). Routes: SV_ROUTE_WALK, the chained cluster walk (one
- * launch, two with the top-8 prepass over the draft rows for a bias set or top-F ids);
+ * launch for a greedy batch; three for a stochastic one, whose draws two launches chained after
+ * the walk take as the walk decides each sequence; two with the top-8 prepass over the draft
+ * rows for a bias set or top-F ids, the walk then drawing itself);
  * SV_ROUTE_GREEDY_ROWS, greedy batches whose padded target rows fit in 64 MiB (an argmax per row
  * slice of every target row, then one warp per sequence: two launches); SV_ROUTE_SMALL,
  * stochastic batches whose padded rows fit in 256 MiB (every row's statistics, the draw's slice

@@ -15,22 +15,24 @@
 //  - a producer warp streams the units' rows through a ring of shared-memory stages with bulk
 //    asynchronous copies;
 //  - eight chunk warps reduce every 64-element group of a row to its maximum g and (sampling)
-//    its mass, the sum of 2^(z c - fl(g c)), written to one of two group buffers, and each
-//    row to its maximum and softmax sum;
+//    its mass, the sum of 2^(z c - fl(g c)), or (residual) the target and draft maxima and the
+//    largest log-ratio max (z_t - z_d), written to one of two group buffers, and each row to its
+//    maximum and softmax sum;
 //  - a team of four epilogue warps finishes a unit from its group buffer while the chunk warps
 //    fill the other buffer with the next unit, so the stream never waits for an epilogue.
 //
 // The epilogue works from the group values, with a handful of groups read again:
 //  - the row maximum and sum come with the buffer (softmax normaliser, exit confidence 1 / sum);
-//  - the bias set (the bias_k largest draft logits): a lower bound of the 8th largest element is
-//    the largest of the warps' 8th-largest per-thread maxima, and only the groups whose maximum
-//    reaches it (a few) are looked at element by element;
+//  - the bias set (the bias_k largest draft logits): its elements lie in the 8 groups with the
+//    largest maxima, and those in the threads' runs of groups whose maximum reaches a lower
+//    bound of the 8th largest run maximum; one warp keeps the 8 largest such groups and reads
+//    their elements;
 //  - the draw: group masses scaled to the row maximum (the biased ids corrected) give the
 //    fixed-point masses of the inverse CDF; the chosen group's 64 weights are recomputed to find
 //    the element;
-//  - the residual top 8: the residual never exceeds the target weight 2^(z_t c - M_t c), so the
-//    groups holding the largest target elements give a lower bound of the 8th best residual, and
-//    only the groups whose largest target weight reaches it are evaluated.
+//  - the residual top F: each group's residual is bounded from its target maximum and its
+//    log-ratio maximum once the normalisers are known, and groups are read in rounds of
+//    decreasing bound until no bound left reaches the F-th best residual found.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -57,8 +59,8 @@ constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s) per
 constexpr int MODE_SAMPLE = 0, MODE_RESID = 1, MODE_TOP8 = 2;
 constexpr int kEnd = -1;  // unit tag after the last unit
 constexpr int kBatch = 8;  // residual: groups an epilogue warp reads per round trip
-constexpr int kCandCap = 64;  // sampling: candidate groups of the bias set kept in shared memory
-constexpr int kTierCap = 256;  // residual: groups of one tier listed in shared memory at once
+constexpr int kCandCap = 64;  // candidate groups of the bias set listed in shared memory
+constexpr int kRoundCap = 256;  // residual: groups of one round listed in shared memory at once
 
 static_assert(RT == CT + ET + 32, "chunk warps, epilogue warps, one producer warp");
 static_assert(kStage % (8 * kGroup) == 0, "whole groups per stage");
@@ -71,7 +73,7 @@ struct RowShared {
   float hdr[2][4];         // per buffer: row maximum and sum (target, then draft for a residual)
   float cm[NCW], cs[NCW];  // chunk-warp scratch
   // epilogue scratch
-  float rmax[NEW], rsum[NEW], rb[NEW];
+  float rmax[NEW], rb[NEW];
   unsigned long long ru[NEW];
   unsigned long long wtop[NEW][8];
   unsigned long long top[8];  // the last team top 8
@@ -81,15 +83,14 @@ struct RowShared {
   float S_z[8];
   int sgrp[8];  // the groups of S_ids
   unsigned long long t_loc;
-  // sampling with a bias set: the candidate groups of the 8 largest, and the corrections of the
-  // groups that hold ids of the set
+  // a bias set: the candidate groups of the 8 largest; sampling: the corrections of the groups
+  // that hold ids of the set
   unsigned long long cand[kCandCap];
   int ncand;
   int dg[8];
   long long dq[8];
-  uint32_t tm8[NEW * 8];
-  // residual: the groups of the current tier
-  int tl[kTierCap];
+  // residual: the groups of the current round
+  int tl[kRoundCap];
   int ntl;
 };
 
@@ -1359,7 +1360,7 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const GV
   // Rounds of groups in decreasing bound, a visited group's bound set to -1. Each round takes the
   // groups left whose bound reaches both the F-th best residual found so far and a lower bound
   // of the 8th largest bound left (some warp has 8 threads whose largest bound left reaches its
-  // 8th largest), so a round reads the next few groups in bound order (up to kTierCap; the rest
+  // 8th largest), so a round reads the next few groups in bound order (up to kRoundCap; the rest
   // stay for the next round), each warp kBatch groups per round trip. The listing pass also
   // finds each thread's largest bound left: the rounds end when none reaches the F-th best (or
   // none is positive while fewer than F residuals are known).
@@ -1382,7 +1383,7 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const GV
       bool listed = false;
       if (bg > 0.f && bg >= lr) {
         const int at = atomicAdd(&S.ntl, 1);
-        if (at < kTierCap) {
+        if (at < kRoundCap) {
           S.tl[at] = g;
           gv_put(gdel, g, -1.f);
           listed = true;
@@ -1397,7 +1398,7 @@ __device__ void resid_epilogue(const RowParams& P, RowShared& S, int u, const GV
       S.rmax[warp] = rm;
     }
     esync();
-    const int n = min(S.ntl, kTierCap);
+    const int n = min(S.ntl, kRoundCap);
     if (n > 0)
       for (int j0 = kBatch * warp; j0 < n; j0 += kBatch * NEW)
         offer_groups<T, BIAS>(top, zt, zd, S.tl, j0, n, V, vec, c, Mtc, Mdc, rho, rhoS, S, nS);

@@ -229,6 +229,18 @@ def test_beta_bias_without_topf():
     check(d, w, run_gpu(d, w))
 
 
+@pytest.mark.parametrize("hint", [0, 4])
+def test_fanout_with_zero_widths(hint):
+    """Fan-out widths of 0 leave a position's top-F ids at -1 and the others take the first F_i
+    of the draft row's order: on the small route (no hint at this size) and on the cluster walk
+    with the top-8 prepass (hint 4)."""
+    w = W.small_variant(W.WORKLOADS[4], B=12, V=20000).replace(fanout=(3, 0, 5, 0, 1))
+    d = W.make_inputs(w)
+    g = run_gpu(d, w, cluster_hint=hint)
+    check(d, w, g)
+    assert (g["topf"][:, 1] == -1).all() and (g["topf"][:, 3] == -1).all()
+
+
 # ---------------------------------------------------------------------------------------------
 # other entry points give the same answer
 # ---------------------------------------------------------------------------------------------

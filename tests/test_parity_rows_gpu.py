@@ -281,6 +281,16 @@ def test_residual_topf_planted_bias_sets(dtype):
     compare_residual(d, w3, residual_gpu(d, w3)["r2"], range(B))
 
 
+def test_residual_topf_zero_widths():
+    """Positions whose fan-out width is 0 get no residual ids (all -1); the others their first
+    F_i."""
+    w = W.small_variant(W.WORKLOADS[4], B=6, V=20000).replace(fanout=(3, 0, 5, 0, 1))
+    d = W.make_inputs(w)
+    r2 = residual_gpu(d, w)["r2"]
+    compare_residual(d, w, r2, range(w.B))
+    assert (r2[:, 1] == -1).all() and (r2[:, 3] == -1).all()
+
+
 def test_residual_topf_fewer_positive_than_wanted():
     """Draft rows equal to the target rows: with beta = 1 every residual is zero (all ids -1);
     with beta = 0.5 on 3 ids exactly those 3 are positive (p - beta q / N > 0 there, p - q / N < 0

@@ -60,6 +60,22 @@ __device__ __forceinline__ const void* small_row(const SmallParams& P, int b, in
   return base + ((static_cast<long long>(b) * rows + i) * stride) * static_cast<long long>(elt);
 }
 
+// An L2 cache policy under which the lines a load brings in are the first to be evicted.
+__device__ __forceinline__ unsigned long long l2_policy_evict_first() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// A 16-byte read-only global load that does not allocate in L1, under an L2 cache policy.
+__device__ __forceinline__ uint4 ldg_nc_v4_hint(const void* p, unsigned long long pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
 // 8 elements as they sit in memory: one 16-byte word for bf16, two for float
 template <typename T>
 struct Raw8 {
@@ -71,6 +87,12 @@ __device__ __forceinline__ void raw_load(const T* p, Raw8<T>& r) {
 #pragma unroll
   for (int k = 0; k < static_cast<int>(sizeof(T) / 2); ++k)
     r.w[k] = ldg_nc_v4(reinterpret_cast<const char*>(p) + 16 * k);
+}
+template <typename T>
+__device__ __forceinline__ void raw_load(const T* p, Raw8<T>& r, unsigned long long pol) {
+#pragma unroll
+  for (int k = 0; k < static_cast<int>(sizeof(T) / 2); ++k)
+    r.w[k] = ldg_nc_v4_hint(reinterpret_cast<const char*>(p) + 16 * k, pol);
 }
 
 __device__ __forceinline__ void raw_unpack(const Raw8<uint16_t>& r, float (&z)[8]) {
@@ -690,7 +712,7 @@ constexpr int kMassUnroll = 8 / static_cast<int>(sizeof(T));
 // The draw's weights summed over slice `sl` of sequence b's decided rows (decision d): per
 // 8-element vector the sequential float sums of the residual and of p, truncated to integers of
 // 2^-44, summed per slice into P.mass. Block-wide.
-template <typename T, bool BIAS>
+template <typename T, bool BIAS, bool EF = false>
 __device__ void slice_masses(const SmallParams& P, int b, const SmallDecision& d, int sl) {
   __shared__ unsigned long long s_r[kMassThreads / 32], s_p[kMassThreads / 32];
   const int tid = threadIdx.x;
@@ -713,14 +735,20 @@ __device__ void slice_masses(const SmallParams& P, int b, const SmallDecision& d
       maybe |= j < d.nS && o >= 0 && d.ids[j] < e1 && ((o >> 3) % kMassThreads) == tid;
     }
   unsigned long long own_r = 0, own_p = 0;
+  const unsigned long long pol = EF ? l2_policy_evict_first() : 0ull;
   for (int g0 = tid; g0 < nv; g0 += U * kMassThreads) {
     Raw8<T> vt[U], vd[U];
 #pragma unroll
     for (int k = 0; k < U; ++k) {
       const int e = e0 + 8 * (g0 + k * kMassThreads);
       if (al && e + 8 <= e1) {
-        raw_load(gt + e, vt[k]);
-        if (two) raw_load(gd + e, vd[k]);
+        if (EF) {
+          raw_load(gt + e, vt[k], pol);
+          if (two) raw_load(gd + e, vd[k], pol);
+        } else {
+          raw_load(gt + e, vt[k]);
+          if (two) raw_load(gd + e, vd[k]);
+        }
       }
     }
 #pragma unroll
@@ -803,7 +831,7 @@ __global__ void __launch_bounds__(kMassThreads, 8) walk_mass(const SmallParams P
   if (b < 0 || b >= P.B) return;
   const SmallDecision d = P.dec[b];
   if (!d.ok || d.a < 0 || d.a > P.K) return;
-  slice_masses<T, BIAS>(P, b, d, sl);
+  slice_masses<T, BIAS, true>(P, b, d, sl);
 }
 
 template <typename T, bool BIAS>
